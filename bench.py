@@ -1,0 +1,449 @@
+"""Benchmark of the paged decode-attention step on GB300.
+
+Default workload (`long32k`): batch 8, every context 32,768 tokens, GQA 32
+query / 8 KV heads, head_dim 128, bf16 K/V, block size 16, physical blocks a
+random permutation of a 16,384-block pool, split-KV over 16 chunks merged
+with lse_merge.  One step = slot mapping + kv_append of the 8 decode tokens
++ the split attention kernel + the LSE merge (the exact launches that
+pkv_paged_decode_attn makes), with the KV cache resident in HBM.
+
+Metric: HBM GB/s over the step's algorithmic bytes (every cached K/V byte
+once, plus q, block tables, appended tokens, out and lse), its fraction of the
+measured peak, and sequence-tokens/s.  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "paged decode-attn HBM GB/s (% of GB300 peak), seq-tokens/s at 32K ctx GQA"
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_HBM_GBS = 6800.0
+PROFILE = os.path.join(ROOT, "profiles", "decode_tma_long32k.txt")
+KERNEL_SOURCES = [os.path.join(ROOT, "paged_kv_cache_93_gb300", "csrc", f)
+                  for f in ("decode_tma.cu", "pkv_device.cuh")]
+
+
+# ----------------------------------------------------------------- helpers
+
+def kv_bytes_per_token(w) -> int:
+    """K and V bytes one token occupies in one layer: (Dk + Dv) x Hkv x 2 B."""
+    return (w.head_dim_k + w.head_dim_v) * w.num_kv_heads * 2
+
+
+def step_bytes(w, splits: int):
+    """Algorithmic bytes of one step, and of one launch of the split kernel."""
+    lens = w.seq_lens.to(torch.int64)
+    kv = int(lens.sum()) * kv_bytes_per_token(w)
+    B, Hq = w.batch, w.num_q_heads
+    q = B * Hq * w.head_dim_k * 4
+    tables = int(((lens + w.block_size - 1) // w.block_size).sum()) * 4 + B * 4
+    out = B * Hq * (w.head_dim_v + 1) * 4
+    T = int(w.new_pos.numel())
+    append = 2 * T * kv_bytes_per_token(w) + T * (8 + 4 + 8)
+    kernel = kv + q + tables
+    return kv + q + tables + out + append, kernel
+
+
+def load_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def stored_traffic():
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    try:
+        h = hashlib.sha256()
+        for p in KERNEL_SOURCES:
+            with open(p, "rb") as f:
+                h.update(f.read())
+        vals = {}
+        with open(PROFILE, encoding="utf-8") as f:
+            for line in f:
+                if "=" in line and not line.lstrip().startswith("#"):
+                    k, v = line.split("=", 1)
+                    vals[k.strip()] = v.strip()
+        if vals.get("source_sha256") != h.hexdigest():
+            return None
+        return int(vals["traffic_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.samples = []
+        self.proc = None
+        self.window = None
+        ident = str(device_index)
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            ident = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+        except Exception:
+            pass
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", ident, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def wait_ready(self, timeout=5.0):
+        t = time.time()
+        while self.proc and not self.samples and time.time() - t < timeout:
+            time.sleep(0.02)
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = [s for ts, s in self.samples if t0 <= ts <= t1 and len(s) >= 8]
+        if not rows:
+            rows = [s for _, s in self.samples if len(s) >= 8][-3:]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[0]) for r in rows if num(r[0]) is not None]
+        mx = [num(r[1]) for r in rows if num(r[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[4:8]) if v.strip() == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def bits_view(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+# ------------------------------------------------------------ device state
+
+class Step:
+    """Device-resident state of one workload and its decode step."""
+
+    def __init__(self, pkv, w, dev, splits):
+        self.pkv, self.w, self.splits = pkv, w, splits
+        self.k = w.k_pool.to(dev)
+        self.v = w.v_pool.to(dev)
+        self.bt = w.block_tables.to(dev)
+        self.lens = w.seq_lens.to(dev)
+        self.q = w.q.to(dev)
+        self.new_seq = w.new_seq.to(dev)
+        self.new_pos = w.new_pos.to(dev)
+        self.k_new = w.k_new.to(dev)
+        self.v_new = w.v_new.to(dev)
+        B, Hq = w.batch, w.num_q_heads
+        self.slots = torch.empty(w.new_pos.numel(), dtype=torch.int64, device=dev)
+        self.out = torch.empty(B, Hq, w.head_dim_v, device=dev)
+        self.lse = torch.empty(B, Hq, device=dev)
+        self.out_part = torch.empty(splits, B, Hq, w.head_dim_v, device=dev)
+        self.lse_part = torch.empty(splits, B, Hq, device=dev)
+
+    def run(self, ev_a=None, ev_b=None):
+        p, w = self.pkv, self.w
+        p.slot_mapping(self.k, self.v, self.bt, self.new_seq, self.new_pos, out=self.slots)
+        p.kv_append(self.k, self.v, self.k_new, self.v_new, self.slots)
+        if ev_a is not None:
+            ev_a.record()
+        p.paged_decode_attn_partial(self.q, self.k, self.v, self.bt, self.lens, w.scale,
+                                    self.splits, out_part=self.out_part, lse_part=self.lse_part)
+        if ev_b is not None:
+            ev_b.record()
+        p.lse_merge(self.out_part, self.lse_part, out=self.out, lse=self.lse)
+
+
+# ------------------------------------------------------------------ arms
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def oracle_gbs(w, tokens: int | None, repeats: int = 1):
+    """Time the CPU oracle (all host cores) over every row of `w`, restricted
+    to the first `tokens` tokens of each sequence when given."""
+    import oracle
+    kp, vp = bits_view(w.k_pool), bits_view(w.v_pool)
+    q, bt, lens = w.q.numpy(), w.block_tables.numpy(), w.seq_lens.numpy()
+    end = None
+    if tokens is not None:
+        end = np.minimum(lens, tokens).astype(np.int32)
+    used = int((end if end is not None else lens).astype(np.int64).sum()) * kv_bytes_per_token(w)
+    times = []
+    for _ in range(repeats):
+        t = time.perf_counter()
+        oracle.paged_decode_attn(q, kp, vp, bt, lens, w.scale, tok_end=end)
+        times.append(time.perf_counter() - t)
+    return used, times
+
+
+def workload_desc(w, splits):
+    return (f"{w.name}: batch {w.batch} x {int(w.seq_lens.max())} tokens, GQA "
+            f"{w.num_q_heads}/{w.num_kv_heads} heads, head_dim {w.head_dim_k}, bf16 K/V, block "
+            f"{w.block_size}, {w.num_blocks}-block randomly permuted pool, {splits} splits + "
+            f"lse_merge")
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    w = workloads.make(args.workload)
+    cores = os.cpu_count()
+    # Size the per-step sample so that warm-up + timed steps stay near a minute.
+    probe_tokens = 512
+    used, t = oracle_gbs(w, probe_tokens)
+    per_token_s = t[0] / probe_tokens
+    budget = 60.0 / max(1, args.steps + args.warmup)
+    tokens = int(max(64, min(int(w.seq_lens.max()), budget / max(per_token_s, 1e-9))))
+    for _ in range(args.warmup):
+        oracle_gbs(w, tokens)
+    times = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        used, tt = oracle_gbs(w, tokens)
+        times.append(tt[0])
+    wall = time.perf_counter() - t0
+    gbs = used * args.steps / sum(times) / 1e9
+    sample = (f"every (sequence, query head) row of {args.workload}, first {tokens} of "
+              f"{int(w.seq_lens.max())} tokens per sequence, per step")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * wall / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_desc(w, args.splits), "oracle": "C, fp64, all host cores"},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }))
+
+
+def run_gpu(args, world, rank, local):
+    import paged_kv_cache_93_gb300 as pkv
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = workloads.make(args.workload)
+    splits = args.splits
+    st = Step(pkv, w, dev, splits)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    total_bytes, kernel_bytes = step_bytes(w, splits)
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        st.run()
+    torch.cuda.synchronize()
+    if pkv.device_status(reset=True) != 0:
+        raise RuntimeError("device status word set during warm-up")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.wait_ready()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(K):
+        flush.zero_()                       # L2 flush (outside the timed events)
+        e = ev[i]
+        e[0].record(stream)
+        st.run(e[1], e[2])
+        e[3].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    t1 = time.time()
+    step_ms = [e[0].elapsed_time(e[3]) for e in ev]
+    kern_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    clocks = sampler.summary(t0, t1) if sampler else None
+    if sampler:
+        sampler.stop()
+    if pkv.device_status(reset=True) != 0:
+        raise RuntimeError("device status word set during the timed steps")
+
+    ms = max_over_ranks(statistics.fmean(step_ms), world)
+    kms = max_over_ranks(statistics.fmean(kern_ms), world)
+    value = world * total_bytes / (ms * 1e-3) / 1e9
+    peak, peak_kind = load_peak()
+    kernel_gbs = kernel_bytes / (kms * 1e-3) / 1e9
+
+    # ---- end to end through the public API, host buffers in pinned memory
+    pin = {n: getattr(w, n).pin_memory() for n in
+           ("q", "block_tables", "seq_lens", "new_seq", "new_pos", "k_new", "v_new")}
+    h_out = torch.empty(w.batch, w.num_q_heads, w.head_dim_v).pin_memory()
+    h_lse = torch.empty(w.batch, w.num_q_heads).pin_memory()
+    d = {n: torch.empty_like(t, device=dev) for n, t in pin.items()}
+    ws = torch.empty(max(1, pkv.decode_workspace_size(w.batch, w.num_q_heads, w.head_dim_v,
+                                                      splits)), dtype=torch.uint8, device=dev)
+    h2d = sum(t.numel() * t.element_size() for t in pin.values())
+    d2h = h_out.numel() * 4 + h_lse.numel() * 4
+    ke = max(3, min(K, 200))
+
+    def e2e_step():
+        for n, t in pin.items():
+            d[n].copy_(t, non_blocking=True)
+        slots = pkv.slot_mapping(st.k, st.v, d["block_tables"], d["new_seq"], d["new_pos"])
+        pkv.kv_append(st.k, st.v, d["k_new"], d["v_new"], slots)
+        out, lse = pkv.paged_decode_attn(d["q"], st.k, st.v, d["block_tables"], d["seq_lens"],
+                                         w.scale, num_splits=splits, workspace=ws)
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    te = time.perf_counter()
+    for _ in range(ke):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks((time.perf_counter() - te) / ke, world)
+    barrier(world)
+
+    if rank != 0:
+        return
+
+    # ---- CPU baseline: the oracle on this host's cores, the whole workload
+    used, times = oracle_gbs(w, None if not args.quick_cpu else 2048, repeats=1)
+    cpu_gbs = used / min(times) / 1e9
+    traffic = stored_traffic()
+    seq_tokens = int(w.seq_lens.sum())
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": workload_desc(w, splits), "batch": w.batch,
+            "context": int(w.seq_lens.max()), "num_q_heads": w.num_q_heads,
+            "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim_k,
+            "block_size": w.block_size, "num_splits": splits,
+            "step": "slot_mapping + kv_append (8 decode tokens) + split attention + lse_merge",
+            "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MiB write, untimed); "
+                  f"KV {total_bytes / 1e9:.3f} GB > 129 MB L2",
+            "parallelism": "replicas" if world > 1 else "single GPU",
+            "compute": "bf16 tensor-core products (fp32 query and probabilities split "
+                       "into bf16 hi+lo), fp32 accumulate and softmax",
+        },
+        "pct_of_peak": round(100 * value / world / peak, 2),
+        "seq_tokens_per_s": round(world * seq_tokens / (ms * 1e-3), 1),
+        "decode_steps_per_s": round(world * 1e3 / ms, 2),
+        "roofline": {
+            "bound": "hbm", "achieved": round(kernel_gbs, 2), "peak": peak,
+            "unit": "GB/s", "frac": round(kernel_gbs / peak, 4), "traffic": traffic,
+            "kernel": "decode_tma_kernel<128,4,4> (split attention)",
+            "algorithmic_bytes_per_launch": kernel_bytes,
+            "launch_ms": round(kms, 5), "peak_kind": f"{peak_kind} hbm_gbs",
+        },
+        "cpu_baseline": {
+            "value": round(cpu_gbs, 4), "unit": "GB/s", "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": "whole workload (every row, every token), C fp64 oracle, all host cores"
+            if not args.quick_cpu else "every row, first 2048 tokens",
+        },
+        "e2e": {
+            "value": round(total_bytes / e2e_s / 1e9 * world, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(e2e_s * 1e3, 4), "steps": ke,
+            "api": "pinned host inputs -> slot_mapping + kv_append + paged_decode_attn -> "
+                   "pinned host out/lse",
+        },
+        "gpu_launches": 4 * K,
+        "clocks": clocks,
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default="long32k", choices=["long32k", "mix", "tiny"])
+    ap.add_argument("--splits", type=int, default=16)
+    ap.add_argument("--quick-cpu", action="store_true", help="smaller oracle sample")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_gpu(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,274 @@
+/*
+ * pkv.h -- C ABI of libpkv: paged KV-cache decode attention for GB300 (sm_103a).
+ *
+ * The operations follow these pages (cited by title and section):
+ *   [PA]  "PagedAttentionとは？KVキャッシュを分割してLLMのメモリの無駄を減らす仕組み":
+ *         "PagedAttentionはブロック表で論理順序と物理配置を分ける" (block tables),
+ *         "要求の終了で空いたブロックを再利用する具体例" (allocation and reuse),
+ *         "共通ブロックの共有とコピーオンライト" (ref counts, copy-on-write).
+ *   [KVB] "1,000 人が同時に AI に質問したら、誰が最初に答えをもらうのか? KV キャッシュと
+ *         continuous batching": "KV キャッシュは何を保持するのか?" (a decode step
+ *         appends the new token's K/V, then attends over everything stored).
+ *   [DCP] "なぜ長文LLMは遅くなるのか｜Decode Context ParallelismでKVキャッシュを分散する":
+ *         interleaved assignment of tokens to partitions, the attention backend
+ *         returning the softmax LSE, and the three-stage decode step whose last
+ *         stage corrects the partial outputs with the shared LSEs and sums them.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Every tensor pointer is a DEVICE pointer owned by the caller; the library
+ *    allocates no device memory.  Pointers must be 16-byte aligned.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream) and returns a pkv_status.  A nonzero status from the host
+ *    checks means nothing was launched.
+ *  - Conditions only the device can see (a block id outside the pool, a slot
+ *    out of range, a sequence longer than its table, overlapping copy pairs,
+ *    a pipeline wait that gave up) never fault: the offending item is skipped
+ *    and a bit is OR-ed into a per-device status word, read with
+ *    pkv_device_status().
+ *  - Cache layout (one layer): k_pool [num_blocks][num_kv_heads][block_size][head_dim_k]
+ *    and v_pool [num_blocks][num_kv_heads][block_size][head_dim_v], bf16.  One
+ *    (block, KV head) tile is contiguous.  Token j of sequence b lives in
+ *    physical block block_tables[b][j / block_size] at offset j % block_size.
+ *  - Query head h uses KV head h / (num_q_heads / num_kv_heads).
+ *  - Head dims: any multiple of 8 up to 1024 (the tensor-core kernel takes
+ *    64 and 128); q, out and lse are fp32; lse is the natural log of
+ *    sum_j exp(s_j) over the scaled scores s_j = scale * q . k_j.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *pkv_stream_t; /* same type as cudaStream_t */
+
+typedef enum pkv_status {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = -1,     /* null pointer, negative count, bad flag */
+    PKV_ERR_SHAPE = -2,           /* unsupported or inconsistent dimensions */
+    PKV_ERR_ALIGNMENT = -3,       /* a pointer is not 16-byte aligned */
+    PKV_ERR_WORKSPACE_TOO_SMALL = -4,
+    PKV_ERR_CUDA = -5,            /* a CUDA runtime call failed */
+    PKV_ERR_DEVICE = -6,          /* the device status word holds an error bit */
+    PKV_ERR_NO_SPACE = -7,        /* block manager: not enough free blocks */
+    PKV_ERR_NOT_FOUND = -8        /* block manager: unknown sequence id */
+} pkv_status;
+
+/* Bits of the per-device status word (see pkv_device_status). */
+#define PKV_DEV_BLOCK_ID      0x1u  /* a block id outside [0, num_blocks) was met */
+#define PKV_DEV_SLOT          0x2u  /* a slot outside [0, num_blocks*block_size) */
+#define PKV_DEV_SEQ_LEN       0x4u  /* seq_len < 0 or > max_blocks * block_size */
+#define PKV_DEV_COPY_CONFLICT 0x8u  /* copy pairs share a destination, or a
+                                       destination is another pair's source */
+#define PKV_DEV_TIMEOUT       0x10u /* a pipeline wait gave up (library bug) */
+#define PKV_DEV_TABLE_RANGE   0x20u /* a position past the end of its table row */
+
+/* Shape of one layer's paged KV cache. */
+typedef struct pkv_cache_desc {
+    int32_t num_blocks;
+    int32_t block_size;   /* tokens per block, 1..256 */
+    int32_t num_kv_heads;
+    int32_t head_dim_k;
+    int32_t head_dim_v;
+} pkv_cache_desc;
+
+/* Human-readable name of a pkv_status value. */
+const char *pkv_status_string(int status);
+
+/* Reads the current device's status word into *flags after synchronizing
+ * `stream`; clears it when `reset` is nonzero.  Returns PKV_OK, or
+ * PKV_ERR_CUDA if the copy failed.  The word is shared by every call on the
+ * device; it is never cleared implicitly. */
+int pkv_device_status(uint32_t *flags, int reset, pkv_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * pkv_slot_mapping -- [PA] "PagedAttentionはブロック表で論理順序と物理配置を分ける":
+ * the slot (physical block * block_size + offset) of logical position
+ * positions[t] of sequence seq_ids[t]:
+ *     slot = block_tables[seq][pos / block_size] * block_size + pos % block_size.
+ * seq_ids [T] int32, positions [T] int64, block_tables [batch][max_blocks] int32,
+ * slot_mapping [T] int64 (output).  A negative seq id or position gives -1
+ * (padding).  A position past the table row or a block id outside the pool
+ * gives -1 and sets PKV_DEV_TABLE_RANGE / PKV_DEV_BLOCK_ID.
+ * ------------------------------------------------------------------------- */
+int pkv_slot_mapping(const pkv_cache_desc *cache, const int32_t *block_tables,
+                     int32_t batch, int32_t max_blocks, const int32_t *seq_ids,
+                     const int64_t *positions, int64_t num_tokens, int64_t *slot_mapping,
+                     pkv_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * pkv_kv_append -- [KVB] "KV キャッシュは何を保持するのか?": write each new token's
+ * key and value into the cache.  Token t's K row for KV head g
+ * (k_new[t][g][0..head_dim_k)) goes to k_pool[slot / bs][g][slot % bs][:], and
+ * likewise for V, with slot = slot_mapping[t].  k_new [T][num_kv_heads][head_dim_k]
+ * and v_new [T][num_kv_heads][head_dim_v] bf16; slot_mapping [T] int64.
+ * Negative slots are skipped (padding); slots >= num_blocks * block_size are
+ * skipped and set PKV_DEV_SLOT.  Two tokens with the same slot race.
+ * ------------------------------------------------------------------------- */
+int pkv_kv_append(const pkv_cache_desc *cache, void *k_pool, void *v_pool,
+                  const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                  int64_t num_tokens, pkv_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * pkv_copy_blocks -- [PA] "共通ブロックの共有とコピーオンライト": before a sequence
+ * writes into a block it shares, the block is duplicated (and the caller then
+ * points that sequence's table at the copy).  For each i < num_pairs, every KV
+ * head's K and V tile of block src[i] is copied to block dst[i].  src, dst:
+ * [num_pairs] int32 device arrays.  A pair whose ids are out of range sets
+ * PKV_DEV_BLOCK_ID; a pair whose destination is also another pair's
+ * destination or any pair's source sets PKV_DEV_COPY_CONFLICT; such pairs are
+ * skipped, so the others never race with them.
+ * ------------------------------------------------------------------------- */
+int pkv_copy_blocks(const pkv_cache_desc *cache, void *k_pool, void *v_pool,
+                    const int32_t *src, const int32_t *dst, int32_t num_pairs,
+                    pkv_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * pkv_interleave_slot_mapping -- [DCP] interleaved assignment: the KV of token i
+ * belongs to partition (i / interleave) mod num_parts, and each partition
+ * keeps its tokens in their original order.  For tokens
+ * i = first_token .. first_token + num_tokens - 1 this writes the slot of
+ * token i inside its partition's table: part_block_tables [num_parts][max_blocks]
+ * int32 (each partition's table over a shared pool), slot_mapping [num_tokens]
+ * int64, and, when part_of_token is not NULL, the partition [num_tokens] int32.
+ * A local position past the partition's table gives -1 and sets
+ * PKV_DEV_TABLE_RANGE.
+ * ------------------------------------------------------------------------- */
+int pkv_interleave_slot_mapping(const pkv_cache_desc *cache, int64_t first_token,
+                                int64_t num_tokens, int32_t num_parts, int32_t interleave,
+                                const int32_t *part_block_tables, int32_t max_blocks,
+                                int64_t *slot_mapping, int32_t *part_of_token,
+                                pkv_stream_t stream);
+
+/* Host helper: how many of tokens 0..num_tokens-1 partition `part` holds
+ * under the same rule.  Returns -1 on invalid arguments. */
+int64_t pkv_interleave_partition_len(int64_t num_tokens, int32_t num_parts,
+                                     int32_t interleave, int32_t part);
+
+/* ---------------------------------------------------------------------------
+ * Decode attention.  [KVB] the new token's query is compared with the keys
+ * of all stored tokens and weights their values; [PA] the KV is read through
+ * the block table and the result is the same as for contiguous storage;
+ * [DCP] the backend also returns the softmax LSE.  For sequence b, query head
+ * h, KV head g = h / (num_q_heads / num_kv_heads) and j < seq_lens[b]:
+ *     s_j = scale * sum_d q[b][h][d] * K_j[d]
+ *     out[b][h][:] = sum_j e^{s_j} V_j / sum_j e^{s_j},  lse[b][h] = ln sum_j e^{s_j}
+ * q [batch][num_q_heads][head_dim_k] fp32; out [batch][num_q_heads][head_dim_v]
+ * fp32; lse [batch][num_q_heads] fp32.  seq_lens[b] == 0 gives out = 0 and
+ * lse = -inf.  A seq_len outside [0, max_blocks * block_size] is treated as 0
+ * and sets PKV_DEV_SEQ_LEN.  A table entry outside [0, num_blocks) is never
+ * dereferenced: its tokens read some in-pool block instead, the row's result
+ * is unspecified, and PKV_DEV_BLOCK_ID is set.
+ *
+ * Split-KV: with num_splits = S > 1 each sequence's tokens are cut into S
+ * contiguous chunks, chunk s covering [s*C_b, min(seq_lens[b], (s+1)*C_b)) with
+ * C_b = 64 * ceil(seq_lens[b] / (64 * S)); each chunk's partial (out, lse) is
+ * computed separately and the partials are merged exactly as pkv_lse_merge
+ * does.  num_splits = 0 picks S from the batch, the heads and the SM count.
+ * S must be <= 256.  The partials live in `workspace`, which must hold at
+ * least pkv_decode_workspace_size(batch, num_q_heads, head_dim_v, S) bytes
+ * (0 when S == 1; `workspace` may then be NULL).
+ *
+ * flags: 0 = choose the kernel by shape (the TMA + tensor-core kernel for
+ * head_dim_k == head_dim_v in {64, 128}, query groups of 1, 2, 4 or 8 and
+ * power-of-two block sizes >= 8; the generic CUDA-core kernel otherwise);
+ * PKV_DECODE_GENERIC forces the generic kernel.
+ * ------------------------------------------------------------------------- */
+#define PKV_DECODE_GENERIC 0x1
+
+size_t pkv_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t head_dim_v,
+                                 int32_t num_splits);
+
+/* The split count num_splits = 0 resolves to for this batch on the current device. */
+int32_t pkv_decode_auto_splits(const pkv_cache_desc *cache, int32_t batch,
+                               int32_t num_q_heads, int32_t max_seq_len);
+
+int pkv_paged_decode_attn(const pkv_cache_desc *cache, const float *q, int32_t batch,
+                          int32_t num_q_heads, const void *k_pool, const void *v_pool,
+                          const int32_t *block_tables, int32_t max_blocks,
+                          const int32_t *seq_lens, float scale, int32_t num_splits,
+                          void *workspace, size_t workspace_bytes, float *out, float *lse,
+                          int32_t flags, pkv_stream_t stream);
+
+/* The per-chunk partials themselves: out_part [S][batch][num_q_heads][head_dim_v]
+ * and lse_part [S][batch][num_q_heads], chunks as above; an empty chunk gives
+ * out = 0, lse = -inf.  pkv_lse_merge of these equals pkv_paged_decode_attn. */
+int pkv_paged_decode_attn_partial(const pkv_cache_desc *cache, const float *q, int32_t batch,
+                                  int32_t num_q_heads, const void *k_pool, const void *v_pool,
+                                  const int32_t *block_tables, int32_t max_blocks,
+                                  const int32_t *seq_lens, float scale, int32_t num_splits,
+                                  float *out_part, float *lse_part, int32_t flags,
+                                  pkv_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * pkv_lse_merge -- [DCP] decode step, stage 3: correct each partial output
+ * with the shared LSEs and sum.  For each row r:
+ *     M = max_p lse_part[p][r],  w_p = e^{lse_part[p][r] - M},
+ *     out[r][:] = sum_p w_p out_part[p][r][:] / sum_p w_p,  lse[r] = M + ln sum_p w_p.
+ * out_part [num_parts][rows][head_dim_v], lse_part [num_parts][rows],
+ * out [rows][head_dim_v], lse [rows], all fp32.  Rows whose partials are all
+ * empty (lse = -inf) give out = 0 and lse = -inf.  out/lse must not alias the
+ * partials.
+ * ------------------------------------------------------------------------- */
+int pkv_lse_merge(int32_t num_parts, const float *out_part, const float *lse_part,
+                  int64_t rows, int32_t head_dim_v, float *out, float *lse,
+                  pkv_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Host block manager -- [PA] "PagedAttentionはブロック表で論理順序と物理配置を分ける",
+ * "要求の終了で空いたブロックを再利用する具体例", "共通ブロックの共有とコピーオンライト".
+ * Host memory only; not thread-safe (one owner thread per manager).
+ *  - A sequence uses its last block until it is full, then takes a free block.
+ *  - Freed blocks return to the pool (last freed, first reused) and may be
+ *    used by any sequence; nothing is compacted.
+ *  - fork() makes a child that shares every block of its parent (each
+ *    block's reference count goes up); a block returns to the pool only when
+ *    its count reaches zero.
+ *  - append() into a last block that other sequences still reference first
+ *    takes a fresh block, reports (old, new) as a copy-on-write pair for
+ *    pkv_copy_blocks, and points this sequence's table at the new block.
+ *    Full shared blocks are never copied.
+ * ------------------------------------------------------------------------- */
+typedef struct pkv_block_manager pkv_block_manager;
+
+/* `initial_order` (may be NULL = 0,1,2,...) is the order in which free blocks
+ * are first handed out; it must be a permutation of 0..num_blocks-1. */
+pkv_block_manager *pkv_bm_create(int32_t num_blocks, int32_t block_size,
+                                 const int32_t *initial_order);
+void pkv_bm_destroy(pkv_block_manager *bm);
+
+/* New empty sequence; its id is written to *seq_id. */
+int pkv_bm_add_sequence(pkv_block_manager *bm, int64_t *seq_id);
+
+/* New sequence sharing all of `parent`'s blocks and length. */
+int pkv_bm_fork(pkv_block_manager *bm, int64_t parent, int64_t *child);
+
+/* Reserve slots for `num_tokens` new tokens of `seq`: slots_out[num_tokens]
+ * receives their slots in order.  Copy-on-write pairs are written to
+ * cow_src/cow_dst (capacity `cow_capacity`, at most 1 pair per call) and
+ * their count to *num_cow.  All-or-nothing: PKV_ERR_NO_SPACE leaves the
+ * manager unchanged. */
+int pkv_bm_append(pkv_block_manager *bm, int64_t seq, int32_t num_tokens, int64_t *slots_out,
+                  int32_t *cow_src, int32_t *cow_dst, int32_t cow_capacity, int32_t *num_cow);
+
+/* Drop `seq`: every block's count goes down; blocks at zero return to the pool. */
+int pkv_bm_free(pkv_block_manager *bm, int64_t seq);
+
+/* Copy `seq`'s block table (logical order) into table_out[capacity]; the
+ * number of blocks goes to *num_blocks and the token count to *seq_len. */
+int pkv_bm_block_table(const pkv_block_manager *bm, int64_t seq, int32_t *table_out,
+                       int32_t capacity, int32_t *num_blocks, int64_t *seq_len);
+
+int32_t pkv_bm_num_free(const pkv_block_manager *bm);
+/* Reference count of a physical block (0 = free), or -1 if out of range. */
+int32_t pkv_bm_ref_count(const pkv_block_manager *bm, int32_t block);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PKV_H_ */

@@ -1,0 +1,140 @@
+// api.cu -- C ABI entry points of the decode-attention path: argument
+// validation, split selection, kernel choice and the split -> merge sequence.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "pkv.h"
+#include "pkv_host.h"
+
+using namespace pkv;
+
+namespace {
+
+constexpr int32_t kMaxSplits = 256;
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int validate_decode(const pkv_cache_desc *c, const float *q, int32_t batch, int32_t hq,
+                    const void *k_pool, const void *v_pool, const int32_t *block_tables,
+                    int32_t max_blocks, const int32_t *seq_lens, int32_t num_splits,
+                    int32_t flags) {
+    if (!c || batch < 0 || hq <= 0 || max_blocks < 0 || num_splits < 0 ||
+        num_splits > kMaxSplits || (flags & ~PKV_DECODE_GENERIC) != 0)
+        return PKV_ERR_INVALID_ARG;
+    if (c->num_blocks <= 0 || c->block_size < 1 || c->block_size > 256 || c->num_kv_heads <= 0 ||
+        c->head_dim_k <= 0 || c->head_dim_v <= 0)
+        return PKV_ERR_INVALID_ARG;
+    if (hq % c->num_kv_heads != 0 || c->head_dim_k % 8 != 0 || c->head_dim_v % 8 != 0 ||
+        c->head_dim_k > 1024 || c->head_dim_v > 1024 || batch > 65535)
+        return PKV_ERR_SHAPE;
+    if (batch == 0) return PKV_OK;
+    if (!q || !k_pool || !v_pool || !block_tables || !seq_lens) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool)) return PKV_ERR_ALIGNMENT;
+    return PKV_OK;
+}
+
+int32_t auto_splits(const pkv_cache_desc &c, int32_t batch, int32_t max_seq_len) {
+    // Enough (sequence, KV head, split) items for ~4 per SM, each item at
+    // least 512 tokens long.
+    const int64_t units = std::max<int64_t>(1, int64_t(batch) * c.num_kv_heads);
+    const int64_t want = (int64_t(sm_count()) * 4 + units - 1) / units;
+    const int64_t cap = std::max<int64_t>(1, (int64_t(max_seq_len) + 511) / 512);
+    return int32_t(std::max<int64_t>(1, std::min<int64_t>({want, cap, kMaxSplits})));
+}
+
+int run_split_kernel(const DecodeArgs &a, int32_t flags) {
+    if (!(flags & PKV_DECODE_GENERIC) && tma_kernel_supports(a.cache, a.num_q_heads))
+        return launch_decode_tma(a);
+    return launch_decode_generic(a);
+}
+
+}  // namespace
+
+extern "C" size_t pkv_decode_workspace_size(int32_t batch, int32_t num_q_heads,
+                                            int32_t head_dim_v, int32_t num_splits) {
+    if (batch <= 0 || num_q_heads <= 0 || head_dim_v <= 0 || num_splits <= 1) return 0;
+    const size_t rows = size_t(num_splits) * batch * num_q_heads;
+    return align256(rows * head_dim_v * sizeof(float)) + align256(rows * sizeof(float));
+}
+
+extern "C" int32_t pkv_decode_auto_splits(const pkv_cache_desc *cache, int32_t batch,
+                                          int32_t num_q_heads, int32_t max_seq_len) {
+    (void)num_q_heads;
+    if (!cache || cache->num_kv_heads <= 0) return 1;
+    return auto_splits(*cache, batch, max_seq_len);
+}
+
+extern "C" int pkv_paged_decode_attn_partial(const pkv_cache_desc *cache, const float *q,
+                                             int32_t batch, int32_t num_q_heads,
+                                             const void *k_pool, const void *v_pool,
+                                             const int32_t *block_tables, int32_t max_blocks,
+                                             const int32_t *seq_lens, float scale,
+                                             int32_t num_splits, float *out_part,
+                                             float *lse_part, int32_t flags,
+                                             pkv_stream_t stream) {
+    int st = validate_decode(cache, q, batch, num_q_heads, k_pool, v_pool, block_tables,
+                             max_blocks, seq_lens, num_splits, flags);
+    if (st != PKV_OK || batch == 0) return st;
+    if (num_splits < 1) return PKV_ERR_INVALID_ARG;
+    if (!out_part || !lse_part) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(out_part)) return PKV_ERR_ALIGNMENT;
+    uint32_t *status = status_word();
+    if (!status) return PKV_ERR_CUDA;
+    DecodeArgs a{*cache, q, batch, num_q_heads, k_pool, v_pool, block_tables, max_blocks,
+                 seq_lens, scale, num_splits, out_part, lse_part, status,
+                 reinterpret_cast<cudaStream_t>(stream)};
+    return run_split_kernel(a, flags);
+}
+
+extern "C" int pkv_paged_decode_attn(const pkv_cache_desc *cache, const float *q, int32_t batch,
+                                     int32_t num_q_heads, const void *k_pool, const void *v_pool,
+                                     const int32_t *block_tables, int32_t max_blocks,
+                                     const int32_t *seq_lens, float scale, int32_t num_splits,
+                                     void *workspace, size_t workspace_bytes, float *out,
+                                     float *lse, int32_t flags, pkv_stream_t stream) {
+    int st = validate_decode(cache, q, batch, num_q_heads, k_pool, v_pool, block_tables,
+                             max_blocks, seq_lens, num_splits, flags);
+    if (st != PKV_OK || batch == 0) return st;
+    if (!out || !lse) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(out)) return PKV_ERR_ALIGNMENT;
+    int32_t S = num_splits;
+    if (S == 0) {
+        // Without a host copy of seq_lens, size the splits by the table width.
+        S = auto_splits(*cache, batch, int32_t(std::min<int64_t>(
+                                           int64_t(max_blocks) * cache->block_size, INT32_MAX)));
+    }
+    const size_t need = pkv_decode_workspace_size(batch, num_q_heads, cache->head_dim_v, S);
+    if (S > 1 && (!workspace || workspace_bytes < need)) return PKV_ERR_WORKSPACE_TOO_SMALL;
+    if (S > 1 && !aligned16(workspace)) return PKV_ERR_ALIGNMENT;
+    uint32_t *status = status_word();
+    if (!status) return PKV_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    DecodeArgs a{*cache, q, batch, num_q_heads, k_pool, v_pool, block_tables, max_blocks,
+                 seq_lens, scale, S, out, lse, status, s};
+    if (S == 1) return run_split_kernel(a, flags);
+
+    const size_t rows = size_t(S) * batch * num_q_heads;
+    float *out_part = static_cast<float *>(workspace);
+    float *lse_part = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                                align256(rows * cache->head_dim_v * sizeof(float)));
+    a.out_part = out_part;
+    a.lse_part = lse_part;
+    st = run_split_kernel(a, flags);
+    if (st != PKV_OK) return st;
+    return launch_lse_merge(S, out_part, lse_part, int64_t(batch) * num_q_heads,
+                            cache->head_dim_v, out, lse, s);
+}
+
+extern "C" int pkv_lse_merge(int32_t num_parts, const float *out_part, const float *lse_part,
+                             int64_t rows, int32_t head_dim_v, float *out, float *lse,
+                             pkv_stream_t stream) {
+    if (num_parts <= 0 || rows < 0 || head_dim_v <= 0 || head_dim_v % 4 != 0)
+        return PKV_ERR_INVALID_ARG;
+    if (rows == 0) return PKV_OK;
+    if (!out_part || !lse_part || !out || !lse) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(out_part) || !aligned16(out)) return PKV_ERR_ALIGNMENT;
+    if (rows > int64_t(INT32_MAX) * 8) return PKV_ERR_SHAPE;
+    return launch_lse_merge(num_parts, out_part, lse_part, rows, head_dim_v, out, lse,
+                            reinterpret_cast<cudaStream_t>(stream));
+}

@@ -1,0 +1,586 @@
+// decode_tma.cu -- paged decode attention for GQA shapes on sm_103a.
+//
+// Work item = (sequence b, KV head g, split s): the chunk of tokens
+// [s*C, min(L, (s+1)*C)) of sequence b, C = 64 * ceil(L / (64 * S)), for all
+// G = Hq / Hkv query heads that share KV head g.  A persistent grid walks the
+// items round-robin; each CTA has one producer warp and four consumer warps.
+//
+// Producer warp: reads block-table entries (one per lane, 32 segments at a
+// time), and issues 2-D TMA tensor copies of each (block, KV head) tile into a
+// ring of shared-memory stages.  A stage holds 64 tokens of K and of V; each
+// 64-column half of a row is a separate 128-byte-swizzled box, so ldmatrix
+// reads are bank-conflict free.  Segments past the end of the chunk (and
+// table entries outside the pool) are fetched from block 0 of the same KV
+// head, a row that always exists; the consumers mask those tokens' scores
+// and zero their value rows, so whatever that row holds never reaches the
+// result.  Every box is therefore fully in bounds.  Stage
+// hand-off uses mbarriers (full: producer expect_tx + TMA bytes; empty: one
+// arrival per consumer warp).  Every wait is bounded.
+//
+// Consumer warps: warp w owns tokens [16w, 16w+16) of every stage.  Scores are
+// computed transposed, S^T[16 tokens x 8 cols] = K[16 x D] . [q_hi | q_lo]^T,
+// with bf16 mma.sync (fp32 accumulate); the fp32 query is split into two bf16
+// terms (hi + lo) packed side by side in the N dimension, so the split costs
+// no extra MMA and scores keep ~16 mantissa bits of the query.  The online
+// softmax runs in base 2 (query pre-scaled by scale*log2 e); probabilities
+// are split the same way (p_hi | p_lo) and the value product is
+// O^T[D x 8 cols] += V^T[D x 16] . [p_hi | p_lo]^T, again one MMA per 16 rows
+// of D.  At the end of an item the four warps' (m, l, O) are merged through
+// shared memory and written as that chunk's partial (or final) result.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "pkv.h"
+#include "pkv_device.cuh"
+#include "pkv_host.h"
+
+namespace pkv {
+namespace {
+
+constexpr int kStageTokens = 64;
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kRowBytes = 128;                          // one 64-column half-row of bf16
+constexpr int kHalfBytes = kStageTokens * kRowBytes;    // 8 KiB
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+template <int D, int G, int NSTAGES>
+struct Cfg {
+    static constexpr int kHalves = D / 64;
+    static constexpr int kTileBytes = kHalves * kHalfBytes;   // K (or V) of one stage
+    static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kNT = (2 * G + 7) / 8;               // 8-column n-tiles (hi|lo)
+    static constexpr int kKSteps = D / 16;
+    static constexpr int kMTiles = D / 16;
+    static constexpr int kMergeFloats = kConsumerWarps * (2 * G + G * D);
+    static constexpr int kPbufFloats = kConsumerWarps * 16 * G;
+    static constexpr size_t kSmemBytes = 1024 + size_t(NSTAGES) * kStageBytes +
+                                         2 * NSTAGES * sizeof(uint64_t) +
+                                         sizeof(float) * (kMergeFloats + kPbufFloats) + 16;
+    static_assert(NSTAGES <= 32, "stage bit masks are 32 bits wide");
+};
+
+__device__ __forceinline__ int64_t lmin(int64_t x, int64_t y) { return x < y ? x : y; }
+__device__ __forceinline__ int64_t lmax(int64_t x, int64_t y) { return x > y ? x : y; }
+
+struct ItemRange {
+    int b, g, s;
+    int64_t begin, end;
+    int nstages;
+};
+
+__device__ __forceinline__ ItemRange item_range(const DecodeArgs &a, int item, bool report) {
+    ItemRange r;
+    r.s = item % a.num_splits;
+    const int t = item / a.num_splits;
+    r.g = t % a.cache.num_kv_heads;
+    r.b = t / a.cache.num_kv_heads;
+    int64_t L = a.seq_lens[r.b];
+    if (L < 0 || L > int64_t(a.max_blocks) * a.cache.block_size) {
+        if (report && r.s == 0) raise_status(a.status, PKV_DEV_SEQ_LEN);
+        L = 0;
+    }
+    const int64_t chunk = 64 * ((L + 64LL * a.num_splits - 1) / (64LL * a.num_splits));
+    r.begin = int64_t(r.s) * chunk;
+    r.end = lmin(L, r.begin + chunk);
+    r.nstages = r.end > r.begin ? int((r.end - r.begin + kStageTokens - 1) / kStageTokens) : 0;
+    return r;
+}
+
+// Column n (0..8*NT-1) of the packed [hi | lo] operand -> (head, is_lo), or
+// head = -1 for a zero padding column.
+template <int G>
+__device__ __forceinline__ int col_head(int n, bool &is_lo) {
+    if constexpr (G == 8) {
+        is_lo = n >= 8;
+        return n & 7;
+    } else {
+        is_lo = n >= G;
+        return n < 2 * G ? (n % G) : -1;
+    }
+}
+
+template <int D, int G, int NSTAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+decode_tma_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                  const __grid_constant__ CUtensorMap tmap_v, const DecodeArgs a) {
+    using C = Cfg<D, G, NSTAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *full_bar = reinterpret_cast<uint64_t *>(smem + size_t(NSTAGES) * C::kStageBytes);
+    uint64_t *empty_bar = full_bar + NSTAGES;
+    float *merge = reinterpret_cast<float *>(empty_bar + NSTAGES);
+    float *pbuf = merge + C::kMergeFloats;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(pbuf + C::kPbufFloats);
+    volatile int *stop_flag = abort_flag + 1;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int num_items = a.batch * a.cache.num_kv_heads * a.num_splits;
+    const int bs = a.cache.block_size;
+    const int hkv = a.cache.num_kv_heads;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NSTAGES; ++s) {
+            mbar_init(smem_addr(&full_bar[s]), 1);
+            mbar_init(smem_addr(&empty_bar[s]), kConsumerWarps);
+        }
+        *abort_flag = 0;
+        *stop_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tmap_k);
+            tma_prefetch_desc(&tmap_v);
+        }
+        const int seg_rows = bs < kStageTokens ? bs : kStageTokens;
+        const int segs_per_stage = kStageTokens / seg_rows;
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t armed = 0, armed_parity = 0;   // per stage: ever armed / parity armed last
+        bool ok = true;
+        for (int item = blockIdx.x; item < num_items && ok; item += gridDim.x) {
+            const ItemRange r = item_range(a, item, false);
+            const int total_segs = r.nstages * segs_per_stage;
+            const int32_t *table = a.block_tables + int64_t(r.b) * a.max_blocks;
+            for (int base = 0; base < total_segs && ok; base += 32) {
+                // Lane i resolves segment base + i to a global row; block 0
+                // of this KV head stands in for segments without a token.
+                int32_t y = r.g * bs;
+                const int sg = base + lane;
+                if (sg < total_segs) {
+                    const int64_t ts = r.begin + int64_t(sg) * seg_rows;
+                    if (ts < r.end) {
+                        const int32_t phys = table[ts / bs];
+                        if (phys >= 0 && phys < a.cache.num_blocks)
+                            y = (phys * hkv + r.g) * bs + int32_t(ts % bs);
+                        else
+                            raise_status(a.status, PKV_DEV_BLOCK_ID);
+                    }
+                }
+                const int nseg = min(32, total_segs - base);
+                for (int k = 0; k < nseg; k += segs_per_stage) {
+                    const uint32_t eb = smem_addr(&empty_bar[stage]);
+                    const uint32_t fb = smem_addr(&full_bar[stage]);
+                    int fail = 0;
+                    if (lane == 0) fail = !mbar_wait(eb, phase ^ 1u, a.status) || *abort_flag;
+                    if (__shfl_sync(0xffffffffu, fail, 0)) {
+                        if (lane == 0) *abort_flag = 1;
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0) mbar_arrive_expect_tx(fb, C::kStageBytes);
+                    armed |= 1u << stage;
+                    armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                    const uint32_t kdst = smem_addr(smem + size_t(stage) * C::kStageBytes);
+                    const uint32_t vdst = kdst + C::kTileBytes;
+                    for (int q = 0; q < segs_per_stage; ++q) {
+                        const int32_t yq = __shfl_sync(0xffffffffu, y, k + q);
+                        if (lane == 0) {
+                            const uint32_t off = q * seg_rows * kRowBytes;
+#pragma unroll
+                            for (int h = 0; h < C::kHalves; ++h) {
+                                tma_load_2d(kdst + h * kHalfBytes + off, &tmap_k, h * 64, yq, fb);
+                                tma_load_2d(vdst + h * kHalfBytes + off, &tmap_v, h * 64, yq, fb);
+                            }
+                        }
+                    }
+                    if (++stage == NSTAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
+        // Do not leave while copies issued by this CTA may still be landing
+        // in its shared memory (matters only if the consumers gave up).
+        if (lane == 0)
+            for (int s = 0; s < NSTAGES; ++s)
+                if (armed & (1u << s))
+                    mbar_wait(smem_addr(&full_bar[s]), (armed_parity >> s) & 1u, a.status);
+        return;
+    }
+
+    // -------------------------------------------------------------- consumers
+    float *pw = pbuf + warp * 16 * G;                  // this warp's p transpose buffer
+    float *mw = merge + warp * (2 * G + G * D);         // this warp's (m, l, O) for the merge
+    const int r0 = lane >> 2;                           // token row (and +8) inside the slice
+    const int tq = lane & 3;
+    // Head slots of this lane (columns 2*tq and 2*tq+1 of the packed tiles).
+    int slot_head[2];
+    bool slot_ok[2];
+    if constexpr (G == 8) {
+        slot_head[0] = 2 * tq; slot_head[1] = 2 * tq + 1; slot_ok[0] = slot_ok[1] = true;
+    } else if constexpr (G == 4) {
+        slot_head[0] = 2 * (tq & 1); slot_head[1] = 2 * (tq & 1) + 1; slot_ok[0] = slot_ok[1] = true;
+    } else if constexpr (G == 2) {
+        slot_head[0] = 0; slot_head[1] = 1; slot_ok[0] = slot_ok[1] = tq < 2;
+    } else {
+        slot_head[0] = 0; slot_head[1] = 0; slot_ok[0] = tq == 0; slot_ok[1] = false;
+    }
+    const float qscale = a.scale * kLog2e;
+
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < num_items; item += gridDim.x) {
+        const ItemRange r = item_range(a, item, warp == 0 && lane == 0);
+
+        // Query fragments: B operand of S^T = K . Q^T, columns [q_hi | q_lo].
+        uint32_t qf[C::kKSteps][C::kNT][2];
+        {
+            const float *qbase = a.q + (int64_t(r.b) * a.num_q_heads + r.g * G) * D;
+#pragma unroll
+            for (int nt = 0; nt < C::kNT; ++nt) {
+                bool is_lo;
+                const int head = col_head<G>(nt * 8 + r0, is_lo);
+#pragma unroll
+                for (int ks = 0; ks < C::kKSteps; ++ks) {
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        float v[2] = {0.f, 0.f};
+                        if (head >= 0) {
+                            const int d = ks * 16 + 2 * tq + half * 8;
+                            const float2 x = *reinterpret_cast<const float2 *>(qbase + head * D + d);
+                            const float xs[2] = {x.x * qscale, x.y * qscale};
+#pragma unroll
+                            for (int e = 0; e < 2; ++e) {
+                                const float hi = __uint_as_float(f32_to_bf16_bits(xs[e]) << 16);
+                                v[e] = is_lo ? xs[e] - hi : hi;
+                            }
+                        }
+                        qf[ks][nt][half] = pack_bf16x2(v[0], v[1]);
+                    }
+                }
+            }
+        }
+
+        float acc[C::kMTiles][C::kNT][4];
+#pragma unroll
+        for (int mt = 0; mt < C::kMTiles; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < C::kNT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.f;
+        float m2[2] = {-INFINITY, -INFINITY};
+        float l2[2] = {0.f, 0.f};
+
+        for (int st = 0; st < r.nstages && ok; ++st) {
+            const uint32_t fb = smem_addr(&full_bar[stage]);
+            const bool waited = mbar_wait(fb, phase, a.status);
+            if (__any_sync(0xffffffffu, !waited || *abort_flag)) {
+                if (lane == 0) *abort_flag = 1;
+                ok = false;
+                break;
+            }
+            uint8_t *kstage = smem + size_t(stage) * C::kStageBytes;
+            const uint32_t kbase = smem_addr(kstage);
+            const uint32_t vbase = kbase + C::kTileBytes;
+            const int64_t tok0 = r.begin + int64_t(st) * kStageTokens + 16 * warp;
+            const int nvalid = int(lmax(0, lmin(16, r.end - tok0)));
+            if (nvalid < 16) {
+                // Rows past the end may hold any bits (unused slots of the last
+                // block): zero this warp's V rows there so 0 * garbage cannot
+                // reach the accumulator.
+                const int nrows = 16 - nvalid;
+                for (int idx = lane; idx < nrows * C::kHalves * 8; idx += 32) {
+                    const int row = 16 * warp + nvalid + idx / (C::kHalves * 8);
+                    const int rest = idx % (C::kHalves * 8);
+                    *reinterpret_cast<uint4 *>(kstage + C::kTileBytes + (rest / 8) * kHalfBytes +
+                                               row * kRowBytes + (rest % 8) * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
+            if (nvalid > 0) {
+                // ---- S^T = K . [q_hi | q_lo]^T  (two accumulator sets for ILP)
+                float sacc[2][C::kNT][4];
+#pragma unroll
+                for (int x = 0; x < 2; ++x)
+#pragma unroll
+                    for (int nt = 0; nt < C::kNT; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) sacc[x][nt][e] = 0.f;
+                {
+                    const int row = 16 * warp + (lane & 7) + ((lane >> 3) & 1) * 8;
+                    const uint32_t rbase = kbase + row * kRowBytes;
+                    const int sw = row & 7;
+#pragma unroll
+                    for (int ks = 0; ks < C::kKSteps; ++ks) {
+                        const int chunk = (ks & 3) * 2 + (lane >> 4);
+                        const uint32_t addr = rbase + (ks >> 2) * kHalfBytes + ((chunk ^ sw) << 4);
+                        uint32_t a0, a1, a2, a3;
+                        ldsm_x4(addr, a0, a1, a2, a3);
+#pragma unroll
+                        for (int nt = 0; nt < C::kNT; ++nt)
+                            mma_bf16_16816(sacc[ks & 1][nt], a0, a1, a2, a3, qf[ks][nt][0],
+                                           qf[ks][nt][1]);
+                    }
+                }
+                float sraw[C::kNT][4];
+#pragma unroll
+                for (int nt = 0; nt < C::kNT; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) sraw[nt][e] = sacc[0][nt][e] + sacc[1][nt][e];
+
+                // ---- combine hi + lo: s[i][j] for token r0 + 8i, head slot j
+                float s[2][2];
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        float v;
+                        if constexpr (G == 8) {
+                            v = sraw[0][2 * i + j] + sraw[1][2 * i + j];
+                        } else if constexpr (G == 4) {
+                            v = sraw[0][2 * i + j] + __shfl_xor_sync(0xffffffffu, sraw[0][2 * i + j], 2);
+                        } else if constexpr (G == 2) {
+                            v = sraw[0][2 * i + j] + __shfl_xor_sync(0xffffffffu, sraw[0][2 * i + j], 1);
+                        } else {
+                            v = sraw[0][2 * i] + sraw[0][2 * i + 1];
+                        }
+                        const bool valid_tok = (r0 + 8 * i) < nvalid;
+                        s[i][j] = slot_ok[j] ? (valid_tok ? v : -INFINITY) : 0.f;
+                    }
+                }
+                // ---- online softmax (base 2)
+                float alpha[2], p[2][2];
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    float mx = fmaxf(s[0][j], s[1][j]);
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                    const float m_new = fmaxf(m2[j], mx);     // finite: this slice has a token
+                    alpha[j] = exp2f(m2[j] - m_new);
+                    p[0][j] = exp2f(s[0][j] - m_new);
+                    p[1][j] = exp2f(s[1][j] - m_new);
+                    l2[j] = l2[j] * alpha[j] + p[0][j] + p[1][j];
+                    m2[j] = m_new;
+                }
+                const float a_c0 = alpha[0];
+                const float a_c1 = (G == 1) ? alpha[0] : alpha[1];
+#pragma unroll
+                for (int mt = 0; mt < C::kMTiles; ++mt)
+#pragma unroll
+                    for (int nt = 0; nt < C::kNT; ++nt) {
+                        acc[mt][nt][0] *= a_c0; acc[mt][nt][1] *= a_c1;
+                        acc[mt][nt][2] *= a_c0; acc[mt][nt][3] *= a_c1;
+                    }
+
+                // ---- P^T fragments through the per-warp transpose buffer
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 2; ++i)
+#pragma unroll
+                    for (int j = 0; j < 2; ++j)
+                        if (slot_ok[j]) pw[(r0 + 8 * i) * G + slot_head[j]] = p[i][j];
+                __syncwarp();
+                uint32_t pf[C::kNT][2];
+#pragma unroll
+                for (int nt = 0; nt < C::kNT; ++nt) {
+                    bool is_lo;
+                    const int head = col_head<G>(nt * 8 + r0, is_lo);
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        float v[2] = {0.f, 0.f};
+                        if (head >= 0) {
+#pragma unroll
+                            for (int e = 0; e < 2; ++e) {
+                                const float x = pw[(2 * tq + e + 8 * half) * G + head];
+                                const float hi = __uint_as_float(f32_to_bf16_bits(x) << 16);
+                                v[e] = is_lo ? x - hi : hi;
+                            }
+                        }
+                        pf[nt][half] = pack_bf16x2(v[0], v[1]);
+                    }
+                }
+
+                // ---- O^T += V^T . [p_hi | p_lo]^T
+                {
+                    const int row = 16 * warp + (lane & 7) + (lane >> 4) * 8;
+                    const uint32_t rbase = vbase + row * kRowBytes;
+                    const int sw = row & 7;
+#pragma unroll
+                    for (int mt = 0; mt < C::kMTiles; ++mt) {
+                        const int chunk = (mt & 3) * 2 + ((lane >> 3) & 1);
+                        const uint32_t addr = rbase + (mt >> 2) * kHalfBytes + ((chunk ^ sw) << 4);
+                        uint32_t a0, a1, a2, a3;
+                        ldsm_x4_trans(addr, a0, a1, a2, a3);
+#pragma unroll
+                        for (int nt = 0; nt < C::kNT; ++nt)
+                            mma_bf16_16816(acc[mt][nt], a0, a1, a2, a3, pf[nt][0], pf[nt][1]);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&empty_bar[stage]));
+            if (++stage == NSTAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+
+        // ---- per-warp finalize: full l, hi+lo columns combined
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            l2[j] += __shfl_xor_sync(0xffffffffu, l2[j], 4);
+            l2[j] += __shfl_xor_sync(0xffffffffu, l2[j], 8);
+            l2[j] += __shfl_xor_sync(0xffffffffu, l2[j], 16);
+        }
+#pragma unroll
+        for (int mt = 0; mt < C::kMTiles; ++mt) {
+            float o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                if constexpr (G == 8) {
+                    o[e] = acc[mt][0][e] + acc[mt][1][e];
+                } else if constexpr (G == 4) {
+                    o[e] = acc[mt][0][e] + __shfl_xor_sync(0xffffffffu, acc[mt][0][e], 2);
+                } else if constexpr (G == 2) {
+                    o[e] = acc[mt][0][e] + __shfl_xor_sync(0xffffffffu, acc[mt][0][e], 1);
+                } else {
+                    o[e] = acc[mt][0][e & 2] + acc[mt][0][(e & 2) + 1];
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+                    if (slot_ok[j])
+                        mw[2 * G + slot_head[j] * D + mt * 16 + r0 + 8 * i] = o[2 * i + j];
+        }
+        if (lane < 4) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+                if (slot_ok[j]) {
+                    mw[slot_head[j]] = m2[j];
+                    mw[G + slot_head[j]] = l2[j];
+                }
+        }
+        named_barrier_sync(1, kConsumerWarps * 32);
+        if (threadIdx.x == 0) *stop_flag = *abort_flag;
+
+        // ---- CTA merge of the four warps' partial states
+        const int64_t row0 = (int64_t(r.s) * a.batch + r.b) * a.num_q_heads + int64_t(r.g) * G;
+        for (int idx = threadIdx.x; idx < G * D; idx += kConsumerWarps * 32) {
+            const int head = idx / D, d = idx % D;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w)
+                M = fmaxf(M, merge[w * (2 * G + G * D) + head]);
+            float out = 0.f, lsum = 0.f;
+            if (M != -INFINITY) {
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w) {
+                    const float *mwx = merge + w * (2 * G + G * D);
+                    const float wt = exp2f(mwx[head] - M);
+                    lsum = fmaf(wt, mwx[G + head], lsum);
+                    out = fmaf(wt, mwx[2 * G + head * D + d], out);
+                }
+                out /= lsum;
+            }
+            a.out_part[(row0 + head) * D + d] = out;
+            if (d == 0) a.lse_part[row0 + head] = M != -INFINITY ? (M + log2f(lsum)) * kLn2 : -INFINITY;
+        }
+        named_barrier_sync(1, kConsumerWarps * 32);
+        if (*stop_flag) break;   // same value in every consumer warp
+    }
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+bool make_pool_map(CUtensorMap *map, const void *pool, int64_t rows, int dim, int box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t gdim[2] = {cuuint64_t(dim), cuuint64_t(rows)};
+    cuuint64_t gstride[1] = {cuuint64_t(dim) * 2};
+    cuuint32_t box[2] = {64, cuuint32_t(box_rows)};
+    cuuint32_t estride[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(pool), gdim, gstride,
+              box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, int G, int NSTAGES>
+int launch(const DecodeArgs &a) {
+    using C = Cfg<D, G, NSTAGES>;
+    auto kernel = decode_tma_kernel<D, G, NSTAGES>;
+    const int64_t rows = int64_t(a.cache.num_blocks) * a.cache.num_kv_heads * a.cache.block_size;
+    const int box_rows = std::min(a.cache.block_size, kStageTokens);
+    CUtensorMap tk, tv;
+    if (!make_pool_map(&tk, a.k_pool, rows, D, box_rows) ||
+        !make_pool_map(&tv, a.v_pool, rows, D, box_rows))
+        return PKV_ERR_CUDA;
+    static thread_local int configured_dev = -1;  // attribute set per device, per thread
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_dev != dev) {
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(C::kSmemBytes)) != cudaSuccess)
+            return PKV_ERR_CUDA;
+        configured_dev = dev;
+    }
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, C::kSmemBytes) !=
+            cudaSuccess || per_sm < 1)
+        return PKV_ERR_CUDA;
+    const int64_t items = int64_t(a.batch) * a.cache.num_kv_heads * a.num_splits;
+    const int grid = int(std::min<int64_t>(items, int64_t(sm_count()) * per_sm));
+    if (grid <= 0) return PKV_OK;
+    kernel<<<grid, kThreads, C::kSmemBytes, a.stream>>>(tk, tv, a);
+    return cuda_status(cudaGetLastError());
+}
+
+template <int D, int NSTAGES>
+int launch_g(const DecodeArgs &a, int G) {
+    switch (G) {
+        case 1: return launch<D, 1, NSTAGES>(a);
+        case 2: return launch<D, 2, NSTAGES>(a);
+        case 4: return launch<D, 4, NSTAGES>(a);
+        case 8: return launch<D, 8, NSTAGES>(a);
+        default: return PKV_ERR_SHAPE;
+    }
+}
+
+}  // namespace
+
+bool tma_kernel_supports(const pkv_cache_desc &c, int32_t num_q_heads) {
+    const int G = num_q_heads / c.num_kv_heads;
+    const bool pow2_bs = c.block_size >= 8 && c.block_size <= 256 &&
+                         (c.block_size & (c.block_size - 1)) == 0;
+    const int64_t rows = int64_t(c.num_blocks) * c.num_kv_heads * c.block_size;
+    return c.head_dim_k == c.head_dim_v && (c.head_dim_k == 64 || c.head_dim_k == 128) &&
+           (G == 1 || G == 2 || G == 4 || G == 8) && pow2_bs && rows < (int64_t(1) << 31) - 1;
+}
+
+int launch_decode_tma(const DecodeArgs &a) {
+    const int G = a.num_q_heads / a.cache.num_kv_heads;
+    if (a.cache.head_dim_k == 128) return launch_g<128, 4>(a, G);
+    return launch_g<64, 8>(a, G);
+}
+
+}  // namespace pkv

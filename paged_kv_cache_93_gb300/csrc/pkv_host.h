@@ -1,0 +1,47 @@
+// pkv_host.h -- host-side declarations shared by the libpkv translation units
+// (not part of the public C ABI).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "pkv.h"
+
+namespace pkv {
+
+// Device address of the current device's status word (set up once per
+// device, with that device current).  nullptr if the CUDA runtime failed.
+uint32_t *status_word();
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA; }
+
+// Launch the per-split decode kernels.  Arguments are already validated;
+// `out_part`/`lse_part` are [S][B][Hq][Dv] / [S][B][Hq].
+struct DecodeArgs {
+    pkv_cache_desc cache;
+    const float *q;
+    int32_t batch, num_q_heads;
+    const void *k_pool, *v_pool;
+    const int32_t *block_tables;
+    int32_t max_blocks;
+    const int32_t *seq_lens;
+    float scale;
+    int32_t num_splits;
+    float *out_part, *lse_part;
+    uint32_t *status;
+    cudaStream_t stream;
+};
+bool tma_kernel_supports(const pkv_cache_desc &c, int32_t num_q_heads);
+int launch_decode_tma(const DecodeArgs &a);
+int launch_decode_generic(const DecodeArgs &a);
+int launch_lse_merge(int32_t num_parts, const float *out_part, const float *lse_part,
+                     int64_t rows, int32_t head_dim_v, float *out, float *lse,
+                     cudaStream_t stream);
+
+}  // namespace pkv

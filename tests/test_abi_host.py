@@ -1,0 +1,185 @@
+"""CPU tests of the C ABI library: it loads, exports every function
+include/pkv.h declares, and its host-only logic (argument checks that fail
+before any CUDA call, workspace sizing, the partition-length rule and the
+block manager) is right.  No compute call reaches a GPU here."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from tests._util import golden
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pkv.h")
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    import __graft_entry__
+    __graft_entry__.build()
+    import paged_kv_cache_93_gb300 as m
+    return m
+
+
+def declared_functions():
+    text = open(HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b(pkv_[a-z0-9_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ["pkv_kv_append", "pkv_paged_decode_attn", "pkv_paged_decode_attn_partial",
+              "pkv_lse_merge", "pkv_copy_blocks", "pkv_slot_mapping",
+              "pkv_interleave_slot_mapping", "pkv_decode_workspace_size", "pkv_status_string",
+              "pkv_device_status", "pkv_bm_create", "pkv_bm_append"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(pkv):
+    lib = ctypes.CDLL(pkv.library_path)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+    from paged_kv_cache_93_gb300 import _lib
+    assert set(_lib.SIGNATURES) == set(declared_functions())
+
+
+def test_status_strings(pkv):
+    for code in range(0, -9, -1):
+        s = pkv.lib.pkv_status_string(code).decode()
+        assert s and s != "unknown status"
+    assert pkv.lib.pkv_status_string(-99).decode() == "unknown status"
+
+
+def test_host_validation_rejects_before_any_launch(pkv):
+    lib = pkv.lib
+    desc = pkv.CacheDesc(16, 16, 8, 128, 128)
+    # null pools / inputs: rejected by the host checks
+    assert lib.pkv_kv_append(ctypes.byref(desc), None, None, None, None, None, 4, None) == -1
+    assert lib.pkv_copy_blocks(ctypes.byref(desc), None, None, None, None, 2, None) == -1
+    assert lib.pkv_slot_mapping(ctypes.byref(desc), None, 1, 1, None, None, 3, None, None) == -1
+    # zero-sized work is a no-op success
+    assert lib.pkv_kv_append(ctypes.byref(desc), None, None, None, None, None, 0, None) == 0
+    # misaligned pointers
+    bad = ctypes.c_void_p(0x1008)
+    assert lib.pkv_kv_append(ctypes.byref(desc), bad, bad, bad, bad, bad, 1, None) == -3
+    # Hq not a multiple of Hkv -> shape error; bad flag -> invalid arg
+    p = ctypes.c_void_p(0x1000)
+    assert lib.pkv_paged_decode_attn(ctypes.byref(desc), p, 1, 12, p, p, p, 4, p, 1.0, 1, None, 0,
+                                     p, p, 0, None) == -2
+    assert lib.pkv_paged_decode_attn(ctypes.byref(desc), p, 1, 16, p, p, p, 4, p, 1.0, 1, None, 0,
+                                     p, p, 4, None) == -1
+    assert lib.pkv_paged_decode_attn(ctypes.byref(desc), p, 1, 16, p, p, p, 4, p, 1.0, 300, None,
+                                     0, p, p, 0, None) == -1
+    # splits > 1 without workspace
+    assert lib.pkv_paged_decode_attn(ctypes.byref(desc), p, 1, 16, p, p, p, 4, p, 1.0, 4, None, 0,
+                                     p, p, 0, None) == -4
+    # head dim not a multiple of 8
+    d2 = pkv.CacheDesc(16, 16, 8, 100, 128)
+    assert lib.pkv_paged_decode_attn(ctypes.byref(d2), p, 1, 16, p, p, p, 4, p, 1.0, 1, None, 0,
+                                     p, p, 0, None) in (-1, -2)
+    assert lib.pkv_lse_merge(0, p, p, 4, 128, p, p, None) == -1
+
+
+def test_workspace_size(pkv):
+    assert pkv.decode_workspace_size(8, 32, 128, 1) == 0
+    n = pkv.decode_workspace_size(8, 32, 128, 16)
+    rows = 16 * 8 * 32
+    assert n >= rows * 128 * 4 + rows * 4
+    assert n % 256 == 0
+
+
+@pytest.mark.parametrize("N,P,I", [(200_000, 4, 1), (200_000, 4, 16), (1000, 3, 7), (5, 4, 2),
+                                   (0, 2, 3), (17, 1, 4)])
+def test_partition_len_matches_oracle_count(pkv, N, P, I):
+    part, _ = oracle.interleave(N, P, I)
+    counts = np.bincount(part, minlength=P)
+    assert [pkv.interleave_partition_len(N, P, I, r) for r in range(P)] == counts.tolist()
+
+
+def test_partition_len_dcp_example(pkv):
+    gd = golden("dcp_interleave.txt")
+    for I in (1, 16):
+        assert [pkv.interleave_partition_len(gd["num_tokens"], gd["dcp_size"], I, r)
+                for r in range(gd["dcp_size"])] == [gd["tokens_per_partition"]] * gd["dcp_size"]
+
+
+# ------------------------------------------------------------- block manager
+
+def test_block_manager_accounting_example(pkv):
+    """The worked example: block size 4; A holds 6 tokens, B 9; A ends and its
+    blocks serve a new request; B grows to 12 (no new block) then 13 (one)."""
+    gd = golden("block_accounting.txt")
+    bs = gd["block_size"]
+    bm = pkv.BlockManager(8, bs)
+    a, b = bm.add_sequence(), bm.add_sequence()
+    slots_a, _ = bm.append(a, gd["tokens_A"])
+    slots_b, _ = bm.append(b, gd["tokens_B"])
+    ta, tb = bm.block_table(a), bm.block_table(b)
+    assert (len(ta), len(tb)) == (gd["blocks_A"], gd["blocks_B"])
+    assert (len(ta) + len(tb)) * bs - gd["total_tokens"] == gd["slack_slots"]
+    assert bm.num_free == 8 - gd["blocks_A"] - gd["blocks_B"]
+    # slots follow each table
+    assert slots_b == [oracle.slot_of(np.array(tb, np.int32), j, bs) for j in range(len(slots_b))]
+    bm.free(a)
+    assert bm.num_free == 8 - gd["blocks_B"]
+    assert all(bm.ref_count(x) == 0 for x in ta)
+    c = bm.add_sequence()
+    bm.append(c, 3)
+    assert bm.block_table(c)[0] in ta        # a returned block is reused
+    bm.append(b, gd["B_grown_tokens"] - gd["tokens_B"])
+    assert len(bm.block_table(b)) == gd["B_grown_blocks"]
+    bm.append(b, gd["B_next_tokens"] - gd["B_grown_tokens"])
+    tb2 = bm.block_table(b)
+    assert len(tb2) == gd["B_next_blocks"] and tb2[:3] == tb   # no compaction
+    assert tb2[3] in ta                                        # A's other block
+
+
+def test_block_manager_shared_blocks_and_copy_on_write(pkv):
+    bm = pkv.BlockManager(10, 4, initial_order=[9, 8, 7, 6, 5, 4, 3, 2, 1, 0])
+    p = bm.add_sequence()
+    bm.append(p, 10)                     # blocks 9, 8, 7 (tail holds 2)
+    tp = bm.block_table(p)
+    assert tp == [9, 8, 7]
+    c1, c2 = bm.fork(p), bm.fork(p)
+    assert all(bm.ref_count(x) == 3 for x in tp)
+    slots, cow = bm.append(c1, 1)        # writes into shared tail -> copy-on-write
+    assert len(cow) == 1 and cow[0][0] == 7
+    new_tail = cow[0][1]
+    assert bm.block_table(c1) == [9, 8, new_tail] and slots == [new_tail * 4 + 2]
+    assert bm.ref_count(7) == 2 and bm.ref_count(new_tail) == 1
+    assert bm.block_table(p) == tp and bm.block_table(c2) == tp   # others unchanged
+    # a full shared block is never copied: fill c2's tail privately, then grow
+    _, cow2 = bm.append(c2, 2)
+    assert len(cow2) == 1
+    _, cow3 = bm.append(c2, 1)
+    assert cow3 == []
+    # freeing keeps blocks that others still use
+    bm.free(p)
+    assert bm.ref_count(9) == 2 and bm.ref_count(7) == 0
+    bm.free(c1)
+    bm.free(c2)
+    assert bm.num_free == 10
+
+
+def test_block_manager_no_space_is_all_or_nothing(pkv):
+    bm = pkv.BlockManager(3, 4)
+    s = bm.add_sequence()
+    bm.append(s, 10)
+    with pytest.raises(pkv.PkvError) as e:
+        bm.append(s, 5)                  # needs 2 more blocks, only 0 free
+    assert e.value.status == -7
+    assert bm.seq_len(s) == 10 and bm.num_free == 0
+    with pytest.raises(pkv.PkvError):
+        bm.free(12345)
+
+
+def test_block_manager_rejects_bad_order(pkv):
+    with pytest.raises(ValueError):
+        pkv.BlockManager(3, 4, initial_order=[0, 0, 1])

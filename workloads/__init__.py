@@ -39,7 +39,7 @@ from dataclasses import dataclass, field
 import torch
 
 __all__ = ["Workload", "make", "NAMES", "tiny", "mix", "long32k", "dcp200k", "agent_mla",
-           "random_partials"]
+           "custom", "random_partials"]
 
 NAMES = ("tiny", "mix", "long32k", "dcp200k", "agent_mla")
 
@@ -234,6 +234,26 @@ def agent_mla(seed: int = 5, num_seqs: int = 32, prefix: int = 136_040,
     w.info = {"prefix": prefix, "suffix": suffix, "shared_blocks": shared,
               "shared_tail": shared_tail}
     return w
+
+
+def custom(seed: int, cached: list[int], hq: int, hkv: int, dk: int, dv: int, bs: int,
+           extra_blocks: int = 3, name: str = "custom") -> Workload:
+    """Any GQA/MLA shape: sequences holding `cached` tokens, one decode token
+    each, blocks drawn from a shuffled pool with `extra_blocks` spare."""
+    g = torch.Generator().manual_seed(seed)
+    B = len(cached)
+    lens = [c + 1 for c in cached]
+    counts = [_ceil_div(n, bs) for n in lens]
+    num_blocks = sum(counts) + extra_blocks
+    perm = torch.randperm(num_blocks, generator=g)
+    tables = _tables(perm, counts, max(counts))
+    k_pool = _normal(g, (num_blocks, hkv, bs, dk), torch.bfloat16)
+    v_pool = _normal(g, (num_blocks, hkv, bs, dv), torch.bfloat16)
+    q = _normal(g, (B, hq, dk))
+    new_seq, new_pos, k_new, v_new = _decode_tokens(g, cached, hkv, dk, dv)
+    return Workload(name, hq, hkv, dk, dv, bs, q, k_pool, v_pool, tables,
+                    torch.tensor(lens, dtype=torch.int32), 1.0 / math.sqrt(dk),
+                    new_seq, new_pos, k_new, v_new)
 
 
 def make(name: str, **kw) -> Workload:
