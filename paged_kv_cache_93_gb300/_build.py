@@ -2,7 +2,8 @@
 C++ block manager (g++), linked into paged_kv_cache_93_gb300/libpkv.so.
 
 Sources compile in parallel; an object is rebuilt only when its source or a
-header is newer.  Run ``python -m paged_kv_cache_93_gb300._build``.
+header is newer.  Run ``python paged_kv_cache_93_gb300/_build.py`` (importing the
+package needs the built library, so this file is run or loaded by path).
 """
 from __future__ import annotations
 

@@ -70,7 +70,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     if not os.path.exists(path):
         raise ImportError(
             f"{path} is missing: build the CUDA library first "
-            "(python -m paged_kv_cache_93_gb300._build, or __graft_entry__.build())")
+            "(python paged_kv_cache_93_gb300/_build.py, or __graft_entry__.build())")
     lib = ctypes.CDLL(path)
     for name, (res, args) in SIGNATURES.items():
         fn = getattr(lib, name)
