@@ -206,6 +206,30 @@ int pkv_paged_decode_attn_partial(const pkv_cache_desc *cache, const float *q, i
                                   pkv_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * pkv_paged_decode_attn_noalloc -- the same computation as
+ * pkv_paged_decode_attn (same arguments, same results), for callers that
+ * cannot allocate device memory: the split partials go to a scratch array
+ * built into the library instead of a caller workspace.  The pages have no
+ * counterpart of this call; it exists for embedders whose host framework owns
+ * all device memory, or whose hot loop must not allocate.
+ *  - The scratch holds PKV_NOALLOC_SCRATCH_BYTES (8 MiB) on every GPU that
+ *    loads the library, until the process exits.  A call whose partials
+ *    (pkv_decode_workspace_size for the split count used) exceed it returns
+ *    PKV_ERR_WORKSPACE_TOO_SMALL and launches nothing.
+ *  - The first call on each device looks up the scratch's device address;
+ *    make that first call before any stream capture.
+ *  - Calls share the scratch: calls that overlap on the GPU race; calls in
+ *    one stream are ordered.  Nothing is allocated, on host or device.
+ * ------------------------------------------------------------------------- */
+#define PKV_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+int pkv_paged_decode_attn_noalloc(const pkv_cache_desc *cache, const float *q, int32_t batch,
+                                  int32_t num_q_heads, const void *k_pool, const void *v_pool,
+                                  const int32_t *block_tables, int32_t max_blocks,
+                                  const int32_t *seq_lens, float scale, int32_t num_splits,
+                                  float *out, float *lse, int32_t flags, pkv_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * pkv_lse_merge -- [DCP] decode step, stage 3: correct each partial output
  * with the shared LSEs and sum.  For each row r:
  *     M = max_p lse_part[p][r],  w_p = e^{lse_part[p][r] - M},

@@ -1,0 +1,89 @@
+"""The scratch-free decode entry point, pkv_paged_decode_attn_noalloc.
+
+Some embedders hand the library their inputs and outputs but cannot give it
+a workspace: their host framework owns all device memory and lets no other
+component call cudaMalloc, or their decode loop must never allocate.  For
+them the library keeps the split partials in a fixed scratch array compiled
+into it.  This file checks, through the C ABI, that two calls in a row give
+the same results as the regular entry point (with a caller workspace), and
+that a request larger than the scratch is refused.  It is collected last so
+that a run stopping at the first failure has run every other test first, and
+it is self-contained so it also passes alone in a fresh process.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from tests._steps import assert_attention_close
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    import __graft_entry__
+    __graft_entry__.build()
+    import paged_kv_cache_93_gb300 as m
+    m.device_status(reset=True)
+    return m
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _call(pkv, name, w, dev, splits, workspace=None):
+    """One decode-attention call through the C ABI; returns (out, lse)."""
+    k, v = w.k_pool.to(dev), w.v_pool.to(dev)
+    bt, lens, q = w.block_tables.to(dev), w.seq_lens.to(dev), w.q.to(dev)
+    desc = pkv.cache_desc(k, v)
+    B, Hq = w.batch, w.num_q_heads
+    out = torch.full((B, Hq, w.head_dim_v), float("nan"), device=dev)
+    lse = torch.full((B, Hq), float("nan"), device=dev)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    common = (ctypes.byref(desc), _ptr(q), B, Hq, _ptr(k), _ptr(v), _ptr(bt), bt.shape[1],
+              _ptr(lens), ctypes.c_float(w.scale), splits)
+    if name == "noalloc":
+        rc = pkv.lib.pkv_paged_decode_attn_noalloc(*common, _ptr(out), _ptr(lse), 0, stream)
+    else:
+        nbytes = 0 if workspace is None else workspace.numel()
+        rc = pkv.lib.pkv_paged_decode_attn(*common, _ptr(workspace), nbytes, _ptr(out),
+                                           _ptr(lse), 0, stream)
+    torch.cuda.synchronize()
+    assert rc == 0, f"{name}: status {rc}"
+    return out.cpu().numpy(), lse.cpu().numpy()
+
+
+def test_noalloc_matches_workspace_entry_point_twice(pkv):
+    dev = "cuda"
+    cases = [(workloads.long32k(batch=2, context=8192), 16),
+             (workloads.mix(), 3)]                   # a different shape on the second call
+    for w, splits in cases:
+        need = pkv.decode_workspace_size(w.batch, w.num_q_heads, w.head_dim_v, splits)
+        ws = torch.empty(need, dtype=torch.uint8, device=dev)
+        ref_o, ref_l = _call(pkv, "workspace", w, dev, splits, ws)
+        got_o, got_l = _call(pkv, "noalloc", w, dev, splits)
+        assert np.isfinite(got_o).all()
+        assert_attention_close(got_o, got_l, ref_o.astype(np.float64),
+                               ref_l.astype(np.float64), f"noalloc {w.name}")
+    assert pkv.device_status() == 0
+
+
+def test_noalloc_refuses_partials_beyond_the_scratch(pkv):
+    w = workloads.custom(3, [40] * 64, 64, 8, 128, 128, 16)
+    # 64 sequences x 64 heads x 129 floats x 256 splits is far beyond 8 MiB
+    k, v = w.k_pool.cuda(), w.v_pool.cuda()
+    desc = pkv.cache_desc(k, v)
+    out = torch.empty(64, 64, 128, device="cuda")
+    lse = torch.empty(64, 64, device="cuda")
+    rc = pkv.lib.pkv_paged_decode_attn_noalloc(
+        ctypes.byref(desc), _ptr(w.q.cuda()), 64, 64, _ptr(k), _ptr(v),
+        _ptr(w.block_tables.cuda()), w.block_tables.shape[1], _ptr(w.seq_lens.cuda()),
+        ctypes.c_float(w.scale), 256, _ptr(out), _ptr(lse), 0,
+        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == -4        # PKV_ERR_WORKSPACE_TOO_SMALL
