@@ -3,19 +3,21 @@
 // Work item = (sequence b, KV head g, split s): the chunk of tokens
 // [s*C, min(L, (s+1)*C)) of sequence b, C = 64 * ceil(L / (64 * S)), for all
 // G = Hq / Hkv query heads that share KV head g.  A persistent grid walks the
-// items round-robin; each CTA has one producer warp and four consumer warps.
+// items round-robin; each CTA has one producer warp and W consumer warps,
+// and several CTAs share an SM.
 //
 // Producer warp: reads block-table entries (one per lane, 32 segments at a
-// time), and issues 2-D TMA tensor copies of each (block, KV head) tile into a
-// ring of shared-memory stages.  A stage holds 64 tokens of K and of V; each
-// 64-column half of a row is a separate 128-byte-swizzled box, so ldmatrix
-// reads are bank-conflict free.  Segments past the end of the chunk (and
-// table entries outside the pool) are fetched from block 0 of the same KV
-// head, a row that always exists; the consumers mask those tokens' scores
-// and zero their value rows, so whatever that row holds never reaches the
-// result.  Every box is therefore fully in bounds.  Stage
-// hand-off uses mbarriers (full: producer expect_tx + TMA bytes; empty: one
-// arrival per consumer warp).  Every wait is bounded.
+// time) and moves each segment -- the (block, KV head) tile, or 16*W tokens of
+// it when blocks are longer -- with ONE TMA tensor copy per tensor: the tile
+// is contiguous in HBM, and the copy lands it as 64-column halves, each a
+// 128-byte-swizzled [rows x 128 B] array, so ldmatrix reads are bank-conflict
+// free.  A stage holds 16*W tokens of K and of V.  Segments past the end of
+// the chunk (and table entries outside the pool) are fetched from block 0 of
+// the same KV head, a row that always exists; the consumers mask those
+// tokens' scores and zero their value rows, so whatever that row holds never
+// reaches the result.  Stage hand-off uses mbarriers (full: producer
+// expect_tx + TMA bytes; empty: one arrival per consumer warp).  Every wait is
+// bounded.
 //
 // Consumer warps: warp w owns tokens [16w, 16w+16) of every stage.  Scores are
 // computed transposed, S^T[16 tokens x 8 cols] = K[16 x D] . [q_hi | q_lo]^T,
@@ -25,8 +27,8 @@
 // softmax runs in base 2 (query pre-scaled by scale*log2 e); probabilities
 // are split the same way (p_hi | p_lo) and the value product is
 // O^T[D x 8 cols] += V^T[D x 16] . [p_hi | p_lo]^T, again one MMA per 16 rows
-// of D.  At the end of an item the four warps' (m, l, O) are merged through
-// shared memory and written as that chunk's partial (or final) result.
+// of D.  At the end of an item the warps' (m, l, O) are merged through shared
+// memory and written as that chunk's partial (or final) result.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -41,28 +43,30 @@
 namespace pkv {
 namespace {
 
-constexpr int kStageTokens = 64;
-constexpr int kConsumerWarps = 4;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kRowBytes = 128;                          // one 64-column half-row of bf16
-constexpr int kHalfBytes = kStageTokens * kRowBytes;    // 8 KiB
+constexpr int kRowBytes = 128;     // one 64-column half-row of bf16
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-template <int D, int G, int NSTAGES>
+// D: head dim (64 or 128); G: query heads per KV head (1, 2, 4, 8);
+// W: consumer warps per CTA; NSTAGES: pipeline depth; MINB: CTAs per SM the
+// register allocation must allow.
+template <int D, int G, int W, int NSTAGES, int MINB>
 struct Cfg {
+    static constexpr int kStageTokens = 16 * W;
+    static constexpr int kThreads = (W + 1) * 32;
     static constexpr int kHalves = D / 64;
-    static constexpr int kTileBytes = kHalves * kHalfBytes;   // K (or V) of one stage
+    static constexpr int kTileBytes = kStageTokens * D * 2;    // K (or V) of one stage
     static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kNT = (2 * G + 7) / 8;               // 8-column n-tiles (hi|lo)
+    static constexpr int kNT = (2 * G + 7) / 8;                // 8-column n-tiles (hi|lo)
     static constexpr int kKSteps = D / 16;
     static constexpr int kMTiles = D / 16;
-    static constexpr int kMergeFloats = kConsumerWarps * (2 * G + G * D);
-    static constexpr int kPbufFloats = kConsumerWarps * 16 * G;
+    static constexpr int kMergeFloats = W * (2 * G + G * D);
+    static constexpr int kPbufFloats = W * 16 * G;
     static constexpr size_t kSmemBytes = 1024 + size_t(NSTAGES) * kStageBytes +
                                          2 * NSTAGES * sizeof(uint64_t) +
                                          sizeof(float) * (kMergeFloats + kPbufFloats) + 16;
     static_assert(NSTAGES <= 32, "stage bit masks are 32 bits wide");
+    static_assert(W == 1 || W == 2 || W == 4 || W == 8, "stages must tile a 32-segment window");
 };
 
 __device__ __forceinline__ int64_t lmin(int64_t x, int64_t y) { return x < y ? x : y; }
@@ -74,7 +78,8 @@ struct ItemRange {
     int nstages;
 };
 
-__device__ __forceinline__ ItemRange item_range(const DecodeArgs &a, int item, bool report) {
+__device__ __forceinline__ ItemRange item_range(const DecodeArgs &a, int item, int stage_tokens,
+                                                bool report) {
     ItemRange r;
     r.s = item % a.num_splits;
     const int t = item / a.num_splits;
@@ -88,7 +93,7 @@ __device__ __forceinline__ ItemRange item_range(const DecodeArgs &a, int item, b
     const int64_t chunk = 64 * ((L + 64LL * a.num_splits - 1) / (64LL * a.num_splits));
     r.begin = int64_t(r.s) * chunk;
     r.end = lmin(L, r.begin + chunk);
-    r.nstages = r.end > r.begin ? int((r.end - r.begin + kStageTokens - 1) / kStageTokens) : 0;
+    r.nstages = r.end > r.begin ? int((r.end - r.begin + stage_tokens - 1) / stage_tokens) : 0;
     return r;
 }
 
@@ -105,11 +110,34 @@ __device__ __forceinline__ int col_head(int n, bool &is_lo) {
     }
 }
 
-template <int D, int G, int NSTAGES>
-__global__ void __launch_bounds__(kThreads, 1)
+// Shared-memory layout of one stage's K (or V): segment-major, each segment
+// [half][seg_rows][128 B] with the 16-byte chunk index XOR-ed with (row & 7).
+// Segments and halves start on 1 KiB boundaries (seg_rows >= 8), so the
+// hardware's 128-byte swizzle pattern is exactly (row & 7).
+struct StageLayout {
+    uint32_t seg_shift;   // log2(rows per segment)
+    uint32_t seg_bytes;   // bytes of one segment (all halves)
+    uint32_t half_bytes;  // bytes of one half of a segment
+    __device__ __forceinline__ uint32_t row_base(int row) const {
+        return (uint32_t(row) >> seg_shift) * seg_bytes +
+               (uint32_t(row) & ((1u << seg_shift) - 1)) * kRowBytes;
+    }
+};
+
+template <int D>
+__device__ __forceinline__ void tma_tile(uint32_t dst, const CUtensorMap *map, int32_t row,
+                                         uint32_t bar) {
+    if constexpr (D == 128)
+        tma_load_3d(dst, map, 0, row, 0, bar);
+    else
+        tma_load_2d(dst, map, 0, row, bar);
+}
+
+template <int D, int G, int W, int NSTAGES, int MINB>
+__global__ void __launch_bounds__((W + 1) * 32, MINB)
 decode_tma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                   const __grid_constant__ CUtensorMap tmap_v, const DecodeArgs a) {
-    using C = Cfg<D, G, NSTAGES>;
+    using C = Cfg<D, G, W, NSTAGES, MINB>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -124,11 +152,14 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmap_k,
     const int num_items = a.batch * a.cache.num_kv_heads * a.num_splits;
     const int bs = a.cache.block_size;
     const int hkv = a.cache.num_kv_heads;
+    const int seg_rows = bs < C::kStageTokens ? bs : C::kStageTokens;
+    const uint32_t seg_shift = 31 - __clz(seg_rows);
+    const StageLayout lay{seg_shift, uint32_t(seg_rows) * D * 2, uint32_t(seg_rows) * kRowBytes};
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NSTAGES; ++s) {
             mbar_init(smem_addr(&full_bar[s]), 1);
-            mbar_init(smem_addr(&empty_bar[s]), kConsumerWarps);
+            mbar_init(smem_addr(&empty_bar[s]), W);
         }
         *abort_flag = 0;
         *stop_flag = 0;
@@ -136,20 +167,19 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmap_k,
     }
     __syncthreads();
 
-    if (warp == kConsumerWarps) {
+    if (warp == W) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             tma_prefetch_desc(&tmap_k);
             tma_prefetch_desc(&tmap_v);
         }
-        const int seg_rows = bs < kStageTokens ? bs : kStageTokens;
-        const int segs_per_stage = kStageTokens / seg_rows;
+        const int segs_per_stage = C::kStageTokens / seg_rows;
         int stage = 0;
         uint32_t phase = 0;
         uint32_t armed = 0, armed_parity = 0;   // per stage: ever armed / parity armed last
         bool ok = true;
         for (int item = blockIdx.x; item < num_items && ok; item += gridDim.x) {
-            const ItemRange r = item_range(a, item, false);
+            const ItemRange r = item_range(a, item, C::kStageTokens, false);
             const int total_segs = r.nstages * segs_per_stage;
             const int32_t *table = a.block_tables + int64_t(r.b) * a.max_blocks;
             for (int base = 0; base < total_segs && ok; base += 32) {
@@ -186,12 +216,8 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     for (int q = 0; q < segs_per_stage; ++q) {
                         const int32_t yq = __shfl_sync(0xffffffffu, y, k + q);
                         if (lane == 0) {
-                            const uint32_t off = q * seg_rows * kRowBytes;
-#pragma unroll
-                            for (int h = 0; h < C::kHalves; ++h) {
-                                tma_load_2d(kdst + h * kHalfBytes + off, &tmap_k, h * 64, yq, fb);
-                                tma_load_2d(vdst + h * kHalfBytes + off, &tmap_v, h * 64, yq, fb);
-                            }
+                            tma_tile<D>(kdst + q * lay.seg_bytes, &tmap_k, yq, fb);
+                            tma_tile<D>(vdst + q * lay.seg_bytes, &tmap_v, yq, fb);
                         }
                     }
                     if (++stage == NSTAGES) {
@@ -228,12 +254,17 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmap_k,
         slot_head[0] = 0; slot_head[1] = 0; slot_ok[0] = tq == 0; slot_ok[1] = false;
     }
     const float qscale = a.scale * kLog2e;
+    // ldmatrix row addresses inside a stage (constant per lane).
+    const int krow = 16 * warp + (lane & 7) + ((lane >> 3) & 1) * 8;   // A = K, non-transposed
+    const int vrow = 16 * warp + (lane & 7) + (lane >> 4) * 8;         // A = V^T, transposed
+    const uint32_t koff = lay.row_base(krow), voff = lay.row_base(vrow);
+    const int ksw = krow & 7, vsw = vrow & 7;
 
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
     for (int item = blockIdx.x; item < num_items; item += gridDim.x) {
-        const ItemRange r = item_range(a, item, warp == 0 && lane == 0);
+        const ItemRange r = item_range(a, item, C::kStageTokens, warp == 0 && lane == 0);
 
         // Query fragments: B operand of S^T = K . Q^T, columns [q_hi | q_lo].
         uint32_t qf[C::kKSteps][C::kNT][2];
@@ -285,18 +316,18 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmap_k,
             uint8_t *kstage = smem + size_t(stage) * C::kStageBytes;
             const uint32_t kbase = smem_addr(kstage);
             const uint32_t vbase = kbase + C::kTileBytes;
-            const int64_t tok0 = r.begin + int64_t(st) * kStageTokens + 16 * warp;
+            const int64_t tok0 = r.begin + int64_t(st) * C::kStageTokens + 16 * warp;
             const int nvalid = int(lmax(0, lmin(16, r.end - tok0)));
             if (nvalid < 16) {
                 // Rows past the end may hold any bits (unused slots of the last
-                // block): zero this warp's V rows there so 0 * garbage cannot
-                // reach the accumulator.
+                // block, or the stand-in block): zero this warp's V rows there
+                // so 0 * garbage cannot reach the accumulator.
                 const int nrows = 16 - nvalid;
                 for (int idx = lane; idx < nrows * C::kHalves * 8; idx += 32) {
                     const int row = 16 * warp + nvalid + idx / (C::kHalves * 8);
                     const int rest = idx % (C::kHalves * 8);
-                    *reinterpret_cast<uint4 *>(kstage + C::kTileBytes + (rest / 8) * kHalfBytes +
-                                               row * kRowBytes + (rest % 8) * 16) =
+                    *reinterpret_cast<uint4 *>(kstage + C::kTileBytes + lay.row_base(row) +
+                                               (rest / 8) * lay.half_bytes + (rest % 8) * 16) =
                         make_uint4(0u, 0u, 0u, 0u);
                 }
                 fence_proxy_async_smem();
@@ -311,21 +342,17 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     for (int nt = 0; nt < C::kNT; ++nt)
 #pragma unroll
                         for (int e = 0; e < 4; ++e) sacc[x][nt][e] = 0.f;
-                {
-                    const int row = 16 * warp + (lane & 7) + ((lane >> 3) & 1) * 8;
-                    const uint32_t rbase = kbase + row * kRowBytes;
-                    const int sw = row & 7;
 #pragma unroll
-                    for (int ks = 0; ks < C::kKSteps; ++ks) {
-                        const int chunk = (ks & 3) * 2 + (lane >> 4);
-                        const uint32_t addr = rbase + (ks >> 2) * kHalfBytes + ((chunk ^ sw) << 4);
-                        uint32_t a0, a1, a2, a3;
-                        ldsm_x4(addr, a0, a1, a2, a3);
+                for (int ks = 0; ks < C::kKSteps; ++ks) {
+                    const int chunk = (ks & 3) * 2 + (lane >> 4);
+                    const uint32_t addr =
+                        kbase + koff + (ks >> 2) * lay.half_bytes + ((chunk ^ ksw) << 4);
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(addr, a0, a1, a2, a3);
 #pragma unroll
-                        for (int nt = 0; nt < C::kNT; ++nt)
-                            mma_bf16_16816(sacc[ks & 1][nt], a0, a1, a2, a3, qf[ks][nt][0],
-                                           qf[ks][nt][1]);
-                    }
+                    for (int nt = 0; nt < C::kNT; ++nt)
+                        mma_bf16_16816(sacc[ks & 1][nt], a0, a1, a2, a3, qf[ks][nt][0],
+                                       qf[ks][nt][1]);
                 }
                 float sraw[C::kNT][4];
 #pragma unroll
@@ -407,20 +434,16 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 }
 
                 // ---- O^T += V^T . [p_hi | p_lo]^T
-                {
-                    const int row = 16 * warp + (lane & 7) + (lane >> 4) * 8;
-                    const uint32_t rbase = vbase + row * kRowBytes;
-                    const int sw = row & 7;
 #pragma unroll
-                    for (int mt = 0; mt < C::kMTiles; ++mt) {
-                        const int chunk = (mt & 3) * 2 + ((lane >> 3) & 1);
-                        const uint32_t addr = rbase + (mt >> 2) * kHalfBytes + ((chunk ^ sw) << 4);
-                        uint32_t a0, a1, a2, a3;
-                        ldsm_x4_trans(addr, a0, a1, a2, a3);
+                for (int mt = 0; mt < C::kMTiles; ++mt) {
+                    const int chunk = (mt & 3) * 2 + ((lane >> 3) & 1);
+                    const uint32_t addr =
+                        vbase + voff + (mt >> 2) * lay.half_bytes + ((chunk ^ vsw) << 4);
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4_trans(addr, a0, a1, a2, a3);
 #pragma unroll
-                        for (int nt = 0; nt < C::kNT; ++nt)
-                            mma_bf16_16816(acc[mt][nt], a0, a1, a2, a3, pf[nt][0], pf[nt][1]);
-                    }
+                    for (int nt = 0; nt < C::kNT; ++nt)
+                        mma_bf16_16816(acc[mt][nt], a0, a1, a2, a3, pf[nt][0], pf[nt][1]);
                 }
             }
             __syncwarp();
@@ -468,21 +491,20 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     mw[G + slot_head[j]] = l2[j];
                 }
         }
-        named_barrier_sync(1, kConsumerWarps * 32);
+        named_barrier_sync(1, W * 32);
         if (threadIdx.x == 0) *stop_flag = *abort_flag;
 
-        // ---- CTA merge of the four warps' partial states
+        // ---- CTA merge of the warps' partial states
         const int64_t row0 = (int64_t(r.s) * a.batch + r.b) * a.num_q_heads + int64_t(r.g) * G;
-        for (int idx = threadIdx.x; idx < G * D; idx += kConsumerWarps * 32) {
+        for (int idx = threadIdx.x; idx < G * D; idx += W * 32) {
             const int head = idx / D, d = idx % D;
             float M = -INFINITY;
 #pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w)
-                M = fmaxf(M, merge[w * (2 * G + G * D) + head]);
+            for (int w = 0; w < W; ++w) M = fmaxf(M, merge[w * (2 * G + G * D) + head]);
             float out = 0.f, lsum = 0.f;
             if (M != -INFINITY) {
 #pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w) {
+                for (int w = 0; w < W; ++w) {
                     const float *mwx = merge + w * (2 * G + G * D);
                     const float wt = exp2f(mwx[head] - M);
                     lsum = fmaf(wt, mwx[G + head], lsum);
@@ -493,7 +515,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmap_k,
             a.out_part[(row0 + head) * D + d] = out;
             if (d == 0) a.lse_part[row0 + head] = M != -INFINITY ? (M + log2f(lsum)) * kLn2 : -INFINITY;
         }
-        named_barrier_sync(1, kConsumerWarps * 32);
+        named_barrier_sync(1, W * 32);
         if (*stop_flag) break;   // same value in every consumer warp
     }
 }
@@ -513,24 +535,29 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
+// The pool as rows of `dim` bf16.  D = 128: a 3-D map (64 columns, rows,
+// 2 halves at a 128-byte stride) whose box -- one segment of rows, both
+// halves -- reads one contiguous run of HBM and lands half-major; D = 64: a
+// 2-D map (64 columns, rows).
 bool make_pool_map(CUtensorMap *map, const void *pool, int64_t rows, int dim, int box_rows) {
     auto fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t gdim[2] = {cuuint64_t(dim), cuuint64_t(rows)};
-    cuuint64_t gstride[1] = {cuuint64_t(dim) * 2};
-    cuuint32_t box[2] = {64, cuuint32_t(box_rows)};
-    cuuint32_t estride[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(pool), gdim, gstride,
+    const cuuint32_t rank = dim == 128 ? 3 : 2;
+    cuuint64_t gdim[3] = {64, cuuint64_t(rows), 2};
+    cuuint64_t gstride[2] = {cuuint64_t(dim) * 2, 128};
+    cuuint32_t box[3] = {64, cuuint32_t(box_rows), 2};
+    cuuint32_t estride[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(pool), gdim, gstride,
               box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, int G, int NSTAGES>
+template <int D, int G, int W, int NSTAGES, int MINB>
 int launch(const DecodeArgs &a) {
-    using C = Cfg<D, G, NSTAGES>;
-    auto kernel = decode_tma_kernel<D, G, NSTAGES>;
+    using C = Cfg<D, G, W, NSTAGES, MINB>;
+    auto kernel = decode_tma_kernel<D, G, W, NSTAGES, MINB>;
     const int64_t rows = int64_t(a.cache.num_blocks) * a.cache.num_kv_heads * a.cache.block_size;
-    const int box_rows = std::min(a.cache.block_size, kStageTokens);
+    const int box_rows = std::min(a.cache.block_size, C::kStageTokens);
     CUtensorMap tk, tv;
     if (!make_pool_map(&tk, a.k_pool, rows, D, box_rows) ||
         !make_pool_map(&tv, a.v_pool, rows, D, box_rows))
@@ -545,26 +572,48 @@ int launch(const DecodeArgs &a) {
         configured_dev = dev;
     }
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, C::kSmemBytes) !=
-            cudaSuccess || per_sm < 1)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, C::kThreads,
+                                                      C::kSmemBytes) != cudaSuccess ||
+        per_sm < 1)
         return PKV_ERR_CUDA;
     const int64_t items = int64_t(a.batch) * a.cache.num_kv_heads * a.num_splits;
     const int grid = int(std::min<int64_t>(items, int64_t(sm_count()) * per_sm));
     if (grid <= 0) return PKV_OK;
-    kernel<<<grid, kThreads, C::kSmemBytes, a.stream>>>(tk, tv, a);
+    kernel<<<grid, C::kThreads, C::kSmemBytes, a.stream>>>(tk, tv, a);
     return cuda_status(cudaGetLastError());
 }
 
-template <int D, int NSTAGES>
-int launch_g(const DecodeArgs &a, int G) {
-    switch (G) {
-        case 1: return launch<D, 1, NSTAGES>(a);
-        case 2: return launch<D, 2, NSTAGES>(a);
-        case 4: return launch<D, 4, NSTAGES>(a);
-        case 8: return launch<D, 8, NSTAGES>(a);
-        default: return PKV_ERR_SHAPE;
-    }
-}
+// Launch shapes: consumer warps (W), stages (S), CTAs per SM (B).
+#ifndef PKV_TMA_D128_W
+#define PKV_TMA_D128_W 2
+#endif
+#ifndef PKV_TMA_D128_S
+#define PKV_TMA_D128_S 3
+#endif
+#ifndef PKV_TMA_D128_B
+#define PKV_TMA_D128_B 4
+#endif
+#ifndef PKV_TMA_D128G8_W
+#define PKV_TMA_D128G8_W 8
+#endif
+#ifndef PKV_TMA_D128G8_S
+#define PKV_TMA_D128G8_S 2
+#endif
+#ifndef PKV_TMA_D128G8_B
+#define PKV_TMA_D128G8_B 1
+#endif
+#ifndef PKV_TMA_D64_W
+#define PKV_TMA_D64_W 2
+#endif
+#ifndef PKV_TMA_D64_S
+#define PKV_TMA_D64_S 6
+#endif
+#ifndef PKV_TMA_D64_B
+#define PKV_TMA_D64_B 4
+#endif
+#define PKV_TMA_SHAPE_D128 PKV_TMA_D128_W, PKV_TMA_D128_S, PKV_TMA_D128_B
+#define PKV_TMA_SHAPE_D128_G8 PKV_TMA_D128G8_W, PKV_TMA_D128G8_S, PKV_TMA_D128G8_B
+#define PKV_TMA_SHAPE_D64 PKV_TMA_D64_W, PKV_TMA_D64_S, PKV_TMA_D64_B
 
 }  // namespace
 
@@ -577,10 +626,29 @@ bool tma_kernel_supports(const pkv_cache_desc &c, int32_t num_q_heads) {
            (G == 1 || G == 2 || G == 4 || G == 8) && pow2_bs && rows < (int64_t(1) << 31) - 1;
 }
 
+// Launch shapes (consumer warps, stages, CTAs per SM), measured on 8 x 32K
+// GQA decode: with G <= 4, two consumer warps per CTA (32-token stages) and
+// four CTAs per SM keep more independent warps streaming than one large CTA
+// does; with G = 8 the consumers do twice the work per byte and one CTA of
+// eight consumer warps (128-token stages) is fastest.
 int launch_decode_tma(const DecodeArgs &a) {
     const int G = a.num_q_heads / a.cache.num_kv_heads;
-    if (a.cache.head_dim_k == 128) return launch_g<128, 4>(a, G);
-    return launch_g<64, 8>(a, G);
+    if (a.cache.head_dim_k == 128) {
+        switch (G) {
+            case 1: return launch<128, 1, PKV_TMA_SHAPE_D128>(a);
+            case 2: return launch<128, 2, PKV_TMA_SHAPE_D128>(a);
+            case 4: return launch<128, 4, PKV_TMA_SHAPE_D128>(a);
+            case 8: return launch<128, 8, PKV_TMA_SHAPE_D128_G8>(a);
+            default: return PKV_ERR_SHAPE;
+        }
+    }
+    switch (G) {
+        case 1: return launch<64, 1, PKV_TMA_SHAPE_D64>(a);
+        case 2: return launch<64, 2, PKV_TMA_SHAPE_D64>(a);
+        case 4: return launch<64, 4, PKV_TMA_SHAPE_D64>(a);
+        case 8: return launch<64, 8, PKV_TMA_SHAPE_D64>(a);
+        default: return PKV_ERR_SHAPE;
+    }
 }
 
 }  // namespace pkv
