@@ -5,7 +5,15 @@ query / 8 KV heads, head_dim 128, bf16 K/V, block size 16, physical blocks a
 random permutation of a 16,384-block pool, split-KV over 16 chunks merged
 with lse_merge.  One step = slot mapping + kv_append of the 8 decode tokens
 + the split attention kernel + the LSE merge (the exact launches that
-pkv_paged_decode_attn makes), with the KV cache resident in HBM.
+pkv_paged_decode_attn makes), with the KV cache resident in HBM.  Steps run
+back to back: the 1.07 GB of KV a step reads is 8x the 129 MB L2, so no
+flush is needed between them (a flush would add its own write-back traffic).
+
+Other workloads (--workload): `dcp200k` (one 200,000-token sequence split
+into 4 interleaved partitions, each attended separately and merged) and
+`agent_mla` (32 sequences sharing a 136K-token prefix, MLA-shaped 128 heads
+over one 576/512 latent head, copy-on-write of the shared tail + append +
+attention).
 
 Metric: HBM GB/s over the step's algorithmic bytes (every cached K/V byte
 once, plus q, block tables, appended tokens, out and lse), its fraction of the
@@ -34,7 +42,6 @@ import torch  # noqa: E402
 import workloads  # noqa: E402
 
 METRIC = "paged decode-attn HBM GB/s (% of GB300 peak), seq-tokens/s at 32K ctx GQA"
-L2_FLUSH_BYTES = 256 << 20
 FALLBACK_HBM_GBS = 6800.0
 PROFILE = os.path.join(ROOT, "profiles", "decode_tma_long32k.txt")
 KERNEL_SOURCES = [os.path.join(ROOT, "paged_kv_cache_93_gb300", "csrc", f)
@@ -48,10 +55,23 @@ def kv_bytes_per_token(w) -> int:
     return (w.head_dim_k + w.head_dim_v) * w.num_kv_heads * 2
 
 
+def unique_kv_tokens(w) -> int:
+    """Tokens of K/V the step must read, a physical block shared by several
+    sequences counted once (the most tokens any of them uses in it)."""
+    used = {}
+    tables = w.block_tables.tolist()
+    for b, L in enumerate(w.seq_lens.tolist()):
+        for i in range(-(-L // w.block_size)):
+            n = min(w.block_size, L - i * w.block_size)
+            phys = tables[b][i]
+            used[phys] = max(used.get(phys, 0), n)
+    return sum(used.values())
+
+
 def step_bytes(w, splits: int):
     """Algorithmic bytes of one step, and of one launch of the split kernel."""
     lens = w.seq_lens.to(torch.int64)
-    kv = int(lens.sum()) * kv_bytes_per_token(w)
+    kv = unique_kv_tokens(w) * kv_bytes_per_token(w)
     B, Hq = w.batch, w.num_q_heads
     q = B * Hq * w.head_dim_k * 4
     tables = int(((lens + w.block_size - 1) // w.block_size).sum()) * 4 + B * 4
@@ -163,7 +183,8 @@ def bits_view(t: torch.Tensor) -> np.ndarray:
 # ------------------------------------------------------------ device state
 
 class Step:
-    """Device-resident state of one workload and its decode step."""
+    """Device-resident state of one GQA workload and its decode step."""
+    kernel_name = "decode_tma_kernel (split attention)"
 
     def __init__(self, pkv, w, dev, splits):
         self.pkv, self.w, self.splits = pkv, w, splits
@@ -180,20 +201,127 @@ class Step:
         self.slots = torch.empty(w.new_pos.numel(), dtype=torch.int64, device=dev)
         self.out = torch.empty(B, Hq, w.head_dim_v, device=dev)
         self.lse = torch.empty(B, Hq, device=dev)
+        self.ws = torch.zeros(max(1, pkv.decode_workspace_size(B, Hq, w.head_dim_v, splits)),
+                              dtype=torch.uint8, device=dev)
         self.out_part = torch.empty(splits, B, Hq, w.head_dim_v, device=dev)
         self.lse_part = torch.empty(splits, B, Hq, device=dev)
+        self.launches = 4   # slot, append, split, merge
+        self.desc = (f"slot_mapping + kv_append ({w.new_pos.numel()} decode tokens) + "
+                     f"paged_decode_attn ({splits} splits) = split kernel + lse_merge")
+
+    def kernel(self):
+        """The split attention kernel alone (the roofline's kernel)."""
+        self.pkv.paged_decode_attn_partial(self.q, self.k, self.v, self.bt, self.lens,
+                                           self.w.scale, self.splits, out_part=self.out_part,
+                                           lse_part=self.lse_part)
+
+    def attend(self, ev_a=None, ev_b=None):
+        """What pkv_paged_decode_attn launches: the split kernel, then the merge
+        (events, if given, bracket the split kernel)."""
+        if self.splits == 1 or ev_a is None:
+            self.pkv.paged_decode_attn(self.q, self.k, self.v, self.bt, self.lens, self.w.scale,
+                                       num_splits=self.splits, workspace=self.ws, out=self.out,
+                                       lse=self.lse)
+            return
+        ev_a.record()
+        self.kernel()
+        ev_b.record()
+        self.pkv.lse_merge(self.out_part, self.lse_part, out=self.out, lse=self.lse)
+
+    def run(self, ev_a=None, ev_b=None):
+        p = self.pkv
+        p.slot_mapping(self.k, self.v, self.bt, self.new_seq, self.new_pos, out=self.slots)
+        p.kv_append(self.k, self.v, self.k_new, self.v_new, self.slots)
+        self.attend(ev_a, ev_b)
+
+
+class DcpStep(Step):
+    """200K tokens in P interleaved partitions: the decode token goes to its
+    partition, each partition is attended separately (its own block table),
+    and the P partial results are merged."""
+
+    def __init__(self, pkv, w, dev, splits):
+        super().__init__(pkv, w, dev, splits)
+        N, P = int(w.seq_lens[0]), w.num_parts
+        self.ptab = w.part_tables.to(dev)
+        kt, vt = w.k_tokens.to(dev), w.v_tokens.to(dev)
+        pkv.kv_append(self.k, self.v, kt[:N - 1], vt[:N - 1],
+                      pkv.interleave_slot_mapping(self.k, self.v, 0, N - 1, P, w.interleave,
+                                                  self.ptab))
+        del kt, vt
+        self.N, self.P = N, P
+        # The P partitions are attended in ONE launch, as P rows of a batch
+        # that share the query and each read their own table -- the
+        # single-GPU image of P DCP ranks attending concurrently.
+        self.plen = torch.tensor([pkv.interleave_partition_len(N, P, w.interleave, r)
+                                  for r in range(P)], dtype=torch.int32, device=dev)
+        Hq, Dv = w.num_q_heads, w.head_dim_v
+        self.pq = self.q.expand(P, Hq, w.head_dim_k).contiguous()
+        self.pout = torch.empty(P, Hq, Dv, device=dev)
+        self.plse = torch.empty(P, Hq, device=dev)
+        self.ws = torch.zeros(pkv.decode_workspace_size(P, Hq, Dv, splits), dtype=torch.uint8,
+                              device=dev)
+        self.sp_out = torch.empty(splits, P, Hq, Dv, device=dev)
+        self.sp_lse = torch.empty(splits, P, Hq, device=dev)
+        self.launches = 2 + 2 + 1
+        self.desc = (f"interleave slot + kv_append (decode token) + paged_decode_attn over the "
+                     f"{P} partitions in one launch ({splits} splits each) + lse_merge over the "
+                     f"{P} partition results")
+
+    def kernel(self):
+        self.pkv.paged_decode_attn_partial(self.pq, self.k, self.v, self.ptab, self.plen,
+                                           self.w.scale, self.splits, out_part=self.sp_out,
+                                           lse_part=self.sp_lse)
 
     def run(self, ev_a=None, ev_b=None):
         p, w = self.pkv, self.w
-        p.slot_mapping(self.k, self.v, self.bt, self.new_seq, self.new_pos, out=self.slots)
+        p.interleave_slot_mapping(self.k, self.v, self.N - 1, 1, self.P, w.interleave, self.ptab,
+                                  out=self.slots)
         p.kv_append(self.k, self.v, self.k_new, self.v_new, self.slots)
-        if ev_a is not None:
+        if ev_a is None:
+            p.paged_decode_attn(self.pq, self.k, self.v, self.ptab, self.plen, w.scale,
+                                num_splits=self.splits, workspace=self.ws, out=self.pout,
+                                lse=self.plse)
+        else:
             ev_a.record()
-        p.paged_decode_attn_partial(self.q, self.k, self.v, self.bt, self.lens, w.scale,
-                                    self.splits, out_part=self.out_part, lse_part=self.lse_part)
-        if ev_b is not None:
+            self.kernel()
             ev_b.record()
-        p.lse_merge(self.out_part, self.lse_part, out=self.out, lse=self.lse)
+            p.lse_merge(self.sp_out, self.sp_lse, out=self.pout, lse=self.plse)
+        p.lse_merge(self.pout, self.plse, out=self.out[0], lse=self.lse[0])
+
+
+class AgentStep(Step):
+    """Shared-prefix MLA-shaped step: copy-on-write of each sequence's shared
+    tail, append of the decode tokens, attention (the suffixes are appended
+    once, before timing)."""
+    kernel_name = "decode_generic_kernel (split attention, CUDA cores)"
+
+    def __init__(self, pkv, w, dev, splits):
+        super().__init__(pkv, w, dev, splits)
+        self.src, self.dst = w.cow_src.to(dev), w.cow_dst.to(dev)
+        pkv.copy_blocks(self.k, self.v, self.src, self.dst)
+        last = torch.zeros(w.new_seq.numel(), dtype=torch.bool)
+        last[torch.cumsum(torch.bincount(w.new_seq.long()), 0) - 1] = True
+        setup = ~last
+        sl = pkv.slot_mapping(self.k, self.v, self.bt, self.new_seq[setup.to(dev)],
+                              self.new_pos[setup.to(dev)])
+        pkv.kv_append(self.k, self.v, self.k_new[setup.to(dev)], self.v_new[setup.to(dev)], sl)
+        keep = last.to(dev)
+        self.new_seq, self.new_pos = self.new_seq[keep], self.new_pos[keep]
+        self.k_new, self.v_new = self.k_new[keep].contiguous(), self.v_new[keep].contiguous()
+        self.slots = torch.empty(self.new_pos.numel(), dtype=torch.int64, device=dev)
+        self.launches = 5   # copy, slot, append, split, merge
+        self.desc = (f"copy_blocks ({self.src.numel()} CoW pairs) + slot_mapping + kv_append "
+                     f"({self.new_pos.numel()} decode tokens) + split attention ({splits} "
+                     f"splits) + lse_merge")
+
+    def run(self, ev_a=None, ev_b=None):
+        self.pkv.copy_blocks(self.k, self.v, self.src, self.dst)
+        super().run(ev_a, ev_b)
+
+
+STEPS = {"long32k": Step, "mix": Step, "tiny": Step, "dcp200k": DcpStep, "agent_mla": AgentStep}
+DEFAULT_SPLITS = {"long32k": 16, "mix": 4, "tiny": 1, "dcp200k": 19, "agent_mla": 8}
 
 
 # ------------------------------------------------------------------ arms
@@ -280,7 +408,8 @@ def run_reference(args, world, rank):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * wall / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": workload_desc(w, args.splits), "oracle": "C, fp64, all host cores"},
+        "config": {"workload": workload_desc(w, args.splits or DEFAULT_SPLITS[args.workload]),
+                   "oracle": "C, fp64, all host cores"},
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": cores,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -293,9 +422,8 @@ def run_gpu(args, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     w = workloads.make(args.workload)
-    splits = args.splits
-    st = Step(pkv, w, dev, splits)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    splits = args.splits or DEFAULT_SPLITS[args.workload]
+    st = STEPS[args.workload](pkv, w, dev, splits)
     total_bytes, kernel_bytes = step_bytes(w, splits)
     stream = torch.cuda.current_stream()
 
@@ -305,77 +433,111 @@ def run_gpu(args, world, rank, local):
     if pkv.device_status(reset=True) != 0:
         raise RuntimeError("device status word set during warm-up")
 
+    # ---- timed region: K steps back to back; events around the attention
+    # kernel(s) of every step give its launch duration.
+    # ---- timed region: K steps back to back, events only at its two ends
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    ev_start = torch.cuda.Event(enable_timing=True)
+    ev_end = torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
         sampler.wait_ready()
     barrier(world)
     torch.cuda.synchronize()
     t0 = time.time()
-    for i in range(K):
-        flush.zero_()                       # L2 flush (outside the timed events)
-        e = ev[i]
-        e[0].record(stream)
-        st.run(e[1], e[2])
-        e[3].record(stream)
+    ev_start.record(stream)
+    for _ in range(K):
+        st.run()
+    ev_end.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     t1 = time.time()
-    step_ms = [e[0].elapsed_time(e[3]) for e in ev]
-    kern_ms = [e[1].elapsed_time(e[2]) for e in ev]
     clocks = sampler.summary(t0, t1) if sampler else None
     if sampler:
         sampler.stop()
     if pkv.device_status(reset=True) != 0:
         raise RuntimeError("device status word set during the timed steps")
+    ms = max_over_ranks(ev_start.elapsed_time(ev_end) / K, world)
 
-    ms = max_over_ranks(statistics.fmean(step_ms), world)
-    kms = max_over_ranks(statistics.fmean(kern_ms), world)
+    # ---- the same K steps again, with events around the split attention
+    # kernel of every step: its average launch duration (for the roofline)
+    ev_k = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(K)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(K):
+        st.run(*ev_k[i])
+    torch.cuda.synchronize()
+    barrier(world)
+    kms = max_over_ranks(statistics.fmean(a.elapsed_time(b) for a, b in ev_k), world)
+
+    # ---- the split kernel alone, launched back to back (context only)
+    torch.cuda.synchronize()
+    a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    kb = min(K, 200)
+    a_ev.record(stream)
+    for _ in range(kb):
+        st.kernel()
+    b_ev.record(stream)
+    torch.cuda.synchronize()
+    kms_b2b = a_ev.elapsed_time(b_ev) / kb
+
     value = world * total_bytes / (ms * 1e-3) / 1e9
     peak, peak_kind = load_peak()
     kernel_gbs = kernel_bytes / (kms * 1e-3) / 1e9
 
     # ---- end to end through the public API, host buffers in pinned memory
-    pin = {n: getattr(w, n).pin_memory() for n in
-           ("q", "block_tables", "seq_lens", "new_seq", "new_pos", "k_new", "v_new")}
-    h_out = torch.empty(w.batch, w.num_q_heads, w.head_dim_v).pin_memory()
-    h_lse = torch.empty(w.batch, w.num_q_heads).pin_memory()
-    d = {n: torch.empty_like(t, device=dev) for n, t in pin.items()}
-    ws = torch.empty(max(1, pkv.decode_workspace_size(w.batch, w.num_q_heads, w.head_dim_v,
-                                                      splits)), dtype=torch.uint8, device=dev)
-    h2d = sum(t.numel() * t.element_size() for t in pin.values())
-    d2h = h_out.numel() * 4 + h_lse.numel() * 4
-    ke = max(3, min(K, 200))
+    e2e = None
+    if args.workload in ("long32k", "mix", "tiny"):
+        pin = {n: getattr(w, n).pin_memory() for n in
+               ("q", "block_tables", "seq_lens", "new_seq", "new_pos", "k_new", "v_new")}
+        h_out = torch.empty(w.batch, w.num_q_heads, w.head_dim_v).pin_memory()
+        h_lse = torch.empty(w.batch, w.num_q_heads).pin_memory()
+        d = {n: torch.empty_like(t, device=dev) for n, t in pin.items()}
+        ws = torch.zeros(max(1, pkv.decode_workspace_size(w.batch, w.num_q_heads, w.head_dim_v,
+                                                          splits)), dtype=torch.uint8,
+                         device=dev)
+        h2d = sum(t.numel() * t.element_size() for t in pin.values())
+        d2h = h_out.numel() * 4 + h_lse.numel() * 4
+        ke = max(3, min(K, 200))
 
-    def e2e_step():
-        for n, t in pin.items():
-            d[n].copy_(t, non_blocking=True)
-        slots = pkv.slot_mapping(st.k, st.v, d["block_tables"], d["new_seq"], d["new_pos"])
-        pkv.kv_append(st.k, st.v, d["k_new"], d["v_new"], slots)
-        out, lse = pkv.paged_decode_attn(d["q"], st.k, st.v, d["block_tables"], d["seq_lens"],
-                                         w.scale, num_splits=splits, workspace=ws)
-        h_out.copy_(out, non_blocking=True)
-        h_lse.copy_(lse, non_blocking=True)
+        def e2e_step():
+            for n, t in pin.items():
+                d[n].copy_(t, non_blocking=True)
+            slots = pkv.slot_mapping(st.k, st.v, d["block_tables"], d["new_seq"], d["new_pos"])
+            pkv.kv_append(st.k, st.v, d["k_new"], d["v_new"], slots)
+            out, lse = pkv.paged_decode_attn(d["q"], st.k, st.v, d["block_tables"],
+                                             d["seq_lens"], w.scale, num_splits=splits,
+                                             workspace=ws)
+            h_out.copy_(out, non_blocking=True)
+            h_lse.copy_(lse, non_blocking=True)
 
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize()
-    barrier(world)
-    te = time.perf_counter()
-    for _ in range(ke):
-        e2e_step()
-    torch.cuda.synchronize()
-    e2e_s = max_over_ranks((time.perf_counter() - te) / ke, world)
-    barrier(world)
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        te = time.perf_counter()
+        for _ in range(ke):
+            e2e_step()
+        torch.cuda.synchronize()
+        e2e_s = max_over_ranks((time.perf_counter() - te) / ke, world)
+        barrier(world)
+        e2e = {"value": round(total_bytes / e2e_s / 1e9 * world, 2), "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": round(e2e_s * 1e3, 4), "steps": ke,
+               "api": "pinned host inputs -> slot_mapping + kv_append + paged_decode_attn -> "
+                      "pinned host out/lse, wall clock"}
+    if pkv.device_status(reset=True) != 0:
+        raise RuntimeError("device status word set")
 
     if rank != 0:
         return
 
-    # ---- CPU baseline: the oracle on this host's cores, the whole workload
-    used, times = oracle_gbs(w, None if not args.quick_cpu else 2048, repeats=1)
+    # ---- CPU baseline: the oracle on this host's cores
+    tokens = None if (args.workload in ("long32k", "mix", "tiny") and not args.quick_cpu) else 2048
+    used, times = oracle_gbs(w, tokens, repeats=1)
     cpu_gbs = used / min(times) / 1e9
-    traffic = stored_traffic()
+    traffic = stored_traffic() if args.workload == "long32k" else None
     seq_tokens = int(w.seq_lens.sum())
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
@@ -385,14 +547,16 @@ def run_gpu(args, world, rank, local):
         "config": {
             "workload": workload_desc(w, splits), "batch": w.batch,
             "context": int(w.seq_lens.max()), "num_q_heads": w.num_q_heads,
-            "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim_k,
-            "block_size": w.block_size, "num_splits": splits,
-            "step": "slot_mapping + kv_append (8 decode tokens) + split attention + lse_merge",
-            "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MiB write, untimed); "
-                  f"KV {total_bytes / 1e9:.3f} GB > 129 MB L2",
+            "num_kv_heads": w.num_kv_heads, "head_dim_k": w.head_dim_k,
+            "head_dim_v": w.head_dim_v, "block_size": w.block_size, "num_splits": splits,
+            "step": st.desc,
+            "l2": f"no flush: the {total_bytes / 1e9:.3f} GB a step reads exceeds the 129 MB "
+                  f"L2 (steps back to back)",
             "parallelism": "replicas" if world > 1 else "single GPU",
-            "compute": "bf16 tensor-core products (fp32 query and probabilities split "
-                       "into bf16 hi+lo), fp32 accumulate and softmax",
+            "compute": "bf16 tensor-core products (fp32 query and probabilities split into bf16 "
+                       "hi+lo), fp32 accumulate and softmax" if st.kernel_name.startswith(
+                           "decode_tma") else "fp32 CUDA-core dot products and softmax",
+            "bytes": "unique K/V bytes (shared blocks once) + q + tables + appends + out/lse",
         },
         "pct_of_peak": round(100 * value / world / peak, 2),
         "seq_tokens_per_s": round(world * seq_tokens / (ms * 1e-3), 1),
@@ -400,24 +564,21 @@ def run_gpu(args, world, rank, local):
         "roofline": {
             "bound": "hbm", "achieved": round(kernel_gbs, 2), "peak": peak,
             "unit": "GB/s", "frac": round(kernel_gbs / peak, 4), "traffic": traffic,
-            "kernel": "decode_tma_kernel<128,4,4> (split attention)",
+            "kernel": st.kernel_name,
             "algorithmic_bytes_per_launch": kernel_bytes,
-            "launch_ms": round(kms, 5), "peak_kind": f"{peak_kind} hbm_gbs",
+            "launch_ms": round(kms, 5),
+            "launch_ms_back_to_back": round(kms_b2b, 5),
+            "peak_kind": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json copy bandwidth)",
         },
         "cpu_baseline": {
             "value": round(cpu_gbs, 4), "unit": "GB/s", "cores": os.cpu_count(),
             "kind": "oracle",
-            "sample": "whole workload (every row, every token), C fp64 oracle, all host cores"
-            if not args.quick_cpu else "every row, first 2048 tokens",
+            "sample": ("whole workload (every row, every token)" if tokens is None else
+                       f"every row, first {tokens} tokens of each sequence") +
+                      ", C fp64 oracle, all host cores",
         },
-        "e2e": {
-            "value": round(total_bytes / e2e_s / 1e9 * world, 2), "unit": "GB/s",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "ms_per_step": round(e2e_s * 1e3, 4), "steps": ke,
-            "api": "pinned host inputs -> slot_mapping + kv_append + paged_decode_attn -> "
-                   "pinned host out/lse",
-        },
-        "gpu_launches": 4 * K,
+        "e2e": e2e,
+        "gpu_launches": st.launches * K,
         "clocks": clocks,
     }
     print(json.dumps(line))
@@ -429,8 +590,8 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--workload", default="long32k", choices=["long32k", "mix", "tiny"])
-    ap.add_argument("--splits", type=int, default=16)
+    ap.add_argument("--workload", default="long32k", choices=sorted(STEPS))
+    ap.add_argument("--splits", type=int, default=0, help="0 = the workload's default")
     ap.add_argument("--quick-cpu", action="store_true", help="smaller oracle sample")
     args = ap.parse_args()
     if args.warmup < 3:

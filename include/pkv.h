@@ -172,7 +172,8 @@ int64_t pkv_interleave_partition_len(int64_t num_tokens, int32_t num_parts,
  * does.  num_splits = 0 picks S from the batch, the heads and the SM count.
  * S must be <= 256.  The partials live in `workspace`, which must hold at
  * least pkv_decode_workspace_size(batch, num_q_heads, head_dim_v, S) bytes
- * (0 when S == 1; `workspace` may then be NULL).
+ * (0 when S == 1; `workspace` may then be NULL).  Its contents on entry do
+ * not matter.
  *
  * flags: 0 = choose the kernel by shape (the TMA + tensor-core kernel for
  * head_dim_k == head_dim_v in {64, 128}, query groups of 1, 2, 4 or 8 and

@@ -51,6 +51,8 @@ int run_split_kernel(const DecodeArgs &a, int32_t flags) {
 
 }  // namespace
 
+// Workspace layout: [partial outputs S x batch x heads x Dv fp32][partial
+// LSEs S x batch x heads fp32], each region 256-byte aligned.
 extern "C" size_t pkv_decode_workspace_size(int32_t batch, int32_t num_q_heads,
                                             int32_t head_dim_v, int32_t num_splits) {
     if (batch <= 0 || num_q_heads <= 0 || head_dim_v <= 0 || num_splits <= 1) return 0;
@@ -115,11 +117,14 @@ extern "C" int pkv_paged_decode_attn(const pkv_cache_desc *cache, const float *q
     if (S == 1) return run_split_kernel(a, flags);
 
     const size_t rows = size_t(S) * batch * num_q_heads;
-    float *out_part = static_cast<float *>(workspace);
-    float *lse_part = reinterpret_cast<float *>(static_cast<char *>(workspace) +
-                                                align256(rows * cache->head_dim_v * sizeof(float)));
+    char *ws = static_cast<char *>(workspace);
+    float *out_part = reinterpret_cast<float *>(ws);
+    float *lse_part =
+        reinterpret_cast<float *>(ws + align256(rows * cache->head_dim_v * sizeof(float)));
     a.out_part = out_part;
     a.lse_part = lse_part;
+    // The split kernel lets the merge launch early (programmatic dependent
+    // launch): the merge's CTAs wait on the device for the partials.
     st = run_split_kernel(a, flags);
     if (st != PKV_OK) return st;
     return launch_lse_merge(S, out_part, lse_part, int64_t(batch) * num_q_heads,
@@ -129,12 +134,13 @@ extern "C" int pkv_paged_decode_attn(const pkv_cache_desc *cache, const float *q
 extern "C" int pkv_lse_merge(int32_t num_parts, const float *out_part, const float *lse_part,
                              int64_t rows, int32_t head_dim_v, float *out, float *lse,
                              pkv_stream_t stream) {
-    if (num_parts <= 0 || rows < 0 || head_dim_v <= 0 || head_dim_v % 4 != 0)
+    if (num_parts <= 0 || rows < 0 || head_dim_v <= 0 || head_dim_v % 4 != 0 ||
+        head_dim_v > 1024)
         return PKV_ERR_INVALID_ARG;
     if (rows == 0) return PKV_OK;
     if (!out_part || !lse_part || !out || !lse) return PKV_ERR_INVALID_ARG;
     if (!aligned16(out_part) || !aligned16(out)) return PKV_ERR_ALIGNMENT;
-    if (rows > int64_t(INT32_MAX) * 8) return PKV_ERR_SHAPE;
+    if (rows > int64_t(INT32_MAX)) return PKV_ERR_SHAPE;
     return launch_lse_merge(num_parts, out_part, lse_part, rows, head_dim_v, out, lse,
                             reinterpret_cast<cudaStream_t>(stream));
 }

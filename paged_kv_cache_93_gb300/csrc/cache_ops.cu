@@ -71,6 +71,8 @@ __global__ void slot_mapping_kernel(const int32_t *__restrict__ block_tables, in
                                     const int32_t *__restrict__ seq_ids,
                                     const int64_t *__restrict__ positions, int64_t num_tokens,
                                     int64_t *__restrict__ slots, uint32_t *status) {
+    pdl_wait();
+    pdl_launch_dependents();
     for (int64_t t = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; t < num_tokens;
          t += int64_t(gridDim.x) * blockDim.x) {
         const int32_t b = seq_ids[t];
@@ -100,6 +102,8 @@ __global__ void kv_append_kernel(uint4 *__restrict__ k_pool, uint4 *__restrict__
                                  const int64_t *__restrict__ slots, int64_t num_tokens,
                                  int32_t num_kv_heads, int32_t block_size, int64_t num_slots,
                                  int32_t vk, int32_t vv, uint32_t *status) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int64_t per_token = int64_t(num_kv_heads) * (vk + vv);
     const int64_t total = num_tokens * per_token;
     for (int64_t u = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; u < total;
@@ -133,6 +137,8 @@ __global__ void copy_blocks_kernel(uint4 *__restrict__ k_pool, uint4 *__restrict
                                    const int32_t *__restrict__ src, const int32_t *__restrict__ dst,
                                    int32_t num_pairs, int32_t num_blocks, int64_t k_vecs,
                                    int64_t v_vecs, uint32_t *status) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int32_t p = blockIdx.x;
     const int32_t s = src[p], d = dst[p];
     const bool in_range = s >= 0 && s < num_blocks && d >= 0 && d < num_blocks;
@@ -162,6 +168,8 @@ __global__ void interleave_slots_kernel(int64_t first_token, int64_t num_tokens,
                                         const int32_t *__restrict__ part_tables, int32_t max_blocks,
                                         int64_t *__restrict__ slots, int32_t *__restrict__ parts,
                                         uint32_t *status) {
+    pdl_wait();
+    pdl_launch_dependents();
     for (int64_t t = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; t < num_tokens;
          t += int64_t(gridDim.x) * blockDim.x) {
         const int64_t i = first_token + t;
@@ -229,11 +237,10 @@ extern "C" int pkv_slot_mapping(const pkv_cache_desc *cache, const int32_t *bloc
     uint32_t *status = status_word();
     if (!status) return PKV_ERR_CUDA;
     const int threads = 256;
-    slot_mapping_kernel<<<grid_for(num_tokens, threads), threads, 0,
-                          reinterpret_cast<cudaStream_t>(stream)>>>(
-        block_tables, batch, max_blocks, cache->block_size, cache->num_blocks, seq_ids, positions,
-        num_tokens, slot_mapping, status);
-    return cuda_status(cudaGetLastError());
+    return launch_pdl(slot_mapping_kernel, dim3(grid_for(num_tokens, threads)), dim3(threads), 0,
+                      reinterpret_cast<cudaStream_t>(stream), block_tables, batch, max_blocks,
+                      cache->block_size, cache->num_blocks, seq_ids, positions, num_tokens,
+                      slot_mapping, status);
 }
 
 extern "C" int pkv_kv_append(const pkv_cache_desc *cache, void *k_pool, void *v_pool,
@@ -249,13 +256,12 @@ extern "C" int pkv_kv_append(const pkv_cache_desc *cache, void *k_pool, void *v_
     const int32_t vk = cache->head_dim_k / 8, vv = cache->head_dim_v / 8;  // 16-byte vectors
     const int64_t work = num_tokens * cache->num_kv_heads * (vk + vv);
     const int threads = 256;
-    kv_append_kernel<<<grid_for(work, threads), threads, 0,
-                       reinterpret_cast<cudaStream_t>(stream)>>>(
-        static_cast<uint4 *>(k_pool), static_cast<uint4 *>(v_pool),
-        static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), slot_mapping,
-        num_tokens, cache->num_kv_heads, cache->block_size,
-        int64_t(cache->num_blocks) * cache->block_size, vk, vv, status);
-    return cuda_status(cudaGetLastError());
+    return launch_pdl(kv_append_kernel, dim3(grid_for(work, threads)), dim3(threads), 0,
+                      reinterpret_cast<cudaStream_t>(stream), static_cast<uint4 *>(k_pool),
+                      static_cast<uint4 *>(v_pool), static_cast<const uint4 *>(k_new),
+                      static_cast<const uint4 *>(v_new), slot_mapping, num_tokens,
+                      cache->num_kv_heads, cache->block_size,
+                      int64_t(cache->num_blocks) * cache->block_size, vk, vv, status);
 }
 
 extern "C" int pkv_copy_blocks(const pkv_cache_desc *cache, void *k_pool, void *v_pool,
@@ -275,10 +281,10 @@ extern "C" int pkv_copy_blocks(const pkv_cache_desc *cache, void *k_pool, void *
     int64_t per_pair = (k_vecs + v_vecs + threads - 1) / threads;
     int64_t want = std::max<int64_t>(1, (int64_t(sm_count()) * 4 + num_pairs - 1) / num_pairs);
     dim3 grid(num_pairs, static_cast<unsigned>(std::min<int64_t>({per_pair, want, 65535})));
-    copy_blocks_kernel<<<grid, threads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        static_cast<uint4 *>(k_pool), static_cast<uint4 *>(v_pool), src, dst, num_pairs,
-        cache->num_blocks, k_vecs, v_vecs, status);
-    return cuda_status(cudaGetLastError());
+    return launch_pdl(copy_blocks_kernel, grid, dim3(threads), 0,
+                      reinterpret_cast<cudaStream_t>(stream), static_cast<uint4 *>(k_pool),
+                      static_cast<uint4 *>(v_pool), src, dst, num_pairs, cache->num_blocks, k_vecs,
+                      v_vecs, status);
 }
 
 extern "C" int64_t pkv_interleave_partition_len(int64_t num_tokens, int32_t num_parts,
@@ -305,9 +311,8 @@ extern "C" int pkv_interleave_slot_mapping(const pkv_cache_desc *cache, int64_t 
     uint32_t *status = status_word();
     if (!status) return PKV_ERR_CUDA;
     const int threads = 256;
-    interleave_slots_kernel<<<grid_for(num_tokens, threads), threads, 0,
-                              reinterpret_cast<cudaStream_t>(stream)>>>(
-        first_token, num_tokens, num_parts, interleave, cache->block_size, cache->num_blocks,
-        part_block_tables, max_blocks, slot_mapping, part_of_token, status);
-    return cuda_status(cudaGetLastError());
+    return launch_pdl(interleave_slots_kernel, dim3(grid_for(num_tokens, threads)), dim3(threads),
+                      0, reinterpret_cast<cudaStream_t>(stream), first_token, num_tokens,
+                      num_parts, interleave, cache->block_size, cache->num_blocks,
+                      part_block_tables, max_blocks, slot_mapping, part_of_token, status);
 }

@@ -7,6 +7,7 @@
 // accumulator) runs in base 2 with the query pre-multiplied by scale*log2(e).
 // It handles any head dims (multiples of 8 up to 1024), any query group and
 // any block size; the TMA + tensor-core kernel covers the common GQA shapes.
+// The LSE merge kernel lives here too.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -39,6 +40,8 @@ __device__ __forceinline__ void unpack8(const uint4 &u, float (&f)[8]) {
 template <int KC, int VC>
 __global__ void __launch_bounds__(kGenericWarps * 32)
 decode_generic_kernel(DecodeArgs a) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int h = blockIdx.y * kGenericWarps + (threadIdx.x >> 5);
     const int b = blockIdx.z;
@@ -127,49 +130,70 @@ decode_generic_kernel(DecodeArgs a) {
     if (lane == 0) a.lse_part[orow] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
 }
 
-// One warp per row: pass 1 finds the largest partial LSE, pass 2 sums the
-// weights e^(lse_p - M) and the weighted partial outputs.
+// Dv/4 threads per row, one float4 of the output each.  The partials are
+// taken 16 at a time: all 16 LSEs and output float4s of a chunk are loaded
+// at once (independent loads, one memory round trip), then folded into a
+// running (max, weight sum, weighted sum) that is rescaled whenever the max
+// grows -- the same exact merge, in chunks.
 __global__ void lse_merge_kernel(int32_t num_parts, const float *__restrict__ out_part,
                                  const float *__restrict__ lse_part, int64_t rows,
                                  int32_t head_dim_v, float *__restrict__ out,
                                  float *__restrict__ lse) {
-    const int lane = threadIdx.x & 31;
-    const int64_t r = blockIdx.x * int64_t(blockDim.x / 32) + (threadIdx.x >> 5);
+    pdl_wait();
+    pdl_launch_dependents();
+    const int tpr = head_dim_v / 4;
+    const int64_t r = blockIdx.x * int64_t(blockDim.x / tpr) + threadIdx.x / tpr;
+    const int c = threadIdx.x % tpr;
     if (r >= rows) return;
-    float M = -INFINITY;
-    for (int p = lane; p < num_parts; p += 32) M = fmaxf(M, lse_part[int64_t(p) * rows + r]);
+    const float4 *op = reinterpret_cast<const float4 *>(out_part + r * head_dim_v) + c;
+    const int64_t pstride = rows * tpr;   // float4s between consecutive partials
+    float M = -INFINITY, W = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int p0 = 0; p0 < num_parts; p0 += 16) {
+        float l[16];
+        float4 x[16];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    const int nv4 = head_dim_v / 4;
+        for (int u = 0; u < 16; ++u) {
+            const bool in = p0 + u < num_parts;
+            l[u] = in ? lse_part[int64_t(p0 + u) * rows + r] : -INFINITY;
+            x[u] = in ? op[int64_t(p0 + u) * pstride] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        float mc = M;
+#pragma unroll
+        for (int u = 0; u < 16; ++u) mc = fmaxf(mc, l[u]);
+        if (mc == -INFINITY) continue;               // every partial so far is empty
+        const float rescale = expf(M - mc);          // 0 when M = -inf
+        W *= rescale;
+        acc = make_float4(acc.x * rescale, acc.y * rescale, acc.z * rescale, acc.w * rescale);
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            const float w = expf(l[u] - mc);
+            // An empty partial has w = 0 and out = 0; skip it so stray values
+            // in an empty partial's output cannot reach the sum.
+            if (w != 0.f) {
+                W += w;
+                acc.x = fmaf(w, x[u].x, acc.x); acc.y = fmaf(w, x[u].y, acc.y);
+                acc.z = fmaf(w, x[u].z, acc.z); acc.w = fmaf(w, x[u].w, acc.w);
+            }
+        }
+        M = mc;
+    }
     float4 *orow = reinterpret_cast<float4 *>(out + r * head_dim_v);
     if (M == -INFINITY) {
-        for (int v = lane; v < nv4; v += 32) orow[v] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (lane == 0) lse[r] = -INFINITY;
+        orow[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (c == 0) lse[r] = -INFINITY;
         return;
     }
-    float W = 0.f;
-    for (int p = 0; p < num_parts; ++p) W += __expf(lse_part[int64_t(p) * rows + r] - M);
     const float inv = 1.f / W;
-    for (int v = lane; v < nv4; v += 32) {
-        float4 accv = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int p = 0; p < num_parts; ++p) {
-            const float w = __expf(lse_part[int64_t(p) * rows + r] - M);
-            if (w == 0.f) continue;
-            const float4 x =
-                reinterpret_cast<const float4 *>(out_part + (int64_t(p) * rows + r) * head_dim_v)[v];
-            accv.x = fmaf(w, x.x, accv.x); accv.y = fmaf(w, x.y, accv.y);
-            accv.z = fmaf(w, x.z, accv.z); accv.w = fmaf(w, x.w, accv.w);
-        }
-        orow[v] = make_float4(accv.x * inv, accv.y * inv, accv.z * inv, accv.w * inv);
-    }
-    if (lane == 0) lse[r] = M + logf(W);
+    orow[c] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    if (c == 0) lse[r] = M + logf(W);
 }
 
 template <int KC, int VC>
 int launch_generic(const DecodeArgs &a) {
     dim3 grid(a.num_splits, (a.num_q_heads + kGenericWarps - 1) / kGenericWarps, a.batch);
-    decode_generic_kernel<KC, VC><<<grid, kGenericWarps * 32, 0, a.stream>>>(a);
-    return cuda_status(cudaGetLastError());
+    return launch_pdl(decode_generic_kernel<KC, VC>, grid, dim3(kGenericWarps * 32), 0, a.stream,
+                      a);
 }
 
 }  // namespace
@@ -186,11 +210,14 @@ int launch_decode_generic(const DecodeArgs &a) {
 int launch_lse_merge(int32_t num_parts, const float *out_part, const float *lse_part,
                      int64_t rows, int32_t head_dim_v, float *out, float *lse,
                      cudaStream_t stream) {
-    const int warps = 8;
-    const int64_t blocks = (rows + warps - 1) / warps;
-    lse_merge_kernel<<<static_cast<unsigned>(blocks), warps * 32, 0, stream>>>(
-        num_parts, out_part, lse_part, rows, head_dim_v, out, lse);
-    return cuda_status(cudaGetLastError());
+    // Two rows per CTA for Dv = 128 (64 threads): enough CTAs to spread even
+    // a few hundred rows over the SMs.
+    const int tpr = head_dim_v / 4;
+    const int rows_per_cta = tpr >= 64 ? 1 : 64 / tpr;
+    const int64_t blocks = (rows + rows_per_cta - 1) / rows_per_cta;
+    return launch_pdl(lse_merge_kernel, dim3(static_cast<unsigned>(blocks)),
+                      dim3(rows_per_cta * tpr), 0, stream, num_parts, out_part, lse_part, rows,
+                      head_dim_v, out, lse);
 }
 
 }  // namespace pkv

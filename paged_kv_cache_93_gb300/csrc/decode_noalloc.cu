@@ -15,7 +15,7 @@
 // share it, so calls that overlap on the GPU (different streams, or graphs
 // replayed concurrently) race on it; calls on one stream are ordered and safe.
 // Nothing in it needs to start at zero: the split kernel writes every partial
-// row (empty chunks included) before the merge reads them.
+// row (empty chunks included) before the merge reads it.
 #include <cuda_runtime.h>
 
 #include <atomic>

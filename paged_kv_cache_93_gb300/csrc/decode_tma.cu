@@ -166,6 +166,10 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmap_k,
         fence_mbar_init();
     }
     __syncthreads();
+    // Everything above overlaps the previous kernel's tail; inputs are read
+    // only after it has finished.
+    pdl_launch_dependents();
+    pdl_wait();
 
     if (warp == W) {
         // ------------------------------------------------------------ producer
@@ -579,8 +583,7 @@ int launch(const DecodeArgs &a) {
     const int64_t items = int64_t(a.batch) * a.cache.num_kv_heads * a.num_splits;
     const int grid = int(std::min<int64_t>(items, int64_t(sm_count()) * per_sm));
     if (grid <= 0) return PKV_OK;
-    kernel<<<grid, C::kThreads, C::kSmemBytes, a.stream>>>(tk, tv, a);
-    return cuda_status(cudaGetLastError());
+    return launch_pdl(kernel, dim3(grid), dim3(C::kThreads), C::kSmemBytes, a.stream, tk, tv, a);
 }
 
 // Launch shapes: consumer warps (W), stages (S), CTAs per SM (B).

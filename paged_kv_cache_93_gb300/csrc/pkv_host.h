@@ -21,6 +21,25 @@ inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA; }
 
+// Launch with programmatic stream serialization, so the kernel may be
+// scheduled while the previous kernel in the stream drains; every libpkv
+// kernel calls pdl_wait() before it reads anything that kernel may write.
+template <typename... Params, typename... Args>
+int launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+               Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cuda_status(cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...));
+}
+
 // Launch the per-split decode kernels.  Arguments are already validated;
 // `out_part`/`lse_part` are [S][B][Hq][Dv] / [S][B][Hq].
 struct DecodeArgs {

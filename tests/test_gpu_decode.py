@@ -184,3 +184,23 @@ def test_scale_is_applied(pkv):
     out, lse, *_ = gpu_step(pkv, w, num_splits=2)
     ro, rl, *_ = oracle_step(w)
     assert_attention_close(out.cpu().numpy(), lse.cpu().numpy(), ro, rl, "scale")
+
+
+def test_workspace_reused_across_calls(pkv):
+    """One workspace, filled with garbage first, serves many calls, shapes and
+    split counts in a row: each call clears the completion counters it uses."""
+    big = workloads.custom(41, [300, 90, 1000, 0, 17, 64], 32, 8, 128, 128, 16)
+    small = workloads.custom(42, [40, 700], 16, 2, 128, 128, 32)
+    need = max(pkv.decode_workspace_size(6, 32, 128, 7), pkv.decode_workspace_size(2, 16, 128, 5))
+    ws = torch.randint(0, 255, (need,), dtype=torch.uint8, device="cuda")
+    for w, splits in [(big, 7), (small, 5), (big, 3), (small, 5), (big, 7)]:
+        ro, rl, *_ = oracle_step(w)
+        k, v = w.k_pool.cuda(), w.v_pool.cuda()
+        slots = pkv.slot_mapping(k, v, w.block_tables.cuda(), w.new_seq.cuda(), w.new_pos.cuda())
+        pkv.kv_append(k, v, w.k_new.cuda(), w.v_new.cuda(), slots)
+        out, lse = pkv.paged_decode_attn(w.q.cuda(), k, v, w.block_tables.cuda(),
+                                         w.seq_lens.cuda(), w.scale, num_splits=splits,
+                                         workspace=ws)
+        torch.cuda.synchronize()
+        assert_attention_close(out.cpu().numpy(), lse.cpu().numpy(), ro, rl, f"reuse {splits}")
+    assert pkv.device_status() == 0
