@@ -219,9 +219,13 @@ class Step:
         """What pkv_paged_decode_attn launches: the split kernel, then the merge
         (events, if given, bracket the split kernel)."""
         if self.splits == 1 or ev_a is None:
+            if ev_a is not None:
+                ev_a.record()
             self.pkv.paged_decode_attn(self.q, self.k, self.v, self.bt, self.lens, self.w.scale,
                                        num_splits=self.splits, workspace=self.ws, out=self.out,
                                        lse=self.lse)
+            if ev_b is not None:
+                ev_b.record()
             return
         ev_a.record()
         self.kernel()
@@ -321,7 +325,7 @@ class AgentStep(Step):
 
 
 STEPS = {"long32k": Step, "mix": Step, "tiny": Step, "dcp200k": DcpStep, "agent_mla": AgentStep}
-DEFAULT_SPLITS = {"long32k": 16, "mix": 4, "tiny": 1, "dcp200k": 19, "agent_mla": 8}
+DEFAULT_SPLITS = {"long32k": 16, "mix": 1, "tiny": 1, "dcp200k": 19, "agent_mla": 8}
 
 
 # ------------------------------------------------------------------ arms

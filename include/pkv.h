@@ -175,10 +175,13 @@ int64_t pkv_interleave_partition_len(int64_t num_tokens, int32_t num_parts,
  * (0 when S == 1; `workspace` may then be NULL).  Its contents on entry do
  * not matter.
  *
- * flags: 0 = choose the kernel by shape (the TMA + tensor-core kernel for
- * head_dim_k == head_dim_v in {64, 128}, query groups of 1, 2, 4 or 8 and
- * power-of-two block sizes >= 8; the generic CUDA-core kernel otherwise);
- * PKV_DECODE_GENERIC forces the generic kernel.
+ * flags: 0 = choose the kernel by shape: the TMA + tensor-core GQA kernel
+ * for head_dim_k == head_dim_v in {64, 128}, query groups of 1, 2, 4 or 8
+ * and power-of-two block sizes >= 8; the TMA + tensor-core large-group
+ * kernel for query groups that are a multiple of 32 (MLA-shaped, e.g. 128
+ * heads over one 576/512 latent head; head dims multiples of 64, head_dim_v
+ * <= 512, power-of-two block sizes >= 32); the generic CUDA-core kernel
+ * otherwise.  PKV_DECODE_GENERIC forces the generic kernel.
  * ------------------------------------------------------------------------- */
 #define PKV_DECODE_GENERIC 0x1
 

@@ -34,18 +34,24 @@ int validate_decode(const pkv_cache_desc *c, const float *q, int32_t batch, int3
     return PKV_OK;
 }
 
-int32_t auto_splits(const pkv_cache_desc &c, int32_t batch, int32_t max_seq_len) {
-    // Enough (sequence, KV head, split) items for ~4 per SM, each item at
-    // least 512 tokens long.
-    const int64_t units = std::max<int64_t>(1, int64_t(batch) * c.num_kv_heads);
+int32_t auto_splits(const pkv_cache_desc &c, int32_t batch, int32_t num_q_heads,
+                    int32_t max_seq_len) {
+    // Enough (sequence, KV head [, head block], split) items for ~4 per SM,
+    // each item at least 512 tokens long.
+    const int64_t units = std::max<int64_t>(
+        1, mla_kernel_supports(c, num_q_heads) && !tma_kernel_supports(c, num_q_heads)
+               ? int64_t(mla_work_units(c, batch, num_q_heads))
+               : int64_t(batch) * c.num_kv_heads);
     const int64_t want = (int64_t(sm_count()) * 4 + units - 1) / units;
     const int64_t cap = std::max<int64_t>(1, (int64_t(max_seq_len) + 511) / 512);
     return int32_t(std::max<int64_t>(1, std::min<int64_t>({want, cap, kMaxSplits})));
 }
 
 int run_split_kernel(const DecodeArgs &a, int32_t flags) {
-    if (!(flags & PKV_DECODE_GENERIC) && tma_kernel_supports(a.cache, a.num_q_heads))
-        return launch_decode_tma(a);
+    if (!(flags & PKV_DECODE_GENERIC)) {
+        if (tma_kernel_supports(a.cache, a.num_q_heads)) return launch_decode_tma(a);
+        if (mla_kernel_supports(a.cache, a.num_q_heads)) return launch_decode_mla(a);
+    }
     return launch_decode_generic(a);
 }
 
@@ -62,9 +68,8 @@ extern "C" size_t pkv_decode_workspace_size(int32_t batch, int32_t num_q_heads,
 
 extern "C" int32_t pkv_decode_auto_splits(const pkv_cache_desc *cache, int32_t batch,
                                           int32_t num_q_heads, int32_t max_seq_len) {
-    (void)num_q_heads;
-    if (!cache || cache->num_kv_heads <= 0) return 1;
-    return auto_splits(*cache, batch, max_seq_len);
+    if (!cache || cache->num_kv_heads <= 0 || num_q_heads <= 0) return 1;
+    return auto_splits(*cache, batch, num_q_heads, max_seq_len);
 }
 
 extern "C" int pkv_paged_decode_attn_partial(const pkv_cache_desc *cache, const float *q,
@@ -103,8 +108,9 @@ extern "C" int pkv_paged_decode_attn(const pkv_cache_desc *cache, const float *q
     int32_t S = num_splits;
     if (S == 0) {
         // Without a host copy of seq_lens, size the splits by the table width.
-        S = auto_splits(*cache, batch, int32_t(std::min<int64_t>(
-                                           int64_t(max_blocks) * cache->block_size, INT32_MAX)));
+        S = auto_splits(*cache, batch, num_q_heads,
+                        int32_t(std::min<int64_t>(int64_t(max_blocks) * cache->block_size,
+                                                  INT32_MAX)));
     }
     const size_t need = pkv_decode_workspace_size(batch, num_q_heads, cache->head_dim_v, S);
     if (S > 1 && (!workspace || workspace_bytes < need)) return PKV_ERR_WORKSPACE_TOO_SMALL;

@@ -597,13 +597,13 @@ int launch(const DecodeArgs &a) {
 #define PKV_TMA_D128_B 4
 #endif
 #ifndef PKV_TMA_D128G8_W
-#define PKV_TMA_D128G8_W 8
+#define PKV_TMA_D128G8_W 2
 #endif
 #ifndef PKV_TMA_D128G8_S
 #define PKV_TMA_D128G8_S 2
 #endif
 #ifndef PKV_TMA_D128G8_B
-#define PKV_TMA_D128G8_B 1
+#define PKV_TMA_D128G8_B 4
 #endif
 #ifndef PKV_TMA_D64_W
 #define PKV_TMA_D64_W 2
@@ -630,10 +630,10 @@ bool tma_kernel_supports(const pkv_cache_desc &c, int32_t num_q_heads) {
 }
 
 // Launch shapes (consumer warps, stages, CTAs per SM), measured on 8 x 32K
-// GQA decode: with G <= 4, two consumer warps per CTA (32-token stages) and
-// four CTAs per SM keep more independent warps streaming than one large CTA
-// does; with G = 8 the consumers do twice the work per byte and one CTA of
-// eight consumer warps (128-token stages) is fastest.
+// GQA decode: two consumer warps per CTA (32-token stages) and four CTAs per
+// SM keep more independent warps streaming than one large CTA does (G <= 4:
+// three stages; G = 8, whose registers leave room for only two stages at
+// four CTAs per SM: two).
 int launch_decode_tma(const DecodeArgs &a) {
     const int G = a.num_q_heads / a.cache.num_kv_heads;
     if (a.cache.head_dim_k == 128) {

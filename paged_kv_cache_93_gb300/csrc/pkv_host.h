@@ -58,6 +58,11 @@ struct DecodeArgs {
 };
 bool tma_kernel_supports(const pkv_cache_desc &c, int32_t num_q_heads);
 int launch_decode_tma(const DecodeArgs &a);
+// Large query groups (G a multiple of 32, e.g. MLA-shaped 128 heads over one
+// 576/512 latent head): tensor-core kernel with 32-head work items.
+bool mla_kernel_supports(const pkv_cache_desc &c, int32_t num_q_heads);
+int32_t mla_work_units(const pkv_cache_desc &c, int32_t batch, int32_t num_q_heads);
+int launch_decode_mla(const DecodeArgs &a);
 int launch_decode_generic(const DecodeArgs &a);
 int launch_lse_merge(int32_t num_parts, const float *out_part, const float *lse_part,
                      int64_t rows, int32_t head_dim_v, float *out, float *lse,

@@ -204,3 +204,55 @@ def test_workspace_reused_across_calls(pkv):
         torch.cuda.synchronize()
         assert_attention_close(out.cpu().numpy(), lse.cpu().numpy(), ro, rl, f"reuse {splits}")
     assert pkv.device_status() == 0
+
+
+# Large query groups (multiples of 32) run on the MLA-shaped tensor-core
+# kernel: (cached lengths, Hq, Hkv, Dk, Dv, block size).
+MLA_SHAPES = [
+    ([70, 3, 200], 32, 1, 576, 512, 64),
+    ([130, 1], 128, 1, 576, 512, 64),
+    ([300, 45], 64, 2, 128, 128, 32),
+    ([513, 0, 31], 64, 1, 192, 256, 128),
+    ([1000], 32, 1, 64, 64, 256),
+]
+
+
+@pytest.mark.parametrize("shape", MLA_SHAPES,
+                         ids=lambda s: f"G{s[1]//s[2]}_Dk{s[3]}_Dv{s[4]}_bs{s[5]}")
+@pytest.mark.parametrize("splits", [1, 3, 0])
+def test_large_group_kernel(pkv, shape, splits):
+    cached, hq, hkv, dk, dv, bs = shape
+    w = workloads.custom(200 + dk + bs, cached, hq, hkv, dk, dv, bs)
+    out, lse, *_ = gpu_step(pkv, w, num_splits=splits)
+    ro, rl, *_ = oracle_step(w)
+    assert_attention_close(out.cpu().numpy(), lse.cpu().numpy(), ro, rl, f"{shape}/{splits}")
+    assert pkv.device_status() == 0
+
+
+def test_large_group_partials_and_nan_tail(pkv):
+    """Per-split partials of the large-group kernel against the oracle's token
+    ranges, with NaN bits in the unused slots of each last block."""
+    w = workloads.custom(77, [150, 9], 64, 1, 576, 512, 64, extra_blocks=0)
+    k, v = w.k_pool.clone(), w.v_pool.clone()
+    for b in range(2):
+        L = int(w.seq_lens[b])
+        last = int(w.block_tables[b, (L - 1) // 64])
+        k[last, :, L % 64 or 64:] = float("nan")
+        v[last, :, L % 64 or 64:] = float("nan")
+    w.k_pool, w.v_pool = k, v
+    S = 3
+    dev = "cuda"
+    op, lp = pkv.paged_decode_attn_partial(w.q.to(dev), w.k_pool.to(dev), w.v_pool.to(dev),
+                                           w.block_tables.to(dev), w.seq_lens.to(dev), w.scale, S)
+    torch.cuda.synchronize()
+    assert torch.isfinite(op).all()
+    kb, vb = bits(w.k_pool), bits(w.v_pool)
+    L = w.seq_lens.numpy().astype(np.int64)
+    C = 64 * (-(-L // (64 * S)))
+    for s in range(S):
+        begin = np.minimum(s * C, L).astype(np.int32)
+        end = np.minimum((s + 1) * C, L).astype(np.int32)
+        ro, rl = oracle.paged_decode_attn(w.q.numpy(), kb, vb, w.block_tables.numpy(), L,
+                                          w.scale, tok_begin=begin, tok_end=end)
+        assert_attention_close(op[s].cpu().numpy(), lp[s].cpu().numpy(), ro, rl, f"split {s}")
+    assert pkv.device_status() == 0
