@@ -43,6 +43,7 @@ import workloads  # noqa: E402
 
 METRIC = "paged decode-attn HBM GB/s (% of GB300 peak), seq-tokens/s at 32K ctx GQA"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
 PROFILE = os.path.join(ROOT, "profiles", "decode_tma_long32k.txt")
 KERNEL_SOURCES = [os.path.join(ROOT, "paged_kv_cache_93_gb300", "csrc", f)
                   for f in ("decode_tma.cu", "pkv_device.cuh")]
@@ -82,13 +83,20 @@ def step_bytes(w, splits: int):
     return kv + q + tables + out + append, kernel
 
 
-def load_peak():
+def load_peak(key="hbm_gbs", fallback=None):
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
-            return float(json.load(f)["hbm_gbs"]), "measured"
+            return float(json.load(f)[key]), "measured"
     except Exception:
-        return FALLBACK_HBM_GBS, "fallback"
+        return (FALLBACK_HBM_GBS if fallback is None else fallback), "fallback"
+
+
+def kernel_flops(w):
+    """Algorithmic flops of one split-kernel launch: every (token, query head)
+    pair costs a Dk-long and a Dv-long multiply-add chain."""
+    return int(w.seq_lens.to(torch.int64).sum()) * w.num_q_heads * \
+        (w.head_dim_k + w.head_dim_v) * 2
 
 
 def stored_traffic():
@@ -298,7 +306,8 @@ class AgentStep(Step):
     """Shared-prefix MLA-shaped step: copy-on-write of each sequence's shared
     tail, append of the decode tokens, attention (the suffixes are appended
     once, before timing)."""
-    kernel_name = "decode_generic_kernel (split attention, CUDA cores)"
+    kernel_name = "decode_mla_tc_kernel (split attention, tcgen05 + TMEM)"
+    bound = "tensor"
 
     def __init__(self, pkv, w, dev, splits):
         super().__init__(pkv, w, dev, splits)
@@ -489,6 +498,23 @@ def run_gpu(args, world, rank, local):
     value = world * total_bytes / (ms * 1e-3) / 1e9
     peak, peak_kind = load_peak()
     kernel_gbs = kernel_bytes / (kms * 1e-3) / 1e9
+    if getattr(st, "bound", "hbm") == "tensor":
+        # a math-bound launch inside seconds of back-to-back steps: the
+        # sustained bf16 tensor throughput is the denominator
+        tpeak, tkind = load_peak("bf16_tflops_sustained", FALLBACK_BF16_TFLOPS_SUSTAINED)
+        flops = kernel_flops(w)
+        tflops = flops / (kms * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "achieved": round(tflops, 2), "peak": tpeak,
+                    "unit": "TFLOP/s", "frac": round(tflops / tpeak, 4), "traffic": None,
+                    "algorithmic_flops_per_launch": flops,
+                    "hbm_gbs_on_unique_bytes": round(kernel_gbs, 2),
+                    "peak_kind": f"{tkind} bf16_tflops_sustained (MEASURED_PEAKS.json cuBLAS "
+                                 f"bf16 GEMM, seconds-long loop)"}
+    else:
+        roofline = {"bound": "hbm", "achieved": round(kernel_gbs, 2), "peak": peak,
+                    "unit": "GB/s", "frac": round(kernel_gbs / peak, 4), "traffic": None,
+                    "algorithmic_bytes_per_launch": kernel_bytes,
+                    "peak_kind": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json copy bandwidth)"}
 
     # ---- end to end through the public API, host buffers in pinned memory
     e2e = None
@@ -558,22 +584,14 @@ def run_gpu(args, world, rank, local):
                   f"L2 (steps back to back)",
             "parallelism": "replicas" if world > 1 else "single GPU",
             "compute": "bf16 tensor-core products (fp32 query and probabilities split into bf16 "
-                       "hi+lo), fp32 accumulate and softmax" if st.kernel_name.startswith(
-                           "decode_tma") else "fp32 CUDA-core dot products and softmax",
+                       "hi+lo), fp32 accumulate and softmax",
             "bytes": "unique K/V bytes (shared blocks once) + q + tables + appends + out/lse",
         },
         "pct_of_peak": round(100 * value / world / peak, 2),
         "seq_tokens_per_s": round(world * seq_tokens / (ms * 1e-3), 1),
         "decode_steps_per_s": round(world * 1e3 / ms, 2),
-        "roofline": {
-            "bound": "hbm", "achieved": round(kernel_gbs, 2), "peak": peak,
-            "unit": "GB/s", "frac": round(kernel_gbs / peak, 4), "traffic": traffic,
-            "kernel": st.kernel_name,
-            "algorithmic_bytes_per_launch": kernel_bytes,
-            "launch_ms": round(kms, 5),
-            "launch_ms_back_to_back": round(kms_b2b, 5),
-            "peak_kind": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json copy bandwidth)",
-        },
+        "roofline": dict(roofline, traffic=traffic, kernel=st.kernel_name,
+                         launch_ms=round(kms, 5), launch_ms_back_to_back=round(kms_b2b, 5)),
         "cpu_baseline": {
             "value": round(cpu_gbs, 4), "unit": "GB/s", "cores": os.cpu_count(),
             "kind": "oracle",

@@ -177,13 +177,19 @@ int64_t pkv_interleave_partition_len(int64_t num_tokens, int32_t num_parts,
  *
  * flags: 0 = choose the kernel by shape: the TMA + tensor-core GQA kernel
  * for head_dim_k == head_dim_v in {64, 128}, query groups of 1, 2, 4 or 8
- * and power-of-two block sizes >= 8; the TMA + tensor-core large-group
- * kernel for query groups that are a multiple of 32 (MLA-shaped, e.g. 128
- * heads over one 576/512 latent head; head dims multiples of 64, head_dim_v
- * <= 512, power-of-two block sizes >= 32); the generic CUDA-core kernel
- * otherwise.  PKV_DECODE_GENERIC forces the generic kernel.
+ * and power-of-two block sizes >= 8; for query groups that are a multiple
+ * of 64 (MLA-shaped, e.g. 128 heads over one 576/512 latent head) with
+ * head_dim_k a multiple of 64 up to 576, head_dim_v a multiple of 128 up to
+ * 512 and power-of-two block sizes 64..256, the tcgen05 kernel (5th-
+ * generation tensor cores, accumulators in tensor memory); for other query
+ * groups that are a multiple of 32 (head dims multiples of 64, head_dim_v
+ * <= 512, power-of-two block sizes >= 32) the warp-level-MMA large-group
+ * kernel; the generic CUDA-core kernel otherwise.  PKV_DECODE_GENERIC forces
+ * the generic kernel; PKV_DECODE_NO_TCGEN05 passes over the tcgen05 kernel
+ * (the warp-level-MMA large-group kernel takes its shapes).
  * ------------------------------------------------------------------------- */
 #define PKV_DECODE_GENERIC 0x1
+#define PKV_DECODE_NO_TCGEN05 0x2
 
 size_t pkv_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t head_dim_v,
                                  int32_t num_splits);

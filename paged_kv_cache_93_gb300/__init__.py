@@ -17,14 +17,15 @@ import ctypes
 import torch
 
 from . import _lib
-from ._lib import (DECODE_GENERIC, DEV_BLOCK_ID, DEV_COPY_CONFLICT, DEV_SEQ_LEN, DEV_SLOT,
+from ._lib import (DECODE_GENERIC, DECODE_NO_TCGEN05, DEV_BLOCK_ID, DEV_COPY_CONFLICT, DEV_SEQ_LEN, DEV_SLOT,
                    DEV_TABLE_RANGE, DEV_TIMEOUT, CacheDesc, PkvError)
 
 __all__ = [
     "CacheDesc", "PkvError", "cache_desc", "kv_append", "slot_mapping", "copy_blocks",
     "interleave_slot_mapping", "interleave_partition_len", "decode_workspace_size",
     "decode_auto_splits", "paged_decode_attn", "paged_decode_attn_partial", "lse_merge",
-    "device_status", "BlockManager", "library_path", "DECODE_GENERIC", "DEV_BLOCK_ID",
+    "device_status", "BlockManager", "library_path", "DECODE_GENERIC", "DECODE_NO_TCGEN05",
+    "DEV_BLOCK_ID",
     "DEV_SLOT", "DEV_SEQ_LEN", "DEV_COPY_CONFLICT", "DEV_TIMEOUT", "DEV_TABLE_RANGE",
 ]
 

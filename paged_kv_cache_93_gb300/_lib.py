@@ -24,6 +24,7 @@ DEV_COPY_CONFLICT = 0x8
 DEV_TIMEOUT = 0x10
 DEV_TABLE_RANGE = 0x20
 DECODE_GENERIC = 0x1
+DECODE_NO_TCGEN05 = 0x2
 
 
 class CacheDesc(ctypes.Structure):

@@ -20,7 +20,7 @@ int validate_decode(const pkv_cache_desc *c, const float *q, int32_t batch, int3
                     int32_t max_blocks, const int32_t *seq_lens, int32_t num_splits,
                     int32_t flags) {
     if (!c || batch < 0 || hq <= 0 || max_blocks < 0 || num_splits < 0 ||
-        num_splits > kMaxSplits || (flags & ~PKV_DECODE_GENERIC) != 0)
+        num_splits > kMaxSplits || (flags & ~(PKV_DECODE_GENERIC | PKV_DECODE_NO_TCGEN05)) != 0)
         return PKV_ERR_INVALID_ARG;
     if (c->num_blocks <= 0 || c->block_size < 1 || c->block_size > 256 || c->num_kv_heads <= 0 ||
         c->head_dim_k <= 0 || c->head_dim_v <= 0)
@@ -38,10 +38,14 @@ int32_t auto_splits(const pkv_cache_desc &c, int32_t batch, int32_t num_q_heads,
                     int32_t max_seq_len) {
     // Enough (sequence, KV head [, head block], split) items for ~4 per SM,
     // each item at least 512 tokens long.
-    const int64_t units = std::max<int64_t>(
-        1, mla_kernel_supports(c, num_q_heads) && !tma_kernel_supports(c, num_q_heads)
-               ? int64_t(mla_work_units(c, batch, num_q_heads))
-               : int64_t(batch) * c.num_kv_heads);
+    int64_t units = int64_t(batch) * c.num_kv_heads;
+    if (!tma_kernel_supports(c, num_q_heads)) {
+        if (mla_tc_kernel_supports(c, num_q_heads))
+            units = mla_tc_work_units(c, batch, num_q_heads);
+        else if (mla_kernel_supports(c, num_q_heads))
+            units = mla_work_units(c, batch, num_q_heads);
+    }
+    units = std::max<int64_t>(1, units);
     const int64_t want = (int64_t(sm_count()) * 4 + units - 1) / units;
     const int64_t cap = std::max<int64_t>(1, (int64_t(max_seq_len) + 511) / 512);
     return int32_t(std::max<int64_t>(1, std::min<int64_t>({want, cap, kMaxSplits})));
@@ -50,6 +54,8 @@ int32_t auto_splits(const pkv_cache_desc &c, int32_t batch, int32_t num_q_heads,
 int run_split_kernel(const DecodeArgs &a, int32_t flags) {
     if (!(flags & PKV_DECODE_GENERIC)) {
         if (tma_kernel_supports(a.cache, a.num_q_heads)) return launch_decode_tma(a);
+        if (!(flags & PKV_DECODE_NO_TCGEN05) && mla_tc_kernel_supports(a.cache, a.num_q_heads))
+            return launch_decode_mla_tc(a);
         if (mla_kernel_supports(a.cache, a.num_q_heads)) return launch_decode_mla(a);
     }
     return launch_decode_generic(a);

@@ -1,0 +1,727 @@
+// decode_mla_tc.cu -- paged decode attention for large query groups on the
+// 5th-generation tensor cores of sm_103a (tcgen05 MMAs, fp32 accumulators
+// in tensor memory).  Shape: G >= 64 query heads per KV head, e.g. the
+// MLA-shaped 128 heads over one 576-dim K / 512-dim V latent head.
+//
+// Work item = (sequence b, KV head g, group of 64 query heads, split chunk
+// s), ordered split-major so that items over the same tokens run together
+// and K/V tiles shared by head groups and by sequences with a common prefix
+// come from L2.  One CTA per SM walks its items tile by tile, 128 tokens a
+// tile:
+//   S^T[128 tok x 64 heads] = K_tile . Q^T          (tcgen05, M=128, N=64)
+//   online softmax over the 128 token lanes of S^T    (CUDA cores)
+//   O^T[Dv x 64 heads]     += V_tile^T . P            (tcgen05, M=128, N=64)
+// Tokens are the MMA's M, so the query group is N and 64 heads fit in one
+// CTA's shared memory even with the fp32 query kept exact as bf16 hi + lo
+// (Dk = 576: 147 KB).  S^T (two buffers) and O^T (Dv/128 blocks of 64
+// columns) live in TMEM: 128 + 256 of its 512 columns for Dv = 512.
+//
+// Warp roles (192 threads):
+//   warp 0   TMA producer: K chunks [128 tok x 64 dims] (two 64-row boxes)
+//            and V chunks [64 tok x 128 dims] (one box, two 64-column
+//            segments), 16 KB each, through a ring of 16 KB stages.
+//   warp 1   owns the TMEM allocation; lane 0 issues every MMA and commits
+//            completions to mbarriers.  It zeroes V rows past the end of a
+//            sequence before they meet the tensor core.
+//   warps 2-5  softmax and epilogue, one thread per TMEM lane (token row of
+//            S^T, value row of O^T).  They pre-scale and split the query,
+//            turn scores into probabilities (bf16 hi + lo, written in the
+//            MMA's operand layout), keep per-thread partial sums, and write
+//            the normalised output and LSE.
+// The running max of each head is raised only when a score exceeds it by
+// more than 8 (log2 units); then the tile max is formed across the token
+// lanes and the accumulators are rescaled in TMEM.  Otherwise
+// probabilities up to 2^8 are accumulated as they are -- exact in real
+// arithmetic for any choice of the running max.
+//
+// Every wait is bounded (PKV_DEV_TIMEOUT) and all roles leave their loops
+// together on an abort; out-of-range blocks and lengths are flagged in the
+// status word, never dereferenced.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "pkv.h"
+#include "pkv_device.cuh"
+#include "pkv_host.h"
+#include "pkv_tcgen05.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kN = 64;                  // query heads per work item (MMA N)
+constexpr int kM = 128;                 // tokens per tile (MMA M of the score product)
+constexpr int kHalf = 64;               // tokens per TMA box
+constexpr int kChunk = 16384;           // bytes per ring stage
+constexpr int kMaxRing = 8;
+constexpr int kThreads = 192;
+constexpr int kSoftWarp0 = 2;           // warps 2..5: softmax and epilogue
+constexpr int kSoftThreads = 128;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0;           // S^T buffers at columns 0 and 64
+constexpr uint32_t kColO = 128;         // O^T blocks at columns 128 + 64 j
+constexpr float kSlack = 8.f;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr int kSmemLimit = 232448;
+constexpr uint32_t kIdS = tc::idesc_bf16_f32(128, 64, 0, 0);   // K-major K, K-major Q
+constexpr uint32_t kIdO = tc::idesc_bf16_f32(128, 64, 1, 1);   // MN-major V, MN-major P
+
+// mbarrier slots
+constexpr int kBarFull = 0;             // + stage: chunk landed (TMA bytes)
+constexpr int kBarEmpty = 8;            // + stage: chunk consumed (MMA commit)
+constexpr int kBarSFull = 16;           // + buffer: scores ready (MMA commit)
+constexpr int kBarSEmpty = 18;          // + buffer: scores read (128 arrivals)
+constexpr int kBarPFull = 20;           // probabilities written (128 arrivals)
+constexpr int kBarPvDone = 21;          // value MMAs of a tile done (MMA commit)
+constexpr int kBarQFull = 22;           // query written (128 arrivals)
+constexpr int kBarQEmpty = 23;          // score MMAs of an item done (MMA commit)
+constexpr int kBarOEmpty = 24;          // accumulators read out (128 arrivals)
+constexpr int kBarDrain = 25;   // 26 of the 32 slots
+
+struct TcShape {
+    int dk_segs;      // Dk / 64
+    int dv_blocks;    // Dv / 128
+    int ring;         // ring stages
+};
+
+// Shared-memory map, offsets from a 1024-byte-aligned base.
+struct SmemMap {
+    uint32_t q_hi, q_lo, p_hi, p_lo, ring, bars, mrow, aux, red, slot, flag, end;
+};
+__host__ __device__ inline SmemMap smem_map(const TcShape &s) {
+    SmemMap m;
+    m.q_hi = 0;
+    m.q_lo = m.q_hi + uint32_t(s.dk_segs) * 8192;
+    m.p_hi = m.q_lo + uint32_t(s.dk_segs) * 8192;
+    m.p_lo = m.p_hi + kM * 128;
+    m.ring = m.p_lo + kM * 128;
+    m.bars = m.ring + uint32_t(s.ring) * kChunk;
+    m.mrow = m.bars + 32 * 8;
+    m.aux = m.mrow + kN * 4;
+    m.red = m.aux + kN * 4;
+    m.slot = m.red + 4 * kN * 4;
+    m.flag = m.slot + 4;
+    m.end = m.flag + 12;
+    return m;
+}
+inline size_t tc_smem_bytes(const TcShape &s) { return 1024 + size_t(smem_map(s).end); }
+
+__device__ __forceinline__ int64_t lmin(int64_t x, int64_t y) { return x < y ? x : y; }
+
+struct TcItem {
+    int b, g, hg, s;
+    int64_t begin, end;
+    int ntiles;
+};
+
+__device__ __forceinline__ TcItem tc_item(const DecodeArgs &a, int item, int groups,
+                                          bool report) {
+    TcItem r;
+    const int per_split = a.batch * a.cache.num_kv_heads * groups;
+    r.s = item / per_split;
+    int t = item % per_split;
+    r.hg = t % groups;
+    t /= groups;
+    r.g = t % a.cache.num_kv_heads;
+    r.b = t / a.cache.num_kv_heads;
+    int64_t L = a.seq_lens[r.b];
+    if (L < 0 || L > int64_t(a.max_blocks) * a.cache.block_size) {
+        if (report && r.s == 0 && r.hg == 0 && r.g == 0) raise_status(a.status, PKV_DEV_SEQ_LEN);
+        L = 0;
+    }
+    const int64_t chunk = 64 * ((L + 64LL * a.num_splits - 1) / (64LL * a.num_splits));
+    r.begin = int64_t(r.s) * chunk;
+    r.end = lmin(L, r.begin + chunk);
+    r.ntiles = r.end > r.begin ? int((r.end - r.begin + kM - 1) / kM) : 0;
+    return r;
+}
+
+// Bounded wait that also gives up once any role has aborted.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, uint32_t *status,
+                                         volatile int *abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t start = global_timer_ns();
+    for (;;) {
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (global_timer_ns() - start > kWaitLimitNs) {
+            raise_status(status, PKV_DEV_TIMEOUT);
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
+// Named barrier over the softmax warps that also ORs a predicate: every
+// participant gets the same answer.
+__device__ __forceinline__ bool soft_bar_or(bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{ .reg .pred p, q; setp.ne.u32 p, %1, 0; bar.red.or.pred q, 1, 128, p; "
+        "selp.u32 %0, 1, 0, q; }"
+        : "=r"(r) : "r"(uint32_t(pred)) : "memory");
+    return r != 0;
+}
+
+// Offset of bf16 element (row, col < 64) in a [rows][64] 128-byte-swizzled
+// array whose 8-row atoms are 1024-byte aligned.
+__device__ __forceinline__ uint32_t swz(int row, int col) {
+    return uint32_t(row) * 128 + (uint32_t(((col >> 3) ^ row) & 7) << 4) + uint32_t(col & 7) * 2;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                     const __grid_constant__ CUtensorMap tmap_v, const DecodeArgs a,
+                     const TcShape shp) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const SmemMap sm = smem_map(shp);
+    const uint32_t sb = smem_addr(base);
+    float *mrow = reinterpret_cast<float *>(base + sm.mrow);   // running max per head (log2)
+    float *aux = reinterpret_cast<float *>(base + sm.aux);     // rescale factor / 1 / l
+    float *red = reinterpret_cast<float *>(base + sm.red);     // [4 warps][64 heads]
+    volatile uint32_t *tslot = reinterpret_cast<volatile uint32_t *>(base + sm.slot);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(base + sm.flag);
+    auto bar = [&](int i) { return sb + sm.bars + 8u * uint32_t(i); };
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = a.num_q_heads / a.cache.num_kv_heads;
+    const int groups = G / kN;
+    const int num_items = a.batch * a.cache.num_kv_heads * groups * a.num_splits;
+    const int bs = a.cache.block_size, hkv = a.cache.num_kv_heads;
+    const int Dk = shp.dk_segs * 64, Dv = shp.dv_blocks * 128;
+
+    if (threadIdx.x == 0) {
+        for (int r = 0; r < shp.ring; ++r) {
+            mbar_init(bar(kBarFull + r), 1);
+            mbar_init(bar(kBarEmpty + r), 1);
+        }
+        mbar_init(bar(kBarSFull), 1);
+        mbar_init(bar(kBarSFull + 1), 1);
+        mbar_init(bar(kBarSEmpty), kSoftThreads);
+        mbar_init(bar(kBarSEmpty + 1), kSoftThreads);
+        mbar_init(bar(kBarPFull), kSoftThreads);
+        mbar_init(bar(kBarPvDone), 1);
+        mbar_init(bar(kBarQFull), kSoftThreads);
+        mbar_init(bar(kBarQEmpty), 1);
+        mbar_init(bar(kBarOEmpty), kSoftThreads);
+        mbar_init(bar(kBarDrain), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tc::alloc(sb + sm.slot, kTmemCols);
+        tc::fence_before_sync();
+    }
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tslot;
+    pdl_launch_dependents();
+    pdl_wait();
+
+    if (warp == 0) {
+        // -------------------------------------------------------- producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tmap_k);
+            tma_prefetch_desc(&tmap_v);
+        }
+        int stage = 0;
+        uint32_t phase = 0, armed = 0, armed_parity = 0;
+        bool ok = true;
+        // Wait for a free stage and arm it for one chunk; false on abort.
+        auto acquire = [&](uint32_t &dst) -> bool {
+            const bool w = wait_bar(bar(kBarEmpty + stage), phase ^ 1u, a.status, abort_flag);
+            if (!__all_sync(0xffffffffu, w)) return false;
+            if (lane == 0) mbar_arrive_expect_tx(bar(kBarFull + stage), kChunk);
+            armed |= 1u << stage;
+            armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+            dst = sb + sm.ring + uint32_t(stage) * kChunk;
+            return true;
+        };
+        auto advance = [&]() {
+            if (++stage == shp.ring) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        };
+        for (int item = blockIdx.x; item < num_items && ok; item += gridDim.x) {
+            const TcItem r = tc_item(a, item, groups, false);
+            if (r.ntiles == 0) continue;
+            const int32_t *table = a.block_tables + int64_t(r.b) * a.max_blocks;
+            // Rows of block 0 of this KV head stand in for a half tile past
+            // the end (its values are masked and its V rows zeroed).
+            const int32_t standin = r.g * bs;
+            int32_t yp0 = standin, yp1 = standin;
+            for (int i = 0; i <= r.ntiles && ok; ++i) {
+                int32_t y0 = standin, y1 = standin;
+                if (i < r.ntiles) {
+                    int32_t y = standin;
+                    if (lane < 2) {
+                        const int64_t t = r.begin + int64_t(i) * kM + lane * kHalf;
+                        if (t < r.end) {
+                            const int32_t phys = table[t / bs];
+                            if (phys >= 0 && phys < a.cache.num_blocks)
+                                y = (phys * hkv + r.g) * bs + int32_t(t % bs);
+                            else
+                                raise_status(a.status, PKV_DEV_BLOCK_ID);
+                        }
+                    }
+                    y0 = __shfl_sync(0xffffffffu, y, 0);
+                    y1 = __shfl_sync(0xffffffffu, y, 1);
+                    for (int seg = 0; seg < shp.dk_segs; ++seg) {
+                        uint32_t dst;
+                        if (!acquire(dst)) {
+                            ok = false;
+                            break;
+                        }
+                        if (lane == 0) {
+                            tma_load_3d(dst, &tmap_k, 0, y0, seg, bar(kBarFull + stage));
+                            tma_load_3d(dst + 8192, &tmap_k, 0, y1, seg, bar(kBarFull + stage));
+                        }
+                        advance();
+                    }
+                }
+                if (i > 0 && ok) {
+                    for (int vb = 0; vb < shp.dv_blocks && ok; ++vb)
+                        for (int h = 0; h < 2; ++h) {
+                            uint32_t dst;
+                            if (!acquire(dst)) {
+                                ok = false;
+                                break;
+                            }
+                            if (lane == 0)
+                                tma_load_3d(dst, &tmap_v, 0, h ? yp1 : yp0, 2 * vb,
+                                            bar(kBarFull + stage));
+                            advance();
+                        }
+                }
+                yp0 = y0;
+                yp1 = y1;
+            }
+        }
+        // Leave no copy in flight into this CTA's shared memory.
+        if (lane == 0)
+            for (int s = 0; s < shp.ring; ++s)
+                if (armed & (1u << s))
+                    mbar_wait(bar(kBarFull + s), (armed_parity >> s) & 1u, a.status);
+        __syncwarp();
+    } else if (warp == 1) {
+        // -------------------------------------------------------- MMA issuer
+        int stage = 0;
+        uint32_t phase = 0, tcount = 0, pcount = 0, ne = 0;
+        bool ok = true;
+        const uint32_t qh = sb + sm.q_hi, ql = sb + sm.q_lo;
+        const uint32_t ph = sb + sm.p_hi, pl = sb + sm.p_lo;
+        auto wait_all = [&](uint32_t b, uint32_t parity) {
+            return __all_sync(0xffffffffu, wait_bar(b, parity, a.status, abort_flag));
+        };
+        auto advance = [&]() {
+            if (++stage == shp.ring) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        };
+        for (int item = blockIdx.x; item < num_items && ok; item += gridDim.x) {
+            const TcItem r = tc_item(a, item, groups, false);
+            if (r.ntiles == 0) continue;
+            if (!(ok = wait_all(bar(kBarQFull), ne & 1u))) break;
+            for (int i = 0; i <= r.ntiles && ok; ++i) {
+                if (i < r.ntiles) {
+                    // ---- S^T[buf] = K_tile . (Q_hi + Q_lo)^T
+                    const uint32_t buf = tcount & 1u;
+                    if (!(ok = wait_all(bar(kBarSEmpty + buf), ((tcount >> 1) & 1u) ^ 1u))) break;
+                    const uint32_t d = tmem + kColS + 64 * buf;
+                    for (int seg = 0; seg < shp.dk_segs; ++seg) {
+                        if (!(ok = wait_all(bar(kBarFull + stage), phase))) break;
+                        tc::fence_after_sync();
+                        if (lane == 0) {
+                            const uint32_t kb = sb + sm.ring + uint32_t(stage) * kChunk;
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk) {
+                                const uint64_t ad = tc::smem_desc(kb + 32 * kk, 16, 1024);
+                                const uint32_t qo = uint32_t(seg) * 8192 + 32 * kk;
+                                tc::mma_bf16(d, ad, tc::smem_desc(qh + qo, 16, 1024), kIdS,
+                                             (seg | kk) != 0);
+                                tc::mma_bf16(d, ad, tc::smem_desc(ql + qo, 16, 1024), kIdS, 1);
+                            }
+                            tc::commit(bar(kBarEmpty + stage));
+                        }
+                        __syncwarp();
+                        advance();
+                    }
+                    if (!ok) break;
+                    if (lane == 0) {
+                        tc::commit(bar(kBarSFull + buf));
+                        if (i == r.ntiles - 1) tc::commit(bar(kBarQEmpty));
+                    }
+                    __syncwarp();
+                    ++tcount;
+                }
+                if (i > 0) {
+                    // ---- O^T += V_tile^T . (P_hi + P_lo) for tile j
+                    const int j = i - 1;
+                    if (!(ok = wait_all(bar(kBarPFull), pcount & 1u))) break;
+                    if (j == 0 && !(ok = wait_all(bar(kBarOEmpty), (ne & 1u) ^ 1u))) break;
+                    const int64_t tok0 = r.begin + int64_t(j) * kM;
+                    const int nvalid = int(lmin(kM, r.end - tok0));
+                    for (int vb = 0; vb < shp.dv_blocks && ok; ++vb) {
+                        const uint32_t d = tmem + kColO + 64 * uint32_t(vb);
+                        for (int h = 0; h < 2; ++h) {
+                            if (!(ok = wait_all(bar(kBarFull + stage), phase))) break;
+                            const int first_bad = nvalid - h * kHalf;
+                            if (first_bad < kHalf) {
+                                // Value rows past the end may hold any bits
+                                // (NaN times a zero probability is NaN).
+                                uint8_t *vt = base + sm.ring + size_t(stage) * kChunk;
+                                const int r0 = first_bad > 0 ? first_bad : 0;
+                                for (int idx = lane; idx < (kHalf - r0) * 16; idx += 32) {
+                                    const int row = r0 + (idx >> 4), c = idx & 15;
+                                    *reinterpret_cast<uint4 *>(vt + (c >> 3) * 8192 + row * 128 +
+                                                               (c & 7) * 16) =
+                                        make_uint4(0, 0, 0, 0);
+                                }
+                                fence_proxy_async_smem();
+                                __syncwarp();
+                            }
+                            tc::fence_after_sync();
+                            if (lane == 0) {
+                                const uint32_t vbase = sb + sm.ring + uint32_t(stage) * kChunk;
+#pragma unroll
+                                for (int kk = 0; kk < 4; ++kk) {
+                                    const uint64_t ad =
+                                        tc::smem_desc(vbase + 2048 * kk, 8192, 1024);
+                                    const uint32_t po = uint32_t(h * kHalf + 16 * kk) * 128;
+                                    tc::mma_bf16(d, ad, tc::smem_desc(ph + po, 8192, 1024), kIdO,
+                                                 (j | h | kk) != 0);
+                                    tc::mma_bf16(d, ad, tc::smem_desc(pl + po, 8192, 1024), kIdO,
+                                                 1);
+                                }
+                                tc::commit(bar(kBarEmpty + stage));
+                            }
+                            __syncwarp();
+                            advance();
+                        }
+                    }
+                    if (!ok) break;
+                    if (lane == 0) tc::commit(bar(kBarPvDone));
+                    __syncwarp();
+                    ++pcount;
+                }
+            }
+            ++ne;
+        }
+        // Every issued MMA completes before the accumulators are released.
+        if (lane == 0) {
+            tc::commit(bar(kBarDrain));
+            mbar_wait(bar(kBarDrain), 0, a.status);
+        }
+        __syncwarp();
+    } else {
+        // -------------------------------------------- softmax and epilogue
+        const int t = threadIdx.x - kSoftWarp0 * 32;     // 0..127
+        const int quad = warp & 3;                       // TMEM lane quadrant
+        const int row = quad * 32 + lane;                // token row / value row
+        const uint32_t tl = tmem + (uint32_t(quad * 32) << 16);
+        const float qscale = a.scale * kLog2e;
+        uint8_t *q_hi = base + sm.q_hi, *q_lo = base + sm.q_lo;
+        uint8_t *p_hi = base + sm.p_hi, *p_lo = base + sm.p_lo;
+        uint32_t tcount = 0, pcount = 0, ne = 0;
+        for (int item = blockIdx.x; item < num_items; item += gridDim.x) {
+            const TcItem r = tc_item(a, item, groups, t == 0);
+            const int head0 = r.g * G + r.hg * kN;
+            const int64_t orow0 = (int64_t(r.s) * a.batch + r.b) * a.num_q_heads + head0;
+            if (r.ntiles == 0) {
+                float4 *o = reinterpret_cast<float4 *>(a.out_part + orow0 * Dv);
+                for (int i = t; i < kN * Dv / 4; i += kSoftThreads)
+                    o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (t < kN) a.lse_part[orow0 + t] = -INFINITY;
+                continue;
+            }
+            // ---- the group's queries, pre-scaled by scale*log2(e), as bf16 hi + lo
+            bool w = wait_bar(bar(kBarQEmpty), (ne & 1u) ^ 1u, a.status, abort_flag);
+            if (w) {
+                const float *qsrc = a.q + (int64_t(r.b) * a.num_q_heads + head0) * Dk;
+                for (int i = t; i < kN * Dk / 2; i += kSoftThreads) {
+                    const int h = (2 * i) / Dk, d = (2 * i) % Dk;
+                    const float2 x = *reinterpret_cast<const float2 *>(qsrc + int64_t(h) * Dk + d);
+                    const float x0 = x.x * qscale, x1 = x.y * qscale;
+                    const uint32_t hi = pack_bf16x2(x0, x1);
+                    const uint32_t lo = pack_bf16x2(x0 - bf16_lo_to_f32(hi), x1 - bf16_hi_to_f32(hi));
+                    const uint32_t off = uint32_t(d >> 6) * 8192 + swz(h, d & 63);
+                    *reinterpret_cast<uint32_t *>(q_hi + off) = hi;
+                    *reinterpret_cast<uint32_t *>(q_lo + off) = lo;
+                }
+                fence_proxy_async_smem();
+            }
+            mbar_arrive(bar(kBarQFull));
+            if (t < kN) mrow[t] = -INFINITY;
+            float l_part[kN];
+#pragma unroll
+            for (int h = 0; h < kN; ++h) l_part[h] = 0.f;
+            if (soft_bar_or(!w)) break;
+
+            bool ok = true;
+            for (int i = 0; i < r.ntiles; ++i) {
+                // ---- scores of this thread's token for the 64 heads, read
+                // from TMEM in 16-column slices (first pass: does any score
+                // exceed its head's running max by more than the slack?)
+                const uint32_t buf = tcount & 1u;
+                const uint32_t ts = tl + kColS + 64 * buf;
+                w = wait_bar(bar(kBarSFull + buf), (tcount >> 1) & 1u, a.status, abort_flag);
+                tc::fence_after_sync();
+                const bool valid = r.begin + int64_t(i) * kM + row < r.end;
+                bool need = false;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t v[16];
+                    tc::ld16(ts + 16 * c, v);
+                    tc::wait_ld();
+#pragma unroll
+                    for (int k = 0; k < 16; ++k)
+                        need |= valid && __uint_as_float(v[k]) > mrow[16 * c + k] + kSlack;
+                }
+                if (soft_bar_or(!w)) {
+                    ok = false;
+                    break;
+                }
+                bool pv_waited = false;
+                if (soft_bar_or(need)) {
+                    // ---- raise the running max to this tile's max
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t v[16];
+                        tc::ld16(ts + 16 * c, v);
+                        tc::wait_ld();
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) {
+                            float m = valid ? __uint_as_float(v[k]) : -INFINITY;
+                            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+                            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+                            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+                            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+                            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+                            if (lane == ((16 * c + k) & 31)) red[quad * kN + 16 * c + k] = m;
+                        }
+                    }
+                    named_barrier_sync(1, kSoftThreads);
+                    if (t < kN) {
+                        const float tm = fmaxf(fmaxf(red[t], red[kN + t]),
+                                               fmaxf(red[2 * kN + t], red[3 * kN + t]));
+                        const float mo = mrow[t], mn = fmaxf(mo, tm);
+                        aux[t] = mo == -INFINITY ? 0.f : exp2f(mo - mn);
+                        mrow[t] = mn;
+                    }
+                    named_barrier_sync(1, kSoftThreads);
+#pragma unroll
+                    for (int h = 0; h < kN; ++h) l_part[h] *= aux[h];
+                    if (i > 0) {
+                        // the accumulators are quiet: tile i-1's value MMAs
+                        // are done and tile i's wait for these probabilities
+                        const bool wv =
+                            wait_bar(bar(kBarPvDone), pcount & 1u, a.status, abort_flag);
+                        ++pcount;
+                        pv_waited = true;
+                        tc::fence_after_sync();
+                        if (wv) {
+                            for (int vb = 0; vb < shp.dv_blocks; ++vb) {
+#pragma unroll
+                                for (int c = 0; c < 4; ++c) {
+                                    uint32_t v[16];
+                                    const uint32_t ta = tl + kColO + 64 * uint32_t(vb) + 16 * c;
+                                    tc::ld16(ta, v);
+                                    tc::wait_ld();
+#pragma unroll
+                                    for (int k = 0; k < 16; ++k)
+                                        v[k] = __float_as_uint(__uint_as_float(v[k]) *
+                                                               aux[16 * c + k]);
+                                    tc::st16(ta, v);
+                                }
+                            }
+                            tc::wait_st();
+                        }
+                    }
+                }
+                if (i > 0 && !pv_waited) {
+                    // tile i-1's value MMAs have finished reading the buffer
+                    wait_bar(bar(kBarPvDone), pcount & 1u, a.status, abort_flag);
+                    ++pcount;
+                }
+                // ---- second pass: probabilities, split into bf16 hi + lo,
+                // straight into the value MMA's operand layout (this token's row)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t v[16];
+                    tc::ld16(ts + 16 * c, v);
+                    tc::wait_ld();
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        uint32_t hi[4], lo[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int k = 8 * half + 2 * e, h = 16 * c + k;
+                            const float2 m2 = *reinterpret_cast<const float2 *>(mrow + h);
+                            const float x0 = valid ? __uint_as_float(v[k]) : -INFINITY;
+                            const float x1 = valid ? __uint_as_float(v[k + 1]) : -INFINITY;
+                            const float p0 = exp2f(x0 - m2.x), p1 = exp2f(x1 - m2.y);
+                            l_part[h] += p0;
+                            l_part[h + 1] += p1;
+                            hi[e] = pack_bf16x2(p0, p1);
+                            lo[e] = pack_bf16x2(p0 - bf16_lo_to_f32(hi[e]),
+                                                p1 - bf16_hi_to_f32(hi[e]));
+                        }
+                        const int chunk = 2 * c + half;
+                        const uint32_t off =
+                            uint32_t(row) * 128 + (uint32_t((chunk ^ row) & 7) << 4);
+                        *reinterpret_cast<uint4 *>(p_hi + off) =
+                            make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                        *reinterpret_cast<uint4 *>(p_lo + off) =
+                            make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    }
+                }
+                tc::fence_before_sync();
+                mbar_arrive(bar(kBarSEmpty + buf));
+                ++tcount;
+                fence_proxy_async_smem();
+                tc::fence_before_sync();
+                mbar_arrive(bar(kBarPFull));
+            }
+            if (!ok) break;
+
+            // ---- epilogue: the item's last value MMAs are complete
+            w = wait_bar(bar(kBarPvDone), pcount & 1u, a.status, abort_flag);
+            ++pcount;
+            tc::fence_after_sync();
+#pragma unroll
+            for (int h = 0; h < kN; ++h) {
+                float s = l_part[h];
+                s += __shfl_xor_sync(0xffffffffu, s, 16);
+                s += __shfl_xor_sync(0xffffffffu, s, 8);
+                s += __shfl_xor_sync(0xffffffffu, s, 4);
+                s += __shfl_xor_sync(0xffffffffu, s, 2);
+                s += __shfl_xor_sync(0xffffffffu, s, 1);
+                if (lane == (h & 31)) red[quad * kN + h] = s;
+            }
+            named_barrier_sync(1, kSoftThreads);
+            if (t < kN) {
+                const float l = (red[t] + red[kN + t]) + (red[2 * kN + t] + red[3 * kN + t]);
+                aux[t] = l > 0.f ? 1.f / l : 0.f;
+                a.lse_part[orow0 + t] = l > 0.f ? (mrow[t] + log2f(l)) * kLn2 : -INFINITY;
+            }
+            named_barrier_sync(1, kSoftThreads);
+            if (w) {
+                for (int vb = 0; vb < shp.dv_blocks; ++vb) {
+                    float *orow = a.out_part + orow0 * Dv + vb * 128 + row;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t v[16];
+                        tc::ld16(tl + kColO + 64 * uint32_t(vb) + 16 * c, v);
+                        tc::wait_ld();
+#pragma unroll
+                        for (int k = 0; k < 16; ++k)
+                            orow[int64_t(16 * c + k) * Dv] =
+                                __uint_as_float(v[k]) * aux[16 * c + k];
+                    }
+                }
+            }
+            tc::fence_before_sync();
+            mbar_arrive(bar(kBarOEmpty));
+            ++ne;
+            if (soft_bar_or(!w)) break;
+        }
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::dealloc(tmem, kTmemCols);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tc_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// The pool as rows of `dim` bf16, viewed 3-D as (64 columns, rows, dim/64
+// segments at a 128-byte stride); one box = 64 rows x `segs` segments,
+// landing segment-major with the 128-byte swizzle.
+bool make_box_map(CUtensorMap *map, const void *pool, int64_t rows, int dim, int segs) {
+    auto fn = tc_encode_fn();
+    if (!fn) return false;
+    cuuint64_t gdim[3] = {64, cuuint64_t(rows), cuuint64_t(dim / 64)};
+    cuuint64_t gstride[2] = {cuuint64_t(dim) * 2, 128};
+    cuuint32_t box[3] = {64, cuuint32_t(kHalf), cuuint32_t(segs)};
+    cuuint32_t estride[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(pool), gdim, gstride,
+              box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+TcShape tc_shape(const pkv_cache_desc &c) {
+    TcShape s{c.head_dim_k / 64, c.head_dim_v / 128, 0};
+    const size_t fixed = tc_smem_bytes(s);
+    const int ring = int((kSmemLimit - std::min<size_t>(fixed, kSmemLimit)) / kChunk);
+    s.ring = std::min(ring, kMaxRing);
+    return s;
+}
+
+}  // namespace
+
+bool mla_tc_kernel_supports(const pkv_cache_desc &c, int32_t num_q_heads) {
+    const int G = num_q_heads / c.num_kv_heads;
+    const bool pow2_bs = c.block_size >= kHalf && c.block_size <= 256 &&
+                         (c.block_size & (c.block_size - 1)) == 0;
+    const int64_t rows = int64_t(c.num_blocks) * c.num_kv_heads * c.block_size;
+    if (G % kN != 0 || !pow2_bs || rows >= (int64_t(1) << 31) - 1) return false;
+    if (c.head_dim_k % 64 != 0 || c.head_dim_k < 64 || c.head_dim_v % 128 != 0 ||
+        c.head_dim_v > 512)
+        return false;
+    return tc_shape(c).ring >= 2;
+}
+
+int32_t mla_tc_work_units(const pkv_cache_desc &c, int32_t batch, int32_t num_q_heads) {
+    return batch * num_q_heads / kN;
+}
+
+int launch_decode_mla_tc(const DecodeArgs &a) {
+    const TcShape shp = tc_shape(a.cache);
+    const int64_t rows = int64_t(a.cache.num_blocks) * a.cache.num_kv_heads * a.cache.block_size;
+    CUtensorMap tk, tv;
+    if (!make_box_map(&tk, a.k_pool, rows, a.cache.head_dim_k, 1) ||
+        !make_box_map(&tv, a.v_pool, rows, a.cache.head_dim_v, 2))
+        return PKV_ERR_CUDA;
+    const size_t smem = tc_smem_bytes(shp);
+    static thread_local int configured_dev = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_dev != dev) {
+        if (cudaFuncSetAttribute(decode_mla_tc_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemLimit) != cudaSuccess)
+            return PKV_ERR_CUDA;
+        configured_dev = dev;
+    }
+    const int G = a.num_q_heads / a.cache.num_kv_heads;
+    const int64_t items = int64_t(a.batch) * a.cache.num_kv_heads * (G / kN) * a.num_splits;
+    const int grid = int(std::min<int64_t>(items, sm_count()));
+    if (grid <= 0) return PKV_OK;
+    return launch_pdl(decode_mla_tc_kernel, dim3(grid), dim3(kThreads), smem, a.stream, tk, tv,
+                      a, shp);
+}
+
+}  // namespace pkv

@@ -63,6 +63,11 @@ int launch_decode_tma(const DecodeArgs &a);
 bool mla_kernel_supports(const pkv_cache_desc &c, int32_t num_q_heads);
 int32_t mla_work_units(const pkv_cache_desc &c, int32_t batch, int32_t num_q_heads);
 int launch_decode_mla(const DecodeArgs &a);
+// Query groups that are a multiple of 64 heads on the 5th-generation tensor
+// cores (tcgen05, TMEM accumulators), 64-head work items.
+bool mla_tc_kernel_supports(const pkv_cache_desc &c, int32_t num_q_heads);
+int32_t mla_tc_work_units(const pkv_cache_desc &c, int32_t batch, int32_t num_q_heads);
+int launch_decode_mla_tc(const DecodeArgs &a);
 int launch_decode_generic(const DecodeArgs &a);
 int launch_lse_merge(int32_t num_parts, const float *out_part, const float *lse_part,
                      int64_t rows, int32_t head_dim_v, float *out, float *lse,

@@ -214,18 +214,49 @@ MLA_SHAPES = [
     ([300, 45], 64, 2, 128, 128, 32),
     ([513, 0, 31], 64, 1, 192, 256, 128),
     ([1000], 32, 1, 64, 64, 256),
+    # multiples of 64 heads: the tcgen05 kernel (ragged tiles, two KV heads,
+    # block sizes 64 and 256, head dims up to 576 / 512)
+    ([127, 128, 255, 1, 700], 128, 2, 576, 512, 64),
+    ([2000, 63], 64, 1, 512, 512, 256),
+    ([383], 192, 1, 128, 384, 128),
 ]
 
 
 @pytest.mark.parametrize("shape", MLA_SHAPES,
                          ids=lambda s: f"G{s[1]//s[2]}_Dk{s[3]}_Dv{s[4]}_bs{s[5]}")
 @pytest.mark.parametrize("splits", [1, 3, 0])
-def test_large_group_kernel(pkv, shape, splits):
+@pytest.mark.parametrize("flags", [0, "no_tcgen05"])
+def test_large_group_kernel(pkv, shape, splits, flags):
+    """Large query groups; with no_tcgen05 the warp-level-MMA kernel takes the
+    shapes the tcgen05 kernel would have run."""
     cached, hq, hkv, dk, dv, bs = shape
+    f = pkv.DECODE_NO_TCGEN05 if flags == "no_tcgen05" else 0
     w = workloads.custom(200 + dk + bs, cached, hq, hkv, dk, dv, bs)
-    out, lse, *_ = gpu_step(pkv, w, num_splits=splits)
+    out, lse, *_ = gpu_step(pkv, w, num_splits=splits, flags=f)
     ro, rl, *_ = oracle_step(w)
-    assert_attention_close(out.cpu().numpy(), lse.cpu().numpy(), ro, rl, f"{shape}/{splits}")
+    assert_attention_close(out.cpu().numpy(), lse.cpu().numpy(), ro, rl,
+                           f"{shape}/{splits}/{flags}")
+    assert pkv.device_status() == 0
+
+
+@pytest.mark.parametrize("flags", [0, "no_tcgen05"])
+@pytest.mark.parametrize("splits", [1, 2])
+def test_large_group_rising_scores(pkv, flags, splits):
+    """Keys grow along the sequence, so a head's running max keeps rising
+    (by more than 2^8 in probability between tiles): the kernels must rescale
+    what they have accumulated, in TMEM for the tcgen05 kernel."""
+    w = workloads.custom(91, [1500, 700], 128, 1, 576, 512, 64)
+    k = w.k_pool.float()
+    L = w.seq_lens.tolist()
+    for b in range(2):
+        for j in range(L[b]):
+            blk = int(w.block_tables[b, j // 64])
+            k[blk, :, j % 64] *= 1.0 + 5.0 * j / L[b]
+    w.k_pool = k.to(torch.bfloat16)
+    f = pkv.DECODE_NO_TCGEN05 if flags == "no_tcgen05" else 0
+    out, lse, *_ = gpu_step(pkv, w, num_splits=splits, flags=f)
+    ro, rl, *_ = oracle_step(w)
+    assert_attention_close(out.cpu().numpy(), lse.cpu().numpy(), ro, rl, f"rising/{splits}")
     assert pkv.device_status() == 0
 
 
