@@ -334,7 +334,7 @@ class AgentStep(Step):
 
 
 STEPS = {"long32k": Step, "mix": Step, "tiny": Step, "dcp200k": DcpStep, "agent_mla": AgentStep}
-DEFAULT_SPLITS = {"long32k": 16, "mix": 1, "tiny": 1, "dcp200k": 19, "agent_mla": 8}
+DEFAULT_SPLITS = {"long32k": 16, "mix": 1, "tiny": 1, "dcp200k": 19, "agent_mla": 19}
 
 
 # ------------------------------------------------------------------ arms

@@ -36,17 +36,22 @@ int validate_decode(const pkv_cache_desc *c, const float *q, int32_t batch, int3
 
 int32_t auto_splits(const pkv_cache_desc &c, int32_t batch, int32_t num_q_heads,
                     int32_t max_seq_len) {
-    // Enough (sequence, KV head [, head block], split) items for ~4 per SM,
-    // each item at least 512 tokens long.
+    // Enough (sequence, KV head [, head block], split) items for ~4 per SM
+    // (8 for the tcgen05 kernel), each item at least 512 tokens long.
     int64_t units = int64_t(batch) * c.num_kv_heads;
+    int64_t per_sm = 4;
     if (!tma_kernel_supports(c, num_q_heads)) {
-        if (mla_tc_kernel_supports(c, num_q_heads))
+        if (mla_tc_kernel_supports(c, num_q_heads)) {
+            // one CTA per SM walks its items in turn: ~8 per SM evens out
+            // the tail of unequal sequence lengths
             units = mla_tc_work_units(c, batch, num_q_heads);
-        else if (mla_kernel_supports(c, num_q_heads))
+            per_sm = 8;
+        } else if (mla_kernel_supports(c, num_q_heads)) {
             units = mla_work_units(c, batch, num_q_heads);
+        }
     }
     units = std::max<int64_t>(1, units);
-    const int64_t want = (int64_t(sm_count()) * 4 + units - 1) / units;
+    const int64_t want = (int64_t(sm_count()) * per_sm + units / 2) / units;
     const int64_t cap = std::max<int64_t>(1, (int64_t(max_seq_len) + 511) / 512);
     return int32_t(std::max<int64_t>(1, std::min<int64_t>({want, cap, kMaxSplits})));
 }
