@@ -52,7 +52,10 @@ KERNEL_SOURCES = [os.path.join(ROOT, "paged_kv_cache_93_gb300", "csrc", f)
 # ----------------------------------------------------------------- helpers
 
 def kv_bytes_per_token(w) -> int:
-    """K and V bytes one token occupies in one layer: (Dk + Dv) x Hkv x 2 B."""
+    """K and V bytes one token occupies in one layer: (Dk + Dv) x Hkv x 2 B,
+    or Dk x Hkv x 2 B when the values live inside the key rows."""
+    if w.v_pool is None:
+        return w.head_dim_k * w.num_kv_heads * 2
     return (w.head_dim_k + w.head_dim_v) * w.num_kv_heads * 2
 
 
@@ -197,14 +200,14 @@ class Step:
     def __init__(self, pkv, w, dev, splits):
         self.pkv, self.w, self.splits = pkv, w, splits
         self.k = w.k_pool.to(dev)
-        self.v = w.v_pool.to(dev)
+        self.v = pkv.ValuesInKeys(w.head_dim_v) if w.v_pool is None else w.v_pool.to(dev)
         self.bt = w.block_tables.to(dev)
         self.lens = w.seq_lens.to(dev)
         self.q = w.q.to(dev)
         self.new_seq = w.new_seq.to(dev)
         self.new_pos = w.new_pos.to(dev)
         self.k_new = w.k_new.to(dev)
-        self.v_new = w.v_new.to(dev)
+        self.v_new = None if w.v_new is None else w.v_new.to(dev)
         B, Hq = w.batch, w.num_q_heads
         self.slots = torch.empty(w.new_pos.numel(), dtype=torch.int64, device=dev)
         self.out = torch.empty(B, Hq, w.head_dim_v, device=dev)
@@ -318,10 +321,13 @@ class AgentStep(Step):
         setup = ~last
         sl = pkv.slot_mapping(self.k, self.v, self.bt, self.new_seq[setup.to(dev)],
                               self.new_pos[setup.to(dev)])
-        pkv.kv_append(self.k, self.v, self.k_new[setup.to(dev)], self.v_new[setup.to(dev)], sl)
+        vs = None if self.v_new is None else self.v_new[setup.to(dev)]
+        pkv.kv_append(self.k, self.v, self.k_new[setup.to(dev)], vs, sl)
         keep = last.to(dev)
         self.new_seq, self.new_pos = self.new_seq[keep], self.new_pos[keep]
-        self.k_new, self.v_new = self.k_new[keep].contiguous(), self.v_new[keep].contiguous()
+        self.k_new = self.k_new[keep].contiguous()
+        if self.v_new is not None:
+            self.v_new = self.v_new[keep].contiguous()
         self.slots = torch.empty(self.new_pos.numel(), dtype=torch.int64, device=dev)
         self.launches = 5   # copy, slot, append, split, merge
         self.desc = (f"copy_blocks ({self.src.numel()} CoW pairs) + slot_mapping + kv_append "
@@ -333,8 +339,10 @@ class AgentStep(Step):
         super().run(ev_a, ev_b)
 
 
-STEPS = {"long32k": Step, "mix": Step, "tiny": Step, "dcp200k": DcpStep, "agent_mla": AgentStep}
-DEFAULT_SPLITS = {"long32k": 16, "mix": 1, "tiny": 1, "dcp200k": 19, "agent_mla": 19}
+STEPS = {"long32k": Step, "mix": Step, "tiny": Step, "dcp200k": DcpStep, "agent_mla": AgentStep,
+         "agent_mla_latent": AgentStep}
+DEFAULT_SPLITS = {"long32k": 16, "mix": 1, "tiny": 1, "dcp200k": 19, "agent_mla": 19,
+                  "agent_mla_latent": 19}
 
 
 # ------------------------------------------------------------------ arms
@@ -373,7 +381,9 @@ def oracle_gbs(w, tokens: int | None, repeats: int = 1):
     """Time the CPU oracle (all host cores) over every row of `w`, restricted
     to the first `tokens` tokens of each sequence when given."""
     import oracle
-    kp, vp = bits_view(w.k_pool), bits_view(w.v_pool)
+    kp = bits_view(w.k_pool)
+    vp = (np.ascontiguousarray(kp[..., :w.head_dim_v]) if w.v_pool is None
+          else bits_view(w.v_pool))
     q, bt, lens = w.q.numpy(), w.block_tables.numpy(), w.seq_lens.numpy()
     end = None
     if tokens is not None:
@@ -388,8 +398,10 @@ def oracle_gbs(w, tokens: int | None, repeats: int = 1):
 
 
 def workload_desc(w, splits):
+    kv = (f"head_dim {w.head_dim_k}, values = first {w.head_dim_v} dims of each key row, bf16"
+          if w.v_pool is None else f"head_dim {w.head_dim_k}, bf16 K/V")
     return (f"{w.name}: batch {w.batch} x {int(w.seq_lens.max())} tokens, GQA "
-            f"{w.num_q_heads}/{w.num_kv_heads} heads, head_dim {w.head_dim_k}, bf16 K/V, block "
+            f"{w.num_q_heads}/{w.num_kv_heads} heads, {kv}, block "
             f"{w.block_size}, {w.num_blocks}-block randomly permuted pool, {splits} splits + "
             f"lse_merge")
 

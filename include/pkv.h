@@ -30,6 +30,11 @@
  *    and v_pool [num_blocks][num_kv_heads][block_size][head_dim_v], bf16.  One
  *    (block, KV head) tile is contiguous.  Token j of sequence b lives in
  *    physical block block_tables[b][j / block_size] at offset j % block_size.
+ *  - Values inside the keys (the latent layout of multi-head latent attention,
+ *    where one cached row serves as the key and its first head_dim_v dims as
+ *    the value): pass v_pool = NULL (and v_new = NULL to pkv_kv_append); the
+ *    cache is then k_pool alone and head_dim_v <= head_dim_k.  The pages
+ *    describe no such layout; it halves the bytes per token of the MLA shape.
  *  - Query head h uses KV head h / (num_q_heads / num_kv_heads).
  *  - Head dims: any multiple of 8 up to 1024 (the tensor-core kernel takes
  *    64 and 128); q, out and lse are fp32; lse is the natural log of
@@ -108,7 +113,9 @@ int pkv_slot_mapping(const pkv_cache_desc *cache, const int32_t *block_tables,
  * likewise for V, with slot = slot_mapping[t].  k_new [T][num_kv_heads][head_dim_k]
  * and v_new [T][num_kv_heads][head_dim_v] bf16; slot_mapping [T] int64.
  * Negative slots are skipped (padding); slots >= num_blocks * block_size are
- * skipped and set PKV_DEV_SLOT.  Two tokens with the same slot race.
+ * skipped and set PKV_DEV_SLOT.  Two tokens with the same slot race.  With
+ * v_pool and v_new both NULL (values inside the keys) only K is written; one
+ * of the two NULL is PKV_ERR_INVALID_ARG.
  * ------------------------------------------------------------------------- */
 int pkv_kv_append(const pkv_cache_desc *cache, void *k_pool, void *v_pool,
                   const void *k_new, const void *v_new, const int64_t *slot_mapping,
@@ -122,7 +129,8 @@ int pkv_kv_append(const pkv_cache_desc *cache, void *k_pool, void *v_pool,
  * [num_pairs] int32 device arrays.  A pair whose ids are out of range sets
  * PKV_DEV_BLOCK_ID; a pair whose destination is also another pair's
  * destination or any pair's source sets PKV_DEV_COPY_CONFLICT; such pairs are
- * skipped, so the others never race with them.
+ * skipped, so the others never race with them.  v_pool NULL (values inside
+ * the keys): only the K tiles are copied.
  * ------------------------------------------------------------------------- */
 int pkv_copy_blocks(const pkv_cache_desc *cache, void *k_pool, void *v_pool,
                     const int32_t *src, const int32_t *dst, int32_t num_pairs,
@@ -163,7 +171,8 @@ int64_t pkv_interleave_partition_len(int64_t num_tokens, int32_t num_parts,
  * lse = -inf.  A seq_len outside [0, max_blocks * block_size] is treated as 0
  * and sets PKV_DEV_SEQ_LEN.  A table entry outside [0, num_blocks) is never
  * dereferenced: its tokens read some in-pool block instead, the row's result
- * is unspecified, and PKV_DEV_BLOCK_ID is set.
+ * is unspecified, and PKV_DEV_BLOCK_ID is set.  v_pool NULL: V_j is the first
+ * head_dim_v dims of K_j (head_dim_v > head_dim_k is PKV_ERR_SHAPE).
  *
  * Split-KV: with num_splits = S > 1 each sequence's tokens are cut into S
  * contiguous chunks, chunk s covering [s*C_b, min(seq_lens[b], (s+1)*C_b)) with

@@ -21,7 +21,7 @@ from ._lib import (DECODE_GENERIC, DECODE_NO_TCGEN05, DEV_BLOCK_ID, DEV_COPY_CON
                    DEV_TABLE_RANGE, DEV_TIMEOUT, CacheDesc, PkvError)
 
 __all__ = [
-    "CacheDesc", "PkvError", "cache_desc", "kv_append", "slot_mapping", "copy_blocks",
+    "CacheDesc", "PkvError", "ValuesInKeys", "cache_desc", "kv_append", "slot_mapping", "copy_blocks",
     "interleave_slot_mapping", "interleave_partition_len", "decode_workspace_size",
     "decode_auto_splits", "paged_decode_attn", "paged_decode_attn_partial", "lse_merge",
     "device_status", "BlockManager", "library_path", "DECODE_GENERIC", "DECODE_NO_TCGEN05",
@@ -58,10 +58,27 @@ def _need(t: torch.Tensor, name: str, dtype: torch.dtype, dim: int | None = None
         raise ValueError(f"{name} must have {dim} dims, got {t.dim()}")
 
 
-def cache_desc(k_pool: torch.Tensor, v_pool: torch.Tensor) -> CacheDesc:
+class ValuesInKeys:
+    """Pass as `v_pool` when the cache keeps no separate value pool: the value
+    of a token is the first `head_dim_v` dims of its key row (the latent
+    layout of multi-head latent attention).  Marshalled as a NULL v_pool."""
+
+    def __init__(self, head_dim_v: int):
+        self.head_dim_v = int(head_dim_v)
+
+
+def _v_ptr(v_pool):
+    return None if isinstance(v_pool, ValuesInKeys) else _ptr(v_pool)
+
+
+def cache_desc(k_pool: torch.Tensor, v_pool) -> CacheDesc:
     _need(k_pool, "k_pool", torch.bfloat16, 4)
-    _need(v_pool, "v_pool", torch.bfloat16, 4)
     nb, hkv, bs, dk = k_pool.shape
+    if isinstance(v_pool, ValuesInKeys):
+        if not 0 < v_pool.head_dim_v <= dk:
+            raise ValueError("values inside the keys need 0 < head_dim_v <= head_dim_k")
+        return CacheDesc(nb, bs, hkv, dk, v_pool.head_dim_v)
+    _need(v_pool, "v_pool", torch.bfloat16, 4)
     if tuple(v_pool.shape[:3]) != (nb, hkv, bs):
         raise ValueError("k_pool and v_pool disagree on [num_blocks, Hkv, block_size]")
     return CacheDesc(nb, bs, hkv, dk, v_pool.shape[3])
@@ -91,14 +108,19 @@ def slot_mapping(k_pool, v_pool, block_tables, seq_ids, positions, out=None, str
 
 
 def kv_append(k_pool, v_pool, k_new, v_new, slots, stream=None) -> None:
-    """Write k_new [T, Hkv, Dk] / v_new [T, Hkv, Dv] (bf16) at slots [T] (int64)."""
+    """Write k_new [T, Hkv, Dk] / v_new [T, Hkv, Dv] (bf16) at slots [T] (int64).
+    With v_pool = ValuesInKeys(Dv), v_new must be None (only K is written)."""
     desc = cache_desc(k_pool, v_pool)
     _need(k_new, "k_new", torch.bfloat16, 3)
-    _need(v_new, "v_new", torch.bfloat16, 3)
+    if isinstance(v_pool, ValuesInKeys):
+        if v_new is not None:
+            raise ValueError("v_new must be None when the values are inside the keys")
+    else:
+        _need(v_new, "v_new", torch.bfloat16, 3)
     _need(slots, "slot_mapping", torch.int64, 1)
     _check("pkv_kv_append", lib.pkv_kv_append(
-        ctypes.byref(desc), _ptr(k_pool), _ptr(v_pool), _ptr(k_new), _ptr(v_new), _ptr(slots),
-        slots.numel(), _stream(stream)))
+        ctypes.byref(desc), _ptr(k_pool), _v_ptr(v_pool), _ptr(k_new), _ptr(v_new),
+        _ptr(slots), slots.numel(), _stream(stream)))
 
 
 def copy_blocks(k_pool, v_pool, src, dst, stream=None) -> None:
@@ -109,7 +131,7 @@ def copy_blocks(k_pool, v_pool, src, dst, stream=None) -> None:
     if src.numel() != dst.numel():
         raise ValueError("src and dst lengths differ")
     _check("pkv_copy_blocks", lib.pkv_copy_blocks(
-        ctypes.byref(desc), _ptr(k_pool), _ptr(v_pool), _ptr(src), _ptr(dst), src.numel(),
+        ctypes.byref(desc), _ptr(k_pool), _v_ptr(v_pool), _ptr(src), _ptr(dst), src.numel(),
         _stream(stream)))
 
 
@@ -172,7 +194,7 @@ def paged_decode_attn(q, k_pool, v_pool, block_tables, seq_lens, scale: float,
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check("pkv_paged_decode_attn", lib.pkv_paged_decode_attn(
-        ctypes.byref(desc), _ptr(q), B, Hq, _ptr(k_pool), _ptr(v_pool), _ptr(block_tables),
+        ctypes.byref(desc), _ptr(q), B, Hq, _ptr(k_pool), _v_ptr(v_pool), _ptr(block_tables),
         block_tables.shape[1], _ptr(seq_lens), float(scale), S, _ptr(workspace), ws_bytes,
         _ptr(out), _ptr(lse), int(flags), _stream(stream)))
     return out, lse
@@ -190,7 +212,7 @@ def paged_decode_attn_partial(q, k_pool, v_pool, block_tables, seq_lens, scale: 
     if lse_part is None:
         lse_part = torch.empty(S, B, Hq, dtype=torch.float32, device=q.device)
     _check("pkv_paged_decode_attn_partial", lib.pkv_paged_decode_attn_partial(
-        ctypes.byref(desc), _ptr(q), B, Hq, _ptr(k_pool), _ptr(v_pool), _ptr(block_tables),
+        ctypes.byref(desc), _ptr(q), B, Hq, _ptr(k_pool), _v_ptr(v_pool), _ptr(block_tables),
         block_tables.shape[1], _ptr(seq_lens), float(scale), S, _ptr(out_part), _ptr(lse_part),
         int(flags), _stream(stream)))
     return out_part, lse_part

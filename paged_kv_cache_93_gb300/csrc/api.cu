@@ -29,8 +29,10 @@ int validate_decode(const pkv_cache_desc *c, const float *q, int32_t batch, int3
         c->head_dim_k > 1024 || c->head_dim_v > 1024 || batch > 65535)
         return PKV_ERR_SHAPE;
     if (batch == 0) return PKV_OK;
-    if (!q || !k_pool || !v_pool || !block_tables || !seq_lens) return PKV_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool)) return PKV_ERR_ALIGNMENT;
+    if (!q || !k_pool || !block_tables || !seq_lens) return PKV_ERR_INVALID_ARG;
+    if (!v_pool && c->head_dim_v > c->head_dim_k) return PKV_ERR_SHAPE;   // values inside the keys
+    if (!aligned16(q) || !aligned16(k_pool) || (v_pool && !aligned16(v_pool)))
+        return PKV_ERR_ALIGNMENT;
     return PKV_OK;
 }
 
@@ -54,6 +56,17 @@ int32_t auto_splits(const pkv_cache_desc &c, int32_t batch, int32_t num_q_heads,
     const int64_t want = (int64_t(sm_count()) * per_sm + units / 2) / units;
     const int64_t cap = std::max<int64_t>(1, (int64_t(max_seq_len) + 511) / 512);
     return int32_t(std::max<int64_t>(1, std::min<int64_t>({want, cap, kMaxSplits})));
+}
+
+// Where the values live: their own pool, or (v_pool NULL) the first
+// head_dim_v dims of each key row.
+void values_from(DecodeArgs &a) {
+    if (a.v_pool) {
+        a.v_stride = a.cache.head_dim_v;
+    } else {
+        a.v_pool = a.k_pool;
+        a.v_stride = a.cache.head_dim_k;
+    }
 }
 
 int run_split_kernel(const DecodeArgs &a, int32_t flags) {
@@ -102,6 +115,7 @@ extern "C" int pkv_paged_decode_attn_partial(const pkv_cache_desc *cache, const 
     DecodeArgs a{*cache, q, batch, num_q_heads, k_pool, v_pool, block_tables, max_blocks,
                  seq_lens, scale, num_splits, out_part, lse_part, status,
                  reinterpret_cast<cudaStream_t>(stream)};
+    values_from(a);
     return run_split_kernel(a, flags);
 }
 
@@ -131,6 +145,7 @@ extern "C" int pkv_paged_decode_attn(const pkv_cache_desc *cache, const float *q
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     DecodeArgs a{*cache, q, batch, num_q_heads, k_pool, v_pool, block_tables, max_blocks,
                  seq_lens, scale, S, out, lse, status, s};
+    values_from(a);
     if (S == 1) return run_split_kernel(a, flags);
 
     const size_t rows = size_t(S) * batch * num_q_heads;

@@ -248,12 +248,17 @@ extern "C" int pkv_kv_append(const pkv_cache_desc *cache, void *k_pool, void *v_
                              int64_t num_tokens, pkv_stream_t stream) {
     if (!valid_cache(cache) || num_tokens < 0) return PKV_ERR_INVALID_ARG;
     if (num_tokens == 0) return PKV_OK;
-    if (!k_pool || !v_pool || !k_new || !v_new || !slot_mapping) return PKV_ERR_INVALID_ARG;
-    if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(k_new) || !aligned16(v_new))
+    // v_pool and v_new both NULL: the cache keeps no separate values (they
+    // are the first head_dim_v dims of the key rows); only K is written.
+    if (!k_pool || !k_new || !slot_mapping || !v_pool != !v_new) return PKV_ERR_INVALID_ARG;
+    if (!v_pool && cache->head_dim_v > cache->head_dim_k) return PKV_ERR_SHAPE;
+    if (!aligned16(k_pool) || !aligned16(k_new) || (v_pool && !aligned16(v_pool)) ||
+        (v_new && !aligned16(v_new)))
         return PKV_ERR_ALIGNMENT;
     uint32_t *status = status_word();
     if (!status) return PKV_ERR_CUDA;
-    const int32_t vk = cache->head_dim_k / 8, vv = cache->head_dim_v / 8;  // 16-byte vectors
+    const int32_t vk = cache->head_dim_k / 8;                      // 16-byte vectors
+    const int32_t vv = v_pool ? cache->head_dim_v / 8 : 0;
     const int64_t work = num_tokens * cache->num_kv_heads * (vk + vv);
     const int threads = 256;
     return launch_pdl(kv_append_kernel, dim3(grid_for(work, threads)), dim3(threads), 0,
@@ -269,13 +274,16 @@ extern "C" int pkv_copy_blocks(const pkv_cache_desc *cache, void *k_pool, void *
                                pkv_stream_t stream) {
     if (!valid_cache(cache) || num_pairs < 0) return PKV_ERR_INVALID_ARG;
     if (num_pairs == 0) return PKV_OK;
-    if (!k_pool || !v_pool || !src || !dst) return PKV_ERR_INVALID_ARG;
-    if (!aligned16(k_pool) || !aligned16(v_pool)) return PKV_ERR_ALIGNMENT;
+    // v_pool NULL: the cache keeps no separate values; only K blocks are copied.
+    if (!k_pool || !src || !dst) return PKV_ERR_INVALID_ARG;
+    if (!v_pool && cache->head_dim_v > cache->head_dim_k) return PKV_ERR_SHAPE;
+    if (!aligned16(k_pool) || (v_pool && !aligned16(v_pool))) return PKV_ERR_ALIGNMENT;
     if (num_pairs > 65535) return PKV_ERR_SHAPE;
     uint32_t *status = status_word();
     if (!status) return PKV_ERR_CUDA;
     const int64_t k_vecs = int64_t(cache->num_kv_heads) * cache->block_size * cache->head_dim_k / 8;
-    const int64_t v_vecs = int64_t(cache->num_kv_heads) * cache->block_size * cache->head_dim_v / 8;
+    const int64_t v_vecs =
+        v_pool ? int64_t(cache->num_kv_heads) * cache->block_size * cache->head_dim_v / 8 : 0;
     const int threads = 256;
     // Enough CTAs per pair to cover the device a few times over.
     int64_t per_pair = (k_vecs + v_vecs + threads - 1) / threads;

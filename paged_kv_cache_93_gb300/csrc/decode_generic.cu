@@ -81,6 +81,7 @@ decode_generic_kernel(DecodeArgs a) {
     const int32_t *table = a.block_tables + int64_t(b) * a.max_blocks;
     const uint4 *kp = static_cast<const uint4 *>(a.k_pool);
     const uint4 *vp = static_cast<const uint4 *>(a.v_pool);
+    const int vs = a.v_stride / 8;          // 16-byte vectors from one V row to the next
     for (int64_t j = begin; j < end; ++j) {
         const int32_t phys = table[j / c.block_size];
         const bool ok = phys >= 0 && phys < c.num_blocks;
@@ -108,7 +109,7 @@ decode_generic_kernel(DecodeArgs a) {
         for (int i = 0; i < VC; ++i) {
             const int v = lane + 32 * i;
             float vf[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-            if (v < nv && ok) unpack8(vp[row * nv + v], vf);
+            if (v < nv && ok) unpack8(vp[row * vs + v], vf);
 #pragma unroll
             for (int e = 0; e < 8; ++e) acc[i][e] = fmaf(p, vf[e], acc[i][e] * corr);
         }

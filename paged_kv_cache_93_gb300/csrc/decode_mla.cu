@@ -449,14 +449,15 @@ PFN_cuTensorMapEncodeTiled_v12000 mla_encode_fn() {
     return fn;
 }
 
-// The pool as rows of `dim` bf16, viewed 3-D as (64 columns, rows, dim/64
-// segments at a 128-byte stride): one box = 32 rows, all segments -- one
-// contiguous run of HBM -- landing segment-major.
-bool make_seg_map(CUtensorMap *map, const void *pool, int64_t rows, int dim) {
+// The pool as rows of `dim` bf16 (`stride` elements apart), viewed 3-D as
+// (64 columns, rows, dim/64 segments at a 128-byte stride): one box = 32
+// rows, all segments -- one contiguous run of HBM for a dense pool --
+// landing segment-major.
+bool make_seg_map(CUtensorMap *map, const void *pool, int64_t rows, int dim, int stride) {
     auto fn = mla_encode_fn();
     if (!fn) return false;
     cuuint64_t gdim[3] = {64, cuuint64_t(rows), cuuint64_t(dim / 64)};
-    cuuint64_t gstride[2] = {cuuint64_t(dim) * 2, 128};
+    cuuint64_t gstride[2] = {cuuint64_t(stride) * 2, 128};
     cuuint32_t box[3] = {64, cuuint32_t(kT), cuuint32_t(dim / 64)};
     cuuint32_t estride[3] = {1, 1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(pool), gdim, gstride,
@@ -486,8 +487,8 @@ int launch_decode_mla(const DecodeArgs &a) {
     const MlaShape shp{a.cache.head_dim_k / 64, a.cache.head_dim_v / 64};
     const int64_t rows = int64_t(a.cache.num_blocks) * a.cache.num_kv_heads * a.cache.block_size;
     CUtensorMap tk, tv;
-    if (!make_seg_map(&tk, a.k_pool, rows, a.cache.head_dim_k) ||
-        !make_seg_map(&tv, a.v_pool, rows, a.cache.head_dim_v))
+    if (!make_seg_map(&tk, a.k_pool, rows, a.cache.head_dim_k, a.cache.head_dim_k) ||
+        !make_seg_map(&tv, a.v_pool, rows, a.cache.head_dim_v, a.v_stride))
         return PKV_ERR_CUDA;
     const size_t smem = mla_smem_bytes(shp);
     static thread_local int configured_dev = -1;

@@ -657,14 +657,15 @@ PFN_cuTensorMapEncodeTiled_v12000 tc_encode_fn() {
     return fn;
 }
 
-// The pool as rows of `dim` bf16, viewed 3-D as (64 columns, rows, dim/64
-// segments at a 128-byte stride); one box = 64 rows x `segs` segments,
-// landing segment-major with the 128-byte swizzle.
-bool make_box_map(CUtensorMap *map, const void *pool, int64_t rows, int dim, int segs) {
+// The pool as rows of `dim` bf16 (`stride` elements apart), viewed 3-D as
+// (64 columns, rows, dim/64 segments at a 128-byte stride); one box = 64
+// rows x `segs` segments, landing segment-major with the 128-byte swizzle.
+bool make_box_map(CUtensorMap *map, const void *pool, int64_t rows, int dim, int stride,
+                  int segs) {
     auto fn = tc_encode_fn();
     if (!fn) return false;
     cuuint64_t gdim[3] = {64, cuuint64_t(rows), cuuint64_t(dim / 64)};
-    cuuint64_t gstride[2] = {cuuint64_t(dim) * 2, 128};
+    cuuint64_t gstride[2] = {cuuint64_t(stride) * 2, 128};
     cuuint32_t box[3] = {64, cuuint32_t(kHalf), cuuint32_t(segs)};
     cuuint32_t estride[3] = {1, 1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(pool), gdim, gstride,
@@ -702,8 +703,8 @@ int launch_decode_mla_tc(const DecodeArgs &a) {
     const TcShape shp = tc_shape(a.cache);
     const int64_t rows = int64_t(a.cache.num_blocks) * a.cache.num_kv_heads * a.cache.block_size;
     CUtensorMap tk, tv;
-    if (!make_box_map(&tk, a.k_pool, rows, a.cache.head_dim_k, 1) ||
-        !make_box_map(&tv, a.v_pool, rows, a.cache.head_dim_v, 2))
+    if (!make_box_map(&tk, a.k_pool, rows, a.cache.head_dim_k, a.cache.head_dim_k, 1) ||
+        !make_box_map(&tv, a.v_pool, rows, a.cache.head_dim_v, a.v_stride, 2))
         return PKV_ERR_CUDA;
     const size_t smem = tc_smem_bytes(shp);
     static thread_local int configured_dev = -1;

@@ -55,6 +55,10 @@ struct DecodeArgs {
     float *out_part, *lse_part;
     uint32_t *status;
     cudaStream_t stream;
+    // bf16 elements from one V row to the next: head_dim_v for a separate V
+    // pool; head_dim_k when the values are the first head_dim_v dims of the
+    // key rows (v_pool then points at the K pool).
+    int32_t v_stride = 0;
 };
 bool tma_kernel_supports(const pkv_cache_desc &c, int32_t num_q_heads);
 int launch_decode_tma(const DecodeArgs &a);

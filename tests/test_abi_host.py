@@ -87,6 +87,25 @@ def test_host_validation_rejects_before_any_launch(pkv):
     assert lib.pkv_lse_merge(0, p, p, 4, 128, p, p, None) == -1
 
 
+def test_values_inside_keys_host_rules(pkv):
+    """v_pool NULL = the values are the first head_dim_v dims of each key row:
+    append needs v_new NULL as well, and head_dim_v may not exceed head_dim_k."""
+    lib = pkv.lib
+    p = ctypes.c_void_p(0x1000)
+    latent = pkv.CacheDesc(16, 64, 1, 576, 512)
+    wide = pkv.CacheDesc(16, 64, 1, 128, 256)
+    # one of v_pool / v_new NULL, the other not
+    assert lib.pkv_kv_append(ctypes.byref(latent), p, None, p, p, p, 1, None) == -1
+    assert lib.pkv_kv_append(ctypes.byref(latent), p, p, p, None, p, 1, None) == -1
+    # values wider than the keys cannot live inside them
+    assert lib.pkv_kv_append(ctypes.byref(wide), p, None, p, None, p, 1, None) == -2
+    assert lib.pkv_copy_blocks(ctypes.byref(wide), p, None, p, p, 1, None) == -2
+    assert lib.pkv_paged_decode_attn(ctypes.byref(wide), p, 1, 16, p, None, p, 4, p, 1.0, 1,
+                                     None, 0, p, p, 0, None) == -2
+    assert lib.pkv_paged_decode_attn_partial(ctypes.byref(wide), p, 1, 16, p, None, p, 4, p,
+                                             1.0, 2, p, p, 0, None) == -2
+
+
 def test_workspace_size(pkv):
     assert pkv.decode_workspace_size(8, 32, 128, 1) == 0
     n = pkv.decode_workspace_size(8, 32, 128, 16)

@@ -54,14 +54,14 @@ class Workload:
     block_size: int
     q: torch.Tensor                 # [B, Hq, Dk] fp32
     k_pool: torch.Tensor            # [num_blocks, Hkv, bs, Dk] bf16, cache before the step
-    v_pool: torch.Tensor            # [num_blocks, Hkv, bs, Dv] bf16
+    v_pool: torch.Tensor | None     # [num_blocks, Hkv, bs, Dv] bf16; None: values inside K
     block_tables: torch.Tensor      # [B, max_blocks] int32, -1 past the last used block
     seq_lens: torch.Tensor          # [B] int32, tokens attended after the appends
     scale: float
     new_seq: torch.Tensor           # [T] int32, sequence of each appended token
     new_pos: torch.Tensor           # [T] int64, logical position of each appended token
     k_new: torch.Tensor             # [T, Hkv, Dk] bf16
-    v_new: torch.Tensor             # [T, Hkv, Dv] bf16
+    v_new: torch.Tensor | None      # [T, Hkv, Dv] bf16; None: values inside K
     cow_src: torch.Tensor = field(default_factory=lambda: torch.empty(0, dtype=torch.int32))
     cow_dst: torch.Tensor = field(default_factory=lambda: torch.empty(0, dtype=torch.int32))
     # DCP-style interleaved partitions (dcp200k only): the partition count and
@@ -186,11 +186,13 @@ def dcp200k(seed: int = 4, context: int = 200_000, num_parts: int = 4,
 
 
 def agent_mla(seed: int = 5, num_seqs: int = 32, prefix: int = 136_040,
-              suffix_range=(2000, 10000)) -> Workload:
+              suffix_range=(2000, 10000), latent: bool = False) -> Workload:
     """Shared-prefix MLA-shaped decode.  The prefix fills 2,125 blocks of 64
     tokens plus a shared tail block holding prefix % 64 tokens; every sequence
     first copies the tail into a private block (copy-on-write), then appends its
-    suffix and its decode token, and attends over prefix + suffix + 1 tokens."""
+    suffix and its decode token, and attends over prefix + suffix + 1 tokens.
+    latent: the cache keeps no value pool (v_pool and v_new are None); a
+    token's value is the first 512 dims of its 576-dim key row."""
     g = torch.Generator().manual_seed(seed)
     hq, hkv, dk, dv, bs = 128, 1, 576, 512, 64
     suffix = torch.randint(suffix_range[0], suffix_range[1] + 1, (num_seqs,), generator=g).tolist()
@@ -216,7 +218,7 @@ def agent_mla(seed: int = 5, num_seqs: int = 32, prefix: int = 136_040,
         cow_src = torch.empty(0, dtype=torch.int32)
         cow_dst = torch.empty(0, dtype=torch.int32)
     k_pool = _normal(g, (num_blocks, hkv, bs, dk), torch.bfloat16)
-    v_pool = _normal(g, (num_blocks, hkv, bs, dv), torch.bfloat16)
+    v_pool = None if latent else _normal(g, (num_blocks, hkv, bs, dv), torch.bfloat16)
     q = _normal(g, (num_seqs, hq, dk))
     seq_ids, positions = [], []
     for b in range(num_seqs):
@@ -227,8 +229,9 @@ def agent_mla(seed: int = 5, num_seqs: int = 32, prefix: int = 136_040,
     new_pos = torch.cat(positions)
     T = int(new_seq.numel())
     k_new = _normal(g, (T, hkv, dk), torch.bfloat16)
-    v_new = _normal(g, (T, hkv, dv), torch.bfloat16)
-    w = Workload("agent_mla", hq, hkv, dk, dv, bs, q, k_pool, v_pool, tables,
+    v_new = None if latent else _normal(g, (T, hkv, dv), torch.bfloat16)
+    w = Workload("agent_mla_latent" if latent else "agent_mla", hq, hkv, dk, dv, bs, q, k_pool,
+                 v_pool, tables,
                  torch.tensor(lens, dtype=torch.int32), 1.0 / math.sqrt(dk),
                  new_seq, new_pos, k_new, v_new, cow_src, cow_dst)
     w.info = {"prefix": prefix, "suffix": suffix, "shared_blocks": shared,
@@ -257,6 +260,8 @@ def custom(seed: int, cached: list[int], hq: int, hkv: int, dk: int, dv: int, bs
 
 
 def make(name: str, **kw) -> Workload:
+    if name == "agent_mla_latent":
+        return agent_mla(latent=True, **kw)
     return {"tiny": tiny, "mix": mix, "long32k": long32k, "dcp200k": dcp200k,
             "agent_mla": agent_mla}[name](**kw)
 
