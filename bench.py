@@ -77,9 +77,10 @@ def step_bytes(w, splits: int):
     lens = w.seq_lens.to(torch.int64)
     kv = unique_kv_tokens(w) * kv_bytes_per_token(w)
     B, Hq = w.batch, w.num_q_heads
-    q = B * Hq * w.head_dim_k * 4
+    rows = w.q.numel() // w.head_dim_k          # (sequence, query token, head) rows
+    q = rows * w.head_dim_k * 4
     tables = int(((lens + w.block_size - 1) // w.block_size).sum()) * 4 + B * 4
-    out = B * Hq * (w.head_dim_v + 1) * 4
+    out = rows * (w.head_dim_v + 1) * 4
     T = int(w.new_pos.numel())
     append = 2 * T * kv_bytes_per_token(w) + T * (8 + 4 + 8)
     kernel = kv + q + tables
@@ -339,10 +340,51 @@ class AgentStep(Step):
         super().run(ev_a, ev_b)
 
 
+class MultiStep(Step):
+    """Speculative verification: T new tokens per sequence appended, each
+    attending causally to the cache (one pkv_paged_decode_attn_multi)."""
+
+    def __init__(self, pkv, w, dev, splits):
+        super().__init__(pkv, w, dev, splits)
+        B, T, Hq, Dv = w.batch, w.tokens_per_seq, w.num_q_heads, w.head_dim_v
+        self.out = torch.empty(B, T, Hq, Dv, device=dev)
+        self.lse = torch.empty(B, T, Hq, device=dev)
+        need = pkv.lib.pkv_decode_multi_workspace_size(B, T, Hq, Dv, w.max_blocks, splits)
+        self.ws = torch.zeros(need, dtype=torch.uint8, device=dev)
+        # the rows the multi call attends, for timing its split kernel alone
+        self.q_rows = self.q.view(B * T, Hq, w.head_dim_k)
+        self.x_tables = self.bt.repeat_interleave(T, dim=0)
+        t = torch.arange(T, dtype=torch.int32, device=dev).repeat(B)
+        self.x_lens = (self.lens.repeat_interleave(T) - (T - 1) + t).to(torch.int32)
+        self.out_part = torch.empty(splits, B * T, Hq, Dv, device=dev)
+        self.lse_part = torch.empty(splits, B * T, Hq, device=dev)
+        self.launches = 5   # slot, append, row views, split, merge
+        self.desc = (f"slot_mapping + kv_append ({w.new_pos.numel()} new tokens, {T} per "
+                     f"sequence) + paged_decode_attn_multi ({splits} splits) = row views + "
+                     f"split kernel + lse_merge")
+
+    def kernel(self):
+        self.pkv.paged_decode_attn_partial(self.q_rows, self.k, self.v, self.x_tables,
+                                           self.x_lens, self.w.scale, self.splits,
+                                           out_part=self.out_part, lse_part=self.lse_part)
+
+    def attend(self, ev_a=None, ev_b=None):
+        if ev_a is None:
+            self.pkv.paged_decode_attn_multi(self.q, self.k, self.v, self.bt, self.lens,
+                                             self.w.scale, num_splits=self.splits,
+                                             workspace=self.ws, out=self.out, lse=self.lse)
+            return
+        ev_a.record()
+        self.kernel()
+        ev_b.record()
+        self.pkv.lse_merge(self.out_part, self.lse_part, out=self.out.view(-1, *self.out.shape[2:]),
+                           lse=self.lse.view(-1, self.lse.shape[2]))
+
+
 STEPS = {"long32k": Step, "mix": Step, "tiny": Step, "dcp200k": DcpStep, "agent_mla": AgentStep,
-         "agent_mla_latent": AgentStep}
+         "agent_mla_latent": AgentStep, "spec4_32k": MultiStep}
 DEFAULT_SPLITS = {"long32k": 16, "mix": 1, "tiny": 1, "dcp200k": 19, "agent_mla": 19,
-                  "agent_mla_latent": 19}
+                  "agent_mla_latent": 19, "spec4_32k": 16}
 
 
 # ------------------------------------------------------------------ arms
@@ -392,7 +434,12 @@ def oracle_gbs(w, tokens: int | None, repeats: int = 1):
     times = []
     for _ in range(repeats):
         t = time.perf_counter()
-        oracle.paged_decode_attn(q, kp, vp, bt, lens, w.scale, tok_end=end)
+        if w.tokens_per_seq > 1:
+            # the same step on each sequence's first tokens: query t sees the
+            # sample's tokens up to its own
+            oracle.paged_decode_attn_multi(q, kp, vp, bt, lens if end is None else end, w.scale)
+        else:
+            oracle.paged_decode_attn(q, kp, vp, bt, lens, w.scale, tok_end=end)
         times.append(time.perf_counter() - t)
     return used, times
 

@@ -249,6 +249,33 @@ int pkv_paged_decode_attn_noalloc(const pkv_cache_desc *cache, const float *q, i
                                   float *out, float *lse, int32_t flags, pkv_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * pkv_paged_decode_attn_multi -- several new tokens per sequence in one step
+ * (e.g. verifying speculated tokens; [AX] names a speculative-verification
+ * path among its decode kernels).  The last tokens_per_seq (T) of the
+ * seq_lens[b] stored tokens of sequence b are the new ones, already appended;
+ * query t (0-based) attends causally to the tokens j < seq_lens[b] - T + 1 + t:
+ *     out[b][t][h][:], lse[b][t][h] = decode attention of q[b][t][h][:] over
+ *     those tokens (the definition of pkv_paged_decode_attn).
+ * q [batch][T][num_q_heads][head_dim_k], out [batch][T][num_q_heads][head_dim_v],
+ * lse [batch][T][num_q_heads], fp32.  1 <= T <= 64.  A sequence holding fewer
+ * than T tokens sets PKV_DEV_SEQ_LEN and its rows with no token give out = 0,
+ * lse = -inf.  Splits, kernels and flags as for pkv_paged_decode_attn
+ * (num_splits = 0: chosen for batch * T rows).  workspace: at least
+ * pkv_decode_multi_workspace_size(...) bytes (never 0: it holds the T
+ * per-token views of the block tables); contents on entry do not matter.
+ * ------------------------------------------------------------------------- */
+size_t pkv_decode_multi_workspace_size(int32_t batch, int32_t tokens_per_seq,
+                                       int32_t num_q_heads, int32_t head_dim_v,
+                                       int32_t max_blocks, int32_t num_splits);
+
+int pkv_paged_decode_attn_multi(const pkv_cache_desc *cache, const float *q, int32_t batch,
+                                int32_t tokens_per_seq, int32_t num_q_heads, const void *k_pool,
+                                const void *v_pool, const int32_t *block_tables,
+                                int32_t max_blocks, const int32_t *seq_lens, float scale,
+                                int32_t num_splits, void *workspace, size_t workspace_bytes,
+                                float *out, float *lse, int32_t flags, pkv_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * pkv_lse_merge -- [DCP] decode step, stage 3: correct each partial output
  * with the shared LSEs and sum.  For each row r:
  *     M = max_p lse_part[p][r],  w_p = e^{lse_part[p][r] - M},

@@ -214,3 +214,21 @@ def paged_decode_attn(q, k_pool, v_pool, block_tables, seq_lens, scale: float,
     if rc != 0:
         raise ValueError("oracle_paged_decode_attn: inconsistent arguments")
     return out, lse
+
+
+def paged_decode_attn_multi(q, k_pool, v_pool, block_tables, seq_lens, scale: float,
+                            num_threads: int = 0):
+    """Several new tokens per sequence: q [B, T, Hq, Dk].  The last T of the
+    seq_lens[b] stored tokens are the new ones, and query t attends to the
+    tokens j < seq_lens[b] - T + 1 + t (causal among the new tokens): each
+    (sequence, query token) is an ordinary decode over that token range.
+    Returns (out [B, T, Hq, Dv], lse [B, T, Hq]) in fp64."""
+    q = np.ascontiguousarray(q, dtype=np.float32)
+    B, T, Hq, Dk = q.shape
+    tables = np.repeat(np.asarray(block_tables, dtype=np.int32), T, axis=0)
+    lens = np.repeat(np.asarray(seq_lens, dtype=np.int32), T)
+    t = np.tile(np.arange(T, dtype=np.int32), B)
+    end = np.maximum(lens - (T - 1) + t, 0).astype(np.int32)
+    out, lse = paged_decode_attn(q.reshape(B * T, Hq, Dk), k_pool, v_pool, tables, lens, scale,
+                                 tok_end=end, num_threads=num_threads)
+    return out.reshape(B, T, Hq, -1), lse.reshape(B, T, Hq)

@@ -23,7 +23,8 @@ from ._lib import (DECODE_GENERIC, DECODE_NO_TCGEN05, DEV_BLOCK_ID, DEV_COPY_CON
 __all__ = [
     "CacheDesc", "PkvError", "ValuesInKeys", "cache_desc", "kv_append", "slot_mapping", "copy_blocks",
     "interleave_slot_mapping", "interleave_partition_len", "decode_workspace_size",
-    "decode_auto_splits", "paged_decode_attn", "paged_decode_attn_partial", "lse_merge",
+    "decode_auto_splits", "paged_decode_attn", "paged_decode_attn_partial",
+    "paged_decode_attn_multi", "lse_merge",
     "device_status", "BlockManager", "library_path", "DECODE_GENERIC", "DECODE_NO_TCGEN05",
     "DEV_BLOCK_ID",
     "DEV_SLOT", "DEV_SEQ_LEN", "DEV_COPY_CONFLICT", "DEV_TIMEOUT", "DEV_TABLE_RANGE",
@@ -216,6 +217,36 @@ def paged_decode_attn_partial(q, k_pool, v_pool, block_tables, seq_lens, scale: 
         block_tables.shape[1], _ptr(seq_lens), float(scale), S, _ptr(out_part), _ptr(lse_part),
         int(flags), _stream(stream)))
     return out_part, lse_part
+
+
+def paged_decode_attn_multi(q, k_pool, v_pool, block_tables, seq_lens, scale: float,
+                            num_splits: int = 0, workspace=None, out=None, lse=None,
+                            flags: int = 0, stream=None):
+    """Several new tokens per sequence (q [B, T, Hq, Dk]); query t attends to
+    the first seq_lens[b] - T + 1 + t tokens -> (out [B, T, Hq, Dv], lse [B, T, Hq])."""
+    desc = cache_desc(k_pool, v_pool)
+    _need(q, "q", torch.float32, 4)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    B, T, Hq, _ = q.shape
+    if out is None:
+        out = torch.empty(B, T, Hq, desc.head_dim_v, dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty(B, T, Hq, dtype=torch.float32, device=q.device)
+    S = num_splits
+    if S == 0:
+        S = int(lib.pkv_decode_auto_splits(ctypes.byref(desc), B * T, Hq,
+                                           block_tables.shape[1] * desc.block_size))
+    need = int(lib.pkv_decode_multi_workspace_size(B, T, Hq, desc.head_dim_v,
+                                                   block_tables.shape[1], S))
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    _check("pkv_paged_decode_attn_multi", lib.pkv_paged_decode_attn_multi(
+        ctypes.byref(desc), _ptr(q), B, T, Hq, _ptr(k_pool), _v_ptr(v_pool),
+        _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), float(scale), S,
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out), _ptr(lse),
+        int(flags), _stream(stream)))
+    return out, lse
 
 
 def lse_merge(out_part, lse_part, out=None, lse=None, stream=None):

@@ -55,6 +55,10 @@ SIGNATURES = {
                                                      _P, _f32, _i32, _P, _P, _i32, _P]),
     "pkv_paged_decode_attn_noalloc": (ctypes.c_int, [_DESC, _P, _i32, _i32, _P, _P, _P, _i32,
                                                      _P, _f32, _i32, _P, _P, _i32, _P]),
+    "pkv_decode_multi_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32]),
+    "pkv_paged_decode_attn_multi": (ctypes.c_int, [_DESC, _P, _i32, _i32, _i32, _P, _P, _P,
+                                                   _i32, _P, _f32, _i32, _P, _sz, _P, _P, _i32,
+                                                   _P]),
     "pkv_lse_merge": (ctypes.c_int, [_i32, _P, _P, _i64, _i32, _P, _P, _P]),
     "pkv_bm_create": (_P, [_i32, _i32, _P]),
     "pkv_bm_destroy": (None, [_P]),

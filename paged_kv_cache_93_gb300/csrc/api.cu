@@ -5,6 +5,7 @@
 #include <algorithm>
 
 #include "pkv.h"
+#include "pkv_device.cuh"
 #include "pkv_host.h"
 
 using namespace pkv;
@@ -175,4 +176,114 @@ extern "C" int pkv_lse_merge(int32_t num_parts, const float *out_part, const flo
     if (rows > int64_t(INT32_MAX)) return PKV_ERR_SHAPE;
     return launch_lse_merge(num_parts, out_part, lse_part, rows, head_dim_v, out, lse,
                             reinterpret_cast<cudaStream_t>(stream));
+}
+
+namespace {
+
+constexpr int32_t kMaxQueryTokens = 64;
+
+// Row r = b * T + t of a multi-token step reads sequence b's table and
+// attends to its first seq_lens[b] - T + 1 + t tokens.  A negative length
+// (a sequence holding fewer than T tokens) is flagged by the split kernel
+// and treated as empty there.
+__global__ void multi_rows_kernel(const int32_t *__restrict__ block_tables,
+                                  const int32_t *__restrict__ seq_lens, int32_t batch,
+                                  int32_t tokens, int32_t max_blocks,
+                                  int32_t *__restrict__ row_tables, int32_t *__restrict__ row_lens) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int64_t rows = int64_t(batch) * tokens;
+    const int64_t entries = rows * max_blocks;
+    for (int64_t u = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; u < entries + rows;
+         u += int64_t(gridDim.x) * blockDim.x) {
+        if (u < entries) {
+            const int64_t r = u / max_blocks, i = u - r * max_blocks;
+            row_tables[u] = block_tables[(r / tokens) * max_blocks + i];
+        } else {
+            const int64_t r = u - entries, b = r / tokens;
+            row_lens[r] = seq_lens[b] - (tokens - 1) + int32_t(r - b * tokens);
+        }
+    }
+}
+
+struct MultiLayout {
+    size_t tables, lens, partials, total;
+};
+MultiLayout multi_layout(int32_t batch, int32_t tokens, int32_t num_q_heads, int32_t head_dim_v,
+                         int32_t max_blocks, int32_t num_splits) {
+    MultiLayout m;
+    const size_t rows = size_t(batch) * tokens;
+    m.tables = 0;
+    m.lens = align256(rows * size_t(max_blocks) * sizeof(int32_t));
+    m.partials = m.lens + align256(rows * sizeof(int32_t));
+    m.total = m.partials + pkv_decode_workspace_size(int32_t(rows), num_q_heads, head_dim_v,
+                                                     num_splits);
+    return m;
+}
+
+}  // namespace
+
+extern "C" size_t pkv_decode_multi_workspace_size(int32_t batch, int32_t tokens_per_seq,
+                                                  int32_t num_q_heads, int32_t head_dim_v,
+                                                  int32_t max_blocks, int32_t num_splits) {
+    if (batch <= 0 || tokens_per_seq <= 0 || num_q_heads <= 0 || head_dim_v <= 0 ||
+        max_blocks < 0 || num_splits < 0 || int64_t(batch) * tokens_per_seq > 65535)
+        return 0;
+    return multi_layout(batch, tokens_per_seq, num_q_heads, head_dim_v, max_blocks,
+                        std::max(num_splits, 1)).total;
+}
+
+extern "C" int pkv_paged_decode_attn_multi(const pkv_cache_desc *cache, const float *q,
+                                           int32_t batch, int32_t tokens_per_seq,
+                                           int32_t num_q_heads, const void *k_pool,
+                                           const void *v_pool, const int32_t *block_tables,
+                                           int32_t max_blocks, const int32_t *seq_lens,
+                                           float scale, int32_t num_splits, void *workspace,
+                                           size_t workspace_bytes, float *out, float *lse,
+                                           int32_t flags, pkv_stream_t stream) {
+    if (tokens_per_seq < 1 || tokens_per_seq > kMaxQueryTokens) return PKV_ERR_INVALID_ARG;
+    if (batch > 0 && int64_t(batch) * tokens_per_seq > 65535) return PKV_ERR_SHAPE;
+    const int32_t rows = batch * tokens_per_seq;
+    int st = validate_decode(cache, q, rows, num_q_heads, k_pool, v_pool, block_tables,
+                             max_blocks, seq_lens, num_splits, flags);
+    if (st != PKV_OK || batch == 0) return st;
+    if (!out || !lse) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(out)) return PKV_ERR_ALIGNMENT;
+    int32_t S = num_splits;
+    if (S == 0)
+        S = auto_splits(*cache, rows, num_q_heads,
+                        int32_t(std::min<int64_t>(int64_t(max_blocks) * cache->block_size,
+                                                  INT32_MAX)));
+    const MultiLayout m = multi_layout(batch, tokens_per_seq, num_q_heads, cache->head_dim_v,
+                                       max_blocks, S);
+    if (!workspace || workspace_bytes < m.total) return PKV_ERR_WORKSPACE_TOO_SMALL;
+    if (!aligned16(workspace)) return PKV_ERR_ALIGNMENT;
+    uint32_t *status = status_word();
+    if (!status) return PKV_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    char *ws = static_cast<char *>(workspace);
+    int32_t *row_tables = reinterpret_cast<int32_t *>(ws + m.tables);
+    int32_t *row_lens = reinterpret_cast<int32_t *>(ws + m.lens);
+    const int64_t work = int64_t(rows) * (int64_t(max_blocks) + 1);
+    const int threads = 256;
+    st = launch_pdl(multi_rows_kernel,
+                    dim3(unsigned(std::min<int64_t>((work + threads - 1) / threads,
+                                                    int64_t(sm_count()) * 8))),
+                    dim3(threads), 0, s, block_tables, seq_lens, batch, tokens_per_seq,
+                    max_blocks, row_tables, row_lens);
+    if (st != PKV_OK) return st;
+    DecodeArgs a{*cache, q, rows, num_q_heads, k_pool, v_pool, row_tables, max_blocks,
+                 row_lens, scale, S, out, lse, status, s};
+    values_from(a);
+    if (S == 1) return run_split_kernel(a, flags);
+    const size_t prow = size_t(S) * rows * num_q_heads;
+    float *out_part = reinterpret_cast<float *>(ws + m.partials);
+    float *lse_part = reinterpret_cast<float *>(
+        ws + m.partials + align256(prow * cache->head_dim_v * sizeof(float)));
+    a.out_part = out_part;
+    a.lse_part = lse_part;
+    st = run_split_kernel(a, flags);
+    if (st != PKV_OK) return st;
+    return launch_lse_merge(S, out_part, lse_part, int64_t(rows) * num_q_heads,
+                            cache->head_dim_v, out, lse, s);
 }

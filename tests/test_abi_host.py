@@ -87,6 +87,22 @@ def test_host_validation_rejects_before_any_launch(pkv):
     assert lib.pkv_lse_merge(0, p, p, 4, 128, p, p, None) == -1
 
 
+def test_multi_token_host_rules(pkv):
+    lib = pkv.lib
+    p = ctypes.c_void_p(0x1000)
+    desc = pkv.CacheDesc(16, 16, 8, 128, 128)
+    args = lambda T, S, ws, nbytes: (ctypes.byref(desc), p, 2, T, 32, p, p, p, 4, p, 1.0, S, ws,
+                                     nbytes, p, p, 0, None)
+    assert lib.pkv_paged_decode_attn_multi(*args(0, 2, p, 1 << 30)) == -1     # no query token
+    assert lib.pkv_paged_decode_attn_multi(*args(65, 2, p, 1 << 30)) == -1    # more than 64
+    need = lib.pkv_decode_multi_workspace_size(2, 4, 32, 128, 4, 2)
+    # the per-token views of the tables + the split partials of 8 rows
+    assert need >= 2 * 4 * 4 * 4 + 2 * 4 * 4 + pkv.decode_workspace_size(8, 32, 128, 2)
+    assert lib.pkv_paged_decode_attn_multi(*args(4, 2, None, 0)) == -4
+    assert lib.pkv_paged_decode_attn_multi(*args(4, 2, p, need - 1)) == -4
+    assert lib.pkv_decode_multi_workspace_size(2, 0, 32, 128, 4, 2) == 0
+
+
 def test_values_inside_keys_host_rules(pkv):
     """v_pool NULL = the values are the first head_dim_v dims of each key row:
     append needs v_new NULL as well, and head_dim_v may not exceed head_dim_k."""

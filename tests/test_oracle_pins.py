@@ -438,3 +438,46 @@ def test_copy_on_write_leaves_other_sequence_unchanged():
     after_o, after_l = oracle.paged_decode_attn(q, k, v, tables, np.array([10, 11], np.int32), 0.3)
     assert np.array_equal(after_o[0], before_o[0]) and np.array_equal(after_l[0], before_l[0])
     assert not np.array_equal(after_o[1], before_o[1])
+
+
+# ------------------------------------------------------- multi-token decode
+
+@pytest.mark.parametrize("T", [1, 2, 5])
+def test_multi_token_matches_causal_mask_brute_force(T):
+    """Query t of T new tokens sees the context and new tokens 0..t: one
+    causal mask over the whole [T x L] score matrix, softmax row by row."""
+    B, Hq, Hkv, D, bs = 3, 4, 2, 16, 4
+    _, k, v, tables, L = rand_case(41 + T, B, Hq, Hkv, D, bs, [9, 14, 5])
+    q = np.random.default_rng(7 + T).standard_normal((B, T, Hq, D)).astype(np.float32)
+    out, lse = oracle.paged_decode_attn_multi(q, k, v, tables, L, 0.25)
+    K, V = bf16_values(k), bf16_values(v)
+    for b in range(B):
+        n = int(L[b])
+        idx = np.arange(n)
+        phys, off = tables[b][idx // bs], idx % bs
+        for h in range(Hq):
+            g = h // (Hq // Hkv)
+            Kc, Vc = K[phys, g, off], V[phys, g, off]
+            S = 0.25 * (q[b, :, h].astype(np.float64) @ Kc.T)          # [T, n]
+            future = idx[None, :] > (n - T + np.arange(T))[:, None]
+            S = np.where(future, -np.inf, S)
+            for t in range(T):
+                np.testing.assert_allclose(out[b, t, h], softmax(S[t]) @ Vc, rtol=0, atol=1e-12)
+                assert abs(lse[b, t, h] - logsumexp(S[t])) < 1e-12
+
+
+def test_multi_token_special_cases():
+    """T = 1 is ordinary decode; the last new token sees every stored token;
+    a sequence holding fewer tokens than T leaves its first queries empty."""
+    q1, k, v, tables, L = rand_case(5, 2, 4, 4, 8, 4, [7, 12])
+    o1, l1 = oracle.paged_decode_attn(q1, k, v, tables, L, 0.5)
+    om, lm = oracle.paged_decode_attn_multi(q1[:, None], k, v, tables, L, 0.5)
+    assert np.array_equal(om[:, 0], o1) and np.array_equal(lm[:, 0], l1)
+    q3 = np.random.default_rng(9).standard_normal((2, 3, 4, 8)).astype(np.float32)
+    o3, l3 = oracle.paged_decode_attn_multi(q3, k, v, tables, L, 0.5)
+    of, lf = oracle.paged_decode_attn(q3[:, 2], k, v, tables, L, 0.5)
+    assert np.array_equal(o3[:, 2], of) and np.array_equal(l3[:, 2], lf)
+    short = np.array([1, 12], dtype=np.int32)
+    os_, ls_ = oracle.paged_decode_attn_multi(q3, k, v, tables, short, 0.5)
+    assert np.all(np.isneginf(ls_[0, :2])) and np.all(os_[0, :2] == 0)
+    assert np.isfinite(ls_[0, 2]).all()

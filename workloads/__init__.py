@@ -73,6 +73,9 @@ class Workload:
     k_tokens: torch.Tensor | None = None         # [N, Hkv, Dk] bf16
     v_tokens: torch.Tensor | None = None         # [N, Hkv, Dv] bf16
     info: dict = field(default_factory=dict)
+    # Multi-token steps: q is [B, tokens_per_seq, Hq, Dk] and the last
+    # tokens_per_seq tokens of each sequence are the step's new ones.
+    tokens_per_seq: int = 1
 
     @property
     def batch(self) -> int:
@@ -152,6 +155,32 @@ def long32k(seed: int = 3, batch: int = 8, context: int = 32768) -> Workload:
     num_blocks = batch * context // bs
     return _gqa("long32k", seed, [context - 1] * batch, hq=32, hkv=8, d=128, bs=bs,
                 num_blocks=num_blocks)
+
+
+def spec_verify(seed: int = 6, batch: int = 8, context: int = 32768, tokens: int = 4,
+                hq: int = 32, hkv: int = 8, d: int = 128, bs: int = 16,
+                name: str = "spec4_32k") -> Workload:
+    """Speculative verification: batch x `context` tokens, the last `tokens`
+    of each sequence appended in the step; each new token queries the cache
+    causally (query t sees the context up to and including new token t).
+    Every block of the pool is used when context is a multiple of bs."""
+    g = torch.Generator().manual_seed(seed)
+    counts = [_ceil_div(context, bs)] * batch
+    num_blocks = sum(counts)
+    perm = torch.randperm(num_blocks, generator=g)
+    tables = _tables(perm, counts, max(counts))
+    k_pool = _normal(g, (num_blocks, hkv, bs, d), torch.bfloat16)
+    v_pool = _normal(g, (num_blocks, hkv, bs, d), torch.bfloat16)
+    q = _normal(g, (batch, tokens, hq, d))
+    new_seq = torch.arange(batch, dtype=torch.int32).repeat_interleave(tokens)
+    new_pos = (context - tokens + torch.arange(tokens, dtype=torch.int64)).repeat(batch)
+    k_new = _normal(g, (batch * tokens, hkv, d), torch.bfloat16)
+    v_new = _normal(g, (batch * tokens, hkv, d), torch.bfloat16)
+    w = Workload(name, hq, hkv, d, d, bs, q, k_pool, v_pool, tables,
+                 torch.full((batch,), context, dtype=torch.int32), 1.0 / math.sqrt(d),
+                 new_seq, new_pos, k_new, v_new)
+    w.tokens_per_seq = tokens
+    return w
 
 
 def dcp200k(seed: int = 4, context: int = 200_000, num_parts: int = 4,
@@ -262,6 +291,8 @@ def custom(seed: int, cached: list[int], hq: int, hkv: int, dk: int, dv: int, bs
 def make(name: str, **kw) -> Workload:
     if name == "agent_mla_latent":
         return agent_mla(latent=True, **kw)
+    if name == "spec4_32k":
+        return spec_verify(**kw)
     return {"tiny": tiny, "mix": mix, "long32k": long32k, "dcp200k": dcp200k,
             "agent_mla": agent_mla}[name](**kw)
 
