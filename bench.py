@@ -505,8 +505,31 @@ def run_gpu(args, world, rank, local):
     if pkv.device_status(reset=True) != 0:
         raise RuntimeError("device status word set during warm-up")
 
-    # ---- timed region: K steps back to back; events around the attention
-    # kernel(s) of every step give its launch duration.
+    # One step captured in a CUDA graph (the library's calls allocate nothing
+    # and never synchronise with the host, so they capture as they are); the
+    # timed steps replay it, as a serving loop replays its decode step.
+    graph = None
+    per_graph = max(1, args.graph_steps)
+    if not args.eager:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for _ in range(per_graph):
+                st.run()
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+
+    # eager steps (the calls made one by one from Python), for context
+    ke = min(args.steps, 500)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(ke):
+        st.run()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    eager_ms = max_over_ranks(e0.elapsed_time(e1) / ke, world)
+
     # ---- timed region: K steps back to back, events only at its two ends
     K = args.steps
     ev_start = torch.cuda.Event(enable_timing=True)
@@ -518,8 +541,14 @@ def run_gpu(args, world, rank, local):
     torch.cuda.synchronize()
     t0 = time.time()
     ev_start.record(stream)
-    for _ in range(K):
-        st.run()
+    if graph is not None:
+        for _ in range(K // per_graph):
+            graph.replay()
+        for _ in range(K % per_graph):
+            st.run()
+    else:
+        for _ in range(K):
+            st.run()
     ev_end.record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -639,6 +668,8 @@ def run_gpu(args, world, rank, local):
             "num_kv_heads": w.num_kv_heads, "head_dim_k": w.head_dim_k,
             "head_dim_v": w.head_dim_v, "block_size": w.block_size, "num_splits": splits,
             "step": st.desc,
+            "launch": (f"CUDA graph of {per_graph} steps (captured once, replayed)"
+                       if graph is not None else "calls made one by one from Python"),
             "l2": f"no flush: the {total_bytes / 1e9:.3f} GB a step reads exceeds the 129 MB "
                   f"L2 (steps back to back)",
             "parallelism": "replicas" if world > 1 else "single GPU",
@@ -659,6 +690,9 @@ def run_gpu(args, world, rank, local):
                       ", C fp64 oracle, all host cores",
         },
         "e2e": e2e,
+        "eager": {"ms_per_step": round(eager_ms, 5),
+                  "value": round(world * total_bytes / (eager_ms * 1e-3) / 1e9, 2),
+                  "steps": ke},
         "gpu_launches": st.launches * K,
         "clocks": clocks,
     }
@@ -674,6 +708,10 @@ def main():
     ap.add_argument("--workload", default="long32k", choices=sorted(STEPS))
     ap.add_argument("--splits", type=int, default=0, help="0 = the workload's default")
     ap.add_argument("--quick-cpu", action="store_true", help="smaller oracle sample")
+    ap.add_argument("--eager", action="store_true",
+                    help="time the calls made one by one instead of a CUDA-graph replay")
+    ap.add_argument("--graph-steps", type=int, default=16,
+                    help="steps captured in one CUDA graph")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
