@@ -343,6 +343,8 @@ class AgentStep(Step):
 class MultiStep(Step):
     """Speculative verification: T new tokens per sequence appended, each
     attending causally to the cache (one pkv_paged_decode_attn_multi)."""
+    kernel_name = ("pkv_paged_decode_attn_multi (decode_tma_kernel with the T tokens as rows "
+                   "of each work item, + lse_merge)")
 
     def __init__(self, pkv, w, dev, splits):
         super().__init__(pkv, w, dev, splits)
@@ -351,34 +353,23 @@ class MultiStep(Step):
         self.lse = torch.empty(B, T, Hq, device=dev)
         need = pkv.lib.pkv_decode_multi_workspace_size(B, T, Hq, Dv, w.max_blocks, splits)
         self.ws = torch.zeros(need, dtype=torch.uint8, device=dev)
-        # the rows the multi call attends, for timing its split kernel alone
-        self.q_rows = self.q.view(B * T, Hq, w.head_dim_k)
-        self.x_tables = self.bt.repeat_interleave(T, dim=0)
-        t = torch.arange(T, dtype=torch.int32, device=dev).repeat(B)
-        self.x_lens = (self.lens.repeat_interleave(T) - (T - 1) + t).to(torch.int32)
-        self.out_part = torch.empty(splits, B * T, Hq, Dv, device=dev)
-        self.lse_part = torch.empty(splits, B * T, Hq, device=dev)
-        self.launches = 5   # slot, append, row views, split, merge
+        self.launches = 4   # slot, append, split (T tokens as rows of an item), merge
         self.desc = (f"slot_mapping + kv_append ({w.new_pos.numel()} new tokens, {T} per "
-                     f"sequence) + paged_decode_attn_multi ({splits} splits) = row views + "
-                     f"split kernel + lse_merge")
+                     f"sequence) + paged_decode_attn_multi ({splits} splits) = split kernel "
+                     f"with the {T} tokens as rows of each work item + lse_merge")
 
     def kernel(self):
-        self.pkv.paged_decode_attn_partial(self.q_rows, self.k, self.v, self.x_tables,
-                                           self.x_lens, self.w.scale, self.splits,
-                                           out_part=self.out_part, lse_part=self.lse_part)
+        """The multi-token attention call (its split kernel and merge)."""
+        self.pkv.paged_decode_attn_multi(self.q, self.k, self.v, self.bt, self.lens,
+                                         self.w.scale, num_splits=self.splits,
+                                         workspace=self.ws, out=self.out, lse=self.lse)
 
     def attend(self, ev_a=None, ev_b=None):
-        if ev_a is None:
-            self.pkv.paged_decode_attn_multi(self.q, self.k, self.v, self.bt, self.lens,
-                                             self.w.scale, num_splits=self.splits,
-                                             workspace=self.ws, out=self.out, lse=self.lse)
-            return
-        ev_a.record()
+        if ev_a is not None:
+            ev_a.record()
         self.kernel()
-        ev_b.record()
-        self.pkv.lse_merge(self.out_part, self.lse_part, out=self.out.view(-1, *self.out.shape[2:]),
-                           lse=self.lse.view(-1, self.lse.shape[2]))
+        if ev_b is not None:
+            ev_b.record()
 
 
 STEPS = {"long32k": Step, "mix": Step, "tiny": Step, "dcp200k": DcpStep, "agent_mla": AgentStep,

@@ -260,10 +260,20 @@ int pkv_paged_decode_attn_noalloc(const pkv_cache_desc *cache, const float *q, i
  * lse [batch][T][num_q_heads], fp32.  1 <= T <= 64.  A sequence holding fewer
  * than T tokens sets PKV_DEV_SEQ_LEN and its rows with no token give out = 0,
  * lse = -inf.  Splits, kernels and flags as for pkv_paged_decode_attn
- * (num_splits = 0: chosen for batch * T rows).  workspace: at least
+ * (num_splits = 0: pkv_decode_multi_auto_splits).  When the GQA TMA kernel
+ * takes the shape with G * T <= 16 rows per KV head (G = num_q_heads /
+ * num_kv_heads), the T tokens are extra rows of one work item and each K/V
+ * tile is read once; otherwise every (sequence, token) is attended as its own
+ * row.  workspace: at least
  * pkv_decode_multi_workspace_size(...) bytes (never 0: it holds the T
  * per-token views of the block tables); contents on entry do not matter.
  * ------------------------------------------------------------------------- */
+/* The split count num_splits = 0 resolves to for a multi-token call (same
+ * arguments as that call's shape and flags) on the current device. */
+int32_t pkv_decode_multi_auto_splits(const pkv_cache_desc *cache, int32_t batch,
+                                     int32_t tokens_per_seq, int32_t num_q_heads,
+                                     int32_t max_seq_len, int32_t flags);
+
 size_t pkv_decode_multi_workspace_size(int32_t batch, int32_t tokens_per_seq,
                                        int32_t num_q_heads, int32_t head_dim_v,
                                        int32_t max_blocks, int32_t num_splits);

@@ -235,8 +235,9 @@ def paged_decode_attn_multi(q, k_pool, v_pool, block_tables, seq_lens, scale: fl
         lse = torch.empty(B, T, Hq, dtype=torch.float32, device=q.device)
     S = num_splits
     if S == 0:
-        S = int(lib.pkv_decode_auto_splits(ctypes.byref(desc), B * T, Hq,
-                                           block_tables.shape[1] * desc.block_size))
+        S = int(lib.pkv_decode_multi_auto_splits(ctypes.byref(desc), B, T, Hq,
+                                                 block_tables.shape[1] * desc.block_size,
+                                                 int(flags)))
     need = int(lib.pkv_decode_multi_workspace_size(B, T, Hq, desc.head_dim_v,
                                                    block_tables.shape[1], S))
     if workspace is None or workspace.numel() * workspace.element_size() < need:

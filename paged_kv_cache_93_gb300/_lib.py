@@ -56,6 +56,7 @@ SIGNATURES = {
     "pkv_paged_decode_attn_noalloc": (ctypes.c_int, [_DESC, _P, _i32, _i32, _P, _P, _P, _i32,
                                                      _P, _f32, _i32, _P, _P, _i32, _P]),
     "pkv_decode_multi_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32]),
+    "pkv_decode_multi_auto_splits": (_i32, [_DESC, _i32, _i32, _i32, _i32, _i32]),
     "pkv_paged_decode_attn_multi": (ctypes.c_int, [_DESC, _P, _i32, _i32, _i32, _P, _P, _P,
                                                    _i32, _P, _f32, _i32, _P, _sz, _P, _P, _i32,
                                                    _P]),

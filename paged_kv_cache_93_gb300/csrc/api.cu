@@ -72,7 +72,7 @@ void values_from(DecodeArgs &a) {
 
 int run_split_kernel(const DecodeArgs &a, int32_t flags) {
     if (!(flags & PKV_DECODE_GENERIC)) {
-        if (tma_kernel_supports(a.cache, a.num_q_heads)) return launch_decode_tma(a);
+        if (tma_kernel_supports(a.cache, a.num_q_heads, a.q_tokens)) return launch_decode_tma(a);
         if (!(flags & PKV_DECODE_NO_TCGEN05) && mla_tc_kernel_supports(a.cache, a.num_q_heads))
             return launch_decode_mla_tc(a);
         if (mla_kernel_supports(a.cache, a.num_q_heads)) return launch_decode_mla(a);
@@ -223,6 +223,18 @@ MultiLayout multi_layout(int32_t batch, int32_t tokens, int32_t num_q_heads, int
 
 }  // namespace
 
+extern "C" int32_t pkv_decode_multi_auto_splits(const pkv_cache_desc *cache, int32_t batch,
+                                                int32_t tokens_per_seq, int32_t num_q_heads,
+                                                int32_t max_seq_len, int32_t flags) {
+    if (!cache || cache->num_kv_heads <= 0 || num_q_heads <= 0 || tokens_per_seq <= 0) return 1;
+    // Work items are (sequence, KV head, split) when the GQA kernel takes the
+    // T tokens as rows of one item; (sequence x token, KV head, split) otherwise.
+    const bool folded = !(flags & PKV_DECODE_GENERIC) &&
+                        tma_kernel_supports(*cache, num_q_heads, tokens_per_seq);
+    return auto_splits(*cache, folded ? batch : batch * tokens_per_seq, num_q_heads,
+                       max_seq_len);
+}
+
 extern "C" size_t pkv_decode_multi_workspace_size(int32_t batch, int32_t tokens_per_seq,
                                                   int32_t num_q_heads, int32_t head_dim_v,
                                                   int32_t max_blocks, int32_t num_splits) {
@@ -251,9 +263,9 @@ extern "C" int pkv_paged_decode_attn_multi(const pkv_cache_desc *cache, const fl
     if (!aligned16(out)) return PKV_ERR_ALIGNMENT;
     int32_t S = num_splits;
     if (S == 0)
-        S = auto_splits(*cache, rows, num_q_heads,
-                        int32_t(std::min<int64_t>(int64_t(max_blocks) * cache->block_size,
-                                                  INT32_MAX)));
+        S = pkv_decode_multi_auto_splits(
+            cache, batch, tokens_per_seq, num_q_heads,
+            int32_t(std::min<int64_t>(int64_t(max_blocks) * cache->block_size, INT32_MAX)), flags);
     const MultiLayout m = multi_layout(batch, tokens_per_seq, num_q_heads, cache->head_dim_v,
                                        max_blocks, S);
     if (!workspace || workspace_bytes < m.total) return PKV_ERR_WORKSPACE_TOO_SMALL;
@@ -262,6 +274,27 @@ extern "C" int pkv_paged_decode_attn_multi(const pkv_cache_desc *cache, const fl
     if (!status) return PKV_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     char *ws = static_cast<char *>(workspace);
+    const size_t prow = size_t(S) * rows * num_q_heads;
+    float *out_part = reinterpret_cast<float *>(ws + m.partials);
+    float *lse_part = reinterpret_cast<float *>(
+        ws + m.partials + align256(prow * cache->head_dim_v * sizeof(float)));
+    if (!(flags & PKV_DECODE_GENERIC) &&
+        tma_kernel_supports(*cache, num_q_heads, tokens_per_seq)) {
+        // The GQA kernel takes the T query tokens as extra rows of each work
+        // item (causal limits per row): every K/V tile is read once.
+        DecodeArgs a{*cache, q, batch, num_q_heads, k_pool, v_pool, block_tables, max_blocks,
+                     seq_lens, scale, S, out, lse, status, s};
+        values_from(a);
+        a.q_tokens = tokens_per_seq;
+        if (S == 1) return launch_decode_tma(a);
+        a.out_part = out_part;
+        a.lse_part = lse_part;
+        st = launch_decode_tma(a);
+        if (st != PKV_OK) return st;
+        return launch_lse_merge(S, out_part, lse_part, int64_t(rows) * num_q_heads,
+                                cache->head_dim_v, out, lse, s);
+    }
+    // Otherwise one row per (sequence, token): T views of each table row.
     int32_t *row_tables = reinterpret_cast<int32_t *>(ws + m.tables);
     int32_t *row_lens = reinterpret_cast<int32_t *>(ws + m.lens);
     const int64_t work = int64_t(rows) * (int64_t(max_blocks) + 1);
@@ -276,10 +309,6 @@ extern "C" int pkv_paged_decode_attn_multi(const pkv_cache_desc *cache, const fl
                  row_lens, scale, S, out, lse, status, s};
     values_from(a);
     if (S == 1) return run_split_kernel(a, flags);
-    const size_t prow = size_t(S) * rows * num_q_heads;
-    float *out_part = reinterpret_cast<float *>(ws + m.partials);
-    float *lse_part = reinterpret_cast<float *>(
-        ws + m.partials + align256(prow * cache->head_dim_v * sizeof(float)));
     a.out_part = out_part;
     a.lse_part = lse_part;
     st = run_split_kernel(a, flags);

@@ -2,7 +2,9 @@
 //
 // Work item = (sequence b, KV head g, split s): the chunk of tokens
 // [s*C, min(L, (s+1)*C)) of sequence b, C = 64 * ceil(L / (64 * S)), for all
-// G = Hq / Hkv query heads that share KV head g.  A persistent grid walks the
+// G query rows that share KV head g: the Hq / Hkv query heads of the group,
+// times T query tokens when a step brings T new tokens per sequence (row
+// (t, h) then attends causally: to the first L - T + 1 + t tokens).  A persistent grid walks the
 // items round-robin; each CTA has one producer warp and W consumer warps,
 // and several CTAs share an SM.
 //
@@ -47,7 +49,7 @@ constexpr int kRowBytes = 128;     // one 64-column half-row of bf16
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-// D: head dim (64 or 128); G: query heads per KV head (1, 2, 4, 8);
+// D: head dim (64 or 128); G: query rows per KV head (1, 2, 4, 8, 16);
 // W: consumer warps per CTA; NSTAGES: pipeline depth; MINB: CTAs per SM the
 // register allocation must allow.
 template <int D, int G, int W, int NSTAGES, int MINB>
@@ -58,6 +60,7 @@ struct Cfg {
     static constexpr int kTileBytes = kStageTokens * D * 2;    // K (or V) of one stage
     static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kNT = (2 * G + 7) / 8;                // 8-column n-tiles (hi|lo)
+    static constexpr int kSlots = G >= 8 ? G / 4 : 2;          // query rows held per lane
     static constexpr int kKSteps = D / 16;
     static constexpr int kMTiles = D / 16;
     static constexpr int kMergeFloats = W * (2 * G + G * D);
@@ -74,6 +77,7 @@ __device__ __forceinline__ int64_t lmax(int64_t x, int64_t y) { return x > y ? x
 
 struct ItemRange {
     int b, g, s;
+    int64_t len;                 // the sequence's token count (0 if invalid)
     int64_t begin, end;
     int nstages;
 };
@@ -91,19 +95,28 @@ __device__ __forceinline__ ItemRange item_range(const DecodeArgs &a, int item, i
         L = 0;
     }
     const int64_t chunk = 64 * ((L + 64LL * a.num_splits - 1) / (64LL * a.num_splits));
+    r.len = L;
     r.begin = int64_t(r.s) * chunk;
     r.end = lmin(L, r.begin + chunk);
     r.nstages = r.end > r.begin ? int((r.end - r.begin + stage_tokens - 1) / stage_tokens) : 0;
     return r;
 }
 
+// Row `row` (0..G-1) of an item -> offset of its query / output row in
+// units of one head vector: query token t = row / Gr of sequence b, head
+// g * Gr + row % Gr (Gr = G / T query heads per KV head).
+__device__ __forceinline__ int64_t row_offset(const DecodeArgs &a, int b, int g, int row, int Gr) {
+    const int t = row / Gr, h = row - t * Gr;
+    return (int64_t(b) * a.q_tokens + t) * a.num_q_heads + int64_t(g) * Gr + h;
+}
+
 // Column n (0..8*NT-1) of the packed [hi | lo] operand -> (head, is_lo), or
 // head = -1 for a zero padding column.
 template <int G>
 __device__ __forceinline__ int col_head(int n, bool &is_lo) {
-    if constexpr (G == 8) {
-        is_lo = n >= 8;
-        return n & 7;
+    if constexpr (G >= 8) {
+        is_lo = n >= G;
+        return n & (G - 1);
     } else {
         is_lo = n >= G;
         return n < 2 * G ? (n % G) : -1;
@@ -245,11 +258,18 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmap_k,
     float *mw = merge + warp * (2 * G + G * D);         // this warp's (m, l, O) for the merge
     const int r0 = lane >> 2;                           // token row (and +8) inside the slice
     const int tq = lane & 3;
-    // Head slots of this lane (columns 2*tq and 2*tq+1 of the packed tiles).
-    int slot_head[2];
-    bool slot_ok[2];
-    if constexpr (G == 8) {
-        slot_head[0] = 2 * tq; slot_head[1] = 2 * tq + 1; slot_ok[0] = slot_ok[1] = true;
+    // Query-row slots of this lane: columns 2*tq and 2*tq+1 of each packed
+    // hi tile (G >= 8: G/8 hi tiles, so G/4 slots; G <= 4: two slots, the
+    // hi and lo columns of a row meeting through a shuffle).
+    constexpr int NS = C::kSlots;
+    int slot_head[NS];
+    bool slot_ok[NS];
+    if constexpr (G >= 8) {
+#pragma unroll
+        for (int j = 0; j < NS; ++j) {
+            slot_head[j] = 8 * (j >> 1) + 2 * tq + (j & 1);
+            slot_ok[j] = true;
+        }
     } else if constexpr (G == 4) {
         slot_head[0] = 2 * (tq & 1); slot_head[1] = 2 * (tq & 1) + 1; slot_ok[0] = slot_ok[1] = true;
     } else if constexpr (G == 2) {
@@ -258,6 +278,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmap_k,
         slot_head[0] = 0; slot_head[1] = 0; slot_ok[0] = tq == 0; slot_ok[1] = false;
     }
     const float qscale = a.scale * kLog2e;
+    const int T = a.q_tokens, Gr = G / a.q_tokens;    // query tokens, heads per KV head
     // ldmatrix row addresses inside a stage (constant per lane).
     const int krow = 16 * warp + (lane & 7) + ((lane >> 3) & 1) * 8;   // A = K, non-transposed
     const int vrow = 16 * warp + (lane & 7) + (lane >> 4) * 8;         // A = V^T, transposed
@@ -273,11 +294,12 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmap_k,
         // Query fragments: B operand of S^T = K . Q^T, columns [q_hi | q_lo].
         uint32_t qf[C::kKSteps][C::kNT][2];
         {
-            const float *qbase = a.q + (int64_t(r.b) * a.num_q_heads + r.g * G) * D;
 #pragma unroll
             for (int nt = 0; nt < C::kNT; ++nt) {
                 bool is_lo;
                 const int head = col_head<G>(nt * 8 + r0, is_lo);
+                const float *qrow =
+                    a.q + (head >= 0 ? row_offset(a, r.b, r.g, head, Gr) : 0) * D;
 #pragma unroll
                 for (int ks = 0; ks < C::kKSteps; ++ks) {
 #pragma unroll
@@ -285,7 +307,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         float v[2] = {0.f, 0.f};
                         if (head >= 0) {
                             const int d = ks * 16 + 2 * tq + half * 8;
-                            const float2 x = *reinterpret_cast<const float2 *>(qbase + head * D + d);
+                            const float2 x = *reinterpret_cast<const float2 *>(qrow + d);
                             const float xs[2] = {x.x * qscale, x.y * qscale};
 #pragma unroll
                             for (int e = 0; e < 2; ++e) {
@@ -306,8 +328,14 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmap_k,
             for (int nt = 0; nt < C::kNT; ++nt)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.f;
-        float m2[2] = {-INFINITY, -INFINITY};
-        float l2[2] = {0.f, 0.f};
+        float m2[NS], l2[NS];
+        int64_t lim[NS];          // causal limit of the slot's row (T > 1)
+#pragma unroll
+        for (int j = 0; j < NS; ++j) {
+            m2[j] = -INFINITY;
+            l2[j] = 0.f;
+            lim[j] = r.len - (T - 1 - slot_head[j] / Gr);
+        }
 
         for (int st = 0; st < r.nstages && ok; ++st) {
             const uint32_t fb = smem_addr(&full_bar[stage]);
@@ -338,10 +366,12 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 __syncwarp();
             }
             if (nvalid > 0) {
-                // ---- S^T = K . [q_hi | q_lo]^T  (two accumulator sets for ILP)
-                float sacc[2][C::kNT][4];
+                // ---- S^T = K . [q_hi | q_lo]^T  (two accumulator sets for ILP
+                // when there are few n-tiles; G = 16 has four independent ones)
+                constexpr int kSets = C::kNT >= 4 ? 1 : 2;
+                float sacc[kSets][C::kNT][4];
 #pragma unroll
-                for (int x = 0; x < 2; ++x)
+                for (int x = 0; x < kSets; ++x)
 #pragma unroll
                     for (int nt = 0; nt < C::kNT; ++nt)
 #pragma unroll
@@ -355,24 +385,26 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     ldsm_x4(addr, a0, a1, a2, a3);
 #pragma unroll
                     for (int nt = 0; nt < C::kNT; ++nt)
-                        mma_bf16_16816(sacc[ks & 1][nt], a0, a1, a2, a3, qf[ks][nt][0],
+                        mma_bf16_16816(sacc[ks % kSets][nt], a0, a1, a2, a3, qf[ks][nt][0],
                                        qf[ks][nt][1]);
                 }
                 float sraw[C::kNT][4];
 #pragma unroll
                 for (int nt = 0; nt < C::kNT; ++nt)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) sraw[nt][e] = sacc[0][nt][e] + sacc[1][nt][e];
+                    for (int e = 0; e < 4; ++e)
+                        sraw[nt][e] = kSets == 2 ? sacc[0][nt][e] + sacc[kSets - 1][nt][e]
+                                                 : sacc[0][nt][e];
 
-                // ---- combine hi + lo: s[i][j] for token r0 + 8i, head slot j
-                float s[2][2];
+                // ---- combine hi + lo: s[i][j] for token r0 + 8i, row slot j
+                float s[2][NS];
 #pragma unroll
                 for (int i = 0; i < 2; ++i) {
 #pragma unroll
-                    for (int j = 0; j < 2; ++j) {
+                    for (int j = 0; j < NS; ++j) {
                         float v;
-                        if constexpr (G == 8) {
-                            v = sraw[0][2 * i + j] + sraw[1][2 * i + j];
+                        if constexpr (G >= 8) {
+                            v = sraw[j >> 1][2 * i + (j & 1)] + sraw[(j >> 1) + G / 8][2 * i + (j & 1)];
                         } else if constexpr (G == 4) {
                             v = sraw[0][2 * i + j] + __shfl_xor_sync(0xffffffffu, sraw[0][2 * i + j], 2);
                         } else if constexpr (G == 2) {
@@ -380,33 +412,43 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         } else {
                             v = sraw[0][2 * i] + sraw[0][2 * i + 1];
                         }
-                        const bool valid_tok = (r0 + 8 * i) < nvalid;
+                        const bool valid_tok =
+                            (r0 + 8 * i) < nvalid && tok0 + r0 + 8 * i < lim[j];
                         s[i][j] = slot_ok[j] ? (valid_tok ? v : -INFINITY) : 0.f;
                     }
                 }
-                // ---- online softmax (base 2)
-                float alpha[2], p[2][2];
+                // ---- online softmax (base 2).  A row may have no token yet
+                // (causal rows of a multi-token step): its max stays -inf
+                // and it takes nothing from this slice.
+                float alpha[NS], p[2][NS];
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
+                for (int j = 0; j < NS; ++j) {
                     float mx = fmaxf(s[0][j], s[1][j]);
                     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
                     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
                     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-                    const float m_new = fmaxf(m2[j], mx);     // finite: this slice has a token
-                    alpha[j] = exp2f(m2[j] - m_new);
-                    p[0][j] = exp2f(s[0][j] - m_new);
-                    p[1][j] = exp2f(s[1][j] - m_new);
+                    const float m_new = fmaxf(m2[j], mx);
+                    const float m_use = m_new == -INFINITY ? 0.f : m_new;
+                    alpha[j] = exp2f(m2[j] - m_use);
+                    p[0][j] = exp2f(s[0][j] - m_use);
+                    p[1][j] = exp2f(s[1][j] - m_use);
                     l2[j] = l2[j] * alpha[j] + p[0][j] + p[1][j];
                     m2[j] = m_new;
                 }
-                const float a_c0 = alpha[0];
-                const float a_c1 = (G == 1) ? alpha[0] : alpha[1];
 #pragma unroll
                 for (int mt = 0; mt < C::kMTiles; ++mt)
 #pragma unroll
                     for (int nt = 0; nt < C::kNT; ++nt) {
-                        acc[mt][nt][0] *= a_c0; acc[mt][nt][1] *= a_c1;
-                        acc[mt][nt][2] *= a_c0; acc[mt][nt][3] *= a_c1;
+                        float a0, a1;
+                        if constexpr (G >= 8) {
+                            a0 = alpha[2 * (nt % (G / 8))];
+                            a1 = alpha[2 * (nt % (G / 8)) + 1];
+                        } else {
+                            a0 = alpha[0];
+                            a1 = (G == 1) ? alpha[0] : alpha[1];
+                        }
+                        acc[mt][nt][0] *= a0; acc[mt][nt][1] *= a1;
+                        acc[mt][nt][2] *= a0; acc[mt][nt][3] *= a1;
                     }
 
                 // ---- P^T fragments through the per-warp transpose buffer
@@ -414,7 +456,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmap_k,
 #pragma unroll
                 for (int i = 0; i < 2; ++i)
 #pragma unroll
-                    for (int j = 0; j < 2; ++j)
+                    for (int j = 0; j < NS; ++j)
                         if (slot_ok[j]) pw[(r0 + 8 * i) * G + slot_head[j]] = p[i][j];
                 __syncwarp();
                 uint32_t pf[C::kNT][2];
@@ -460,19 +502,29 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmap_k,
 
         // ---- per-warp finalize: full l, hi+lo columns combined
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
+        for (int j = 0; j < NS; ++j) {
             l2[j] += __shfl_xor_sync(0xffffffffu, l2[j], 4);
             l2[j] += __shfl_xor_sync(0xffffffffu, l2[j], 8);
             l2[j] += __shfl_xor_sync(0xffffffffu, l2[j], 16);
         }
 #pragma unroll
         for (int mt = 0; mt < C::kMTiles; ++mt) {
+            if constexpr (G >= 8) {
+                // hi tile nh and its lo tile nh + G/8: rows 8*nh + 2*tq + c
+#pragma unroll
+                for (int nh = 0; nh < G / 8; ++nh)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int j = 2 * nh + (e & 1);
+                        mw[2 * G + slot_head[j] * D + mt * 16 + r0 + 8 * (e >> 1)] =
+                            acc[mt][nh][e] + acc[mt][nh + G / 8][e];
+                    }
+                continue;
+            }
             float o[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                if constexpr (G == 8) {
-                    o[e] = acc[mt][0][e] + acc[mt][1][e];
-                } else if constexpr (G == 4) {
+                if constexpr (G == 4) {
                     o[e] = acc[mt][0][e] + __shfl_xor_sync(0xffffffffu, acc[mt][0][e], 2);
                 } else if constexpr (G == 2) {
                     o[e] = acc[mt][0][e] + __shfl_xor_sync(0xffffffffu, acc[mt][0][e], 1);
@@ -489,7 +541,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmap_k,
         }
         if (lane < 4) {
 #pragma unroll
-            for (int j = 0; j < 2; ++j)
+            for (int j = 0; j < NS; ++j)
                 if (slot_ok[j]) {
                     mw[slot_head[j]] = m2[j];
                     mw[G + slot_head[j]] = l2[j];
@@ -499,7 +551,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmap_k,
         if (threadIdx.x == 0) *stop_flag = *abort_flag;
 
         // ---- CTA merge of the warps' partial states
-        const int64_t row0 = (int64_t(r.s) * a.batch + r.b) * a.num_q_heads + int64_t(r.g) * G;
+        const int64_t split0 = int64_t(r.s) * a.batch * T * a.num_q_heads;
         for (int idx = threadIdx.x; idx < G * D; idx += W * 32) {
             const int head = idx / D, d = idx % D;
             float M = -INFINITY;
@@ -516,8 +568,9 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 }
                 out /= lsum;
             }
-            a.out_part[(row0 + head) * D + d] = out;
-            if (d == 0) a.lse_part[row0 + head] = M != -INFINITY ? (M + log2f(lsum)) * kLn2 : -INFINITY;
+            const int64_t orow = split0 + row_offset(a, r.b, r.g, head, Gr);
+            a.out_part[orow * D + d] = out;
+            if (d == 0) a.lse_part[orow] = M != -INFINITY ? (M + log2f(lsum)) * kLn2 : -INFINITY;
         }
         named_barrier_sync(1, W * 32);
         if (*stop_flag) break;   // same value in every consumer warp
@@ -605,6 +658,24 @@ int launch(const DecodeArgs &a) {
 #ifndef PKV_TMA_D128G8_B
 #define PKV_TMA_D128G8_B 4
 #endif
+#ifndef PKV_TMA_D128G16_W
+#define PKV_TMA_D128G16_W 4
+#endif
+#ifndef PKV_TMA_D128G16_S
+#define PKV_TMA_D128G16_S 4
+#endif
+#ifndef PKV_TMA_D128G16_B
+#define PKV_TMA_D128G16_B 1
+#endif
+#ifndef PKV_TMA_D64G16_W
+#define PKV_TMA_D64G16_W 2
+#endif
+#ifndef PKV_TMA_D64G16_S
+#define PKV_TMA_D64G16_S 6
+#endif
+#ifndef PKV_TMA_D64G16_B
+#define PKV_TMA_D64G16_B 2
+#endif
 #ifndef PKV_TMA_D64_W
 #define PKV_TMA_D64_W 2
 #endif
@@ -616,32 +687,39 @@ int launch(const DecodeArgs &a) {
 #endif
 #define PKV_TMA_SHAPE_D128 PKV_TMA_D128_W, PKV_TMA_D128_S, PKV_TMA_D128_B
 #define PKV_TMA_SHAPE_D128_G8 PKV_TMA_D128G8_W, PKV_TMA_D128G8_S, PKV_TMA_D128G8_B
+#define PKV_TMA_SHAPE_D128_G16 PKV_TMA_D128G16_W, PKV_TMA_D128G16_S, PKV_TMA_D128G16_B
 #define PKV_TMA_SHAPE_D64 PKV_TMA_D64_W, PKV_TMA_D64_S, PKV_TMA_D64_B
+#define PKV_TMA_SHAPE_D64_G16 PKV_TMA_D64G16_W, PKV_TMA_D64G16_S, PKV_TMA_D64G16_B
 
 }  // namespace
 
-bool tma_kernel_supports(const pkv_cache_desc &c, int32_t num_q_heads) {
-    const int G = num_q_heads / c.num_kv_heads;
+bool tma_kernel_supports(const pkv_cache_desc &c, int32_t num_q_heads, int32_t q_tokens) {
+    const int G = num_q_heads / c.num_kv_heads * q_tokens;     // query rows per work item
     const bool pow2_bs = c.block_size >= 8 && c.block_size <= 256 &&
                          (c.block_size & (c.block_size - 1)) == 0;
     const int64_t rows = int64_t(c.num_blocks) * c.num_kv_heads * c.block_size;
     return c.head_dim_k == c.head_dim_v && (c.head_dim_k == 64 || c.head_dim_k == 128) &&
-           (G == 1 || G == 2 || G == 4 || G == 8) && pow2_bs && rows < (int64_t(1) << 31) - 1;
+           (G == 1 || G == 2 || G == 4 || G == 8 || G == 16) && pow2_bs &&
+           rows < (int64_t(1) << 31) - 1;
 }
 
 // Launch shapes (consumer warps, stages, CTAs per SM), measured on 8 x 32K
 // GQA decode: two consumer warps per CTA (32-token stages) and four CTAs per
 // SM keep more independent warps streaming than one large CTA does (G <= 4:
 // three stages; G = 8, whose registers leave room for only two stages at
-// four CTAs per SM: two).
+// four CTAs per SM: two).  G = 16 holds twice G = 8's accumulators and does
+// four times G = 4's warp-level MMAs per byte: one CTA of four consumer warps
+// and four stages per SM was fastest (8 x 32K, 128/8 heads: 300 us against
+// 361 us for two 2-warp CTAs and 513-570 us for three CTAs per SM).
 int launch_decode_tma(const DecodeArgs &a) {
-    const int G = a.num_q_heads / a.cache.num_kv_heads;
+    const int G = a.num_q_heads / a.cache.num_kv_heads * a.q_tokens;   // rows per work item
     if (a.cache.head_dim_k == 128) {
         switch (G) {
             case 1: return launch<128, 1, PKV_TMA_SHAPE_D128>(a);
             case 2: return launch<128, 2, PKV_TMA_SHAPE_D128>(a);
             case 4: return launch<128, 4, PKV_TMA_SHAPE_D128>(a);
             case 8: return launch<128, 8, PKV_TMA_SHAPE_D128_G8>(a);
+            case 16: return launch<128, 16, PKV_TMA_SHAPE_D128_G16>(a);
             default: return PKV_ERR_SHAPE;
         }
     }
@@ -650,6 +728,7 @@ int launch_decode_tma(const DecodeArgs &a) {
         case 2: return launch<64, 2, PKV_TMA_SHAPE_D64>(a);
         case 4: return launch<64, 4, PKV_TMA_SHAPE_D64>(a);
         case 8: return launch<64, 8, PKV_TMA_SHAPE_D64>(a);
+        case 16: return launch<64, 16, PKV_TMA_SHAPE_D64_G16>(a);
         default: return PKV_ERR_SHAPE;
     }
 }

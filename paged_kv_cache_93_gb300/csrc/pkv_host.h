@@ -59,8 +59,13 @@ struct DecodeArgs {
     // pool; head_dim_k when the values are the first head_dim_v dims of the
     // key rows (v_pool then points at the K pool).
     int32_t v_stride = 0;
+    // Query tokens per sequence (T).  T > 1: q, out and lse hold batch * T
+    // rows (sequence-major), and query token t of sequence b attends to the
+    // first seq_lens[b] - T + 1 + t tokens.  Only the GQA TMA kernel reads
+    // T; the other kernels are given one row per (sequence, token) instead.
+    int32_t q_tokens = 1;
 };
-bool tma_kernel_supports(const pkv_cache_desc &c, int32_t num_q_heads);
+bool tma_kernel_supports(const pkv_cache_desc &c, int32_t num_q_heads, int32_t q_tokens = 1);
 int launch_decode_tma(const DecodeArgs &a);
 // Large query groups (G a multiple of 32, e.g. MLA-shaped 128 heads over one
 // 576/512 latent head): tensor-core kernel with 32-head work items.

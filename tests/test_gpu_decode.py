@@ -48,6 +48,8 @@ SHAPES = [
     ([1000, 513, 7], 16, 2, 128, 64),                     # G=8
     ([700, 129], 8, 1, 64, 128),                          # G=8, D=64, bs 128
     ([520, 3], 4, 1, 128, 256),                           # G=4, bs 256
+    ([0, 300, 1, 77], 128, 8, 128, 16),                   # G=16 (128 heads over 8)
+    ([450, 31], 32, 2, 64, 32),                           # G=16, D=64
     ([90, 45], 12, 4, 128, 16),                           # G=3: generic kernel
     ([33, 17], 4, 2, 96, 16),                             # D=96: generic kernel
     ([40, 21], 8, 2, 128, 4),                             # bs 4: generic kernel
