@@ -480,6 +480,23 @@ def run_reference(args, world, rank):
     }))
 
 
+def staged(dev, tensors):
+    """One pinned host buffer holding `tensors` (256-byte aligned segments),
+    one device buffer of the same layout, and device views of each segment."""
+    offs, at = {}, 0
+    for n, t in tensors.items():
+        offs[n] = at
+        at += (t.numel() * t.element_size() + 255) // 256 * 256
+    host = torch.empty(max(at, 1), dtype=torch.uint8).pin_memory()
+    devb = torch.empty(max(at, 1), dtype=torch.uint8, device=dev)
+    views = {}
+    for n, t in tensors.items():
+        nb = t.numel() * t.element_size()
+        host[offs[n]:offs[n] + nb].view(t.dtype).copy_(t.contiguous().view(-1))
+        views[n] = devb[offs[n]:offs[n] + nb].view(t.dtype).view(t.shape)
+    return host, devb, views
+
+
 def run_gpu(args, world, rank, local):
     import paged_kv_cache_93_gb300 as pkv
     dev = torch.device("cuda", local)
@@ -598,44 +615,111 @@ def run_gpu(args, world, rank, local):
     # ---- end to end through the public API, host buffers in pinned memory
     e2e = None
     if args.workload in ("long32k", "mix", "tiny"):
-        pin = {n: getattr(w, n).pin_memory() for n in
-               ("q", "block_tables", "seq_lens", "new_seq", "new_pos", "k_new", "v_new")}
-        h_out = torch.empty(w.batch, w.num_q_heads, w.head_dim_v).pin_memory()
-        h_lse = torch.empty(w.batch, w.num_q_heads).pin_memory()
-        d = {n: torch.empty_like(t, device=dev) for n, t in pin.items()}
+        # A serving loop's decode step through the public API: the step's
+        # inputs staged in one pinned buffer (one copy in) and its outputs in
+        # one device buffer (one copy out).  Two sets of buffers and a copy
+        # stream: step i+1's inputs go in while step i computes, and step i's
+        # results come back while step i+1 runs; events keep every buffer from
+        # being reused before its copy or its step is done.
+        names = ("q", "block_tables", "seq_lens", "new_seq", "new_pos", "k_new", "v_new")
+        sets = []
+        for _ in range(2):
+            h_in, d_in, d = staged(dev, {n: getattr(w, n) for n in names})
+            h_res, d_res, r = staged(dev, {"out": torch.empty(w.batch, w.num_q_heads,
+                                                              w.head_dim_v),
+                                           "lse": torch.empty(w.batch, w.num_q_heads)})
+            ev = {k: torch.cuda.Event() for k in ("in", "done", "out")}
+            sets.append((h_in, d_in, d, h_res, d_res, r, ev))
         ws = torch.zeros(max(1, pkv.decode_workspace_size(w.batch, w.num_q_heads, w.head_dim_v,
                                                           splits)), dtype=torch.uint8,
                          device=dev)
-        h2d = sum(t.numel() * t.element_size() for t in pin.values())
-        d2h = h_out.numel() * 4 + h_lse.numel() * 4
-        ke = max(3, min(K, 200))
+        h2d = sets[0][0].numel()
+        d2h = sets[0][3].numel()
+        d_slots = torch.empty(w.new_pos.numel(), dtype=torch.int64, device=dev)
+        copy_stream = torch.cuda.Stream(device=dev)
+        ke = max(per_graph, min(K, 400))
 
-        def e2e_step():
-            for n, t in pin.items():
-                d[n].copy_(t, non_blocking=True)
-            slots = pkv.slot_mapping(st.k, st.v, d["block_tables"], d["new_seq"], d["new_pos"])
-            pkv.kv_append(st.k, st.v, d["k_new"], d["v_new"], slots)
-            out, lse = pkv.paged_decode_attn(d["q"], st.k, st.v, d["block_tables"],
-                                             d["seq_lens"], w.scale, num_splits=splits,
-                                             workspace=ws)
-            h_out.copy_(out, non_blocking=True)
-            h_lse.copy_(lse, non_blocking=True)
+        def run_steps(n):
+            """n pipelined steps.  The copy stream forks from the current
+            stream at the start and joins it at the end, and only events
+            recorded within the run are waited on, so a run also captures
+            into a CUDA graph."""
+            comp = torch.cuda.current_stream()
+            seen = set()
 
-        for _ in range(3):
-            e2e_step()
+            def wait(stream, i, key):
+                if (i % 2, key) in seen:
+                    stream.wait_event(sets[i % 2][6][key])
+
+            def record(stream, i, key):
+                sets[i % 2][6][key].record(stream)
+                seen.add((i % 2, key))
+
+            fork = torch.cuda.Event()
+            fork.record(comp)
+            copy_stream.wait_event(fork)
+
+            def stage_in(i):
+                h_in, d_in = sets[i % 2][0], sets[i % 2][1]
+                with torch.cuda.stream(copy_stream):
+                    wait(copy_stream, i, "done")            # step i-2 has read this set
+                    d_in.copy_(h_in, non_blocking=True)
+                    record(copy_stream, i, "in")
+
+            stage_in(0)
+            for i in range(n):
+                _, _, d, h_res, d_res, r, ev = sets[i % 2]
+                if i + 1 < n:
+                    stage_in(i + 1)
+                wait(comp, i, "in")
+                wait(comp, i, "out")                        # step i-2's results are home
+                pkv.slot_mapping(st.k, st.v, d["block_tables"], d["new_seq"], d["new_pos"],
+                                 out=d_slots)
+                pkv.kv_append(st.k, st.v, d["k_new"], d["v_new"], d_slots)
+                pkv.paged_decode_attn(d["q"], st.k, st.v, d["block_tables"], d["seq_lens"],
+                                      w.scale, num_splits=splits, workspace=ws, out=r["out"],
+                                      lse=r["lse"])
+                record(comp, i, "done")
+                with torch.cuda.stream(copy_stream):
+                    wait(copy_stream, i, "done")
+                    h_res.copy_(d_res, non_blocking=True)
+                    record(copy_stream, i, "out")
+            for j in range(min(n, 2)):                      # join: every result is home
+                wait(comp, n - 1 - j, "out")
+
+        run_steps(3)
+        e_graph = None
+        if graph is not None:
+            e_graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(e_graph):
+                run_steps(per_graph)
+            e_graph.replay()
+        ke = ke // per_graph * per_graph if e_graph is not None else ke
         torch.cuda.synchronize()
         barrier(world)
         te = time.perf_counter()
-        for _ in range(ke):
-            e2e_step()
+        if e_graph is not None:
+            for _ in range(ke // per_graph):
+                e_graph.replay()
+        else:
+            run_steps(ke)
         torch.cuda.synchronize()
         e2e_s = max_over_ranks((time.perf_counter() - te) / ke, world)
         barrier(world)
+        # the last step's results came home intact
+        _, _, _, h_res, d_res, _, _ = sets[(ke - 1) % 2]
+        if not torch.equal(h_res, d_res.cpu()):
+            raise RuntimeError("end-to-end results differ between device and host buffers")
         e2e = {"value": round(total_bytes / e2e_s / 1e9 * world, 2), "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": round(e2e_s * 1e3, 4), "steps": ke,
-               "api": "pinned host inputs -> slot_mapping + kv_append + paged_decode_attn -> "
-                      "pinned host out/lse, wall clock"}
+               "api": "pinned host inputs (one staging buffer, one copy per step) -> "
+                      "slot_mapping + kv_append + paged_decode_attn -> pinned host out/lse "
+                      "(one copy per step); two buffer sets and a copy stream overlap each "
+                      "step's copies with the neighbouring steps' compute; " +
+                      (f"{per_graph} such steps captured in a CUDA graph and replayed"
+                       if e_graph is not None else "calls made one by one from Python") +
+                      "; wall clock"}
     if pkv.device_status(reset=True) != 0:
         raise RuntimeError("device status word set")
 
