@@ -36,9 +36,10 @@
  *    cache is then k_pool alone and head_dim_v <= head_dim_k.  The pages
  *    describe no such layout; it halves the bytes per token of the MLA shape.
  *  - Query head h uses KV head h / (num_q_heads / num_kv_heads).
- *  - Head dims: any multiple of 8 up to 1024 (the tensor-core kernel takes
- *    64 and 128); q, out and lse are fp32; lse is the natural log of
- *    sum_j exp(s_j) over the scaled scores s_j = scale * q . k_j.
+ *  - Head dims: any multiple of 8 up to 1024 (which kernel runs a shape is
+ *    listed with pkv_paged_decode_attn's flags); q, out and lse are fp32; lse
+ *    is the natural log of sum_j exp(s_j) over the scaled scores
+ *    s_j = scale * q . k_j.
  */
 #ifndef PKV_H_
 #define PKV_H_
@@ -185,8 +186,8 @@ int64_t pkv_interleave_partition_len(int64_t num_tokens, int32_t num_parts,
  * not matter.
  *
  * flags: 0 = choose the kernel by shape: the TMA + tensor-core GQA kernel
- * for head_dim_k == head_dim_v in {64, 128}, query groups of 1, 2, 4 or 8
- * and power-of-two block sizes >= 8; for query groups that are a multiple
+ * for head_dim_k == head_dim_v in {64, 128}, query groups of 1, 2, 4, 8 or
+ * 16 and power-of-two block sizes >= 8; for query groups that are a multiple
  * of 64 (MLA-shaped, e.g. 128 heads over one 576/512 latent head) with
  * head_dim_k a multiple of 64 up to 576, head_dim_v a multiple of 128 up to
  * 512 and power-of-two block sizes 64..256, the tcgen05 kernel (5th-

@@ -93,6 +93,10 @@ __device__ __forceinline__ ItemRange item_range(const DecodeArgs &a, int item, i
     if (L < 0 || L > int64_t(a.max_blocks) * a.cache.block_size) {
         if (report && r.s == 0) raise_status(a.status, PKV_DEV_SEQ_LEN);
         L = 0;
+    } else if (L < a.q_tokens && report && r.s == 0) {
+        // fewer stored tokens than the step's new ones: the rows of the
+        // missing tokens stay empty
+        raise_status(a.status, PKV_DEV_SEQ_LEN);
     }
     const int64_t chunk = 64 * ((L + 64LL * a.num_splits - 1) / (64LL * a.num_splits));
     r.len = L;

@@ -94,14 +94,21 @@ def test_multi_token_decode(pkv, shape, T, splits):
     assert pkv.device_status() == 0
 
 
-def test_multi_token_short_sequence_is_flagged(pkv):
+@pytest.mark.parametrize("T,hq", [(3, 8), (4, 8), (2, 16)],
+                         ids=["rows12_per_token", "rows16_folded", "rows16_folded_G8"])
+@pytest.mark.parametrize("splits", [1, 2])
+def test_multi_token_short_sequence_is_flagged(pkv, T, hq, splits):
     """A sequence holding fewer tokens than T: the queries with no token are
-    empty (out 0, lse -inf) and the device flags the length."""
-    w = multi_case(3, [20, 0], 3, 8, 2, 64, 64, 16)
-    w.seq_lens = torch.tensor([23, 1], dtype=torch.int32)     # sequence 1 holds 1 < 3 tokens
-    out, lse = gpu_multi(pkv, w, 1)
-    assert np.isneginf(lse[1, :2]).all() and (out[1, :2] == 0).all()
-    assert np.isfinite(lse[1, 2]).all() and np.isfinite(lse[0]).all()
+    empty (out 0, lse -inf), the others attend to what there is, and the
+    device flags the length -- through the per-token rows (G*T = 12) and
+    through the GQA kernel's folded rows (G*T = 16)."""
+    w = multi_case(3, [20, 0], T, hq, 2, 64, 64, 16)
+    w.seq_lens = torch.tensor([20 + T, 1], dtype=torch.int32)  # sequence 1 holds 1 < T tokens
+    out, lse = gpu_multi(pkv, w, splits)
+    assert np.isneginf(lse[1, :T - 1]).all() and (out[1, :T - 1] == 0).all()
+    assert np.isfinite(lse[1, T - 1]).all() and np.isfinite(lse[0]).all()
+    ro, rl = oracle_multi(w)
+    assert_attention_close(out, lse, ro, rl, f"short T{T}")
     assert pkv.device_status() & pkv.DEV_SEQ_LEN
 
 
