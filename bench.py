@@ -343,8 +343,8 @@ class AgentStep(Step):
 class MultiStep(Step):
     """Speculative verification: T new tokens per sequence appended, each
     attending causally to the cache (one pkv_paged_decode_attn_multi)."""
-    kernel_name = ("pkv_paged_decode_attn_multi (decode_tma_kernel with the T tokens as rows "
-                   "of each work item, + lse_merge)")
+    kernel_name = ("pkv_paged_decode_attn_multi (decode_gqa_tc_kernel, tcgen05 + TMEM, with "
+                   "4 heads x 4 tokens as the 16 rows of each work item, + lse_merge)")
 
     def __init__(self, pkv, w, dev, splits):
         super().__init__(pkv, w, dev, splits)
@@ -375,7 +375,7 @@ class MultiStep(Step):
 STEPS = {"long32k": Step, "mix": Step, "tiny": Step, "dcp200k": DcpStep, "agent_mla": AgentStep,
          "agent_mla_latent": AgentStep, "spec4_32k": MultiStep}
 DEFAULT_SPLITS = {"long32k": 16, "mix": 1, "tiny": 1, "dcp200k": 19, "agent_mla": 19,
-                  "agent_mla_latent": 19, "spec4_32k": 16}
+                  "agent_mla_latent": 19, "spec4_32k": 9}
 
 
 # ------------------------------------------------------------------ arms

@@ -195,8 +195,11 @@ int64_t pkv_interleave_partition_len(int64_t num_tokens, int32_t num_parts,
  * groups that are a multiple of 32 (head dims multiples of 64, head_dim_v
  * <= 512, power-of-two block sizes >= 32) the warp-level-MMA large-group
  * kernel; the generic CUDA-core kernel otherwise.  PKV_DECODE_GENERIC forces
- * the generic kernel; PKV_DECODE_NO_TCGEN05 passes over the tcgen05 kernel
- * (the warp-level-MMA large-group kernel takes its shapes).
+ * the generic kernel.  Query groups of 16 (or 16 rows of heads x query
+ * tokens in pkv_paged_decode_attn_multi) with head dims 128 and power-of-two
+ * block sizes >= 16 run on a tcgen05 form of the GQA kernel.
+ * PKV_DECODE_NO_TCGEN05 passes over both tcgen05 kernels (the warp-level-MMA
+ * kernels take their shapes).
  * ------------------------------------------------------------------------- */
 #define PKV_DECODE_GENERIC 0x1
 #define PKV_DECODE_NO_TCGEN05 0x2

@@ -38,7 +38,29 @@ int validate_decode(const pkv_cache_desc *c, const float *q, int32_t batch, int3
 }
 
 int32_t auto_splits(const pkv_cache_desc &c, int32_t batch, int32_t num_q_heads,
-                    int32_t max_seq_len) {
+                    int32_t max_seq_len, int32_t q_tokens = 1) {
+    if (gqa_tc_kernel_supports(c, num_q_heads, q_tokens)) {
+        // The tcgen05 GQA kernel's resident CTAs take the (sequence, KV
+        // head, split) items in turn, an item costing its 128-token tiles
+        // plus about one tile of start-up.  Pick S for the least
+        // rounds x (tiles + 1) on sequences of the longest length; a tie
+        // goes to fewer splits (less to merge).
+        const int64_t units = std::max<int64_t>(1, int64_t(batch) * c.num_kv_heads);
+        const int64_t ctas = gqa_tc_resident_ctas();
+        const int64_t L = std::max<int64_t>(1, max_seq_len);
+        const int64_t s_max = std::min<int64_t>(kMaxSplits, (L + 127) / 128);
+        int64_t best = 1, best_cost = INT64_MAX;
+        for (int64_t s = 1; s <= s_max; ++s) {
+            const int64_t chunk = 64 * ((L + 64 * s - 1) / (64 * s));
+            const int64_t rounds = (units * s + ctas - 1) / ctas;
+            const int64_t cost = rounds * ((chunk + 127) / 128 + 1);
+            if (cost < best_cost) {
+                best = s;
+                best_cost = cost;
+            }
+        }
+        return int32_t(best);
+    }
     // Enough (sequence, KV head [, head block], split) items for ~4 per SM
     // (8 for the tcgen05 kernel), each item at least 512 tokens long.
     int64_t units = int64_t(batch) * c.num_kv_heads;
@@ -72,6 +94,9 @@ void values_from(DecodeArgs &a) {
 
 int run_split_kernel(const DecodeArgs &a, int32_t flags) {
     if (!(flags & PKV_DECODE_GENERIC)) {
+        if (!(flags & PKV_DECODE_NO_TCGEN05) &&
+            gqa_tc_kernel_supports(a.cache, a.num_q_heads, a.q_tokens))
+            return launch_decode_gqa_tc(a);
         if (tma_kernel_supports(a.cache, a.num_q_heads, a.q_tokens)) return launch_decode_tma(a);
         if (!(flags & PKV_DECODE_NO_TCGEN05) && mla_tc_kernel_supports(a.cache, a.num_q_heads))
             return launch_decode_mla_tc(a);
@@ -232,7 +257,7 @@ extern "C" int32_t pkv_decode_multi_auto_splits(const pkv_cache_desc *cache, int
     const bool folded = !(flags & PKV_DECODE_GENERIC) &&
                         tma_kernel_supports(*cache, num_q_heads, tokens_per_seq);
     return auto_splits(*cache, folded ? batch : batch * tokens_per_seq, num_q_heads,
-                       max_seq_len);
+                       max_seq_len, folded ? tokens_per_seq : 1);
 }
 
 extern "C" size_t pkv_decode_multi_workspace_size(int32_t batch, int32_t tokens_per_seq,
@@ -286,10 +311,10 @@ extern "C" int pkv_paged_decode_attn_multi(const pkv_cache_desc *cache, const fl
                      seq_lens, scale, S, out, lse, status, s};
         values_from(a);
         a.q_tokens = tokens_per_seq;
-        if (S == 1) return launch_decode_tma(a);
+        if (S == 1) return run_split_kernel(a, flags);
         a.out_part = out_part;
         a.lse_part = lse_part;
-        st = launch_decode_tma(a);
+            st = run_split_kernel(a, flags);
         if (st != PKV_OK) return st;
         return launch_lse_merge(S, out_part, lse_part, int64_t(rows) * num_q_heads,
                                 cache->head_dim_v, out, lse, s);

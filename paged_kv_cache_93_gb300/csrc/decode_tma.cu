@@ -523,25 +523,25 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         mw[2 * G + slot_head[j] * D + mt * 16 + r0 + 8 * (e >> 1)] =
                             acc[mt][nh][e] + acc[mt][nh + G / 8][e];
                     }
-                continue;
-            }
-            float o[4];
+            } else {
+                float o[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                if constexpr (G == 4) {
-                    o[e] = acc[mt][0][e] + __shfl_xor_sync(0xffffffffu, acc[mt][0][e], 2);
-                } else if constexpr (G == 2) {
-                    o[e] = acc[mt][0][e] + __shfl_xor_sync(0xffffffffu, acc[mt][0][e], 1);
-                } else {
-                    o[e] = acc[mt][0][e & 2] + acc[mt][0][(e & 2) + 1];
+                for (int e = 0; e < 4; ++e) {
+                    if constexpr (G == 4) {
+                        o[e] = acc[mt][0][e] + __shfl_xor_sync(0xffffffffu, acc[mt][0][e], 2);
+                    } else if constexpr (G == 2) {
+                        o[e] = acc[mt][0][e] + __shfl_xor_sync(0xffffffffu, acc[mt][0][e], 1);
+                    } else {
+                        o[e] = acc[mt][0][e & 2] + acc[mt][0][(e & 2) + 1];
+                    }
                 }
+#pragma unroll
+                for (int i = 0; i < 2; ++i)
+#pragma unroll
+                    for (int j = 0; j < 2; ++j)
+                        if (slot_ok[j])
+                            mw[2 * G + slot_head[j] * D + mt * 16 + r0 + 8 * i] = o[2 * i + j];
             }
-#pragma unroll
-            for (int i = 0; i < 2; ++i)
-#pragma unroll
-                for (int j = 0; j < 2; ++j)
-                    if (slot_ok[j])
-                        mw[2 * G + slot_head[j] * D + mt * 16 + r0 + 8 * i] = o[2 * i + j];
         }
         if (lane < 4) {
 #pragma unroll

@@ -66,6 +66,12 @@ struct DecodeArgs {
     int32_t q_tokens = 1;
 };
 bool tma_kernel_supports(const pkv_cache_desc &c, int32_t num_q_heads, int32_t q_tokens = 1);
+// 16 query rows per KV head (heads x query tokens), head dims 128: the
+// tcgen05 form of the GQA kernel.
+bool gqa_tc_kernel_supports(const pkv_cache_desc &c, int32_t num_q_heads, int32_t q_tokens);
+int launch_decode_gqa_tc(const DecodeArgs &a);
+// CTAs the tcgen05 GQA kernel keeps resident (one persistent grid).
+int gqa_tc_resident_ctas();
 int launch_decode_tma(const DecodeArgs &a);
 // Large query groups (G a multiple of 32, e.g. MLA-shaped 128 heads over one
 // 576/512 latent head): tensor-core kernel with 32-head work items.

@@ -68,6 +68,42 @@ def test_shape_sweep(pkv, shape, splits):
     assert pkv.device_status() == 0
 
 
+@pytest.mark.parametrize("cached,hq,hkv,bs", [([0, 300, 1, 77], 128, 8, 16),
+                                              ([600, 65], 64, 4, 64), ([200], 16, 1, 256),
+                                              ([129, 40, 255], 32, 2, 32), ([700, 5], 16, 1, 128)],
+                         ids=["128q_8kv_bs16", "64q_4kv_bs64", "16q_1kv_bs256", "32q_2kv_bs32",
+                              "16q_1kv_bs128"])
+@pytest.mark.parametrize("splits", [1, 4])
+@pytest.mark.parametrize("flags", ["auto", "no_tcgen05"])
+def test_group_of_16(pkv, cached, hq, hkv, bs, splits, flags):
+    """16 query heads per KV head (head dim 128): the tcgen05 GQA kernel, and
+    with no_tcgen05 the warp-level-MMA G = 16 instance."""
+    w = workloads.custom(71 + bs, cached, hq, hkv, 128, 128, bs)
+    f = pkv.DECODE_NO_TCGEN05 if flags == "no_tcgen05" else 0
+    out, lse, *_ = gpu_step(pkv, w, num_splits=splits, flags=f)
+    ro, rl, *_ = oracle_step(w)
+    assert_attention_close(out.cpu().numpy(), lse.cpu().numpy(), ro, rl, f"G16/{splits}/{flags}")
+    assert pkv.device_status() == 0
+
+
+@pytest.mark.parametrize("splits", [1, 3])
+def test_group_of_16_rising_scores(pkv, splits):
+    """Keys grow along the sequence, so each row's running max keeps rising
+    past the slack: the tcgen05 GQA kernel rescales its accumulator in TMEM."""
+    w = workloads.custom(92, [1500, 700], 32, 2, 128, 128, 16)
+    k = w.k_pool.float()
+    L = w.seq_lens.tolist()
+    for b in range(2):
+        for j in range(L[b]):
+            blk = int(w.block_tables[b, j // 16])
+            k[blk, :, j % 16] *= 1.0 + 6.0 * j / L[b]
+    w.k_pool = k.to(torch.bfloat16)
+    out, lse, *_ = gpu_step(pkv, w, num_splits=splits)
+    ro, rl, *_ = oracle_step(w)
+    assert_attention_close(out.cpu().numpy(), lse.cpu().numpy(), ro, rl, f"rising/{splits}")
+    assert pkv.device_status() == 0
+
+
 def test_distinct_k_and_v_dims(pkv):
     w = workloads.custom(7, [70, 3], 16, 1, 576, 512, 64)
     out, lse, *_ = gpu_step(pkv, w, num_splits=2)
@@ -76,9 +112,10 @@ def test_distinct_k_and_v_dims(pkv):
 
 
 @pytest.mark.parametrize("flags", [0, 1])
-def test_partials_match_oracle_token_ranges(pkv, flags):
+@pytest.mark.parametrize("hq", [16, 64], ids=["G4", "G16"])
+def test_partials_match_oracle_token_ranges(pkv, flags, hq):
     """Split s of row b covers [s*C, min(L, (s+1)*C)), C = 64*ceil(L/(64*S))."""
-    w = workloads.custom(31, [400, 70, 1, 0], 16, 4, 128, 128, 16)
+    w = workloads.custom(31, [400, 70, 1, 0], hq, 4, 128, 128, 16)
     S = 5
     dev = "cuda"
     k, v, bt = w.k_pool.to(dev), w.v_pool.to(dev), w.block_tables.to(dev)
@@ -117,26 +154,28 @@ def test_merge_of_far_apart_partials(pkv):
     assert mo.cpu().tolist() == [[3.0] * 8] and ml.cpu().tolist() == [400.0]
 
 
-def test_single_token_is_exact_value(pkv):
-    w = workloads.custom(9, [0, 0], 8, 2, 128, 128, 16)
+@pytest.mark.parametrize("hq", [8, 32], ids=["G4", "G16"])
+def test_single_token_is_exact_value(pkv, hq):
+    w = workloads.custom(9, [0, 0], hq, 2, 128, 128, 16)
     out, lse, k, v, _ = gpu_step(pkv, w, num_splits=1)
     ro, rl, *_ = oracle_step(w)
     # one token: out is exactly its V row (in fp32)
     vv = w.v_new.float().numpy()
     for b in range(2):
-        for h in range(8):
-            assert np.array_equal(out[b, h].cpu().numpy(), vv[b, h // 4])
+        for h in range(hq):
+            assert np.array_equal(out[b, h].cpu().numpy(), vv[b, h // (hq // 2)])
     assert np.abs(lse.cpu().numpy() - rl).max() <= 1e-4
 
 
-def test_bad_seq_len_and_block_id_are_flagged_not_faulted(pkv):
-    w = workloads.custom(12, [100, 100], 8, 2, 128, 128, 16)
+@pytest.mark.parametrize("hq", [8, 32], ids=["G4", "G16"])
+def test_bad_seq_len_and_block_id_are_flagged_not_faulted(pkv, hq):
+    w = workloads.custom(12, [100, 100], hq, 2, 128, 128, 16)
     dev = "cuda"
     k, v = w.k_pool.to(dev), w.v_pool.to(dev)
     q = w.q.to(dev)
     lens = w.seq_lens.clone()
     lens[1] = 10_000                       # longer than its table
-    for flags in (0, 1):
+    for flags in (0, 1, 2):
         out, lse = pkv.paged_decode_attn(q, k, v, w.block_tables.to(dev), lens.to(dev), w.scale,
                                          num_splits=2, flags=flags)
         assert pkv.device_status() == pkv.DEV_SEQ_LEN
@@ -150,9 +189,10 @@ def test_bad_seq_len_and_block_id_are_flagged_not_faulted(pkv):
         assert torch.isfinite(out).all() and torch.isfinite(lse).all()
 
 
-def test_unused_slots_holding_nan_do_not_leak(pkv):
+@pytest.mark.parametrize("hq", [16, 32], ids=["G8", "G16"])
+def test_unused_slots_holding_nan_do_not_leak(pkv, hq):
     """Slots past the end of a sequence's last block may hold any bits."""
-    w = workloads.custom(13, [20, 50], 16, 2, 128, 128, 16, extra_blocks=0)
+    w = workloads.custom(13, [20, 50], hq, 2, 128, 128, 16, extra_blocks=0)
     k, v = w.k_pool.clone(), w.v_pool.clone()
     for b in range(2):
         L = int(w.seq_lens[b])

@@ -85,10 +85,15 @@ SHAPES = [
                          ids=lambda s: f"G{s[1]//s[2]}_Dk{s[3]}_Dv{s[4]}_bs{s[5]}")
 @pytest.mark.parametrize("T", [1, 2, 4])
 @pytest.mark.parametrize("splits", [1, 3, 0])
-def test_multi_token_decode(pkv, shape, T, splits):
+@pytest.mark.parametrize("flags", ["auto", "no_tcgen05"])
+def test_multi_token_decode(pkv, shape, T, splits, flags):
+    """G*T = 16 rows with head dim 128 run on the tcgen05 GQA kernel, other
+    foldable shapes on the warp-level-MMA one; no_tcgen05 checks the latter
+    on the 16-row shapes too."""
     cached, hq, hkv, dk, dv, bs = shape
     w = multi_case(500 + T + dk, cached, T, hq, hkv, dk, dv, bs)
-    out, lse = gpu_multi(pkv, w, splits)
+    f = pkv.DECODE_NO_TCGEN05 if flags == "no_tcgen05" else 0
+    out, lse = gpu_multi(pkv, w, splits, flags=f)
     ro, rl = oracle_multi(w)
     assert_attention_close(out, lse, ro, rl, f"{shape}/T{T}/S{splits}")
     assert pkv.device_status() == 0
@@ -97,12 +102,13 @@ def test_multi_token_decode(pkv, shape, T, splits):
 @pytest.mark.parametrize("T,hq", [(3, 8), (4, 8), (2, 16)],
                          ids=["rows12_per_token", "rows16_folded", "rows16_folded_G8"])
 @pytest.mark.parametrize("splits", [1, 2])
-def test_multi_token_short_sequence_is_flagged(pkv, T, hq, splits):
+@pytest.mark.parametrize("dk", [64, 128])
+def test_multi_token_short_sequence_is_flagged(pkv, T, hq, splits, dk):
     """A sequence holding fewer tokens than T: the queries with no token are
     empty (out 0, lse -inf), the others attend to what there is, and the
     device flags the length -- through the per-token rows (G*T = 12) and
     through the GQA kernel's folded rows (G*T = 16)."""
-    w = multi_case(3, [20, 0], T, hq, 2, 64, 64, 16)
+    w = multi_case(3, [20, 0], T, hq, 2, dk, dk, 16)
     w.seq_lens = torch.tensor([20 + T, 1], dtype=torch.int32)  # sequence 1 holds 1 < T tokens
     out, lse = gpu_multi(pkv, w, splits)
     assert np.isneginf(lse[1, :T - 1]).all() and (out[1, :T - 1] == 0).all()
