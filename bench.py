@@ -44,9 +44,14 @@ import workloads  # noqa: E402
 METRIC = "paged decode-attn HBM GB/s (% of GB300 peak), seq-tokens/s at 32K ctx GQA"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
-PROFILE = os.path.join(ROOT, "profiles", "decode_tma_long32k.txt")
-KERNEL_SOURCES = [os.path.join(ROOT, "paged_kv_cache_93_gb300", "csrc", f)
-                  for f in ("decode_tma.cu", "pkv_device.cuh")]
+# Per workload: the committed ncu summary of its dominant kernel and the
+# sources that kernel is built from (the summary's traffic counts only while
+# their hash matches).
+PROFILES = {
+    "long32k": ("decode_tma_long32k.txt", ("decode_tma.cu", "pkv_device.cuh")),
+    "spec4_32k": ("decode_gqa_tc_spec4_32k.txt",
+                  ("decode_gqa_tc.cu", "pkv_device.cuh", "pkv_tcgen05.cuh")),
+}
 
 
 # ----------------------------------------------------------------- helpers
@@ -103,16 +108,19 @@ def kernel_flops(w):
         (w.head_dim_k + w.head_dim_v) * 2
 
 
-def stored_traffic():
-    """Per-launch DRAM bytes from the committed ncu summary, if it was taken
-    on the current kernel sources (else None)."""
+def stored_traffic(workload):
+    """Per-launch DRAM bytes from the workload's committed ncu summary, if it
+    was taken on the current kernel sources (else None)."""
+    if workload not in PROFILES:
+        return None
+    name, sources = PROFILES[workload]
     try:
         h = hashlib.sha256()
-        for p in KERNEL_SOURCES:
-            with open(p, "rb") as f:
+        for src in sources:
+            with open(os.path.join(ROOT, "paged_kv_cache_93_gb300", "csrc", src), "rb") as f:
                 h.update(f.read())
         vals = {}
-        with open(PROFILE, encoding="utf-8") as f:
+        with open(os.path.join(ROOT, "profiles", name), encoding="utf-8") as f:
             for line in f:
                 if "=" in line and not line.lstrip().startswith("#"):
                     k, v = line.split("=", 1)
@@ -730,7 +738,7 @@ def run_gpu(args, world, rank, local):
     tokens = None if (args.workload in ("long32k", "mix", "tiny") and not args.quick_cpu) else 2048
     used, times = oracle_gbs(w, tokens, repeats=1)
     cpu_gbs = used / min(times) / 1e9
-    traffic = stored_traffic() if args.workload == "long32k" else None
+    traffic = stored_traffic(args.workload)
     seq_tokens = int(w.seq_lens.sum())
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
