@@ -18,7 +18,9 @@ Pages cited (title, section):
   "KV キャッシュのメモリが同時実行数を制限する仕組み" (bytes per token).
 * "なぜ長文LLMは遅くなるのか｜Decode Context ParallelismでKVキャッシュを分散する" --
   interleaved token assignment and the three-stage DCP decode step (LSE
-  correction and sum of the partial outputs).
+  correction and sum of the partial outputs); bytes per cached number by
+  data type (FP8: one byte) and KV-cache quantisation to FP8 (E4M3 storage
+  below).
 """
 from __future__ import annotations
 
@@ -68,6 +70,15 @@ def load_library(path: str) -> ctypes.CDLL:
     lib.oracle_paged_decode_attn.argtypes = [i32, i32, i32, i32, i32, i32, i32, P, P, P,
                                              P, P, P, P, f64, P, P, i32]
     lib.oracle_paged_decode_attn.restype = i32
+    lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+    lib.oracle_e4m3_to_double.restype = f64
+    lib.oracle_e4m3_from_double.argtypes = [f64]
+    lib.oracle_e4m3_from_double.restype = ctypes.c_uint8
+    lib.oracle_kv_append_e4m3.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P, P, P, i64]
+    lib.oracle_kv_append_e4m3.restype = i64
+    lib.oracle_paged_decode_attn_e4m3.argtypes = [i32, i32, i32, i32, i32, i32, i32, P, P, P,
+                                                  P, P, P, P, P, P, f64, P, P, i32]
+    lib.oracle_paged_decode_attn_e4m3.restype = i32
     return lib
 
 
@@ -213,6 +224,72 @@ def paged_decode_attn(q, k_pool, v_pool, block_tables, seq_lens, scale: float,
                                          int(num_threads))
     if rc != 0:
         raise ValueError("oracle_paged_decode_attn: inconsistent arguments")
+    return out, lse
+
+
+def e4m3_to_double(code: int) -> float:
+    """Value of one E4M3 code (NaN for the two NaN codes)."""
+    return _get().oracle_e4m3_to_double(int(code) & 0xFF)
+
+
+def e4m3_from_double(x: float) -> int:
+    """The E4M3 code nearest to x (ties to even, saturating at +-448)."""
+    return int(_get().oracle_e4m3_from_double(float(x)))
+
+
+def e4m3_table() -> np.ndarray:
+    """fp64 value of each of the 256 codes."""
+    lib = _get()
+    return np.array([lib.oracle_e4m3_to_double(c) for c in range(256)], dtype=np.float64)
+
+
+def kv_append_e4m3(k_pool, v_pool, k_new, v_new, k_scale, v_scale, slots,
+                   block_size: int) -> int:
+    """In-place scatter of new bf16 tokens (uint16 bits) into E4M3 pools
+    (uint8 [num_blocks, Hkv, bs, D]), each element stored as the code nearest
+    to x / scale of its KV head.  Returns the count of out-of-range slots."""
+    assert k_pool.dtype == np.uint8 and k_pool.flags.c_contiguous
+    assert v_pool.dtype == np.uint8 and v_pool.flags.c_contiguous
+    nb, hkv, bs, dk = k_pool.shape
+    dv = v_pool.shape[3]
+    assert bs == block_size
+    kn = _c(k_new, np.uint16)
+    vn = _c(v_new, np.uint16)
+    ks = _c(k_scale, np.float32)
+    vs = _c(v_scale, np.float32)
+    assert ks.shape == (hkv,) and vs.shape == (hkv,)
+    sl = _c(slots, np.int64)
+    return int(_get().oracle_kv_append_e4m3(nb, bs, hkv, dk, dv, _ptr(k_pool), _ptr(v_pool),
+                                            _ptr(kn), _ptr(vn), _ptr(ks), _ptr(vs), _ptr(sl),
+                                            len(sl)))
+
+
+def paged_decode_attn_e4m3(q, k_pool, v_pool, k_scale, v_scale, block_tables, seq_lens,
+                           scale: float, tok_begin=None, tok_end=None, num_threads: int = 0):
+    """paged_decode_attn over E4M3 pools (uint8 codes): K_j and V_j are the
+    decoded codes times their KV head's scale.  Returns (out, lse) in fp64."""
+    q = _c(q, np.float32)
+    kp = _c(k_pool, np.uint8)
+    vp = _c(v_pool, np.uint8)
+    ks = _c(k_scale, np.float32)
+    vs = _c(v_scale, np.float32)
+    bt = _c(block_tables, np.int32)
+    sl = _c(seq_lens, np.int32)
+    B, Hq, Dk = q.shape
+    nb, hkv, bs, dk = kp.shape
+    dv = vp.shape[3]
+    assert dk == Dk and bt.shape[0] == B and sl.shape[0] == B
+    assert ks.shape == (hkv,) and vs.shape == (hkv,)
+    tb = None if tok_begin is None else _c(tok_begin, np.int32)
+    te = None if tok_end is None else _c(tok_end, np.int32)
+    out = np.empty((B, Hq, dv), dtype=np.float64)
+    lse = np.empty((B, Hq), dtype=np.float64)
+    rc = _get().oracle_paged_decode_attn_e4m3(B, Hq, hkv, Dk, dv, bs, bt.shape[1], _ptr(q),
+                                              _ptr(kp), _ptr(vp), _ptr(ks), _ptr(vs), _ptr(bt),
+                                              _ptr(sl), _ptr(tb), _ptr(te), float(scale),
+                                              _ptr(out), _ptr(lse), int(num_threads))
+    if rc != 0:
+        raise ValueError("oracle_paged_decode_attn_e4m3: inconsistent arguments")
     return out, lse
 
 

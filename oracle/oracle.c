@@ -39,6 +39,53 @@ double oracle_bf16_to_double(uint16_t bits)
     return (double)f;
 }
 
+/* FP8 storage of the cache.  [DCP] counts a cached number's bytes by data
+ * type (FP8: one byte) and describes KV-cache quantisation as storing the
+ * cache in a low-precision type such as FP8 so that each token takes fewer
+ * bytes; [PA] "Continuous Batching・prefix caching・量子化との違い": quantisation
+ * changes the stored representation, so its effect on accuracy has to be
+ * checked.  The pages fix no format; this oracle reads "FP8" as E4M3: one
+ * sign bit, four exponent bits with bias 7, three mantissa bits; exponent
+ * field 0 holds the subnormals m/8 * 2^-6; there are no infinities and
+ * S.1111.111 is NaN, so the largest finite magnitude is 1.75 * 2^8 = 448. */
+double oracle_e4m3_to_double(uint8_t code)
+{
+    int sign = code >> 7, e = (code >> 3) & 15, m = code & 7;
+    if (e == 15 && m == 7)
+        return NAN;
+    double v = e == 0 ? ldexp(m / 8.0, -6) : ldexp(1.0 + m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/* The E4M3 code nearest to x, a tie going to the even mantissa; magnitudes
+ * of 448 and beyond (infinities too) give +-448, NaN gives NaN. */
+uint8_t oracle_e4m3_from_double(double x)
+{
+    if (isnan(x))
+        return 0x7f;
+    uint8_t sign = signbit(x) ? 0x80 : 0;
+    double a = fabs(x);
+    if (a >= 448.0)
+        return sign | 0x7e;
+    if (a < ldexp(1.0, -6)) {
+        /* subnormal binade, steps of 2^-9; 8 steps is 2^-6, whose code is 8 */
+        double m = nearbyint(a / ldexp(1.0, -9));
+        return sign | (uint8_t)m;
+    }
+    int e;
+    frexp(a, &e);                 /* a = f * 2^e, f in [0.5, 1) */
+    e -= 1;                       /* a in [2^e, 2^(e+1)) */
+    double m = nearbyint((a / ldexp(1.0, e) - 1.0) * 8.0);
+    if (m == 8.0) {
+        m = 0.0;
+        e += 1;
+    }
+    int code = ((e + 7) << 3) | (int)m;
+    if (code > 0x7e)
+        code = 0x7e;
+    return sign | (uint8_t)code;
+}
+
 /* [PA] "PagedAttentionはブロック表で論理順序と物理配置を分ける": the block table maps the
  * n-th logical block of a sequence to the physical block that stores it, so
  * logical token `pos` lives in physical block table_row[pos / bs] at offset
@@ -78,6 +125,46 @@ int64_t oracle_kv_append(int32_t num_blocks, int32_t block_size, int32_t num_kv_
             for (int32_t d = 0; d < head_dim_v; ++d)
                 v_pool[((block * num_kv_heads + g) * block_size + offset) * head_dim_v + d] =
                     v_new[(t * num_kv_heads + g) * head_dim_v + d];
+        }
+    }
+    return bad;
+}
+
+/* The same scatter into E4M3 pools (uint8).  Element x (bf16) of KV head g
+ * is stored as the code nearest to x / s_g, the quotient taken in binary32
+ * (correctly rounded), where s_g = k_scale[g] or v_scale[g] is that head's
+ * dequantisation scale: the stored element reads back as decode * s_g. */
+int64_t oracle_kv_append_e4m3(int32_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                              int32_t head_dim_k, int32_t head_dim_v,
+                              uint8_t *k_pool, uint8_t *v_pool,
+                              const uint16_t *k_new, const uint16_t *v_new,
+                              const float *k_scale, const float *v_scale,
+                              const int64_t *slot_mapping, int64_t num_tokens)
+{
+    int64_t bad = 0;
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        int64_t slot = slot_mapping[t];
+        if (slot < 0)
+            continue;
+        if (slot >= (int64_t)num_blocks * block_size) {
+            ++bad;
+            continue;
+        }
+        int64_t block = slot / block_size;
+        int64_t offset = slot % block_size;
+        for (int32_t g = 0; g < num_kv_heads; ++g) {
+            for (int32_t d = 0; d < head_dim_k; ++d) {
+                float x = (float)oracle_bf16_to_double(k_new[(t * num_kv_heads + g) * head_dim_k + d]);
+                float y = x / k_scale[g];
+                k_pool[((block * num_kv_heads + g) * block_size + offset) * head_dim_k + d] =
+                    oracle_e4m3_from_double((double)y);
+            }
+            for (int32_t d = 0; d < head_dim_v; ++d) {
+                float x = (float)oracle_bf16_to_double(v_new[(t * num_kv_heads + g) * head_dim_v + d]);
+                float y = x / v_scale[g];
+                v_pool[((block * num_kv_heads + g) * block_size + offset) * head_dim_v + d] =
+                    oracle_e4m3_from_double((double)y);
+            }
         }
     }
     return bad;
@@ -179,17 +266,32 @@ void oracle_lse_merge(int32_t num_parts, int64_t rows, int32_t head_dim_v,
  *     M    = max_j s_j,  Z = sum_j exp(s_j - M)
  *     out  = sum_j exp(s_j - M) * V_j / Z,   lse = M + log Z
  * An empty range gives out = 0 and lse = -inf.  begin/end default to
- * [0, seq_lens[b]) when the pointers are NULL.
+ * [0, seq_lens[b]) when the pointers are NULL.  K_j and V_j are the cached
+ * numbers: bf16 values, or for E4M3 pools decode(code) * s_g.
  * ------------------------------------------------------------------------- */
 typedef struct {
     int32_t B, Hq, Hkv, Dk, Dv, bs, max_blocks;
     const float *q;
-    const uint16_t *k_pool, *v_pool;
+    const uint16_t *k_pool, *v_pool;     /* bf16 pools, or NULL */
+    const uint8_t *k8, *v8;              /* E4M3 pools, or NULL */
+    const float *k_scale, *v_scale;      /* E4M3 dequantisation scales per KV head */
     const int32_t *block_tables, *seq_lens, *tok_begin, *tok_end;
     double scale;
     double *out, *lse;
     int64_t row_first, row_step;
 } attn_job;
+
+static double k_elem(const attn_job *J, int64_t idx, int32_t g)
+{
+    return J->k8 ? oracle_e4m3_to_double(J->k8[idx]) * J->k_scale[g]
+                 : oracle_bf16_to_double(J->k_pool[idx]);
+}
+
+static double v_elem(const attn_job *J, int64_t idx, int32_t g)
+{
+    return J->v8 ? oracle_e4m3_to_double(J->v8[idx]) * J->v_scale[g]
+                 : oracle_bf16_to_double(J->v_pool[idx]);
+}
 
 static void attend_row(const attn_job *J, int64_t row, double *scores)
 {
@@ -214,10 +316,10 @@ static void attend_row(const attn_job *J, int64_t row, double *scores)
     for (int64_t j = begin; j < end; ++j) {
         int64_t phys = table_row[j / J->bs];
         int64_t off = j % J->bs;
-        const uint16_t *krow = J->k_pool + ((phys * J->Hkv + g) * J->bs + off) * J->Dk;
+        int64_t krow = ((phys * J->Hkv + g) * J->bs + off) * J->Dk;
         double dot = 0.0;
         for (int32_t d = 0; d < J->Dk; ++d)
-            dot += (double)qrow[d] * oracle_bf16_to_double(krow[d]);
+            dot += (double)qrow[d] * k_elem(J, krow + d, g);
         scores[j - begin] = J->scale * dot;
         if (scores[j - begin] > m)
             m = scores[j - begin];
@@ -228,9 +330,9 @@ static void attend_row(const attn_job *J, int64_t row, double *scores)
         z += p;
         int64_t phys = table_row[j / J->bs];
         int64_t off = j % J->bs;
-        const uint16_t *vrow = J->v_pool + ((phys * J->Hkv + g) * J->bs + off) * J->Dv;
+        int64_t vrow = ((phys * J->Hkv + g) * J->bs + off) * J->Dv;
         for (int32_t d = 0; d < J->Dv; ++d)
-            o[d] += p * oracle_bf16_to_double(vrow[d]);
+            o[d] += p * v_elem(J, vrow + d, g);
     }
     for (int32_t d = 0; d < J->Dv; ++d)
         o[d] /= z;
@@ -252,16 +354,12 @@ static void *attend_rows(void *arg)
     return NULL;
 }
 
-/* Returns 0, or -1 if the arguments are inconsistent.  `num_threads` <= 0 uses
- * every online core; rows are dealt out round-robin, which changes no
+/* Runs `proto` (row_first/row_step ignored) over all rows: `num_threads` <= 0
+ * uses every online core; rows are dealt out round-robin, which changes no
  * arithmetic (each row is computed by exactly one thread, in the order above). */
-int32_t oracle_paged_decode_attn(int32_t B, int32_t Hq, int32_t Hkv, int32_t Dk, int32_t Dv,
-                                 int32_t block_size, int32_t max_blocks, const float *q,
-                                 const uint16_t *k_pool, const uint16_t *v_pool,
-                                 const int32_t *block_tables, const int32_t *seq_lens,
-                                 const int32_t *tok_begin, const int32_t *tok_end,
-                                 double scale, double *out, double *lse, int32_t num_threads)
+static int32_t run_attn(attn_job proto, int32_t num_threads)
 {
+    const int32_t B = proto.B, Hq = proto.Hq, Hkv = proto.Hkv, block_size = proto.bs;
     if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || block_size <= 0)
         return -1;
     if (num_threads <= 0)
@@ -274,10 +372,9 @@ int32_t oracle_paged_decode_attn(int32_t B, int32_t Hq, int32_t Hkv, int32_t Dk,
     attn_job *jobs = malloc(sizeof(attn_job) * (size_t)num_threads);
     pthread_t *tids = malloc(sizeof(pthread_t) * (size_t)num_threads);
     for (int32_t t = 0; t < num_threads; ++t) {
-        attn_job J = {B, Hq, Hkv, Dk, Dv, block_size, max_blocks, q, k_pool, v_pool,
-                      block_tables, seq_lens, tok_begin, tok_end, scale, out, lse,
-                      t, num_threads};
-        jobs[t] = J;
+        jobs[t] = proto;
+        jobs[t].row_first = t;
+        jobs[t].row_step = num_threads;
     }
     if (num_threads == 1) {
         attend_rows(&jobs[0]);
@@ -290,4 +387,34 @@ int32_t oracle_paged_decode_attn(int32_t B, int32_t Hq, int32_t Hkv, int32_t Dk,
     free(jobs);
     free(tids);
     return 0;
+}
+
+/* Returns 0, or -1 if the arguments are inconsistent. */
+int32_t oracle_paged_decode_attn(int32_t B, int32_t Hq, int32_t Hkv, int32_t Dk, int32_t Dv,
+                                 int32_t block_size, int32_t max_blocks, const float *q,
+                                 const uint16_t *k_pool, const uint16_t *v_pool,
+                                 const int32_t *block_tables, const int32_t *seq_lens,
+                                 const int32_t *tok_begin, const int32_t *tok_end,
+                                 double scale, double *out, double *lse, int32_t num_threads)
+{
+    attn_job J = {B, Hq, Hkv, Dk, Dv, block_size, max_blocks, q, k_pool, v_pool,
+                  NULL, NULL, NULL, NULL, block_tables, seq_lens, tok_begin, tok_end,
+                  scale, out, lse, 0, 1};
+    return run_attn(J, num_threads);
+}
+
+/* The same over E4M3 pools with per-KV-head dequantisation scales. */
+int32_t oracle_paged_decode_attn_e4m3(int32_t B, int32_t Hq, int32_t Hkv, int32_t Dk, int32_t Dv,
+                                      int32_t block_size, int32_t max_blocks, const float *q,
+                                      const uint8_t *k_pool, const uint8_t *v_pool,
+                                      const float *k_scale, const float *v_scale,
+                                      const int32_t *block_tables, const int32_t *seq_lens,
+                                      const int32_t *tok_begin, const int32_t *tok_end,
+                                      double scale, double *out, double *lse,
+                                      int32_t num_threads)
+{
+    attn_job J = {B, Hq, Hkv, Dk, Dv, block_size, max_blocks, q, NULL, NULL,
+                  k_pool, v_pool, k_scale, v_scale, block_tables, seq_lens, tok_begin,
+                  tok_end, scale, out, lse, 0, 1};
+    return run_attn(J, num_threads);
 }
