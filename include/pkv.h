@@ -138,6 +138,39 @@ int pkv_copy_blocks(const pkv_cache_desc *cache, void *k_pool, void *v_pool,
                     pkv_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * FP8 cache -- [DCP] counts a cached number's bytes by data type (FP8: one
+ * byte) and names storing the KV cache in a low-precision type such as FP8
+ * as the way to shrink each token's bytes; [PA] "Continuous Batching・prefix
+ * caching・量子化との違い": quantisation changes the stored representation, so
+ * its effect on accuracy has to be checked.  The pages fix no format; here
+ * FP8 is E4M3 (1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits, no
+ * infinities, S.1111.111 = NaN, largest finite 448).  E4M3 pools have the
+ * bf16 pools' shapes with one-byte elements (uint8 codes, 8-byte aligned).
+ * Each KV head g has dequantisation scales k_scale[g] and v_scale[g] (fp32
+ * device arrays [num_kv_heads], caller-owned, positive and finite): code c
+ * of KV head g reads back as value(c) * scale[g].  Scales are chosen by the
+ * caller (e.g. a head's largest magnitude / 448) and stay fixed while a
+ * pool holds values quantised with them.
+ *
+ * pkv_kv_append_e4m3: pkv_kv_append into E4M3 pools.  k_new, v_new bf16 as
+ * for pkv_kv_append (16-byte aligned); element x of KV head g is stored as
+ * the code nearest to x / scale[g] -- the quotient rounded to binary32, a
+ * tie going to the even code, magnitudes of 448 and beyond stored as +-448.
+ * head_dim_k and head_dim_v multiples of 8.  Slots as pkv_kv_append.
+ *
+ * pkv_copy_blocks_e4m3: pkv_copy_blocks for E4M3 pools (both pools given;
+ * num_kv_heads * block_size * head_dim a multiple of 16, else PKV_ERR_SHAPE).
+ * ------------------------------------------------------------------------- */
+int pkv_kv_append_e4m3(const pkv_cache_desc *cache, void *k_pool, void *v_pool,
+                       const void *k_new, const void *v_new, const float *k_scale,
+                       const float *v_scale, const int64_t *slot_mapping, int64_t num_tokens,
+                       pkv_stream_t stream);
+
+int pkv_copy_blocks_e4m3(const pkv_cache_desc *cache, void *k_pool, void *v_pool,
+                         const int32_t *src, const int32_t *dst, int32_t num_pairs,
+                         pkv_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * pkv_interleave_slot_mapping -- [DCP] interleaved assignment: the KV of token i
  * belongs to partition (i / interleave) mod num_parts, and each partition
  * keeps its tokens in their original order.  For tokens
@@ -251,6 +284,31 @@ int pkv_paged_decode_attn_noalloc(const pkv_cache_desc *cache, const float *q, i
                                   const int32_t *block_tables, int32_t max_blocks,
                                   const int32_t *seq_lens, float scale, int32_t num_splits,
                                   float *out, float *lse, int32_t flags, pkv_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * pkv_paged_decode_attn_e4m3 -- pkv_paged_decode_attn over E4M3 pools (the
+ * FP8 cache above): K_j = value(k code) * k_scale[g] and V_j = value(v code)
+ * * v_scale[g]; q, out, lse, splits, workspace (pkv_decode_workspace_size)
+ * and the status bits as pkv_paged_decode_attn.  Shapes: head_dim_k ==
+ * head_dim_v == 128, query groups of 4, 8 or 16 heads per KV head,
+ * power-of-two block sizes 16..256 (other shapes PKV_ERR_SHAPE); flags 0.
+ * It runs on the tcgen05 tensor cores with E4M3 operands: the fp32 query is
+ * carried as four E4M3 terms and the probabilities as five, each term the
+ * rounding residual of the one before scaled by 16, so both keep about 16
+ * significant bits and the result is fp32-accurate attention on the stored
+ * values.
+ * ------------------------------------------------------------------------- */
+/* The split count num_splits = 0 resolves to in pkv_paged_decode_attn_e4m3. */
+int32_t pkv_decode_auto_splits_e4m3(const pkv_cache_desc *cache, int32_t batch,
+                                    int32_t num_q_heads, int32_t max_seq_len);
+
+int pkv_paged_decode_attn_e4m3(const pkv_cache_desc *cache, const float *q, int32_t batch,
+                               int32_t num_q_heads, const void *k_pool, const void *v_pool,
+                               const float *k_scale, const float *v_scale,
+                               const int32_t *block_tables, int32_t max_blocks,
+                               const int32_t *seq_lens, float scale, int32_t num_splits,
+                               void *workspace, size_t workspace_bytes, float *out, float *lse,
+                               int32_t flags, pkv_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * pkv_paged_decode_attn_multi -- several new tokens per sequence in one step

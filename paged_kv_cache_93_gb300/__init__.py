@@ -8,7 +8,9 @@ that the caller does not pass are allocated with torch.
 Layouts (one layer): k_pool [num_blocks, Hkv, block_size, Dk] bf16,
 v_pool [num_blocks, Hkv, block_size, Dv] bf16, block_tables [B, max_blocks]
 int32, seq_lens [B] int32, q [B, Hq, Dk] fp32, out [B, Hq, Dv] fp32,
-lse [B, Hq] fp32 (natural log).
+lse [B, Hq] fp32 (natural log).  An FP8 cache holds E4M3 codes in uint8
+pools of the same shapes, with fp32 dequantisation scales per KV head
+(the *_e4m3 functions).
 """
 from __future__ import annotations
 
@@ -24,7 +26,8 @@ __all__ = [
     "CacheDesc", "PkvError", "ValuesInKeys", "cache_desc", "kv_append", "slot_mapping", "copy_blocks",
     "interleave_slot_mapping", "interleave_partition_len", "decode_workspace_size",
     "decode_auto_splits", "paged_decode_attn", "paged_decode_attn_partial",
-    "paged_decode_attn_multi", "lse_merge",
+    "paged_decode_attn_multi", "lse_merge", "kv_append_e4m3", "copy_blocks_e4m3",
+    "paged_decode_attn_e4m3",
     "device_status", "BlockManager", "library_path", "DECODE_GENERIC", "DECODE_NO_TCGEN05",
     "DEV_BLOCK_ID",
     "DEV_SLOT", "DEV_SEQ_LEN", "DEV_COPY_CONFLICT", "DEV_TIMEOUT", "DEV_TABLE_RANGE",
@@ -73,13 +76,17 @@ def _v_ptr(v_pool):
 
 
 def cache_desc(k_pool: torch.Tensor, v_pool) -> CacheDesc:
-    _need(k_pool, "k_pool", torch.bfloat16, 4)
+    """Shape of a bf16 cache, or of an E4M3 one (uint8 code pools)."""
+    dtype = torch.uint8 if k_pool.dtype == torch.uint8 else torch.bfloat16
+    _need(k_pool, "k_pool", dtype, 4)
     nb, hkv, bs, dk = k_pool.shape
     if isinstance(v_pool, ValuesInKeys):
+        if dtype != torch.bfloat16:
+            raise ValueError("values inside the keys need a bf16 cache")
         if not 0 < v_pool.head_dim_v <= dk:
             raise ValueError("values inside the keys need 0 < head_dim_v <= head_dim_k")
         return CacheDesc(nb, bs, hkv, dk, v_pool.head_dim_v)
-    _need(v_pool, "v_pool", torch.bfloat16, 4)
+    _need(v_pool, "v_pool", dtype, 4)
     if tuple(v_pool.shape[:3]) != (nb, hkv, bs):
         raise ValueError("k_pool and v_pool disagree on [num_blocks, Hkv, block_size]")
     return CacheDesc(nb, bs, hkv, dk, v_pool.shape[3])
@@ -133,6 +140,41 @@ def copy_blocks(k_pool, v_pool, src, dst, stream=None) -> None:
         raise ValueError("src and dst lengths differ")
     _check("pkv_copy_blocks", lib.pkv_copy_blocks(
         ctypes.byref(desc), _ptr(k_pool), _v_ptr(v_pool), _ptr(src), _ptr(dst), src.numel(),
+        _stream(stream)))
+
+
+def _e4m3_desc(k_pool, v_pool, k_scale, v_scale) -> CacheDesc:
+    _need(k_pool, "k_pool", torch.uint8, 4)
+    desc = cache_desc(k_pool, v_pool)
+    _need(k_scale, "k_scale", torch.float32, 1)
+    _need(v_scale, "v_scale", torch.float32, 1)
+    if k_scale.numel() != desc.num_kv_heads or v_scale.numel() != desc.num_kv_heads:
+        raise ValueError("k_scale and v_scale hold one scale per KV head")
+    return desc
+
+
+def kv_append_e4m3(k_pool, v_pool, k_new, v_new, slots, k_scale, v_scale, stream=None) -> None:
+    """Quantise k_new / v_new (bf16 [T, Hkv, D]) into the E4M3 pools at slots
+    [T]: element x of KV head g becomes the code nearest to x / scale[g]."""
+    desc = _e4m3_desc(k_pool, v_pool, k_scale, v_scale)
+    _need(k_new, "k_new", torch.bfloat16, 3)
+    _need(v_new, "v_new", torch.bfloat16, 3)
+    _need(slots, "slot_mapping", torch.int64, 1)
+    _check("pkv_kv_append_e4m3", lib.pkv_kv_append_e4m3(
+        ctypes.byref(desc), _ptr(k_pool), _ptr(v_pool), _ptr(k_new), _ptr(v_new),
+        _ptr(k_scale), _ptr(v_scale), _ptr(slots), slots.numel(), _stream(stream)))
+
+
+def copy_blocks_e4m3(k_pool, v_pool, src, dst, stream=None) -> None:
+    """copy_blocks for E4M3 pools."""
+    _need(k_pool, "k_pool", torch.uint8, 4)
+    desc = cache_desc(k_pool, v_pool)
+    _need(src, "src", torch.int32, 1)
+    _need(dst, "dst", torch.int32, 1)
+    if src.numel() != dst.numel():
+        raise ValueError("src and dst lengths differ")
+    _check("pkv_copy_blocks_e4m3", lib.pkv_copy_blocks_e4m3(
+        ctypes.byref(desc), _ptr(k_pool), _ptr(v_pool), _ptr(src), _ptr(dst), src.numel(),
         _stream(stream)))
 
 
@@ -198,6 +240,33 @@ def paged_decode_attn(q, k_pool, v_pool, block_tables, seq_lens, scale: float,
         ctypes.byref(desc), _ptr(q), B, Hq, _ptr(k_pool), _v_ptr(v_pool), _ptr(block_tables),
         block_tables.shape[1], _ptr(seq_lens), float(scale), S, _ptr(workspace), ws_bytes,
         _ptr(out), _ptr(lse), int(flags), _stream(stream)))
+    return out, lse
+
+
+def paged_decode_attn_e4m3(q, k_pool, v_pool, k_scale, v_scale, block_tables, seq_lens,
+                           scale: float, num_splits: int = 0, workspace=None, out=None,
+                           lse=None, stream=None):
+    """Decode attention over an E4M3 cache (uint8 code pools, fp32 scales per
+    KV head) -> (out, lse); num_splits 0 lets the library choose."""
+    desc = _e4m3_desc(k_pool, v_pool, k_scale, v_scale)
+    _need(q, "q", torch.float32, 3)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    B, Hq, _ = q.shape
+    if out is None:
+        out = torch.empty(B, Hq, desc.head_dim_v, dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty(B, Hq, dtype=torch.float32, device=q.device)
+    S = num_splits or int(lib.pkv_decode_auto_splits_e4m3(
+        ctypes.byref(desc), B, Hq, block_tables.shape[1] * desc.block_size))
+    need = decode_workspace_size(B, Hq, desc.head_dim_v, S)
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("pkv_paged_decode_attn_e4m3", lib.pkv_paged_decode_attn_e4m3(
+        ctypes.byref(desc), _ptr(q), B, Hq, _ptr(k_pool), _ptr(v_pool), _ptr(k_scale),
+        _ptr(v_scale), _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), float(scale),
+        S, _ptr(workspace), ws_bytes, _ptr(out), _ptr(lse), 0, _stream(stream)))
     return out, lse
 
 

@@ -44,6 +44,12 @@ SIGNATURES = {
     "pkv_slot_mapping": (ctypes.c_int, [_DESC, _P, _i32, _i32, _P, _P, _i64, _P, _P]),
     "pkv_kv_append": (ctypes.c_int, [_DESC, _P, _P, _P, _P, _P, _i64, _P]),
     "pkv_copy_blocks": (ctypes.c_int, [_DESC, _P, _P, _P, _P, _i32, _P]),
+    "pkv_kv_append_e4m3": (ctypes.c_int, [_DESC, _P, _P, _P, _P, _P, _P, _P, _i64, _P]),
+    "pkv_copy_blocks_e4m3": (ctypes.c_int, [_DESC, _P, _P, _P, _P, _i32, _P]),
+    "pkv_decode_auto_splits_e4m3": (_i32, [_DESC, _i32, _i32, _i32]),
+    "pkv_paged_decode_attn_e4m3": (ctypes.c_int, [_DESC, _P, _i32, _i32, _P, _P, _P, _P, _P,
+                                                  _i32, _P, _f32, _i32, _P, _sz, _P, _P, _i32,
+                                                  _P]),
     "pkv_interleave_slot_mapping": (ctypes.c_int, [_DESC, _i64, _i64, _i32, _i32, _P, _i32,
                                                    _P, _P, _P]),
     "pkv_interleave_partition_len": (_i64, [_i64, _i32, _i32, _i32]),

@@ -37,30 +37,31 @@ int validate_decode(const pkv_cache_desc *c, const float *q, int32_t batch, int3
     return PKV_OK;
 }
 
+// The tcgen05 GQA kernels' resident CTAs take the (sequence, KV head,
+// split) items in turn, an item costing its 128-token tiles plus about one
+// tile of start-up.  Pick S for the least rounds x (tiles + 1) on sequences
+// of the longest length; a tie goes to fewer splits (less to merge).
+int32_t tc_splits(const pkv_cache_desc &c, int32_t batch, int32_t max_seq_len) {
+    const int64_t units = std::max<int64_t>(1, int64_t(batch) * c.num_kv_heads);
+    const int64_t ctas = gqa_tc_resident_ctas();
+    const int64_t L = std::max<int64_t>(1, max_seq_len);
+    const int64_t s_max = std::min<int64_t>(kMaxSplits, (L + 127) / 128);
+    int64_t best = 1, best_cost = INT64_MAX;
+    for (int64_t s = 1; s <= s_max; ++s) {
+        const int64_t chunk = 64 * ((L + 64 * s - 1) / (64 * s));
+        const int64_t rounds = (units * s + ctas - 1) / ctas;
+        const int64_t cost = rounds * ((chunk + 127) / 128 + 1);
+        if (cost < best_cost) {
+            best = s;
+            best_cost = cost;
+        }
+    }
+    return int32_t(best);
+}
+
 int32_t auto_splits(const pkv_cache_desc &c, int32_t batch, int32_t num_q_heads,
                     int32_t max_seq_len, int32_t q_tokens = 1) {
-    if (gqa_tc_kernel_supports(c, num_q_heads, q_tokens)) {
-        // The tcgen05 GQA kernel's resident CTAs take the (sequence, KV
-        // head, split) items in turn, an item costing its 128-token tiles
-        // plus about one tile of start-up.  Pick S for the least
-        // rounds x (tiles + 1) on sequences of the longest length; a tie
-        // goes to fewer splits (less to merge).
-        const int64_t units = std::max<int64_t>(1, int64_t(batch) * c.num_kv_heads);
-        const int64_t ctas = gqa_tc_resident_ctas();
-        const int64_t L = std::max<int64_t>(1, max_seq_len);
-        const int64_t s_max = std::min<int64_t>(kMaxSplits, (L + 127) / 128);
-        int64_t best = 1, best_cost = INT64_MAX;
-        for (int64_t s = 1; s <= s_max; ++s) {
-            const int64_t chunk = 64 * ((L + 64 * s - 1) / (64 * s));
-            const int64_t rounds = (units * s + ctas - 1) / ctas;
-            const int64_t cost = rounds * ((chunk + 127) / 128 + 1);
-            if (cost < best_cost) {
-                best = s;
-                best_cost = cost;
-            }
-        }
-        return int32_t(best);
-    }
+    if (gqa_tc_kernel_supports(c, num_q_heads, q_tokens)) return tc_splits(c, batch, max_seq_len);
     // Enough (sequence, KV head [, head block], split) items for ~4 per SM
     // (8 for the tcgen05 kernel), each item at least 512 tokens long.
     int64_t units = int64_t(batch) * c.num_kv_heads;
@@ -143,6 +144,54 @@ extern "C" int pkv_paged_decode_attn_partial(const pkv_cache_desc *cache, const 
                  reinterpret_cast<cudaStream_t>(stream)};
     values_from(a);
     return run_split_kernel(a, flags);
+}
+
+extern "C" int32_t pkv_decode_auto_splits_e4m3(const pkv_cache_desc *cache, int32_t batch,
+                                               int32_t num_q_heads, int32_t max_seq_len) {
+    if (!cache || cache->num_kv_heads <= 0 || num_q_heads <= 0) return 1;
+    return tc_splits(*cache, batch, max_seq_len);
+}
+
+extern "C" int pkv_paged_decode_attn_e4m3(const pkv_cache_desc *cache, const float *q,
+                                          int32_t batch, int32_t num_q_heads, const void *k_pool,
+                                          const void *v_pool, const float *k_scale,
+                                          const float *v_scale, const int32_t *block_tables,
+                                          int32_t max_blocks, const int32_t *seq_lens,
+                                          float scale, int32_t num_splits, void *workspace,
+                                          size_t workspace_bytes, float *out, float *lse,
+                                          int32_t flags, pkv_stream_t stream) {
+    if (flags != 0) return PKV_ERR_INVALID_ARG;
+    int st = validate_decode(cache, q, batch, num_q_heads, k_pool, v_pool, block_tables,
+                             max_blocks, seq_lens, num_splits, 0);
+    if (st != PKV_OK || batch == 0) return st;
+    if (!v_pool || !k_scale || !v_scale || !out || !lse) return PKV_ERR_INVALID_ARG;
+    if (!gqa_tc_e4m3_kernel_supports(*cache, num_q_heads)) return PKV_ERR_SHAPE;
+    if (!aligned16(out)) return PKV_ERR_ALIGNMENT;
+    int32_t S = num_splits;
+    if (S == 0)
+        S = pkv_decode_auto_splits_e4m3(
+            cache, batch, num_q_heads,
+            int32_t(std::min<int64_t>(int64_t(max_blocks) * cache->block_size, INT32_MAX)));
+    const size_t need = pkv_decode_workspace_size(batch, num_q_heads, cache->head_dim_v, S);
+    if (S > 1 && (!workspace || workspace_bytes < need)) return PKV_ERR_WORKSPACE_TOO_SMALL;
+    if (S > 1 && !aligned16(workspace)) return PKV_ERR_ALIGNMENT;
+    uint32_t *status = status_word();
+    if (!status) return PKV_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    DecodeArgs a{*cache, q, batch, num_q_heads, k_pool, v_pool, block_tables, max_blocks,
+                 seq_lens, scale, S, out, lse, status, s};
+    a.v_stride = cache->head_dim_v;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    if (S == 1) return launch_decode_gqa_tc_e4m3(a);
+    const size_t rows = size_t(S) * batch * num_q_heads;
+    char *ws = static_cast<char *>(workspace);
+    a.out_part = reinterpret_cast<float *>(ws);
+    a.lse_part = reinterpret_cast<float *>(ws + align256(rows * cache->head_dim_v * sizeof(float)));
+    st = launch_decode_gqa_tc_e4m3(a);
+    if (st != PKV_OK) return st;
+    return launch_lse_merge(S, a.out_part, a.lse_part, int64_t(batch) * num_q_heads,
+                            cache->head_dim_v, out, lse, s);
 }
 
 extern "C" int pkv_paged_decode_attn(const pkv_cache_desc *cache, const float *q, int32_t batch,

@@ -130,6 +130,53 @@ __global__ void kv_append_kernel(uint4 *__restrict__ k_pool, uint4 *__restrict__
     }
 }
 
+// E4M3 pools: one thread per 8 elements of a (token, KV head) row (16 bytes of
+// bf16 in, 8 bytes of codes out).  Element x of KV head g is stored as the
+// code nearest to x / scale[g], the quotient rounded to binary32.
+__global__ void kv_append_e4m3_kernel(uint2 *__restrict__ k_pool, uint2 *__restrict__ v_pool,
+                                      const uint4 *__restrict__ k_new,
+                                      const uint4 *__restrict__ v_new,
+                                      const float *__restrict__ k_scale,
+                                      const float *__restrict__ v_scale,
+                                      const int64_t *__restrict__ slots, int64_t num_tokens,
+                                      int32_t num_kv_heads, int32_t block_size, int64_t num_slots,
+                                      int32_t vk, int32_t vv, uint32_t *status) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int64_t per_token = int64_t(num_kv_heads) * (vk + vv);
+    const int64_t total = num_tokens * per_token;
+    for (int64_t u = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; u < total;
+         u += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t t = u / per_token;
+        int64_t r = u - t * per_token;
+        const int64_t slot = slots[t];
+        if (slot < 0) continue;
+        if (slot >= num_slots) {
+            if (r == 0) raise_status(status, PKV_DEV_SLOT);
+            continue;
+        }
+        const int64_t block = slot / block_size, off = slot - block * block_size;
+        const bool is_k = r < int64_t(num_kv_heads) * vk;
+        if (!is_k) r -= int64_t(num_kv_heads) * vk;
+        const int32_t nv = is_k ? vk : vv;
+        const int64_t g = r / nv, c = r - g * nv;
+        const uint4 x = (is_k ? k_new : v_new)[(t * num_kv_heads + g) * nv + c];
+        const float s = (is_k ? k_scale : v_scale)[g];
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+        uint32_t codes[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const uint32_t c01 = e4m3x2_from_f32(__fdiv_rn(bf16_lo_to_f32(w[2 * i]), s),
+                                                 __fdiv_rn(bf16_hi_to_f32(w[2 * i]), s));
+            const uint32_t c23 = e4m3x2_from_f32(__fdiv_rn(bf16_lo_to_f32(w[2 * i + 1]), s),
+                                                 __fdiv_rn(bf16_hi_to_f32(w[2 * i + 1]), s));
+            codes[i] = c01 | (c23 << 16);
+        }
+        (is_k ? k_pool : v_pool)[((block * num_kv_heads + g) * block_size + off) * nv + c] =
+            make_uint2(codes[0], codes[1]);
+    }
+}
+
 // grid.x = pair, grid.y splits a pair's K+V bytes.  Every CTA of a pair
 // re-derives the same skip decision from the full pair list, so no CTA
 // writes a destination that another pair reads or writes.
@@ -269,9 +316,58 @@ extern "C" int pkv_kv_append(const pkv_cache_desc *cache, void *k_pool, void *v_
                       int64_t(cache->num_blocks) * cache->block_size, vk, vv, status);
 }
 
+extern "C" int pkv_kv_append_e4m3(const pkv_cache_desc *cache, void *k_pool, void *v_pool,
+                                  const void *k_new, const void *v_new,
+                                  const float *k_scale, const float *v_scale,
+                                  const int64_t *slot_mapping, int64_t num_tokens,
+                                  pkv_stream_t stream) {
+    if (!valid_cache(cache) || num_tokens < 0) return PKV_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PKV_OK;
+    if (!k_pool || !v_pool || !k_new || !v_new || !k_scale || !v_scale || !slot_mapping)
+        return PKV_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new) || (reinterpret_cast<uintptr_t>(k_pool) & 7) ||
+        (reinterpret_cast<uintptr_t>(v_pool) & 7))
+        return PKV_ERR_ALIGNMENT;
+    uint32_t *status = status_word();
+    if (!status) return PKV_ERR_CUDA;
+    const int32_t vk = cache->head_dim_k / 8, vv = cache->head_dim_v / 8;   // 8-element groups
+    const int64_t work = num_tokens * cache->num_kv_heads * (vk + vv);
+    const int threads = 256;
+    return launch_pdl(kv_append_e4m3_kernel, dim3(grid_for(work, threads)), dim3(threads), 0,
+                      reinterpret_cast<cudaStream_t>(stream), static_cast<uint2 *>(k_pool),
+                      static_cast<uint2 *>(v_pool), static_cast<const uint4 *>(k_new),
+                      static_cast<const uint4 *>(v_new), k_scale, v_scale, slot_mapping,
+                      num_tokens, cache->num_kv_heads, cache->block_size,
+                      int64_t(cache->num_blocks) * cache->block_size, vk, vv, status);
+}
+
+namespace pkv {
+namespace {
+// Block copies of pools whose numbers take `elem_bytes` bytes each.
+int copy_blocks_bytes(const pkv_cache_desc *cache, void *k_pool, void *v_pool,
+                      const int32_t *src, const int32_t *dst, int32_t num_pairs,
+                      pkv_stream_t stream, int elem_bytes);
+}  // namespace
+}  // namespace pkv
+
 extern "C" int pkv_copy_blocks(const pkv_cache_desc *cache, void *k_pool, void *v_pool,
                                const int32_t *src, const int32_t *dst, int32_t num_pairs,
                                pkv_stream_t stream) {
+    return pkv::copy_blocks_bytes(cache, k_pool, v_pool, src, dst, num_pairs, stream, 2);
+}
+
+extern "C" int pkv_copy_blocks_e4m3(const pkv_cache_desc *cache, void *k_pool, void *v_pool,
+                                    const int32_t *src, const int32_t *dst, int32_t num_pairs,
+                                    pkv_stream_t stream) {
+    if (!v_pool) return PKV_ERR_INVALID_ARG;
+    return pkv::copy_blocks_bytes(cache, k_pool, v_pool, src, dst, num_pairs, stream, 1);
+}
+
+namespace pkv {
+namespace {
+int copy_blocks_bytes(const pkv_cache_desc *cache, void *k_pool, void *v_pool,
+                      const int32_t *src, const int32_t *dst, int32_t num_pairs,
+                      pkv_stream_t stream, int elem_bytes) {
     if (!valid_cache(cache) || num_pairs < 0) return PKV_ERR_INVALID_ARG;
     if (num_pairs == 0) return PKV_OK;
     // v_pool NULL: the cache keeps no separate values; only K blocks are copied.
@@ -279,11 +375,16 @@ extern "C" int pkv_copy_blocks(const pkv_cache_desc *cache, void *k_pool, void *
     if (!v_pool && cache->head_dim_v > cache->head_dim_k) return PKV_ERR_SHAPE;
     if (!aligned16(k_pool) || (v_pool && !aligned16(v_pool))) return PKV_ERR_ALIGNMENT;
     if (num_pairs > 65535) return PKV_ERR_SHAPE;
+    // 16-byte vectors per block
+    const int64_t k_bytes =
+        int64_t(cache->num_kv_heads) * cache->block_size * cache->head_dim_k * elem_bytes;
+    const int64_t v_bytes =
+        v_pool ? int64_t(cache->num_kv_heads) * cache->block_size * cache->head_dim_v * elem_bytes
+               : 0;
+    if (k_bytes % 16 || v_bytes % 16) return PKV_ERR_SHAPE;
+    const int64_t k_vecs = k_bytes / 16, v_vecs = v_bytes / 16;
     uint32_t *status = status_word();
     if (!status) return PKV_ERR_CUDA;
-    const int64_t k_vecs = int64_t(cache->num_kv_heads) * cache->block_size * cache->head_dim_k / 8;
-    const int64_t v_vecs =
-        v_pool ? int64_t(cache->num_kv_heads) * cache->block_size * cache->head_dim_v / 8 : 0;
     const int threads = 256;
     // Enough CTAs per pair to cover the device a few times over.
     int64_t per_pair = (k_vecs + v_vecs + threads - 1) / threads;
@@ -294,6 +395,8 @@ extern "C" int pkv_copy_blocks(const pkv_cache_desc *cache, void *k_pool, void *
                       static_cast<uint4 *>(v_pool), src, dst, num_pairs, cache->num_blocks, k_vecs,
                       v_vecs, status);
 }
+}  // namespace
+}  // namespace pkv
 
 extern "C" int64_t pkv_interleave_partition_len(int64_t num_tokens, int32_t num_parts,
                                                 int32_t interleave, int32_t part) {

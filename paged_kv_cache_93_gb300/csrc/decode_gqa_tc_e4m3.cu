@@ -1,0 +1,643 @@
+// decode_gqa_tc_e4m3.cu -- paged decode attention over an FP8 (E4M3) cache
+// with per-KV-head scales, for query groups of R = 4, 8 or 16 heads and head
+// dims 128, on the 5th-generation tensor cores of sm_103a with E4M3
+// operands (tcgen05.mma kind::f8f6f4, fp32 accumulators in tensor memory).
+//
+// The cache bytes go to the tensor cores as they are stored.  The fp32
+// query cannot: it is carried as four E4M3 terms per element, y = t0 +
+// t1/16 + t2/256 + t3/4096 with y = q * scale * log2(e) * k_scale / s_h
+// (s_h a power of two putting row h's largest element in [128, 256)), each
+// term the E4M3 rounding of the previous residual times 16.  Likewise each
+// probability p in [0, 2^8] becomes five terms.  So the score and value
+// products keep ~16 significant bits of both, as the bf16 hi/lo split of
+// the other kernels does, and the terms ride in the MMA's N:
+//   S^T[128 tok x 4R]   = K_tile . Qterms^T          (M=128, N=4R,  K=32)
+//   O^T[128 dv x NP]   += V_tile^T . Pterms^T        (M=128, N=NP,  K=32)
+// (NP = 5R rounded up to a multiple of 16; the pad rows of P stay zero).
+// Column k*R + h holds term k of row h; the softmax and the epilogue fold
+// the terms back with weights 16^-k.
+//
+// Work item = (sequence b, KV head g, split chunk s), walked in 128-token
+// tiles; a tile of K (or V) is 128 rows of 128 bytes, one 16 KB ring stage,
+// each KV block one TMA box (issued by one lane of the producer warp).
+// Warp roles as in the bf16 tcgen05 GQA kernel: warp 0 TMA producer, warp 1
+// TMEM owner and MMA issuer (it also zeroes value rows past a sequence's
+// end), warps 2-5 one thread per token lane for the query split, the
+// stale-max online softmax (the running max rises only past a slack of 8 in
+// log2 units; the accumulators are then rescaled in TMEM) and the
+// epilogue.  ~111 KB of shared memory: two CTAs per SM.  Every wait is
+// bounded.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "pkv.h"
+#include "pkv_device.cuh"
+#include "pkv_host.h"
+#include "pkv_pipeline.cuh"
+#include "pkv_tcgen05.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kM = 128;                 // tokens per tile
+constexpr int kD = 128;                 // head dim (bytes of an E4M3 row)
+constexpr int kStage = kM * kD;         // one K or V tile: 16 KB
+constexpr int kRing = 5;
+constexpr int kCtas = 2;                // CTAs per SM
+constexpr int kThreads = 192;
+constexpr int kSoftWarp0 = 2;
+constexpr int kSoftThreads = 128;
+constexpr int kQTerms = 4, kPTerms = 5;
+constexpr float kSlack = 8.f;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+template <int R>
+struct Shape {
+    static constexpr int kNQ = kQTerms * R;                         // score MMA N
+    static constexpr int kNP = (kPTerms * R + 15) / 16 * 16;        // value MMA N
+    static constexpr uint32_t kColO = 2 * kNQ;                      // S^T buffers first
+    static constexpr uint32_t kTmemCols = 2 * kNQ + kNP <= 64 ? 64 : 2 * kNQ + kNP <= 128 ? 128 : 256;
+    static constexpr uint32_t kPBytes = kNP * 128;                  // [NP rows][128 tokens]
+};
+
+// mbarrier slots
+constexpr int kBarFull = 0;             // + stage
+constexpr int kBarEmpty = 8;            // + stage
+constexpr int kBarSFull = 16;           // + buffer
+constexpr int kBarSEmpty = 18;          // + buffer
+constexpr int kBarPFull = 20;           // + P buffer
+constexpr int kBarPvDone = 22;          // + P buffer
+constexpr int kBarQFull = 24;
+constexpr int kBarQEmpty = 25;
+constexpr int kBarOEmpty = 26;
+constexpr int kBarDrain = 27;
+
+// Shared memory, offsets from a 1024-byte-aligned base.  The operand arrays
+// are sized for R = 16.
+constexpr uint32_t kOffMrow = 256;                      // running max per row (log2)
+constexpr uint32_t kOffAux = kOffMrow + 64;             // rescale factor, then 1/l
+constexpr uint32_t kOffQsc = kOffAux + 64;              // power-of-two scale s_h of row h
+constexpr uint32_t kOffRed = kOffQsc + 64;              // [4 warps][16 rows]
+constexpr uint32_t kOffSlot = kOffRed + 256;
+constexpr uint32_t kOffFlag = kOffSlot + 4;
+constexpr uint32_t kOffQ = 1024;                        // [4R rows][128 B]
+constexpr uint32_t kOffP = kOffQ + 8192;                // two [NP rows][128 B]
+constexpr uint32_t kOffRing = kOffP + 2 * 10240;
+constexpr uint32_t kSmemBytes = 1024 + kOffRing + kRing * kStage;
+static_assert(kOffRing % 1024 == 0, "operand arrays start on 1024-byte boundaries");
+
+__device__ __forceinline__ int64_t lmin(int64_t x, int64_t y) { return x < y ? x : y; }
+
+// Byte offset of (row, column < 128) in a [rows][128 B] array with the
+// 128-byte swizzle (8-row atoms 1024-byte aligned).
+__device__ __forceinline__ uint32_t swz8(int row, int col) {
+    return uint32_t(row) * 128 + (uint32_t(((col >> 4) ^ row) & 7) << 4) + uint32_t(col & 15);
+}
+
+struct Item {
+    int b, g, s;
+    int64_t len, begin, end;
+    int ntiles;
+};
+
+// Split s of (b, g) covers tokens [s C, min(L, (s + 1) C)), C = 64 ceil(L / 64 S).
+__device__ __forceinline__ Item fp8_item(const DecodeArgs &a, int item, bool report) {
+    Item r;
+    r.s = item % a.num_splits;
+    const int t = item / a.num_splits;
+    r.g = t % a.cache.num_kv_heads;
+    r.b = t / a.cache.num_kv_heads;
+    int64_t L = a.seq_lens[r.b];
+    if (L < 0 || L > int64_t(a.max_blocks) * a.cache.block_size) {
+        if (report && r.s == 0) raise_status(a.status, PKV_DEV_SEQ_LEN);
+        L = 0;
+    }
+    const int64_t chunk = 64 * ((L + 64LL * a.num_splits - 1) / (64LL * a.num_splits));
+    r.len = L;
+    r.begin = int64_t(r.s) * chunk;
+    r.end = lmin(L, r.begin + chunk);
+    r.ntiles = r.end > r.begin ? int((r.end - r.begin + kM - 1) / kM) : 0;
+    return r;
+}
+
+template <int R>
+__global__ void __launch_bounds__(kThreads, kCtas)
+decode_gqa_tc_e4m3_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                          const __grid_constant__ CUtensorMap tmap_v, const DecodeArgs a) {
+    using S = Shape<R>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_addr(base);
+    float *mrow = reinterpret_cast<float *>(base + kOffMrow);
+    float *aux = reinterpret_cast<float *>(base + kOffAux);
+    float *qsc = reinterpret_cast<float *>(base + kOffQsc);
+    float *red = reinterpret_cast<float *>(base + kOffRed);
+    volatile uint32_t *tslot = reinterpret_cast<volatile uint32_t *>(base + kOffSlot);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(base + kOffFlag);
+    auto bar = [&](int i) { return sb + 8u * uint32_t(i); };
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int num_items = a.batch * a.cache.num_kv_heads * a.num_splits;
+    const int bs = a.cache.block_size, hkv = a.cache.num_kv_heads;
+    const int box = bs < kM ? bs : kM;                 // rows per TMA box (one block or less)
+
+    if (threadIdx.x == 0) {
+        for (int r = 0; r < kRing; ++r) {
+            mbar_init(bar(kBarFull + r), 1);
+            mbar_init(bar(kBarEmpty + r), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(kBarSFull + i), 1);
+            mbar_init(bar(kBarSEmpty + i), kSoftThreads);
+            mbar_init(bar(kBarPFull + i), kSoftThreads);
+            mbar_init(bar(kBarPvDone + i), 1);
+        }
+        mbar_init(bar(kBarQFull), kSoftThreads);
+        mbar_init(bar(kBarQEmpty), 1);
+        mbar_init(bar(kBarOEmpty), kSoftThreads);
+        mbar_init(bar(kBarDrain), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tc::alloc(sb + kOffSlot, S::kTmemCols);
+        tc::fence_before_sync();
+    }
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tslot;
+    pdl_launch_dependents();
+    pdl_wait();
+
+    if (warp == 0) {
+        // -------------------------------------------------------- producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tmap_k);
+            tma_prefetch_desc(&tmap_v);
+        }
+        int stage = 0;
+        uint32_t phase = 0, armed = 0, armed_parity = 0;
+        bool ok = true;
+        const int nbox = kM / box;                     // boxes per tile (<= 8)
+        for (int item = blockIdx.x; item < num_items && ok; item += gridDim.x) {
+            const Item r = fp8_item(a, item, false);
+            if (r.ntiles == 0) continue;
+            const int32_t *table = a.block_tables + int64_t(r.b) * a.max_blocks;
+            // Rows of block 0 of this KV head stand in for boxes past the end
+            // (masked scores, zeroed value rows).
+            const int32_t standin = r.g * bs;
+            int32_t yprev = standin;
+            for (int i = 0; i <= r.ntiles && ok; ++i) {
+                int32_t y = standin;                   // lane j < nbox: row of box j of tile i
+                if (i < r.ntiles && lane < nbox) {
+                    const int64_t t = r.begin + int64_t(i) * kM + int64_t(lane) * box;
+                    if (t < r.end) {
+                        const int32_t phys = table[t / bs];
+                        if (phys >= 0 && phys < a.cache.num_blocks)
+                            y = (phys * hkv + r.g) * bs + int32_t(t % bs);
+                        else
+                            raise_status(a.status, PKV_DEV_BLOCK_ID);
+                    }
+                }
+                // K of tile i, then V of tile i - 1: one stage each
+                for (int kv = (i < r.ntiles ? 0 : 1); kv < (i > 0 ? 2 : 1); ++kv) {
+                    const bool w = pipe_wait(bar(kBarEmpty + stage), phase ^ 1u, a.status,
+                                             abort_flag);
+                    if (!__all_sync(0xffffffffu, w)) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0) mbar_arrive_expect_tx(bar(kBarFull + stage), kStage);
+                    armed |= 1u << stage;
+                    armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                    __syncwarp();
+                    if (lane < nbox)
+                        tma_load_2d(sb + kOffRing + uint32_t(stage) * kStage +
+                                        uint32_t(lane * box) * kD,
+                                    kv == 0 ? &tmap_k : &tmap_v, 0, kv == 0 ? y : yprev,
+                                    bar(kBarFull + stage));
+                    if (++stage == kRing) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                yprev = y;
+            }
+        }
+        // leave no copy in flight into this CTA's shared memory
+        if (lane == 0)
+            for (int s = 0; s < kRing; ++s)
+                if (armed & (1u << s))
+                    mbar_wait(bar(kBarFull + s), (armed_parity >> s) & 1u, a.status);
+        __syncwarp();
+    } else if (warp == 1) {
+        // -------------------------------------------------------- MMA issuer
+        constexpr uint32_t kIdS = tc::idesc_e4m3_f32(128, S::kNQ, 0, 0);   // K-major K, K-major Q
+        constexpr uint32_t kIdO = tc::idesc_e4m3_f32(128, S::kNP, 1, 0);   // MN-major V, K-major P
+        int stage = 0;
+        uint32_t phase = 0, tcount = 0, pcount = 0, ne = 0;
+        bool ok = true;
+        const uint32_t qb = sb + kOffQ, pb = sb + kOffP;
+        auto wait_all = [&](uint32_t b, uint32_t parity) {
+            return __all_sync(0xffffffffu, pipe_wait(b, parity, a.status, abort_flag));
+        };
+        auto advance = [&]() {
+            if (++stage == kRing) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        };
+        for (int item = blockIdx.x; item < num_items && ok; item += gridDim.x) {
+            const Item r = fp8_item(a, item, false);
+            if (r.ntiles == 0) continue;
+            if (!(ok = wait_all(bar(kBarQFull), ne & 1u))) break;
+            for (int i = 0; i <= r.ntiles && ok; ++i) {
+                if (i < r.ntiles) {
+                    // ---- S^T[buf] = K_tile . Qterms^T
+                    const uint32_t buf = tcount & 1u;
+                    if (!(ok = wait_all(bar(kBarSEmpty + buf), ((tcount >> 1) & 1u) ^ 1u))) break;
+                    if (!(ok = wait_all(bar(kBarFull + stage), phase))) break;
+                    tc::fence_after_sync();
+                    if (lane == 0) {
+                        const uint32_t kb = sb + kOffRing + uint32_t(stage) * kStage;
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            tc::mma_e4m3(tmem + S::kNQ * buf, tc::smem_desc(kb + 32 * kk, 16, 1024),
+                                         tc::smem_desc(qb + 32 * kk, 16, 1024), kIdS, kk != 0);
+                        tc::commit(bar(kBarEmpty + stage));
+                        tc::commit(bar(kBarSFull + buf));
+                        if (i == r.ntiles - 1) tc::commit(bar(kBarQEmpty));
+                    }
+                    __syncwarp();
+                    advance();
+                    ++tcount;
+                }
+                if (i > 0) {
+                    // ---- O^T += V_tile^T . Pterms^T for tile j
+                    const int j = i - 1;
+                    const uint32_t pbuf = pcount & 1u;
+                    if (!(ok = wait_all(bar(kBarPFull + pbuf), (pcount >> 1) & 1u))) break;
+                    if (j == 0 && !(ok = wait_all(bar(kBarOEmpty), (ne & 1u) ^ 1u))) break;
+                    if (!(ok = wait_all(bar(kBarFull + stage), phase))) break;
+                    const int64_t tok0 = r.begin + int64_t(j) * kM;
+                    const int nvalid = int(lmin(kM, r.end - tok0));
+                    if (nvalid < kM) {
+                        // value rows past the end may hold any bits (NaN
+                        // times a zero probability is NaN): zero them
+                        uint8_t *vt = base + kOffRing + size_t(stage) * kStage;
+                        for (int idx = lane; idx < (kM - nvalid) * 8; idx += 32)
+                            *reinterpret_cast<uint4 *>(vt + (nvalid + (idx >> 3)) * kD +
+                                                       (idx & 7) * 16) = make_uint4(0, 0, 0, 0);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                    }
+                    tc::fence_after_sync();
+                    if (lane == 0) {
+                        const uint32_t vb = sb + kOffRing + uint32_t(stage) * kStage;
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            tc::mma_e4m3(tmem + S::kColO,
+                                         tc::smem_desc(vb + 4096 * kk, 16384, 1024),
+                                         tc::smem_desc(pb + pbuf * S::kPBytes + 32 * kk, 16, 1024),
+                                         kIdO, (j | kk) != 0);
+                        tc::commit(bar(kBarEmpty + stage));
+                        tc::commit(bar(kBarPvDone + pbuf));
+                    }
+                    __syncwarp();
+                    advance();
+                    ++pcount;
+                }
+            }
+            ++ne;
+        }
+        if (lane == 0) {
+            tc::commit(bar(kBarDrain));
+            mbar_wait(bar(kBarDrain), 0, a.status);
+        }
+        __syncwarp();
+    } else {
+        // -------------------------------------------- softmax and epilogue
+        const int t = threadIdx.x - kSoftWarp0 * 32;     // 0..127
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;                // token lane of S^T, value row of O^T
+        const uint32_t tl = tmem + (uint32_t(quad * 32) << 16);
+        uint8_t *qs = base + kOffQ, *ps = base + kOffP;
+        constexpr int kTpr = 128 / R;                    // threads per query row in the split
+        uint32_t tcount = 0, pcount = 0, ne = 0;
+        // the pad rows of both probability buffers stay zero
+        for (int i = t; i < 2 * int(S::kPBytes) / 16; i += kSoftThreads)
+            reinterpret_cast<uint4 *>(ps)[i] = make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
+        auto wait_pv = [&](uint32_t j) {
+            return pipe_wait(bar(kBarPvDone + (j & 1u)), (j >> 1) & 1u, a.status, abort_flag);
+        };
+        for (int item = blockIdx.x; item < num_items; item += gridDim.x) {
+            const Item r = fp8_item(a, item, t == 0);
+            const int64_t row0 = int64_t(r.b) * a.num_q_heads + int64_t(r.g) * R;
+            const int64_t split0 = int64_t(r.s) * a.batch * a.num_q_heads;
+            if (r.ntiles == 0) {
+                float4 *o = reinterpret_cast<float4 *>(a.out_part + (split0 + row0) * kD);
+                for (int i = t; i < R * kD / 4; i += kSoftThreads)
+                    o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (t < R) a.lse_part[split0 + row0 + t] = -INFINITY;
+                continue;
+            }
+            // ---- the item's query rows as four E4M3 terms each (rows k R + h
+            // of the score MMA's K-major B operand); thread t holds R dims of
+            // row t / kTpr
+            bool w = pipe_wait(bar(kBarQEmpty), (ne & 1u) ^ 1u, a.status, abort_flag);
+            if (w) {
+                const int h = t / kTpr, d0 = (t % kTpr) * R;
+                const float qmul = a.scale * kLog2e * a.k_scale[r.g];
+                const float4 *src = reinterpret_cast<const float4 *>(a.q + (row0 + h) * kD + d0);
+                float x[R];
+                float amax = 0.f;
+#pragma unroll
+                for (int v = 0; v < R / 4; ++v) {
+                    const float4 f = src[v];
+                    x[4 * v] = f.x * qmul;
+                    x[4 * v + 1] = f.y * qmul;
+                    x[4 * v + 2] = f.z * qmul;
+                    x[4 * v + 3] = f.w * qmul;
+                }
+#pragma unroll
+                for (int e = 0; e < R; ++e) amax = fmaxf(amax, fabsf(x[e]));
+#pragma unroll
+                for (int o = kTpr / 2; o > 0; o >>= 1)
+                    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+                // s_h = 2^(floor(log2 max|x|) - 7): the row's largest term-0
+                // magnitude lies in [128, 256), below E4M3's 448
+                const int e2 = amax > 0.f ? max(ilogbf(amax), -110) : 0;
+                const float inv = ldexpf(1.f, 7 - e2);
+                if (t % kTpr == 0) qsc[h] = ldexpf(1.f, e2 - 7);
+#pragma unroll
+                for (int e = 0; e < R; ++e) x[e] *= inv;
+#pragma unroll
+                for (int k = 0; k < kQTerms; ++k)
+#pragma unroll
+                    for (int e = 0; e < R; e += 4) {
+                        const uint32_t c01 = e4m3x2_from_f32(x[e], x[e + 1]);
+                        const uint32_t c23 = e4m3x2_from_f32(x[e + 2], x[e + 3]);
+                        *reinterpret_cast<uint32_t *>(qs + swz8(k * R + h, d0 + e)) =
+                            c01 | (c23 << 16);
+                        const float2 v01 = e4m3x2_to_f32(c01), v23 = e4m3x2_to_f32(c23);
+                        x[e] = (x[e] - v01.x) * 16.f;
+                        x[e + 1] = (x[e + 1] - v01.y) * 16.f;
+                        x[e + 2] = (x[e + 2] - v23.x) * 16.f;
+                        x[e + 3] = (x[e + 3] - v23.y) * 16.f;
+                    }
+                fence_proxy_async_smem();
+            }
+            mbar_arrive(bar(kBarQFull));
+            if (t < R) mrow[t] = -INFINITY;
+            float l_part[R];
+#pragma unroll
+            for (int h = 0; h < R; ++h) l_part[h] = 0.f;
+            const int32_t span = int32_t(r.end - r.begin);
+            if (softmax_bar_or(!w)) break;          // also orders qsc and mrow for all
+
+            bool ok = true;
+            for (int i = 0; i < r.ntiles; ++i) {
+                const uint32_t buf = tcount & 1u;
+                w = pipe_wait(bar(kBarSFull + buf), (tcount >> 1) & 1u, a.status, abort_flag);
+                float x[R];
+                {
+                    uint32_t v[S::kNQ];
+                    tc::fence_after_sync();
+#pragma unroll
+                    for (int c = 0; c < S::kNQ / 16; ++c)
+                        tc::ld16(tl + S::kNQ * buf + 16 * c,
+                                 *reinterpret_cast<uint32_t(*)[16]>(v + 16 * c));
+                    tc::wait_ld();
+#pragma unroll
+                    for (int h = 0; h < R; ++h) {      // fold the query terms back
+                        float s = __uint_as_float(v[3 * R + h]);
+                        s = fmaf(s, 0.0625f, __uint_as_float(v[2 * R + h]));
+                        s = fmaf(s, 0.0625f, __uint_as_float(v[R + h]));
+                        s = fmaf(s, 0.0625f, __uint_as_float(v[h]));
+                        x[h] = s * qsc[h];
+                    }
+                }
+                tc::fence_before_sync();
+                mbar_arrive(bar(kBarSEmpty + buf));
+                ++tcount;
+                const bool in_span = i * kM + row < span;
+                bool need = false;
+#pragma unroll
+                for (int h = 0; h < R; ++h) {
+                    x[h] = in_span ? x[h] : -INFINITY;
+                    need |= x[h] > mrow[h] + kSlack;
+                }
+                if (softmax_bar_or(!w)) {
+                    ok = false;
+                    break;
+                }
+                if (softmax_bar_or(need)) {
+#pragma unroll
+                    for (int h = 0; h < R; ++h) {
+                        float m = x[h];
+                        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+                        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+                        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+                        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+                        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+                        if (lane == h) red[quad * 16 + h] = m;
+                    }
+                    named_barrier_sync(1, kSoftThreads);
+                    if (t < R) {
+                        const float tm = fmaxf(fmaxf(red[t], red[16 + t]),
+                                               fmaxf(red[32 + t], red[48 + t]));
+                        const float mo = mrow[t], mn = fmaxf(mo, tm);
+                        aux[t] = (mo == -INFINITY || mn == -INFINITY) ? 0.f : exp2f(mo - mn);
+                        mrow[t] = mn;
+                    }
+                    named_barrier_sync(1, kSoftThreads);
+#pragma unroll
+                    for (int h = 0; h < R; ++h) l_part[h] *= aux[h];
+                    if (i > 0) {
+                        // the accumulators are quiet once the previous tile's
+                        // value MMAs are done
+                        const bool wv = wait_pv(pcount - 1);
+                        tc::fence_after_sync();
+                        if (wv) {
+#pragma unroll
+                            for (int c = 0; c < S::kNP / 16; ++c) {
+                                uint32_t v[16];
+                                const uint32_t ta = tl + S::kColO + 16 * c;
+                                tc::ld16(ta, v);
+                                tc::wait_ld();
+#pragma unroll
+                                for (int k = 0; k < 16; ++k)
+                                    v[k] = __float_as_uint(__uint_as_float(v[k]) *
+                                                           aux[(16 * c + k) % R]);
+                                tc::st16(ta, v);
+                            }
+                            tc::wait_st();
+                        }
+                    }
+                }
+                float p[R];
+#pragma unroll
+                for (int h = 0; h < R; ++h) {
+                    p[h] = x[h] == -INFINITY ? 0.f : exp2f(x[h] - mrow[h]);
+                    l_part[h] += p[h];
+                }
+                // this P buffer was last read by the value MMAs of tile pcount-2
+                if (pcount >= 2) wait_pv(pcount - 2);
+                {
+                    // five E4M3 terms of each probability (p <= 2^8), term k of
+                    // row h at row k R + h of the value MMA's K-major B
+                    // operand, this thread's token its column
+                    uint8_t *pa = ps + (pcount & 1u) * S::kPBytes;
+#pragma unroll
+                    for (int k = 0; k < kPTerms; ++k)
+#pragma unroll
+                        for (int h = 0; h < R; h += 2) {
+                            const uint32_t c = e4m3x2_from_f32(p[h], p[h + 1]);
+                            pa[swz8(k * R + h, row)] = uint8_t(c);
+                            pa[swz8(k * R + h + 1, row)] = uint8_t(c >> 8);
+                            if (k + 1 < kPTerms) {
+                                const float2 v = e4m3x2_to_f32(c);
+                                p[h] = (p[h] - v.x) * 16.f;
+                                p[h + 1] = (p[h + 1] - v.y) * 16.f;
+                            }
+                        }
+                }
+                fence_proxy_async_smem();
+                tc::fence_before_sync();
+                mbar_arrive(bar(kBarPFull + (pcount & 1u)));
+                ++pcount;
+            }
+            if (!ok) break;
+
+            // ---- epilogue: the item's last value MMAs are done
+            w = wait_pv(pcount - 1);
+            tc::fence_after_sync();
+#pragma unroll
+            for (int h = 0; h < R; ++h) {
+                float s = l_part[h];
+                s += __shfl_xor_sync(0xffffffffu, s, 16);
+                s += __shfl_xor_sync(0xffffffffu, s, 8);
+                s += __shfl_xor_sync(0xffffffffu, s, 4);
+                s += __shfl_xor_sync(0xffffffffu, s, 2);
+                s += __shfl_xor_sync(0xffffffffu, s, 1);
+                if (lane == h) red[quad * 16 + h] = s;
+            }
+            named_barrier_sync(1, kSoftThreads);
+            if (t < R) {
+                const float l = (red[t] + red[16 + t]) + (red[32 + t] + red[48 + t]);
+                aux[t] = l > 0.f ? a.v_scale[r.g] / l : 0.f;
+                a.lse_part[split0 + row0 + t] = l > 0.f ? (mrow[t] + log2f(l)) * kLn2 : -INFINITY;
+            }
+            named_barrier_sync(1, kSoftThreads);
+            if (w) {
+                uint32_t v[S::kNP];
+#pragma unroll
+                for (int c = 0; c < S::kNP / 16; ++c)
+                    tc::ld16(tl + S::kColO + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(v + 16 * c));
+                tc::wait_ld();
+#pragma unroll
+                for (int h = 0; h < R; ++h) {          // fold the probability terms back
+                    float o = __uint_as_float(v[4 * R + h]);
+                    o = fmaf(o, 0.0625f, __uint_as_float(v[3 * R + h]));
+                    o = fmaf(o, 0.0625f, __uint_as_float(v[2 * R + h]));
+                    o = fmaf(o, 0.0625f, __uint_as_float(v[R + h]));
+                    o = fmaf(o, 0.0625f, __uint_as_float(v[h]));
+                    a.out_part[(split0 + row0 + h) * kD + row] = o * aux[h];
+                }
+            }
+            tc::fence_before_sync();
+            mbar_arrive(bar(kBarOEmpty));
+            ++ne;
+            if (softmax_bar_or(!w)) break;
+        }
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::dealloc(tmem, S::kTmemCols);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 e4m3_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// The pool as rows of 128 one-byte codes; one box = `box` rows, landing as
+// [rows][128 B] with the 128-byte swizzle.
+bool make_byte_map(CUtensorMap *map, const void *pool, int64_t rows, int box) {
+    auto fn = e4m3_encode_fn();
+    if (!fn) return false;
+    cuuint64_t gdim[2] = {cuuint64_t(kD), cuuint64_t(rows)};
+    cuuint64_t gstride[1] = {cuuint64_t(kD)};
+    cuuint32_t bdim[2] = {cuuint32_t(kD), cuuint32_t(box)};
+    cuuint32_t estride[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(pool), gdim, gstride,
+              bdim, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int R>
+int launch_rows(const DecodeArgs &a) {
+    auto kernel = decode_gqa_tc_e4m3_kernel<R>;
+    const int64_t rows = int64_t(a.cache.num_blocks) * a.cache.num_kv_heads * a.cache.block_size;
+    const int box = std::min(a.cache.block_size, kM);
+    CUtensorMap tk, tv;
+    if (!make_byte_map(&tk, a.k_pool, rows, box) || !make_byte_map(&tv, a.v_pool, rows, box))
+        return PKV_ERR_CUDA;
+    static thread_local int configured_dev = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_dev != dev) {
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(kSmemBytes)) != cudaSuccess)
+            return PKV_ERR_CUDA;
+        configured_dev = dev;
+    }
+    // kCtas CTAs per SM by construction (shared memory, registers and TMEM
+    // columns are sized for it); the persistent loop is correct for any grid.
+    const int64_t items = int64_t(a.batch) * a.cache.num_kv_heads * a.num_splits;
+    const int grid = int(std::min<int64_t>(items, int64_t(sm_count()) * kCtas));
+    if (grid <= 0) return PKV_OK;
+    return launch_pdl(kernel, dim3(grid), dim3(kThreads), kSmemBytes, a.stream, tk, tv, a);
+}
+
+}  // namespace
+
+bool gqa_tc_e4m3_kernel_supports(const pkv_cache_desc &c, int32_t num_q_heads) {
+    if (c.num_kv_heads <= 0 || num_q_heads % c.num_kv_heads != 0) return false;
+    const int G = num_q_heads / c.num_kv_heads;
+    const bool pow2_bs = c.block_size >= 16 && c.block_size <= 256 &&
+                         (c.block_size & (c.block_size - 1)) == 0;
+    const int64_t rows = int64_t(c.num_blocks) * c.num_kv_heads * c.block_size;
+    return (G == 4 || G == 8 || G == 16) && c.head_dim_k == kD && c.head_dim_v == kD && pow2_bs &&
+           rows < (int64_t(1) << 31) - 1;
+}
+
+int launch_decode_gqa_tc_e4m3(const DecodeArgs &a) {
+    switch (a.num_q_heads / a.cache.num_kv_heads) {
+        case 4: return launch_rows<4>(a);
+        case 8: return launch_rows<8>(a);
+        case 16: return launch_rows<16>(a);
+        default: return PKV_ERR_SHAPE;
+    }
+}
+
+}  // namespace pkv

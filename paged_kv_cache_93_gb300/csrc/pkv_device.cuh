@@ -39,6 +39,24 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return out;
 }
 
+// Two fp32 -> two E4M3 codes (nearest, ties to even; magnitudes beyond the
+// largest finite 448 give +-448): `lo` in bits 0-7, `hi` in bits 8-15.
+__device__ __forceinline__ uint32_t e4m3x2_from_f32(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+// The values of the two E4M3 codes in bits 0-7 (.x) and 8-15 (.y): exact
+// (every E4M3 value is an fp16 value).
+__device__ __forceinline__ float2 e4m3x2_to_f32(uint32_t codes) {
+    uint32_t h2;
+    asm("{ .reg .b16 c; cvt.u16.u32 c, %1; cvt.rn.f16x2.e4m3x2 %0, c; }" : "=r"(h2) : "r"(codes));
+    float lo, hi;
+    asm("{ .reg .b16 l, h; mov.b32 {l, h}, %2; cvt.f32.f16 %0, l; cvt.f32.f16 %1, h; }"
+        : "=f"(lo), "=f"(hi) : "r"(h2));
+    return make_float2(lo, hi);
+}
+
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

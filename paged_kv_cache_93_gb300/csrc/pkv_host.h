@@ -64,6 +64,8 @@ struct DecodeArgs {
     // first seq_lens[b] - T + 1 + t tokens.  Only the GQA TMA kernel reads
     // T; the other kernels are given one row per (sequence, token) instead.
     int32_t q_tokens = 1;
+    // E4M3 pools: per-KV-head dequantisation scales (device, [num_kv_heads]).
+    const float *k_scale = nullptr, *v_scale = nullptr;
 };
 bool tma_kernel_supports(const pkv_cache_desc &c, int32_t num_q_heads, int32_t q_tokens = 1);
 // 16 query rows per KV head (heads x query tokens), head dims 128: the
@@ -72,6 +74,10 @@ bool gqa_tc_kernel_supports(const pkv_cache_desc &c, int32_t num_q_heads, int32_
 int launch_decode_gqa_tc(const DecodeArgs &a);
 // CTAs the tcgen05 GQA kernel keeps resident (one persistent grid).
 int gqa_tc_resident_ctas();
+// E4M3 pools, query groups of 4, 8 or 16, head dims 128: the tcgen05 kernel
+// with E4M3 operands.
+bool gqa_tc_e4m3_kernel_supports(const pkv_cache_desc &c, int32_t num_q_heads);
+int launch_decode_gqa_tc_e4m3(const DecodeArgs &a);
 int launch_decode_tma(const DecodeArgs &a);
 // Large query groups (G a multiple of 32, e.g. MLA-shaped 128 heads over one
 // 576/512 latent head): tensor-core kernel with 32-head work items.

@@ -1,0 +1,215 @@
+"""FP8 (E4M3) cache on the GPU against the oracle: the quantising append and
+the block copy byte for byte, and decode attention over E4M3 pools with
+per-KV-head scales within the contract's tolerances (the oracle attends to
+the same stored values, decoded and scaled in fp64)."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from tests._steps import assert_attention_close
+from tests._util import bits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    import __graft_entry__
+    __graft_entry__.build()
+    import paged_kv_cache_93_gb300 as m
+    m.device_status(reset=True)
+    return m
+
+
+def gpu_e4m3_step(pkv, w, splits, dev="cuda"):
+    k, v = w.k_codes.to(dev), w.v_codes.to(dev)
+    ks, vs = w.k_scale.to(dev), w.v_scale.to(dev)
+    bt = w.block_tables.to(dev)
+    slots = pkv.slot_mapping(k, v, bt, w.new_seq.to(dev), w.new_pos.to(dev))
+    pkv.kv_append_e4m3(k, v, w.k_new.to(dev), w.v_new.to(dev), slots, ks, vs)
+    out, lse = pkv.paged_decode_attn_e4m3(w.q.to(dev), k, v, ks, vs, bt, w.seq_lens.to(dev),
+                                          w.scale, num_splits=splits)
+    torch.cuda.synchronize()
+    return out.cpu().numpy(), lse.cpu().numpy(), k.cpu().numpy(), v.cpu().numpy()
+
+
+def oracle_e4m3_cache(w):
+    k, v = w.k_codes.numpy().copy(), w.v_codes.numpy().copy()
+    slots = oracle.slot_mapping(w.block_tables.numpy(), w.new_seq.numpy(), w.new_pos.numpy(),
+                                w.block_size)
+    assert oracle.kv_append_e4m3(k, v, bits(w.k_new), bits(w.v_new), w.k_scale.numpy(),
+                                 w.v_scale.numpy(), slots, w.block_size) == 0
+    return k, v
+
+
+def oracle_e4m3_step(w):
+    k, v = oracle_e4m3_cache(w)
+    out, lse = oracle.paged_decode_attn_e4m3(w.q.numpy(), k, v, w.k_scale.numpy(),
+                                             w.v_scale.numpy(), w.block_tables.numpy(),
+                                             w.seq_lens.numpy(), w.scale)
+    return out, lse, k, v
+
+
+# (cached lengths, Hq, Hkv, block size): groups of 4, 8 and 16; ragged tails,
+# a sequence holding only the new token, block sizes 16..256
+SHAPES = [
+    ([300, 7, 64, 0], 32, 8, 16),
+    ([129, 40, 255], 16, 2, 32),
+    ([600, 65], 64, 4, 64),
+    ([700, 5, 130], 8, 2, 128),
+    ([200, 1], 16, 1, 256),
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: f"G{s[1]//s[2]}_bs{s[3]}")
+@pytest.mark.parametrize("splits", [1, 3, 0])
+def test_e4m3_step_matches_oracle(pkv, shape, splits):
+    cached, hq, hkv, bs = shape
+    w = workloads.e4m3(workloads.custom(40 + bs + hq, cached, hq, hkv, 128, 128, bs))
+    out, lse, k, v = gpu_e4m3_step(pkv, w, splits)
+    ro, rl, rk, rv = oracle_e4m3_step(w)
+    assert np.array_equal(k, rk) and np.array_equal(v, rv), "pools after the append"
+    assert_attention_close(out, lse, ro, rl, f"e4m3 {shape}/{splits}")
+    assert pkv.device_status() == 0
+
+
+def test_e4m3_append_saturates_and_flags(pkv):
+    """Large new values saturate to +-448 codes; skipped and out-of-range
+    slots behave as in the bf16 append."""
+    g = torch.Generator().manual_seed(4)
+    nb, hkv, bs = 6, 2, 16
+    k = torch.zeros(nb, hkv, bs, 128, dtype=torch.uint8)
+    v = torch.zeros(nb, hkv, bs, 128, dtype=torch.uint8)
+    kn = (torch.randn(5, hkv, 128, generator=g) * 20).to(torch.bfloat16)
+    vn = (torch.randn(5, hkv, 128, generator=g) * 3).to(torch.bfloat16)
+    ks = torch.tensor([0.01, 0.2])
+    vs = torch.tensor([0.05, 0.5])
+    slots = torch.tensor([0, 17, -1, 95, 96], dtype=torch.int64)        # 96 is past the pool
+    dev = "cuda"
+    kd, vd = k.to(dev), v.to(dev)
+    pkv.kv_append_e4m3(kd, vd, kn.to(dev), vn.to(dev), slots.to(dev), ks.to(dev), vs.to(dev))
+    assert pkv.device_status() == pkv.DEV_SLOT
+    kh, vh = k.numpy().copy(), v.numpy().copy()
+    assert oracle.kv_append_e4m3(kh, vh, bits(kn), bits(vn), ks.numpy(), vs.numpy(),
+                                 slots.numpy(), bs) == 1
+    assert np.array_equal(kd.cpu().numpy(), kh) and np.array_equal(vd.cpu().numpy(), vh)
+    assert (kh == 0x7E).any() and (kh == 0xFE).any()      # some values saturated
+
+
+def test_e4m3_copy_blocks(pkv):
+    g = torch.Generator().manual_seed(5)
+    k = torch.randint(0, 256, (8, 2, 16, 128), generator=g, dtype=torch.uint8)
+    v = torch.randint(0, 256, (8, 2, 16, 128), generator=g, dtype=torch.uint8)
+    dev = "cuda"
+    kd, vd = k.to(dev), v.to(dev)
+    src = torch.tensor([1, 3], dtype=torch.int32)
+    dst = torch.tensor([6, 0], dtype=torch.int32)
+    pkv.copy_blocks_e4m3(kd, vd, src.to(dev), dst.to(dev))
+    torch.cuda.synchronize()
+    ek, ev = k.clone(), v.clone()
+    ek[dst.long()] = k[src.long()]
+    ev[dst.long()] = v[src.long()]
+    assert torch.equal(kd.cpu(), ek) and torch.equal(vd.cpu(), ev)
+    assert pkv.device_status() == 0
+
+
+@pytest.mark.parametrize("hq", [8, 16, 32], ids=["G4", "G8", "G16"])
+def test_e4m3_single_token_is_exact(pkv, hq):
+    """One token: out is its stored value times the value scale, rounded
+    once to fp32; lse is its score."""
+    w = workloads.e4m3(workloads.custom(9, [0, 0], hq, 2, 128, 128, 16))
+    out, lse, *_ = gpu_e4m3_step(pkv, w, 1)
+    ro, rl, _, rv = oracle_e4m3_step(w)
+    assert np.array_equal(out, ro.astype(np.float32))
+    assert np.abs(lse - rl).max() <= 1e-4
+
+
+def test_e4m3_nan_codes_in_unused_slots_do_not_leak(pkv):
+    w = workloads.e4m3(workloads.custom(13, [20, 50], 32, 2, 128, 128, 16, extra_blocks=0))
+    for b in range(2):
+        L = int(w.seq_lens[b])
+        last = int(w.block_tables[b, (L - 1) // 16])
+        w.k_codes[last, :, L % 16 or 16:] = 0x7F
+        w.v_codes[last, :, L % 16 or 16:] = 0xFF
+    out, lse, *_ = gpu_e4m3_step(pkv, w, 1)
+    assert np.isfinite(out).all() and np.isfinite(lse).all()
+    ro, rl, *_ = oracle_e4m3_step(w)
+    assert_attention_close(out, lse, ro, rl, "nan tail")
+
+
+@pytest.mark.parametrize("splits", [1, 3])
+def test_e4m3_rising_scores(pkv, splits):
+    """Keys grow along the sequence: the running max keeps rising past the
+    slack and the accumulators are rescaled in TMEM."""
+    w = workloads.custom(92, [1500, 700], 32, 2, 128, 128, 16)
+    k = w.k_pool.float()
+    for b in range(2):
+        L = int(w.seq_lens[b])
+        for j in range(L):
+            blk = int(w.block_tables[b, j // 16])
+            k[blk, :, j % 16] *= 1.0 + 6.0 * j / L
+    w.k_pool = k.to(torch.bfloat16)
+    w = workloads.e4m3(w)
+    w.k_scale *= 7.0                                      # keep the grown keys in range
+    w.k_codes = (w.k_pool.float() / w.k_scale.view(1, -1, 1, 1)).clamp(-448, 448).to(
+        torch.float8_e4m3fn).view(torch.uint8)
+    out, lse, *_ = gpu_e4m3_step(pkv, w, splits)
+    ro, rl, *_ = oracle_e4m3_step(w)
+    assert_attention_close(out, lse, ro, rl, f"rising/{splits}")
+    assert pkv.device_status() == 0
+
+
+def test_e4m3_bad_seq_len_and_block_id_are_flagged(pkv):
+    w = workloads.e4m3(workloads.custom(12, [100, 100], 32, 2, 128, 128, 16))
+    dev = "cuda"
+    k, v = w.k_codes.to(dev), w.v_codes.to(dev)
+    ks, vs = w.k_scale.to(dev), w.v_scale.to(dev)
+    q = w.q.to(dev)
+    lens = w.seq_lens.clone()
+    lens[1] = 10_000
+    out, lse = pkv.paged_decode_attn_e4m3(q, k, v, ks, vs, w.block_tables.to(dev), lens.to(dev),
+                                          w.scale, num_splits=2)
+    assert pkv.device_status() == pkv.DEV_SEQ_LEN
+    assert torch.isneginf(lse[1]).all() and (out[1] == 0).all()
+    bt = w.block_tables.clone()
+    bt[0, 3] = 1 << 20
+    out, lse = pkv.paged_decode_attn_e4m3(q, k, v, ks, vs, bt.to(dev), w.seq_lens.to(dev),
+                                          w.scale, num_splits=2)
+    assert pkv.device_status() == pkv.DEV_BLOCK_ID
+    assert torch.isfinite(out).all() and torch.isfinite(lse).all()
+
+
+def test_e4m3_full_size_sampled_rows(pkv):
+    """8 x 32K GQA step (32/8 heads, block 16) over an E4M3 cache: three
+    whole sequences against the oracle."""
+    w = workloads.make("long32k_e4m3")
+    out, lse, *_ = gpu_e4m3_step(pkv, w, 0)
+    assert pkv.device_status() == 0
+    k, v = oracle_e4m3_cache(w)
+    for b in (0, 3, 7):
+        ro, rl = oracle.paged_decode_attn_e4m3(w.q.numpy()[b:b + 1], k, v, w.k_scale.numpy(),
+                                               w.v_scale.numpy(), w.block_tables.numpy()[b:b + 1],
+                                               w.seq_lens.numpy()[b:b + 1], w.scale)
+        assert_attention_close(out[b:b + 1], lse[b:b + 1], ro, rl, f"sequence {b}")
+
+
+def test_e4m3_quantisation_error_is_reported(pkv):
+    """Not parity (the stored values differ from the bf16 ones): the FP8
+    cache's output against the bf16 cache's, on the same data, stays small.
+    The pages ask for the accuracy effect of quantisation to be checked."""
+    w = workloads.custom(21, [2000, 517], 32, 8, 128, 128, 16)
+    dev = "cuda"
+    ob, _ = pkv.paged_decode_attn(w.q.to(dev), w.k_pool.to(dev), w.v_pool.to(dev),
+                                  w.block_tables.to(dev), w.seq_lens.to(dev), w.scale)
+    w = workloads.e4m3(w)
+    k, v = w.k_codes.to(dev), w.v_codes.to(dev)
+    o8, _ = pkv.paged_decode_attn_e4m3(w.q.to(dev), k, v, w.k_scale.to(dev), w.v_scale.to(dev),
+                                       w.block_tables.to(dev), w.seq_lens.to(dev), w.scale)
+    torch.cuda.synchronize()
+    rel = ((o8 - ob).norm(dim=-1) / ob.norm(dim=-1)).max().item()
+    print(f"E4M3 vs bf16 cache: max row rel-L2 {rel:.4f}")
+    assert rel < 0.1

@@ -39,7 +39,7 @@ from dataclasses import dataclass, field
 import torch
 
 __all__ = ["Workload", "make", "NAMES", "tiny", "mix", "long32k", "dcp200k", "agent_mla",
-           "custom", "random_partials"]
+           "custom", "random_partials", "e4m3"]
 
 NAMES = ("tiny", "mix", "long32k", "dcp200k", "agent_mla")
 
@@ -76,6 +76,12 @@ class Workload:
     # Multi-token steps: q is [B, tokens_per_seq, Hq, Dk] and the last
     # tokens_per_seq tokens of each sequence are the step's new ones.
     tokens_per_seq: int = 1
+    # FP8 cache (see e4m3()): uint8 code pools before the step and fp32
+    # dequantisation scales per KV head.
+    k_codes: torch.Tensor | None = None
+    v_codes: torch.Tensor | None = None
+    k_scale: torch.Tensor | None = None
+    v_scale: torch.Tensor | None = None
 
     @property
     def batch(self) -> int:
@@ -288,7 +294,32 @@ def custom(seed: int, cached: list[int], hq: int, hkv: int, dk: int, dv: int, bs
                     new_seq, new_pos, k_new, v_new)
 
 
+def e4m3(w: Workload, seed: int = 11) -> Workload:
+    """The same step over an FP8 (E4M3) cache.  Each KV head gets scales near
+    8/448 (so an 8-sigma value is the largest code); the cache before the
+    step holds torch's float8_e4m3fn cast of the bf16 pools divided by their
+    head's scale, clipped to +-448 -- a stand-in for a cache filled by
+    earlier appends.  The step's new tokens stay bf16 (the append quantises
+    them).  Needs a separate value pool."""
+    assert w.v_pool is not None and w.cow_src.numel() == 0
+    g = torch.Generator().manual_seed(seed)
+    hkv = w.num_kv_heads
+    ks = (8.0 / 448.0) * (1.0 + 0.5 * torch.rand(hkv, generator=g))
+    vs = (8.0 / 448.0) * (1.0 + 0.5 * torch.rand(hkv, generator=g))
+
+    def codes(pool, s):
+        x = pool.float().div_(s.view(1, -1, 1, 1)).clamp_(-448.0, 448.0)
+        return x.to(torch.float8_e4m3fn).view(torch.uint8)
+
+    w.k_codes, w.v_codes = codes(w.k_pool, ks), codes(w.v_pool, vs)
+    w.k_scale, w.v_scale = ks.float(), vs.float()
+    w.name = w.name + "_e4m3"
+    return w
+
+
 def make(name: str, **kw) -> Workload:
+    if name == "long32k_e4m3":
+        return e4m3(long32k(**kw))
     if name == "agent_mla_latent":
         return agent_mla(latent=True, **kw)
     if name == "spec4_32k":
