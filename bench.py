@@ -51,17 +51,25 @@ PROFILES = {
     "long32k": ("decode_tma_long32k.txt", ("decode_tma.cu", "pkv_device.cuh")),
     "spec4_32k": ("decode_gqa_tc_spec4_32k.txt",
                   ("decode_gqa_tc.cu", "pkv_device.cuh", "pkv_tcgen05.cuh")),
+    "long32k_e4m3": ("decode_gqa_tc_e4m3_long32k.txt",
+                     ("decode_gqa_tc_e4m3.cu", "pkv_device.cuh", "pkv_tcgen05.cuh",
+                      "pkv_pipeline.cuh")),
 }
 
 
 # ----------------------------------------------------------------- helpers
 
+def elem_bytes(w) -> int:
+    """Bytes of one cached number: 1 for an E4M3 cache, 2 for bf16."""
+    return 1 if w.k_codes is not None else 2
+
+
 def kv_bytes_per_token(w) -> int:
-    """K and V bytes one token occupies in one layer: (Dk + Dv) x Hkv x 2 B,
-    or Dk x Hkv x 2 B when the values live inside the key rows."""
+    """K and V bytes one token occupies in one layer: (Dk + Dv) x Hkv x the
+    element size, or Dk x Hkv x it when the values live inside the key rows."""
     if w.v_pool is None:
-        return w.head_dim_k * w.num_kv_heads * 2
-    return (w.head_dim_k + w.head_dim_v) * w.num_kv_heads * 2
+        return w.head_dim_k * w.num_kv_heads * elem_bytes(w)
+    return (w.head_dim_k + w.head_dim_v) * w.num_kv_heads * elem_bytes(w)
 
 
 def unique_kv_tokens(w) -> int:
@@ -87,7 +95,8 @@ def step_bytes(w, splits: int):
     tables = int(((lens + w.block_size - 1) // w.block_size).sum()) * 4 + B * 4
     out = rows * (w.head_dim_v + 1) * 4
     T = int(w.new_pos.numel())
-    append = 2 * T * kv_bytes_per_token(w) + T * (8 + 4 + 8)
+    # the append reads bf16 new tokens and writes cache elements
+    append = T * (kv_bytes_per_token(w) // elem_bytes(w)) * (2 + elem_bytes(w)) + T * (8 + 4 + 8)
     kernel = kv + q + tables
     return kv + q + tables + out + append, kernel
 
@@ -380,10 +389,56 @@ class MultiStep(Step):
             ev_b.record()
 
 
+class E4m3Step(Step):
+    """The 32K decode step over an FP8 (E4M3) cache: slot mapping, the
+    quantising append of the decode tokens, one pkv_paged_decode_attn_e4m3."""
+    kernel_name = ("pkv_paged_decode_attn_e4m3 (decode_gqa_tc_e4m3_kernel: tcgen05 "
+                   "kind::f8f6f4, E4M3 K/V as stored, the query as 4 and the probabilities as "
+                   "5 E4M3 terms, + lse_merge)")
+
+    def __init__(self, pkv, w, dev, splits):
+        self.pkv, self.w, self.splits = pkv, w, splits
+        self.k, self.v = w.k_codes.to(dev), w.v_codes.to(dev)
+        self.k_scale, self.v_scale = w.k_scale.to(dev), w.v_scale.to(dev)
+        self.bt, self.lens, self.q = w.block_tables.to(dev), w.seq_lens.to(dev), w.q.to(dev)
+        self.new_seq, self.new_pos = w.new_seq.to(dev), w.new_pos.to(dev)
+        self.k_new, self.v_new = w.k_new.to(dev), w.v_new.to(dev)
+        B, Hq = w.batch, w.num_q_heads
+        self.slots = torch.empty(w.new_pos.numel(), dtype=torch.int64, device=dev)
+        self.out = torch.empty(B, Hq, w.head_dim_v, device=dev)
+        self.lse = torch.empty(B, Hq, device=dev)
+        self.ws = torch.zeros(max(1, pkv.decode_workspace_size(B, Hq, w.head_dim_v, splits)),
+                              dtype=torch.uint8, device=dev)
+        self.launches = 4   # slot, append, split, merge
+        self.desc = (f"slot_mapping + kv_append_e4m3 ({w.new_pos.numel()} decode tokens) + "
+                     f"paged_decode_attn_e4m3 ({splits} splits) = split kernel + lse_merge")
+
+    def kernel(self):
+        """The FP8 attention call (its split kernel and merge)."""
+        self.pkv.paged_decode_attn_e4m3(self.q, self.k, self.v, self.k_scale, self.v_scale,
+                                        self.bt, self.lens, self.w.scale,
+                                        num_splits=self.splits, workspace=self.ws, out=self.out,
+                                        lse=self.lse)
+
+    def attend(self, ev_a=None, ev_b=None):
+        if ev_a is not None:
+            ev_a.record()
+        self.kernel()
+        if ev_b is not None:
+            ev_b.record()
+
+    def run(self, ev_a=None, ev_b=None):
+        p = self.pkv
+        p.slot_mapping(self.k, self.v, self.bt, self.new_seq, self.new_pos, out=self.slots)
+        p.kv_append_e4m3(self.k, self.v, self.k_new, self.v_new, self.slots, self.k_scale,
+                         self.v_scale)
+        self.attend(ev_a, ev_b)
+
+
 STEPS = {"long32k": Step, "mix": Step, "tiny": Step, "dcp200k": DcpStep, "agent_mla": AgentStep,
-         "agent_mla_latent": AgentStep, "spec4_32k": MultiStep}
+         "agent_mla_latent": AgentStep, "spec4_32k": MultiStep, "long32k_e4m3": E4m3Step}
 DEFAULT_SPLITS = {"long32k": 16, "mix": 1, "tiny": 1, "dcp200k": 19, "agent_mla": 19,
-                  "agent_mla_latent": 19, "spec4_32k": 9}
+                  "agent_mla_latent": 19, "spec4_32k": 9, "long32k_e4m3": 7}
 
 
 # ------------------------------------------------------------------ arms
@@ -422,10 +477,13 @@ def oracle_gbs(w, tokens: int | None, repeats: int = 1):
     """Time the CPU oracle (all host cores) over every row of `w`, restricted
     to the first `tokens` tokens of each sequence when given."""
     import oracle
-    kp = bits_view(w.k_pool)
-    vp = (np.ascontiguousarray(kp[..., :w.head_dim_v]) if w.v_pool is None
-          else bits_view(w.v_pool))
     q, bt, lens = w.q.numpy(), w.block_tables.numpy(), w.seq_lens.numpy()
+    if w.k_codes is not None:
+        kp, vp = w.k_codes.numpy(), w.v_codes.numpy()
+    else:
+        kp = bits_view(w.k_pool)
+        vp = (np.ascontiguousarray(kp[..., :w.head_dim_v]) if w.v_pool is None
+              else bits_view(w.v_pool))
     end = None
     if tokens is not None:
         end = np.minimum(lens, tokens).astype(np.int32)
@@ -433,7 +491,10 @@ def oracle_gbs(w, tokens: int | None, repeats: int = 1):
     times = []
     for _ in range(repeats):
         t = time.perf_counter()
-        if w.tokens_per_seq > 1:
+        if w.k_codes is not None:
+            oracle.paged_decode_attn_e4m3(q, kp, vp, w.k_scale.numpy(), w.v_scale.numpy(), bt,
+                                          lens, w.scale, tok_end=end)
+        elif w.tokens_per_seq > 1:
             # the same step on each sequence's first tokens: query t sees the
             # sample's tokens up to its own
             oracle.paged_decode_attn_multi(q, kp, vp, bt, lens if end is None else end, w.scale)
@@ -445,7 +506,9 @@ def oracle_gbs(w, tokens: int | None, repeats: int = 1):
 
 def workload_desc(w, splits):
     kv = (f"head_dim {w.head_dim_k}, values = first {w.head_dim_v} dims of each key row, bf16"
-          if w.v_pool is None else f"head_dim {w.head_dim_k}, bf16 K/V")
+          if w.v_pool is None else
+          f"head_dim {w.head_dim_k}, E4M3 K/V with fp32 scales per KV head"
+          if w.k_codes is not None else f"head_dim {w.head_dim_k}, bf16 K/V")
     return (f"{w.name}: batch {w.batch} x {int(w.seq_lens.max())} tokens, GQA "
             f"{w.num_q_heads}/{w.num_kv_heads} heads, {kv}, block "
             f"{w.block_size}, {w.num_blocks}-block randomly permuted pool, {splits} splits + "

@@ -41,9 +41,8 @@ int validate_decode(const pkv_cache_desc *c, const float *q, int32_t batch, int3
 // split) items in turn, an item costing its 128-token tiles plus about one
 // tile of start-up.  Pick S for the least rounds x (tiles + 1) on sequences
 // of the longest length; a tie goes to fewer splits (less to merge).
-int32_t tc_splits(const pkv_cache_desc &c, int32_t batch, int32_t max_seq_len) {
+int32_t tc_splits(const pkv_cache_desc &c, int32_t batch, int32_t max_seq_len, int64_t ctas) {
     const int64_t units = std::max<int64_t>(1, int64_t(batch) * c.num_kv_heads);
-    const int64_t ctas = gqa_tc_resident_ctas();
     const int64_t L = std::max<int64_t>(1, max_seq_len);
     const int64_t s_max = std::min<int64_t>(kMaxSplits, (L + 127) / 128);
     int64_t best = 1, best_cost = INT64_MAX;
@@ -61,7 +60,8 @@ int32_t tc_splits(const pkv_cache_desc &c, int32_t batch, int32_t max_seq_len) {
 
 int32_t auto_splits(const pkv_cache_desc &c, int32_t batch, int32_t num_q_heads,
                     int32_t max_seq_len, int32_t q_tokens = 1) {
-    if (gqa_tc_kernel_supports(c, num_q_heads, q_tokens)) return tc_splits(c, batch, max_seq_len);
+    if (gqa_tc_kernel_supports(c, num_q_heads, q_tokens))
+        return tc_splits(c, batch, max_seq_len, gqa_tc_resident_ctas());
     // Enough (sequence, KV head [, head block], split) items for ~4 per SM
     // (8 for the tcgen05 kernel), each item at least 512 tokens long.
     int64_t units = int64_t(batch) * c.num_kv_heads;
@@ -149,7 +149,8 @@ extern "C" int pkv_paged_decode_attn_partial(const pkv_cache_desc *cache, const 
 extern "C" int32_t pkv_decode_auto_splits_e4m3(const pkv_cache_desc *cache, int32_t batch,
                                                int32_t num_q_heads, int32_t max_seq_len) {
     if (!cache || cache->num_kv_heads <= 0 || num_q_heads <= 0) return 1;
-    return tc_splits(*cache, batch, max_seq_len);
+    return tc_splits(*cache, batch, max_seq_len,
+                     gqa_tc_e4m3_resident_ctas(num_q_heads / cache->num_kv_heads));
 }
 
 extern "C" int pkv_paged_decode_attn_e4m3(const pkv_cache_desc *cache, const float *q,

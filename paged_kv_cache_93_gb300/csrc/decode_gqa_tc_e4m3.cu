@@ -25,8 +25,8 @@
 // end), warps 2-5 one thread per token lane for the query split, the
 // stale-max online softmax (the running max rises only past a slack of 8 in
 // log2 units; the accumulators are then rescaled in TMEM) and the
-// epilogue.  ~111 KB of shared memory: two CTAs per SM.  Every wait is
-// bounded.
+// epilogue.  Groups of 8 and 16 run two CTAs per SM (up to ~111 KB of
+// shared memory each), groups of 4 three.  Every wait is bounded.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -40,14 +40,22 @@
 #include "pkv_pipeline.cuh"
 #include "pkv_tcgen05.cuh"
 
+// Groups of 4: the smallest operand arrays, so three CTAs per SM with three
+// ring stages each (measured on 8 x 32K: 89.8 us against 96.5 us for two
+// CTAs with five stages).
+#ifndef PKV_E4M3_R4_RING
+#define PKV_E4M3_R4_RING 3
+#endif
+#ifndef PKV_E4M3_R4_CTAS
+#define PKV_E4M3_R4_CTAS 3
+#endif
+
 namespace pkv {
 namespace {
 
 constexpr int kM = 128;                 // tokens per tile
 constexpr int kD = 128;                 // head dim (bytes of an E4M3 row)
 constexpr int kStage = kM * kD;         // one K or V tile: 16 KB
-constexpr int kRing = 5;
-constexpr int kCtas = 2;                // CTAs per SM
 constexpr int kThreads = 192;
 constexpr int kSoftWarp0 = 2;
 constexpr int kSoftThreads = 128;
@@ -56,13 +64,23 @@ constexpr float kSlack = 8.f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-template <int R>
-struct Shape {
+// Rows R per item, ring stages, CTAs per SM.
+template <int R, int RING, int CTAS>
+struct Cfg {
+    static constexpr int kRing = RING;
+    static constexpr int kCtas = CTAS;
     static constexpr int kNQ = kQTerms * R;                         // score MMA N
     static constexpr int kNP = (kPTerms * R + 15) / 16 * 16;        // value MMA N
     static constexpr uint32_t kColO = 2 * kNQ;                      // S^T buffers first
     static constexpr uint32_t kTmemCols = 2 * kNQ + kNP <= 64 ? 64 : 2 * kNQ + kNP <= 128 ? 128 : 256;
     static constexpr uint32_t kPBytes = kNP * 128;                  // [NP rows][128 tokens]
+    // Shared memory after the 1024-byte misc block: the query terms
+    // [4R rows][128 B], two probability buffers [NP rows][128 B], the ring.
+    static constexpr uint32_t kOffP = 1024 + kNQ * 128;
+    static constexpr uint32_t kOffRing = kOffP + 2 * kPBytes;
+    static constexpr uint32_t kSmemBytes = 1024 + kOffRing + RING * kStage;
+    static_assert(kOffP % 1024 == 0 && kOffRing % 1024 == 0, "1024-byte-aligned operands");
+    static_assert(RING <= 8, "mbarrier slots for at most 8 stages");
 };
 
 // mbarrier slots
@@ -77,19 +95,15 @@ constexpr int kBarQEmpty = 25;
 constexpr int kBarOEmpty = 26;
 constexpr int kBarDrain = 27;
 
-// Shared memory, offsets from a 1024-byte-aligned base.  The operand arrays
-// are sized for R = 16.
+// Shared memory, offsets from a 1024-byte-aligned base (the operand arrays
+// follow in Cfg).
 constexpr uint32_t kOffMrow = 256;                      // running max per row (log2)
 constexpr uint32_t kOffAux = kOffMrow + 64;             // rescale factor, then 1/l
 constexpr uint32_t kOffQsc = kOffAux + 64;              // power-of-two scale s_h of row h
 constexpr uint32_t kOffRed = kOffQsc + 64;              // [4 warps][16 rows]
 constexpr uint32_t kOffSlot = kOffRed + 256;
 constexpr uint32_t kOffFlag = kOffSlot + 4;
-constexpr uint32_t kOffQ = 1024;                        // [4R rows][128 B]
-constexpr uint32_t kOffP = kOffQ + 8192;                // two [NP rows][128 B]
-constexpr uint32_t kOffRing = kOffP + 2 * 10240;
-constexpr uint32_t kSmemBytes = 1024 + kOffRing + kRing * kStage;
-static_assert(kOffRing % 1024 == 0, "operand arrays start on 1024-byte boundaries");
+constexpr uint32_t kOffQ = 1024;
 
 __device__ __forceinline__ int64_t lmin(int64_t x, int64_t y) { return x < y ? x : y; }
 
@@ -125,11 +139,13 @@ __device__ __forceinline__ Item fp8_item(const DecodeArgs &a, int item, bool rep
     return r;
 }
 
-template <int R>
-__global__ void __launch_bounds__(kThreads, kCtas)
+template <int R, int RING, int CTAS>
+__global__ void __launch_bounds__(kThreads, CTAS)
 decode_gqa_tc_e4m3_kernel(const __grid_constant__ CUtensorMap tmap_k,
                           const __grid_constant__ CUtensorMap tmap_v, const DecodeArgs a) {
-    using S = Shape<R>;
+    using S = Cfg<R, RING, CTAS>;
+    constexpr int kRing = RING;
+    constexpr uint32_t kOffP = S::kOffP, kOffRing = S::kOffRing;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -594,9 +610,10 @@ bool make_byte_map(CUtensorMap *map, const void *pool, int64_t rows, int box) {
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int R>
+template <int R, int RING, int CTAS>
 int launch_rows(const DecodeArgs &a) {
-    auto kernel = decode_gqa_tc_e4m3_kernel<R>;
+    using S = Cfg<R, RING, CTAS>;
+    auto kernel = decode_gqa_tc_e4m3_kernel<R, RING, CTAS>;
     const int64_t rows = int64_t(a.cache.num_blocks) * a.cache.num_kv_heads * a.cache.block_size;
     const int box = std::min(a.cache.block_size, kM);
     CUtensorMap tk, tv;
@@ -607,16 +624,16 @@ int launch_rows(const DecodeArgs &a) {
     cudaGetDevice(&dev);
     if (configured_dev != dev) {
         if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(kSmemBytes)) != cudaSuccess)
+                                 int(S::kSmemBytes)) != cudaSuccess)
             return PKV_ERR_CUDA;
         configured_dev = dev;
     }
     // kCtas CTAs per SM by construction (shared memory, registers and TMEM
     // columns are sized for it); the persistent loop is correct for any grid.
     const int64_t items = int64_t(a.batch) * a.cache.num_kv_heads * a.num_splits;
-    const int grid = int(std::min<int64_t>(items, int64_t(sm_count()) * kCtas));
+    const int grid = int(std::min<int64_t>(items, int64_t(sm_count()) * CTAS));
     if (grid <= 0) return PKV_OK;
-    return launch_pdl(kernel, dim3(grid), dim3(kThreads), kSmemBytes, a.stream, tk, tv, a);
+    return launch_pdl(kernel, dim3(grid), dim3(kThreads), S::kSmemBytes, a.stream, tk, tv, a);
 }
 
 }  // namespace
@@ -631,11 +648,15 @@ bool gqa_tc_e4m3_kernel_supports(const pkv_cache_desc &c, int32_t num_q_heads) {
            rows < (int64_t(1) << 31) - 1;
 }
 
+int gqa_tc_e4m3_resident_ctas(int32_t group) {
+    return sm_count() * (group == 4 ? PKV_E4M3_R4_CTAS : 2);
+}
+
 int launch_decode_gqa_tc_e4m3(const DecodeArgs &a) {
     switch (a.num_q_heads / a.cache.num_kv_heads) {
-        case 4: return launch_rows<4>(a);
-        case 8: return launch_rows<8>(a);
-        case 16: return launch_rows<16>(a);
+        case 4: return launch_rows<4, PKV_E4M3_R4_RING, PKV_E4M3_R4_CTAS>(a);
+        case 8: return launch_rows<8, 5, 2>(a);
+        case 16: return launch_rows<16, 5, 2>(a);
         default: return PKV_ERR_SHAPE;
     }
 }

@@ -77,6 +77,8 @@ int gqa_tc_resident_ctas();
 // E4M3 pools, query groups of 4, 8 or 16, head dims 128: the tcgen05 kernel
 // with E4M3 operands.
 bool gqa_tc_e4m3_kernel_supports(const pkv_cache_desc &c, int32_t num_q_heads);
+// CTAs that kernel keeps resident for a query group of `group` heads.
+int gqa_tc_e4m3_resident_ctas(int32_t group);
 int launch_decode_gqa_tc_e4m3(const DecodeArgs &a);
 int launch_decode_tma(const DecodeArgs &a);
 // Large query groups (G a multiple of 32, e.g. MLA-shaped 128 heads over one
