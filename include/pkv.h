@@ -289,14 +289,14 @@ int pkv_paged_decode_attn_noalloc(const pkv_cache_desc *cache, const float *q, i
  * pkv_paged_decode_attn_e4m3 -- pkv_paged_decode_attn over E4M3 pools (the
  * FP8 cache above): K_j = value(k code) * k_scale[g] and V_j = value(v code)
  * * v_scale[g]; q, out, lse, splits, workspace (pkv_decode_workspace_size)
- * and the status bits as pkv_paged_decode_attn.  Shapes: head_dim_k ==
- * head_dim_v == 128, query groups of 4, 8 or 16 heads per KV head,
- * power-of-two block sizes 16..256 (other shapes PKV_ERR_SHAPE); flags 0.
- * It runs on the tcgen05 tensor cores with E4M3 operands: the fp32 query is
- * carried as four E4M3 terms and the probabilities as five, each term the
+ * and the status bits as pkv_paged_decode_attn; shapes as there.  Head
+ * dims 128 with query groups of 4, 8 or 16 and power-of-two block sizes
+ * 16..256 run on the tcgen05 tensor cores with E4M3 operands: the fp32 query
+ * is carried as four E4M3 terms and the probabilities as five, each term the
  * rounding residual of the one before scaled by 16, so both keep about 16
  * significant bits and the result is fp32-accurate attention on the stored
- * values.
+ * values.  Other shapes, or flags PKV_DECODE_GENERIC / PKV_DECODE_NO_TCGEN05,
+ * run a CUDA-core kernel that decodes the codes exactly.
  * ------------------------------------------------------------------------- */
 /* The split count num_splits = 0 resolves to in pkv_paged_decode_attn_e4m3. */
 int32_t pkv_decode_auto_splits_e4m3(const pkv_cache_desc *cache, int32_t batch,

@@ -245,7 +245,7 @@ def paged_decode_attn(q, k_pool, v_pool, block_tables, seq_lens, scale: float,
 
 def paged_decode_attn_e4m3(q, k_pool, v_pool, k_scale, v_scale, block_tables, seq_lens,
                            scale: float, num_splits: int = 0, workspace=None, out=None,
-                           lse=None, stream=None):
+                           lse=None, flags: int = 0, stream=None):
     """Decode attention over an E4M3 cache (uint8 code pools, fp32 scales per
     KV head) -> (out, lse); num_splits 0 lets the library choose."""
     desc = _e4m3_desc(k_pool, v_pool, k_scale, v_scale)
@@ -266,7 +266,7 @@ def paged_decode_attn_e4m3(q, k_pool, v_pool, k_scale, v_scale, block_tables, se
     _check("pkv_paged_decode_attn_e4m3", lib.pkv_paged_decode_attn_e4m3(
         ctypes.byref(desc), _ptr(q), B, Hq, _ptr(k_pool), _ptr(v_pool), _ptr(k_scale),
         _ptr(v_scale), _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), float(scale),
-        S, _ptr(workspace), ws_bytes, _ptr(out), _ptr(lse), 0, _stream(stream)))
+        S, _ptr(workspace), ws_bytes, _ptr(out), _ptr(lse), int(flags), _stream(stream)))
     return out, lse
 
 

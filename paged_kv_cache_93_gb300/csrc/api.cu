@@ -149,6 +149,8 @@ extern "C" int pkv_paged_decode_attn_partial(const pkv_cache_desc *cache, const 
 extern "C" int32_t pkv_decode_auto_splits_e4m3(const pkv_cache_desc *cache, int32_t batch,
                                                int32_t num_q_heads, int32_t max_seq_len) {
     if (!cache || cache->num_kv_heads <= 0 || num_q_heads <= 0) return 1;
+    if (!gqa_tc_e4m3_kernel_supports(*cache, num_q_heads))
+        return auto_splits(*cache, batch, num_q_heads, max_seq_len);
     return tc_splits(*cache, batch, max_seq_len,
                      gqa_tc_e4m3_resident_ctas(num_q_heads / cache->num_kv_heads));
 }
@@ -161,13 +163,17 @@ extern "C" int pkv_paged_decode_attn_e4m3(const pkv_cache_desc *cache, const flo
                                           float scale, int32_t num_splits, void *workspace,
                                           size_t workspace_bytes, float *out, float *lse,
                                           int32_t flags, pkv_stream_t stream) {
-    if (flags != 0) return PKV_ERR_INVALID_ARG;
     int st = validate_decode(cache, q, batch, num_q_heads, k_pool, v_pool, block_tables,
-                             max_blocks, seq_lens, num_splits, 0);
+                             max_blocks, seq_lens, num_splits, flags);
     if (st != PKV_OK || batch == 0) return st;
     if (!v_pool || !k_scale || !v_scale || !out || !lse) return PKV_ERR_INVALID_ARG;
-    if (!gqa_tc_e4m3_kernel_supports(*cache, num_q_heads)) return PKV_ERR_SHAPE;
     if (!aligned16(out)) return PKV_ERR_ALIGNMENT;
+    // the tensor-core kernel where it takes the shape, the CUDA-core one
+    // otherwise (or when a flag asks for it)
+    const bool tc = flags == 0 && gqa_tc_e4m3_kernel_supports(*cache, num_q_heads);
+    auto launch = [&](const DecodeArgs &d) {
+        return tc ? launch_decode_gqa_tc_e4m3(d) : launch_decode_generic_e4m3(d);
+    };
     int32_t S = num_splits;
     if (S == 0)
         S = pkv_decode_auto_splits_e4m3(
@@ -184,12 +190,12 @@ extern "C" int pkv_paged_decode_attn_e4m3(const pkv_cache_desc *cache, const flo
     a.v_stride = cache->head_dim_v;
     a.k_scale = k_scale;
     a.v_scale = v_scale;
-    if (S == 1) return launch_decode_gqa_tc_e4m3(a);
+    if (S == 1) return launch(a);
     const size_t rows = size_t(S) * batch * num_q_heads;
     char *ws = static_cast<char *>(workspace);
     a.out_part = reinterpret_cast<float *>(ws);
     a.lse_part = reinterpret_cast<float *>(ws + align256(rows * cache->head_dim_v * sizeof(float)));
-    st = launch_decode_gqa_tc_e4m3(a);
+    st = launch(a);
     if (st != PKV_OK) return st;
     return launch_lse_merge(S, a.out_part, a.lse_part, int64_t(batch) * num_q_heads,
                             cache->head_dim_v, out, lse, s);

@@ -7,6 +7,9 @@
 // accumulator) runs in base 2 with the query pre-multiplied by scale*log2(e).
 // It handles any head dims (multiples of 8 up to 1024), any query group and
 // any block size; the TMA + tensor-core kernel covers the common GQA shapes.
+// With E4 set the pools hold E4M3 codes (8 bytes per 8 elements, decoded
+// exactly through fp16); the key scale folds into the query and the value
+// scale into the final 1/l.
 // The LSE merge kernel lives here too.
 #include <cuda_runtime.h>
 
@@ -36,8 +39,26 @@ __device__ __forceinline__ void unpack8(const uint4 &u, float (&f)[8]) {
     f[6] = bf16_lo_to_f32(u.w); f[7] = bf16_hi_to_f32(u.w);
 }
 
-// KC / VC: 16-byte vectors per lane for K and V (ceil(dim / 8 / 32)).
-template <int KC, int VC>
+// 8 E4M3 codes -> their values.
+__device__ __forceinline__ void unpack8_e4m3(const uint2 &u, float (&f)[8]) {
+    const float2 a = e4m3x2_to_f32(u.x & 0xffffu), b = e4m3x2_to_f32(u.x >> 16);
+    const float2 c = e4m3x2_to_f32(u.y & 0xffffu), d = e4m3x2_to_f32(u.y >> 16);
+    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+    f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
+}
+
+// Elements 8v .. 8v+7 of row `row` of a pool whose rows hold `n8` groups of 8.
+template <bool E4>
+__device__ __forceinline__ void load8(const void *pool, int64_t row, int n8, int v,
+                                      float (&f)[8]) {
+    if constexpr (E4)
+        unpack8_e4m3(static_cast<const uint2 *>(pool)[row * n8 + v], f);
+    else
+        unpack8(static_cast<const uint4 *>(pool)[row * n8 + v], f);
+}
+
+// KC / VC: 8-element groups per lane for K and V (ceil(dim / 8 / 32)).
+template <int KC, int VC, bool E4>
 __global__ void __launch_bounds__(kGenericWarps * 32)
 decode_generic_kernel(DecodeArgs a) {
     pdl_wait();
@@ -63,7 +84,7 @@ decode_generic_kernel(DecodeArgs a) {
 
     // q, pre-scaled so that scores come out in base-2 log units.
     float qv[KC][8];
-    const float qscale = a.scale * kLog2e;
+    const float qscale = a.scale * kLog2e * (E4 ? a.k_scale[g] : 1.f);
     const float *qrow = a.q + (int64_t(b) * a.num_q_heads + h) * c.head_dim_k;
 #pragma unroll
     for (int i = 0; i < KC; ++i) {
@@ -79,9 +100,7 @@ decode_generic_kernel(DecodeArgs a) {
     float m = -INFINITY, l = 0.f;
 
     const int32_t *table = a.block_tables + int64_t(b) * a.max_blocks;
-    const uint4 *kp = static_cast<const uint4 *>(a.k_pool);
-    const uint4 *vp = static_cast<const uint4 *>(a.v_pool);
-    const int vs = a.v_stride / 8;          // 16-byte vectors from one V row to the next
+    const int vs = a.v_stride / 8;          // 8-element groups from one V row to the next
     for (int64_t j = begin; j < end; ++j) {
         const int32_t phys = table[j / c.block_size];
         const bool ok = phys >= 0 && phys < c.num_blocks;
@@ -94,7 +113,7 @@ decode_generic_kernel(DecodeArgs a) {
             const int v = lane + 32 * i;
             if (v < nk && ok) {
                 float kf[8];
-                unpack8(kp[row * nk + v], kf);
+                load8<E4>(a.k_pool, row, nk, v, kf);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) part = fmaf(qv[i][e], kf[e], part);
             }
@@ -109,14 +128,14 @@ decode_generic_kernel(DecodeArgs a) {
         for (int i = 0; i < VC; ++i) {
             const int v = lane + 32 * i;
             float vf[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-            if (v < nv && ok) unpack8(vp[row * vs + v], vf);
+            if (v < nv && ok) load8<E4>(a.v_pool, row, vs, v, vf);
 #pragma unroll
             for (int e = 0; e < 8; ++e) acc[i][e] = fmaf(p, vf[e], acc[i][e] * corr);
         }
     }
 
     const int64_t orow = (int64_t(split) * a.batch + b) * a.num_q_heads + h;
-    const float inv = l > 0.f ? 1.f / l : 0.f;
+    const float inv = l > 0.f ? (E4 ? a.v_scale[g] : 1.f) / l : 0.f;
     float *o = a.out_part + orow * c.head_dim_v;
 #pragma unroll
     for (int i = 0; i < VC; ++i) {
@@ -190,23 +209,28 @@ __global__ void lse_merge_kernel(int32_t num_parts, const float *__restrict__ ou
     if (c == 0) lse[r] = M + logf(W);
 }
 
-template <int KC, int VC>
+template <int KC, int VC, bool E4>
 int launch_generic(const DecodeArgs &a) {
     dim3 grid(a.num_splits, (a.num_q_heads + kGenericWarps - 1) / kGenericWarps, a.batch);
-    return launch_pdl(decode_generic_kernel<KC, VC>, grid, dim3(kGenericWarps * 32), 0, a.stream,
-                      a);
+    return launch_pdl(decode_generic_kernel<KC, VC, E4>, grid, dim3(kGenericWarps * 32), 0,
+                      a.stream, a);
+}
+
+template <bool E4>
+int launch_generic_dims(const DecodeArgs &a) {
+    const int kc = (a.cache.head_dim_k / 8 + 31) / 32;
+    const int vc = (a.cache.head_dim_v / 8 + 31) / 32;
+    if (kc <= 1 && vc <= 1) return launch_generic<1, 1, E4>(a);
+    if (kc <= 2 && vc <= 2) return launch_generic<2, 2, E4>(a);
+    if (kc <= 3 && vc <= 2) return launch_generic<3, 2, E4>(a);
+    return launch_generic<4, 4, E4>(a);
 }
 
 }  // namespace
 
-int launch_decode_generic(const DecodeArgs &a) {
-    const int kc = (a.cache.head_dim_k / 8 + 31) / 32;
-    const int vc = (a.cache.head_dim_v / 8 + 31) / 32;
-    if (kc <= 1 && vc <= 1) return launch_generic<1, 1>(a);
-    if (kc <= 2 && vc <= 2) return launch_generic<2, 2>(a);
-    if (kc <= 3 && vc <= 2) return launch_generic<3, 2>(a);
-    return launch_generic<4, 4>(a);
-}
+int launch_decode_generic(const DecodeArgs &a) { return launch_generic_dims<false>(a); }
+
+int launch_decode_generic_e4m3(const DecodeArgs &a) { return launch_generic_dims<true>(a); }
 
 int launch_lse_merge(int32_t num_parts, const float *out_part, const float *lse_part,
                      int64_t rows, int32_t head_dim_v, float *out, float *lse,

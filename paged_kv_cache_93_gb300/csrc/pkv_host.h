@@ -92,6 +92,8 @@ bool mla_tc_kernel_supports(const pkv_cache_desc &c, int32_t num_q_heads);
 int32_t mla_tc_work_units(const pkv_cache_desc &c, int32_t batch, int32_t num_q_heads);
 int launch_decode_mla_tc(const DecodeArgs &a);
 int launch_decode_generic(const DecodeArgs &a);
+// The same over E4M3 pools (a.k_scale, a.v_scale set).
+int launch_decode_generic_e4m3(const DecodeArgs &a);
 int launch_lse_merge(int32_t num_parts, const float *out_part, const float *lse_part,
                      int64_t rows, int32_t head_dim_v, float *out, float *lse,
                      cudaStream_t stream);

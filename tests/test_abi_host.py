@@ -221,26 +221,25 @@ def test_block_manager_rejects_bad_order(pkv):
 
 
 def test_e4m3_host_rules(pkv):
-    """The E4M3 entry points refuse, before any device work: flags, missing
-    scales or value pool, shapes the E4M3 kernel does not take, misaligned
-    code pools, block copies whose rows are not whole 16-byte vectors."""
+    """The E4M3 entry points refuse, before any device work: undefined flags,
+    missing scales or value pool, bad shapes, misaligned code pools, block
+    copies whose rows are not whole 16-byte vectors."""
     lib = pkv.lib
     p = ctypes.c_void_p(0x1000)
     odd = ctypes.c_void_p(0x1004)
     ok = pkv.CacheDesc(16, 16, 2, 128, 128)
-    d64 = pkv.CacheDesc(16, 16, 2, 64, 64)
+    d12 = pkv.CacheDesc(16, 16, 2, 12, 12)
 
     def attn(desc, hq, k_scale=p, v_scale=p, v_pool=p, flags=0):
         return lib.pkv_paged_decode_attn_e4m3(ctypes.byref(desc), p, 1, hq, p, v_pool, k_scale,
                                               v_scale, p, 4, p, 1.0, 1, None, 0, p, p, flags,
                                               None)
-    assert attn(ok, 8, flags=1) == -1                  # no flags for this path
+    assert attn(ok, 8, flags=8) == -1                  # undefined flag bit
     assert attn(ok, 8, k_scale=None) == -1
     assert attn(ok, 8, v_scale=None) == -1
     assert attn(ok, 8, v_pool=None) == -1
-    assert attn(ok, 2) == -2                           # groups of 4, 8 or 16 only
-    assert attn(ok, 64) == -2
-    assert attn(d64, 8) == -2                          # head dims 128 only
+    assert attn(ok, 3) == -2                           # heads not a multiple of KV heads
+    assert attn(d12, 8) == -2                          # head dims multiples of 8
     assert lib.pkv_kv_append_e4m3(ctypes.byref(ok), p, p, p, p, None, p, p, 1, None) == -1
     assert lib.pkv_kv_append_e4m3(ctypes.byref(ok), odd, p, p, p, p, p, p, 1, None) == -3
     assert lib.pkv_copy_blocks_e4m3(ctypes.byref(ok), p, None, p, p, 1, None) == -1

@@ -25,14 +25,14 @@ def pkv():
     return m
 
 
-def gpu_e4m3_step(pkv, w, splits, dev="cuda"):
+def gpu_e4m3_step(pkv, w, splits, dev="cuda", flags=0):
     k, v = w.k_codes.to(dev), w.v_codes.to(dev)
     ks, vs = w.k_scale.to(dev), w.v_scale.to(dev)
     bt = w.block_tables.to(dev)
     slots = pkv.slot_mapping(k, v, bt, w.new_seq.to(dev), w.new_pos.to(dev))
     pkv.kv_append_e4m3(k, v, w.k_new.to(dev), w.v_new.to(dev), slots, ks, vs)
     out, lse = pkv.paged_decode_attn_e4m3(w.q.to(dev), k, v, ks, vs, bt, w.seq_lens.to(dev),
-                                          w.scale, num_splits=splits)
+                                          w.scale, num_splits=splits, flags=flags)
     torch.cuda.synchronize()
     return out.cpu().numpy(), lse.cpu().numpy(), k.cpu().numpy(), v.cpu().numpy()
 
@@ -74,6 +74,38 @@ def test_e4m3_step_matches_oracle(pkv, shape, splits):
     ro, rl, rk, rv = oracle_e4m3_step(w)
     assert np.array_equal(k, rk) and np.array_equal(v, rv), "pools after the append"
     assert_attention_close(out, lse, ro, rl, f"e4m3 {shape}/{splits}")
+    assert pkv.device_status() == 0
+
+
+# shapes the tensor-core kernel does not take: the CUDA-core kernel
+GENERIC_SHAPES = [
+    ([37, 5], 8, 2, 64, 64, 8),            # head dim 64, group 4
+    ([90, 1, 33], 6, 2, 64, 64, 16),       # group 3
+    ([70, 9], 16, 1, 576, 512, 64),        # MLA-shaped dims
+    ([40], 2, 2, 128, 128, 16),            # group 1
+]
+
+
+@pytest.mark.parametrize("shape", GENERIC_SHAPES,
+                         ids=lambda s: f"G{s[1]//s[2]}_Dk{s[3]}_Dv{s[4]}_bs{s[5]}")
+@pytest.mark.parametrize("splits", [1, 3])
+def test_e4m3_generic_shapes(pkv, shape, splits):
+    cached, hq, hkv, dk, dv, bs = shape
+    w = workloads.e4m3(workloads.custom(60 + dk + hq, cached, hq, hkv, dk, dv, bs))
+    out, lse, k, v = gpu_e4m3_step(pkv, w, splits)
+    ro, rl, rk, rv = oracle_e4m3_step(w)
+    assert np.array_equal(k, rk) and np.array_equal(v, rv)
+    assert_attention_close(out, lse, ro, rl, f"e4m3 generic {shape}/{splits}")
+    assert pkv.device_status() == 0
+
+
+@pytest.mark.parametrize("shape", SHAPES[:3], ids=lambda s: f"G{s[1]//s[2]}_bs{s[3]}")
+def test_e4m3_forced_generic_matches_oracle(pkv, shape):
+    cached, hq, hkv, bs = shape
+    w = workloads.e4m3(workloads.custom(80 + bs, cached, hq, hkv, 128, 128, bs))
+    out, lse, *_ = gpu_e4m3_step(pkv, w, 3, flags=pkv.DECODE_GENERIC)
+    ro, rl, *_ = oracle_e4m3_step(w)
+    assert_attention_close(out, lse, ro, rl, f"e4m3 forced generic {shape}")
     assert pkv.device_status() == 0
 
 
