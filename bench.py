@@ -323,6 +323,65 @@ class DcpStep(Step):
         p.lse_merge(self.pout, self.plse, out=self.out[0], lse=self.lse[0])
 
 
+class DcpE4m3Step(DcpStep):
+    """The DCP step over an FP8 (E4M3) cache: the 200K tokens are quantised
+    into their partitions by the E4M3 append, the partitions attended in one
+    pkv_paged_decode_attn_e4m3 call and merged."""
+    kernel_name = ("pkv_paged_decode_attn_e4m3 over the partitions (decode_gqa_tc_e4m3_kernel, "
+                   "groups of 8) + its split merge")
+
+    def __init__(self, pkv, w, dev, splits):
+        self.pkv, self.w, self.splits = pkv, w, splits
+        self.k, self.v = w.k_codes.to(dev), w.v_codes.to(dev)
+        self.k_scale, self.v_scale = w.k_scale.to(dev), w.v_scale.to(dev)
+        self.q = w.q.to(dev)
+        self.k_new, self.v_new = w.k_new.to(dev), w.v_new.to(dev)
+        N, P = int(w.seq_lens[0]), w.num_parts
+        self.ptab = w.part_tables.to(dev)
+        kt, vt = w.k_tokens.to(dev), w.v_tokens.to(dev)
+        pkv.kv_append_e4m3(self.k, self.v, kt[:N - 1], vt[:N - 1],
+                           pkv.interleave_slot_mapping(self.k, self.v, 0, N - 1, P,
+                                                       w.interleave, self.ptab),
+                           self.k_scale, self.v_scale)
+        del kt, vt
+        self.N, self.P = N, P
+        self.plen = torch.tensor([pkv.interleave_partition_len(N, P, w.interleave, r)
+                                  for r in range(P)], dtype=torch.int32, device=dev)
+        Hq, Dv = w.num_q_heads, w.head_dim_v
+        self.pq = self.q.expand(P, Hq, w.head_dim_k).contiguous()
+        self.pout = torch.empty(P, Hq, Dv, device=dev)
+        self.plse = torch.empty(P, Hq, device=dev)
+        self.out = torch.empty(1, Hq, Dv, device=dev)
+        self.lse = torch.empty(1, Hq, device=dev)
+        self.slots = torch.empty(1, dtype=torch.int64, device=dev)
+        self.ws = torch.zeros(max(1, pkv.decode_workspace_size(P, Hq, Dv, splits)),
+                              dtype=torch.uint8, device=dev)
+        self.launches = 2 + 2 + 1
+        self.desc = (f"interleave slot + kv_append_e4m3 (decode token) + "
+                     f"paged_decode_attn_e4m3 over the {P} partitions in one launch "
+                     f"({splits} splits each, + its merge) + lse_merge over the {P} "
+                     f"partition results")
+
+    def kernel(self):
+        self.pkv.paged_decode_attn_e4m3(self.pq, self.k, self.v, self.k_scale, self.v_scale,
+                                        self.ptab, self.plen, self.w.scale,
+                                        num_splits=self.splits, workspace=self.ws, out=self.pout,
+                                        lse=self.plse)
+
+    def run(self, ev_a=None, ev_b=None):
+        p, w = self.pkv, self.w
+        p.interleave_slot_mapping(self.k, self.v, self.N - 1, 1, self.P, w.interleave, self.ptab,
+                                  out=self.slots)
+        p.kv_append_e4m3(self.k, self.v, self.k_new, self.v_new, self.slots, self.k_scale,
+                         self.v_scale)
+        if ev_a is not None:
+            ev_a.record()
+        self.kernel()
+        if ev_b is not None:
+            ev_b.record()
+        p.lse_merge(self.pout, self.plse, out=self.out[0], lse=self.lse[0])
+
+
 class AgentStep(Step):
     """Shared-prefix MLA-shaped step: copy-on-write of each sequence's shared
     tail, append of the decode tokens, attention (the suffixes are appended
@@ -436,9 +495,11 @@ class E4m3Step(Step):
 
 
 STEPS = {"long32k": Step, "mix": Step, "tiny": Step, "dcp200k": DcpStep, "agent_mla": AgentStep,
-         "agent_mla_latent": AgentStep, "spec4_32k": MultiStep, "long32k_e4m3": E4m3Step}
+         "agent_mla_latent": AgentStep, "spec4_32k": MultiStep, "long32k_e4m3": E4m3Step,
+         "dcp200k_e4m3": DcpE4m3Step}
 DEFAULT_SPLITS = {"long32k": 16, "mix": 1, "tiny": 1, "dcp200k": 19, "agent_mla": 19,
-                  "agent_mla_latent": 19, "spec4_32k": 9, "long32k_e4m3": 7}
+                  "agent_mla_latent": 19, "spec4_32k": 9, "long32k_e4m3": 7,
+                  "dcp200k_e4m3": 14}
 
 
 # ------------------------------------------------------------------ arms

@@ -25,8 +25,8 @@
 // end), warps 2-5 one thread per token lane for the query split, the
 // stale-max online softmax (the running max rises only past a slack of 8 in
 // log2 units; the accumulators are then rescaled in TMEM) and the
-// epilogue.  Groups of 8 and 16 run two CTAs per SM (up to ~111 KB of
-// shared memory each), groups of 4 three.  Every wait is bounded.
+// epilogue.  Groups of 16 run two CTAs per SM (~111 KB of shared memory
+// each), groups of 4 and 8 three.  Every wait is bounded.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -40,14 +40,22 @@
 #include "pkv_pipeline.cuh"
 #include "pkv_tcgen05.cuh"
 
-// Groups of 4: the smallest operand arrays, so three CTAs per SM with three
+// Groups of 4 and 8: small operand arrays, so three CTAs per SM with three
 // ring stages each (measured on 8 x 32K: 89.8 us against 96.5 us for two
-// CTAs with five stages).
+// CTAs with five stages at groups of 4; 97.4 us against 102.5 us at groups
+// of 8, whose registers then go from 121 to 96 with a 24-byte spill).
+// Groups of 16 keep two CTAs with five stages.
 #ifndef PKV_E4M3_R4_RING
 #define PKV_E4M3_R4_RING 3
 #endif
 #ifndef PKV_E4M3_R4_CTAS
 #define PKV_E4M3_R4_CTAS 3
+#endif
+#ifndef PKV_E4M3_R8_RING
+#define PKV_E4M3_R8_RING 3
+#endif
+#ifndef PKV_E4M3_R8_CTAS
+#define PKV_E4M3_R8_CTAS 3
 #endif
 
 namespace pkv {
@@ -649,13 +657,13 @@ bool gqa_tc_e4m3_kernel_supports(const pkv_cache_desc &c, int32_t num_q_heads) {
 }
 
 int gqa_tc_e4m3_resident_ctas(int32_t group) {
-    return sm_count() * (group == 4 ? PKV_E4M3_R4_CTAS : 2);
+    return sm_count() * (group == 4 ? PKV_E4M3_R4_CTAS : group == 8 ? PKV_E4M3_R8_CTAS : 2);
 }
 
 int launch_decode_gqa_tc_e4m3(const DecodeArgs &a) {
     switch (a.num_q_heads / a.cache.num_kv_heads) {
         case 4: return launch_rows<4, PKV_E4M3_R4_RING, PKV_E4M3_R4_CTAS>(a);
-        case 8: return launch_rows<8, 5, 2>(a);
+        case 8: return launch_rows<8, PKV_E4M3_R8_RING, PKV_E4M3_R8_CTAS>(a);
         case 16: return launch_rows<16, 5, 2>(a);
         default: return PKV_ERR_SHAPE;
     }
