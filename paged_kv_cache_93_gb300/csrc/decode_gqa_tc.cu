@@ -44,6 +44,7 @@
 #include "pkv.h"
 #include "pkv_device.cuh"
 #include "pkv_host.h"
+#include "pkv_pipeline.cuh"
 #include "pkv_tcgen05.cuh"
 
 namespace pkv {
@@ -137,31 +138,6 @@ __device__ __forceinline__ int64_t row_offset(const DecodeArgs &a, int b, int g,
     return (int64_t(b) * a.q_tokens + t) * a.num_q_heads + int64_t(g) * Gr + h;
 }
 
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, uint32_t *status,
-                                         volatile int *abort_flag) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t start = global_timer_ns();
-    for (;;) {
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (global_timer_ns() - start > kWaitLimitNs) {
-            raise_status(status, PKV_DEV_TIMEOUT);
-            *abort_flag = 1;
-            return false;
-        }
-    }
-}
-
-__device__ __forceinline__ bool soft_bar_or(bool pred) {
-    uint32_t r;
-    asm volatile(
-        "{ .reg .pred p, q; setp.ne.u32 p, %1, 0; bar.red.or.pred q, 1, 128, p; "
-        "selp.u32 %0, 1, 0, q; }"
-        : "=r"(r) : "r"(uint32_t(pred)) : "memory");
-    return r != 0;
-}
-
 // Offset of bf16 element (row, col < 64) in a [rows][64] 128-byte-swizzled
 // array whose 8-row atoms are 1024-byte aligned.
 __device__ __forceinline__ uint32_t swz(int row, int col) {
@@ -228,7 +204,7 @@ decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
         uint32_t phase = 0, armed = 0, armed_parity = 0;
         bool ok = true;
         auto acquire = [&](uint32_t &dst) -> bool {
-            const bool w = wait_bar(bar(kBarEmpty + stage), phase ^ 1u, a.status, abort_flag);
+            const bool w = pipe_wait(bar(kBarEmpty + stage), phase ^ 1u, a.status, abort_flag);
             if (!__all_sync(0xffffffffu, w)) return false;
             if (lane == 0) mbar_arrive_expect_tx(bar(kBarFull + stage), kChunk);
             armed |= 1u << stage;
@@ -299,7 +275,7 @@ decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
         bool ok = true;
         const uint32_t qb = sb + kOffQ, pb = sb + kOffP;
         auto wait_all = [&](uint32_t b, uint32_t parity) {
-            return __all_sync(0xffffffffu, wait_bar(b, parity, a.status, abort_flag));
+            return __all_sync(0xffffffffu, pipe_wait(b, parity, a.status, abort_flag));
         };
         auto advance = [&]() {
             if (++stage == kRing) {
@@ -407,14 +383,14 @@ decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
         // j & 1) are done; waiting twice for one tile is harmless (the
         // buffer's next phase needs probabilities not yet written).
         auto wait_pv = [&](uint32_t j) {
-            return wait_bar(bar(kBarPvDone + (j & 1u)), (j >> 1) & 1u, a.status, abort_flag);
+            return pipe_wait(bar(kBarPvDone + (j & 1u)), (j >> 1) & 1u, a.status, abort_flag);
         };
         // The item's 16 query rows, pre-scaled, as bf16 hi (rows 0-15) and
         // lo (rows 16-31) of the score MMA's B operand, once the previous
         // item's score MMAs are done (completion `qphase` of QEmpty).
         auto stage_q = [&](const Item &q_item, uint32_t qphase) {
             const bool ok_q =
-                wait_bar(bar(kBarQEmpty), (qphase & 1u) ^ 1u, a.status, abort_flag);
+                pipe_wait(bar(kBarQEmpty), (qphase & 1u) ^ 1u, a.status, abort_flag);
             if (ok_q) {
                 for (int i = t; i < kRows * kD / 2; i += kSoftThreads) {
                     const int rr = i / (kD / 2), d = 2 * (i % (kD / 2));
@@ -475,12 +451,12 @@ decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
             const int64_t lim0 = r.len - (T - 1) - r.begin;
             const int64_t lim_min = lmin(lim0, span);
             const int gr_shift = __ffs(Gr) - 1;
-            if (soft_bar_or(!w)) break;
+            if (softmax_bar_or(!w)) break;
 
             bool ok = true;
             for (int i = 0; i < r.ntiles; ++i) {
                 const uint32_t buf = tcount & 1u;
-                w = wait_bar(bar(kBarSFull + buf), (tcount >> 1) & 1u, a.status, abort_flag);
+                w = pipe_wait(bar(kBarSFull + buf), (tcount >> 1) & 1u, a.status, abort_flag);
                 float x[kRows];
                 {
                     uint32_t hv[16], lv[16];
@@ -506,11 +482,11 @@ decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 bool need = false;
 #pragma unroll
                 for (int h = 0; h < kRows; ++h) need |= x[h] > mrow[h] + kSlack;
-                if (soft_bar_or(!w)) {
+                if (softmax_bar_or(!w)) {
                     ok = false;
                     break;
                 }
-                if (soft_bar_or(need)) {
+                if (softmax_bar_or(need)) {
 #pragma unroll
                     for (int h = 0; h < kRows; ++h) {
                         float m = x[h];
@@ -583,7 +559,7 @@ decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
             // the next item's score MMAs may start while this one finishes
             if (next >= 0) {
                 staged = true;
-                if (soft_bar_or(!stage_q(nx, ne + 1))) break;
+                if (softmax_bar_or(!stage_q(nx, ne + 1))) break;
             }
 
             // ---- epilogue: the item's last value MMAs are done
@@ -620,7 +596,7 @@ decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
             tc::fence_before_sync();
             mbar_arrive(bar(kBarOEmpty));
             ++ne;
-            if (soft_bar_or(!w)) break;
+            if (softmax_bar_or(!w)) break;
         }
     }
 

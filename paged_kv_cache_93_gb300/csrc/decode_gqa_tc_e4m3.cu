@@ -80,7 +80,8 @@ struct Cfg {
     static constexpr int kNQ = kQTerms * R;                         // score MMA N
     static constexpr int kNP = (kPTerms * R + 15) / 16 * 16;        // value MMA N
     static constexpr uint32_t kColO = 2 * kNQ;                      // S^T buffers first
-    static constexpr uint32_t kTmemCols = 2 * kNQ + kNP <= 64 ? 64 : 2 * kNQ + kNP <= 128 ? 128 : 256;
+    static constexpr uint32_t kTmemCols =
+        2 * kNQ + kNP <= 64 ? 64 : 2 * kNQ + kNP <= 128 ? 128 : 256;
     static constexpr uint32_t kPBytes = kNP * 128;                  // [NP rows][128 tokens]
     // Shared memory after the 1024-byte misc block: the query terms
     // [4R rows][128 B], two probability buffers [NP rows][128 B], the ring.
@@ -564,7 +565,8 @@ decode_gqa_tc_e4m3_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 uint32_t v[S::kNP];
 #pragma unroll
                 for (int c = 0; c < S::kNP / 16; ++c)
-                    tc::ld16(tl + S::kColO + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(v + 16 * c));
+                    tc::ld16(tl + S::kColO + 16 * c,
+                             *reinterpret_cast<uint32_t(*)[16]>(v + 16 * c));
                 tc::wait_ld();
 #pragma unroll
                 for (int h = 0; h < R; ++h) {          // fold the probability terms back

@@ -47,6 +47,7 @@
 #include "pkv.h"
 #include "pkv_device.cuh"
 #include "pkv_host.h"
+#include "pkv_pipeline.cuh"
 #include "pkv_tcgen05.cuh"
 
 namespace pkv {
@@ -140,34 +141,6 @@ __device__ __forceinline__ TcItem tc_item(const DecodeArgs &a, int item, int gro
     return r;
 }
 
-// Bounded wait that also gives up once any role has aborted.
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, uint32_t *status,
-                                         volatile int *abort_flag) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t start = global_timer_ns();
-    for (;;) {
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (global_timer_ns() - start > kWaitLimitNs) {
-            raise_status(status, PKV_DEV_TIMEOUT);
-            *abort_flag = 1;
-            return false;
-        }
-    }
-}
-
-// Named barrier over the softmax warps that also ORs a predicate: every
-// participant gets the same answer.
-__device__ __forceinline__ bool soft_bar_or(bool pred) {
-    uint32_t r;
-    asm volatile(
-        "{ .reg .pred p, q; setp.ne.u32 p, %1, 0; bar.red.or.pred q, 1, 128, p; "
-        "selp.u32 %0, 1, 0, q; }"
-        : "=r"(r) : "r"(uint32_t(pred)) : "memory");
-    return r != 0;
-}
-
 // Offset of bf16 element (row, col < 64) in a [rows][64] 128-byte-swizzled
 // array whose 8-row atoms are 1024-byte aligned.
 __device__ __forceinline__ uint32_t swz(int row, int col) {
@@ -236,7 +209,7 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
         bool ok = true;
         // Wait for a free stage and arm it for one chunk; false on abort.
         auto acquire = [&](uint32_t &dst) -> bool {
-            const bool w = wait_bar(bar(kBarEmpty + stage), phase ^ 1u, a.status, abort_flag);
+            const bool w = pipe_wait(bar(kBarEmpty + stage), phase ^ 1u, a.status, abort_flag);
             if (!__all_sync(0xffffffffu, w)) return false;
             if (lane == 0) mbar_arrive_expect_tx(bar(kBarFull + stage), kChunk);
             armed |= 1u << stage;
@@ -319,7 +292,7 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
         const uint32_t qh = sb + sm.q_hi, ql = sb + sm.q_lo;
         const uint32_t ph = sb + sm.p_hi, pl = sb + sm.p_lo;
         auto wait_all = [&](uint32_t b, uint32_t parity) {
-            return __all_sync(0xffffffffu, wait_bar(b, parity, a.status, abort_flag));
+            return __all_sync(0xffffffffu, pipe_wait(b, parity, a.status, abort_flag));
         };
         auto advance = [&]() {
             if (++stage == shp.ring) {
@@ -444,7 +417,7 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 continue;
             }
             // ---- the group's queries, pre-scaled by scale*log2(e), as bf16 hi + lo
-            bool w = wait_bar(bar(kBarQEmpty), (ne & 1u) ^ 1u, a.status, abort_flag);
+            bool w = pipe_wait(bar(kBarQEmpty), (ne & 1u) ^ 1u, a.status, abort_flag);
             if (w) {
                 const float *qsrc = a.q + (int64_t(r.b) * a.num_q_heads + head0) * Dk;
                 for (int i = t; i < kN * Dk / 2; i += kSoftThreads) {
@@ -464,7 +437,7 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
             float l_part[kN];
 #pragma unroll
             for (int h = 0; h < kN; ++h) l_part[h] = 0.f;
-            if (soft_bar_or(!w)) break;
+            if (softmax_bar_or(!w)) break;
 
             bool ok = true;
             for (int i = 0; i < r.ntiles; ++i) {
@@ -473,7 +446,7 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 // exceed its head's running max by more than the slack?)
                 const uint32_t buf = tcount & 1u;
                 const uint32_t ts = tl + kColS + 64 * buf;
-                w = wait_bar(bar(kBarSFull + buf), (tcount >> 1) & 1u, a.status, abort_flag);
+                w = pipe_wait(bar(kBarSFull + buf), (tcount >> 1) & 1u, a.status, abort_flag);
                 tc::fence_after_sync();
                 const bool valid = r.begin + int64_t(i) * kM + row < r.end;
                 bool need = false;
@@ -486,12 +459,12 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     for (int k = 0; k < 16; ++k)
                         need |= valid && __uint_as_float(v[k]) > mrow[16 * c + k] + kSlack;
                 }
-                if (soft_bar_or(!w)) {
+                if (softmax_bar_or(!w)) {
                     ok = false;
                     break;
                 }
                 bool pv_waited = false;
-                if (soft_bar_or(need)) {
+                if (softmax_bar_or(need)) {
                     // ---- raise the running max to this tile's max
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
@@ -524,7 +497,7 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         // the accumulators are quiet: tile i-1's value MMAs
                         // are done and tile i's wait for these probabilities
                         const bool wv =
-                            wait_bar(bar(kBarPvDone), pcount & 1u, a.status, abort_flag);
+                            pipe_wait(bar(kBarPvDone), pcount & 1u, a.status, abort_flag);
                         ++pcount;
                         pv_waited = true;
                         tc::fence_after_sync();
@@ -549,7 +522,7 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 }
                 if (i > 0 && !pv_waited) {
                     // tile i-1's value MMAs have finished reading the buffer
-                    wait_bar(bar(kBarPvDone), pcount & 1u, a.status, abort_flag);
+                    pipe_wait(bar(kBarPvDone), pcount & 1u, a.status, abort_flag);
                     ++pcount;
                 }
                 // ---- second pass: probabilities, split into bf16 hi + lo,
@@ -594,7 +567,7 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
             if (!ok) break;
 
             // ---- epilogue: the item's last value MMAs are complete
-            w = wait_bar(bar(kBarPvDone), pcount & 1u, a.status, abort_flag);
+            w = pipe_wait(bar(kBarPvDone), pcount & 1u, a.status, abort_flag);
             ++pcount;
             tc::fence_after_sync();
 #pragma unroll
@@ -632,7 +605,7 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
             tc::fence_before_sync();
             mbar_arrive(bar(kBarOEmpty));
             ++ne;
-            if (soft_bar_or(!w)) break;
+            if (softmax_bar_or(!w)) break;
         }
     }
 
