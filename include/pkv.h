@@ -347,6 +347,23 @@ int pkv_paged_decode_attn_multi(const pkv_cache_desc *cache, const float *q, int
                                 int32_t num_splits, void *workspace, size_t workspace_bytes,
                                 float *out, float *lse, int32_t flags, pkv_stream_t stream);
 
+/* pkv_paged_decode_attn_multi_e4m3 -- the multi-token step over E4M3 pools
+ * (the FP8 cache above): rows, causal lengths, q/out/lse layouts, the
+ * PKV_DEV_SEQ_LEN rule and the workspace (pkv_decode_multi_workspace_size)
+ * as pkv_paged_decode_attn_multi; K_j, V_j, k_scale, v_scale, kernels and
+ * flags as pkv_paged_decode_attn_e4m3.  Every (sequence, token) is attended
+ * as its own row over a per-token view of its table row (the T rows of a
+ * sequence run side by side and read the same tiles).  num_splits = 0 takes
+ * pkv_decode_auto_splits_e4m3 for batch * T rows. */
+int pkv_paged_decode_attn_multi_e4m3(const pkv_cache_desc *cache, const float *q,
+                                     int32_t batch, int32_t tokens_per_seq, int32_t num_q_heads,
+                                     const void *k_pool, const void *v_pool,
+                                     const float *k_scale, const float *v_scale,
+                                     const int32_t *block_tables, int32_t max_blocks,
+                                     const int32_t *seq_lens, float scale, int32_t num_splits,
+                                     void *workspace, size_t workspace_bytes, float *out,
+                                     float *lse, int32_t flags, pkv_stream_t stream);
+
 /* ---------------------------------------------------------------------------
  * pkv_lse_merge -- [DCP] decode step, stage 3: correct each partial output
  * with the shared LSEs and sum.  For each row r:

@@ -27,7 +27,7 @@ __all__ = [
     "interleave_slot_mapping", "interleave_partition_len", "decode_workspace_size",
     "decode_auto_splits", "paged_decode_attn", "paged_decode_attn_partial",
     "paged_decode_attn_multi", "lse_merge", "kv_append_e4m3", "copy_blocks_e4m3",
-    "paged_decode_attn_e4m3",
+    "paged_decode_attn_e4m3", "paged_decode_attn_multi_e4m3",
     "device_status", "BlockManager", "library_path", "DECODE_GENERIC", "DECODE_NO_TCGEN05",
     "DEV_BLOCK_ID",
     "DEV_SLOT", "DEV_SEQ_LEN", "DEV_COPY_CONFLICT", "DEV_TIMEOUT", "DEV_TABLE_RANGE",
@@ -267,6 +267,34 @@ def paged_decode_attn_e4m3(q, k_pool, v_pool, k_scale, v_scale, block_tables, se
         ctypes.byref(desc), _ptr(q), B, Hq, _ptr(k_pool), _ptr(v_pool), _ptr(k_scale),
         _ptr(v_scale), _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), float(scale),
         S, _ptr(workspace), ws_bytes, _ptr(out), _ptr(lse), int(flags), _stream(stream)))
+    return out, lse
+
+
+def paged_decode_attn_multi_e4m3(q, k_pool, v_pool, k_scale, v_scale, block_tables, seq_lens,
+                                 scale: float, num_splits: int = 0, workspace=None, out=None,
+                                 lse=None, flags: int = 0, stream=None):
+    """The multi-token step (q [B, T, Hq, Dk], causal over the last T tokens) over
+    an E4M3 cache -> (out [B, T, Hq, Dv], lse [B, T, Hq])."""
+    desc = _e4m3_desc(k_pool, v_pool, k_scale, v_scale)
+    _need(q, "q", torch.float32, 4)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    B, T, Hq, _ = q.shape
+    if out is None:
+        out = torch.empty(B, T, Hq, desc.head_dim_v, dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty(B, T, Hq, dtype=torch.float32, device=q.device)
+    S = num_splits or int(lib.pkv_decode_auto_splits_e4m3(
+        ctypes.byref(desc), B * T, Hq, block_tables.shape[1] * desc.block_size))
+    need = int(lib.pkv_decode_multi_workspace_size(B, T, Hq, desc.head_dim_v,
+                                                   block_tables.shape[1], S))
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    _check("pkv_paged_decode_attn_multi_e4m3", lib.pkv_paged_decode_attn_multi_e4m3(
+        ctypes.byref(desc), _ptr(q), B, T, Hq, _ptr(k_pool), _ptr(v_pool), _ptr(k_scale),
+        _ptr(v_scale), _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), float(scale),
+        S, _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out), _ptr(lse),
+        int(flags), _stream(stream)))
     return out, lse
 
 

@@ -66,6 +66,9 @@ SIGNATURES = {
     "pkv_paged_decode_attn_multi": (ctypes.c_int, [_DESC, _P, _i32, _i32, _i32, _P, _P, _P,
                                                    _i32, _P, _f32, _i32, _P, _sz, _P, _P, _i32,
                                                    _P]),
+    "pkv_paged_decode_attn_multi_e4m3": (ctypes.c_int, [_DESC, _P, _i32, _i32, _i32, _P, _P,
+                                                        _P, _P, _P, _i32, _P, _f32, _i32, _P,
+                                                        _sz, _P, _P, _i32, _P]),
     "pkv_lse_merge": (ctypes.c_int, [_i32, _P, _P, _i64, _i32, _P, _P, _P]),
     "pkv_bm_create": (_P, [_i32, _i32, _P]),
     "pkv_bm_destroy": (None, [_P]),

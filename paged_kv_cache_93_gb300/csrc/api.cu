@@ -397,3 +397,61 @@ extern "C" int pkv_paged_decode_attn_multi(const pkv_cache_desc *cache, const fl
     return launch_lse_merge(S, out_part, lse_part, int64_t(rows) * num_q_heads,
                             cache->head_dim_v, out, lse, s);
 }
+
+extern "C" int pkv_paged_decode_attn_multi_e4m3(
+    const pkv_cache_desc *cache, const float *q, int32_t batch, int32_t tokens_per_seq,
+    int32_t num_q_heads, const void *k_pool, const void *v_pool, const float *k_scale,
+    const float *v_scale, const int32_t *block_tables, int32_t max_blocks,
+    const int32_t *seq_lens, float scale, int32_t num_splits, void *workspace,
+    size_t workspace_bytes, float *out, float *lse, int32_t flags, pkv_stream_t stream) {
+    if (tokens_per_seq < 1 || tokens_per_seq > kMaxQueryTokens) return PKV_ERR_INVALID_ARG;
+    if (batch > 0 && int64_t(batch) * tokens_per_seq > 65535) return PKV_ERR_SHAPE;
+    const int32_t rows = batch * tokens_per_seq;
+    int st = validate_decode(cache, q, rows, num_q_heads, k_pool, v_pool, block_tables,
+                             max_blocks, seq_lens, num_splits, flags);
+    if (st != PKV_OK || batch == 0) return st;
+    if (!v_pool || !k_scale || !v_scale || !out || !lse) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(out)) return PKV_ERR_ALIGNMENT;
+    int32_t S = num_splits;
+    if (S == 0)
+        S = pkv_decode_auto_splits_e4m3(
+            cache, rows, num_q_heads,
+            int32_t(std::min<int64_t>(int64_t(max_blocks) * cache->block_size, INT32_MAX)));
+    const MultiLayout m = multi_layout(batch, tokens_per_seq, num_q_heads, cache->head_dim_v,
+                                       max_blocks, S);
+    if (!workspace || workspace_bytes < m.total) return PKV_ERR_WORKSPACE_TOO_SMALL;
+    if (!aligned16(workspace)) return PKV_ERR_ALIGNMENT;
+    uint32_t *status = status_word();
+    if (!status) return PKV_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    char *ws = static_cast<char *>(workspace);
+    // one row per (sequence, token): T views of each table row, causal lengths
+    int32_t *row_tables = reinterpret_cast<int32_t *>(ws + m.tables);
+    int32_t *row_lens = reinterpret_cast<int32_t *>(ws + m.lens);
+    const int64_t work = int64_t(rows) * (int64_t(max_blocks) + 1);
+    const int threads = 256;
+    st = launch_pdl(multi_rows_kernel,
+                    dim3(unsigned(std::min<int64_t>((work + threads - 1) / threads,
+                                                    int64_t(sm_count()) * 8))),
+                    dim3(threads), 0, s, block_tables, seq_lens, batch, tokens_per_seq,
+                    max_blocks, row_tables, row_lens);
+    if (st != PKV_OK) return st;
+    const bool tc = flags == 0 && gqa_tc_e4m3_kernel_supports(*cache, num_q_heads);
+    DecodeArgs a{*cache, q, rows, num_q_heads, k_pool, v_pool, row_tables, max_blocks,
+                 row_lens, scale, S, out, lse, status, s};
+    a.v_stride = cache->head_dim_v;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    auto launch = [&](const DecodeArgs &d) {
+        return tc ? launch_decode_gqa_tc_e4m3(d) : launch_decode_generic_e4m3(d);
+    };
+    if (S == 1) return launch(a);
+    const size_t prow = size_t(S) * rows * num_q_heads;
+    a.out_part = reinterpret_cast<float *>(ws + m.partials);
+    a.lse_part = reinterpret_cast<float *>(ws + m.partials +
+                                           align256(prow * cache->head_dim_v * sizeof(float)));
+    st = launch(a);
+    if (st != PKV_OK) return st;
+    return launch_lse_merge(S, a.out_part, a.lse_part, int64_t(rows) * num_q_heads,
+                            cache->head_dim_v, out, lse, s);
+}

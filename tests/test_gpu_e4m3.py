@@ -245,3 +245,90 @@ def test_e4m3_quantisation_error_is_reported(pkv):
     rel = ((o8 - ob).norm(dim=-1) / ob.norm(dim=-1)).max().item()
     print(f"E4M3 vs bf16 cache: max row rel-L2 {rel:.4f}")
     assert rel < 0.1
+
+
+# ---------------------------------------------------------------- multi-token
+
+def multi_e4m3_case(seed, cached, T, hq, hkv, dk, dv, bs):
+    from tests.test_gpu_multi import multi_case
+    return workloads.e4m3(multi_case(seed, cached, T, hq, hkv, dk, dv, bs))
+
+
+def gpu_multi_e4m3(pkv, w, splits, flags=0, dev="cuda"):
+    k, v = w.k_codes.to(dev), w.v_codes.to(dev)
+    ks, vs = w.k_scale.to(dev), w.v_scale.to(dev)
+    bt = w.block_tables.to(dev)
+    slots = pkv.slot_mapping(k, v, bt, w.new_seq.to(dev), w.new_pos.to(dev))
+    pkv.kv_append_e4m3(k, v, w.k_new.to(dev), w.v_new.to(dev), slots, ks, vs)
+    out, lse = pkv.paged_decode_attn_multi_e4m3(w.q.to(dev), k, v, ks, vs, bt,
+                                                w.seq_lens.to(dev), w.scale, num_splits=splits,
+                                                flags=flags)
+    torch.cuda.synchronize()
+    return out.cpu().numpy(), lse.cpu().numpy()
+
+
+def oracle_multi_e4m3(w):
+    """Each (sequence, token) as its own row over the sequence's table, token t
+    of T seeing the first seq_lens[b] - T + 1 + t tokens (none if that is not
+    positive)."""
+    k, v = oracle_e4m3_cache(w)
+    B, T = w.q.shape[0], w.q.shape[1]
+    L = w.seq_lens.numpy().astype(np.int64)
+    q = w.q.numpy().reshape(B * T, *w.q.shape[2:])
+    tables = np.repeat(w.block_tables.numpy(), T, axis=0)
+    lens = np.array([max(0, L[b] - T + 1 + t) for b in range(B) for t in range(T)],
+                    dtype=np.int32)
+    out, lse = oracle.paged_decode_attn_e4m3(q, k, v, w.k_scale.numpy(), w.v_scale.numpy(),
+                                             tables, lens, w.scale)
+    return out.reshape(B, T, *out.shape[1:]), lse.reshape(B, T, -1)
+
+
+# (cached, T, Hq, Hkv, Dk, Dv, block size): the tensor-core kernel's groups of
+# 4, 8 and 16, and shapes only the CUDA-core kernel takes
+MULTI_SHAPES = [
+    ([300, 7, 64], 4, 32, 8, 128, 128, 16),
+    ([129, 40], 2, 16, 2, 128, 128, 32),
+    ([200, 3], 3, 16, 1, 128, 128, 64),
+    ([77, 5], 2, 8, 4, 64, 64, 8),
+    ([60, 9], 2, 16, 1, 576, 512, 64),
+]
+
+
+@pytest.mark.parametrize("shape", MULTI_SHAPES,
+                         ids=lambda s: f"T{s[1]}_G{s[2]//s[3]}_Dk{s[4]}_bs{s[6]}")
+@pytest.mark.parametrize("splits", [1, 3, 0])
+def test_e4m3_multi_token_matches_oracle(pkv, shape, splits):
+    cached, T, hq, hkv, dk, dv, bs = shape
+    w = multi_e4m3_case(700 + T + dk + hq, cached, T, hq, hkv, dk, dv, bs)
+    out, lse = gpu_multi_e4m3(pkv, w, splits)
+    ro, rl = oracle_multi_e4m3(w)
+    assert_attention_close(out, lse, ro, rl, f"e4m3 multi {shape}/{splits}")
+    assert pkv.device_status() == 0
+
+
+def test_e4m3_multi_token_forced_generic_and_causality(pkv):
+    """The CUDA-core kernel on a tensor-core shape gives the oracle's rows too;
+    and token t of a sequence differs from token t+1 only through the one
+    more token it may not see."""
+    w = multi_e4m3_case(5, [150, 20], 4, 32, 8, 128, 128, 16)
+    out_g, lse_g = gpu_multi_e4m3(pkv, w, 2, flags=pkv.DECODE_GENERIC)
+    ro, rl = oracle_multi_e4m3(w)
+    assert_attention_close(out_g, lse_g, ro, rl, "forced generic")
+    # the oracle's own rows differ between tokens (the causal limit matters)
+    assert not np.allclose(rl[:, 0], rl[:, 3])
+    assert pkv.device_status() == 0
+
+
+@pytest.mark.parametrize("splits", [1, 2])
+def test_e4m3_multi_token_short_sequence_is_flagged(pkv, splits):
+    """A sequence holding fewer tokens than T: its rows with no token give
+    out 0 and lse -inf, the device flags the length."""
+    w = multi_e4m3_case(9, [20, 0], 3, 16, 2, 128, 128, 16)
+    w.seq_lens = torch.tensor([23, 1], dtype=torch.int32)
+    pkv.device_status(reset=True)
+    out, lse = gpu_multi_e4m3(pkv, w, splits)
+    assert np.isneginf(lse[1, :2]).all() and (out[1, :2] == 0).all()
+    assert np.isfinite(lse[1, 2]).all() and np.isfinite(lse[0]).all()
+    ro, rl = oracle_multi_e4m3(w)
+    assert_attention_close(out, lse, ro, rl, "short")
+    assert pkv.device_status(reset=True) & pkv.DEV_SEQ_LEN
