@@ -226,16 +226,35 @@ decode_mla_kernel(const __grid_constant__ CUtensorMap tmap_k,
 
         // ---- load the block's queries: pre-scaled, split hi/lo, swizzled
         {
-            const float *qsrc = a.q + (int64_t(r.b) * a.num_q_heads + head0) * Dk;
-            for (int i = tid; i < kHB * Dk / 2; i += kWarps * 32) {
-                const int h = (2 * i) / Dk, d = (2 * i) % Dk;
-                const float2 x = *reinterpret_cast<const float2 *>(qsrc + int64_t(h) * Dk + d);
-                const float x0 = x.x * qscale, x1 = x.y * qscale;
-                const float h0 = __uint_as_float(f32_to_bf16_bits(x0) << 16);
-                const float h1 = __uint_as_float(f32_to_bf16_bits(x1) << 16);
-                const uint32_t off = seg_addr(h, d >> 3) + (d & 7) * 2;
-                *reinterpret_cast<uint32_t *>(q_hi + off) = pack_bf16x2(h0, h1);
-                *reinterpret_cast<uint32_t *>(q_lo + off) = pack_bf16x2(x0 - h0, x1 - h1);
+            // 16-byte loads, eight in flight per thread before any is used
+            const float4 *qsrc =
+                reinterpret_cast<const float4 *>(a.q + (int64_t(r.b) * a.num_q_heads + head0) * Dk);
+            const int n4 = kHB * Dk / 4, nt = kWarps * 32;
+            for (int i0 = 0; i0 < n4; i0 += 8 * nt) {
+                float4 x[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int i = i0 + u * nt + tid;
+                    x[u] = i < n4 ? __ldg(qsrc + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int i = i0 + u * nt + tid;
+                    if (i >= n4) continue;
+                    const int h = (4 * i) / Dk, d = (4 * i) % Dk;
+                    const float x0 = x[u].x * qscale, x1 = x[u].y * qscale;
+                    const float x2 = x[u].z * qscale, x3 = x[u].w * qscale;
+                    const float h0 = __uint_as_float(f32_to_bf16_bits(x0) << 16);
+                    const float h1 = __uint_as_float(f32_to_bf16_bits(x1) << 16);
+                    const float h2 = __uint_as_float(f32_to_bf16_bits(x2) << 16);
+                    const float h3 = __uint_as_float(f32_to_bf16_bits(x3) << 16);
+                    // four consecutive dims share one 16-byte chunk
+                    const uint32_t off = seg_addr(h, d >> 3) + (d & 7) * 2;
+                    *reinterpret_cast<uint2 *>(q_hi + off) =
+                        make_uint2(pack_bf16x2(h0, h1), pack_bf16x2(h2, h3));
+                    *reinterpret_cast<uint2 *>(q_lo + off) =
+                        make_uint2(pack_bf16x2(x0 - h0, x1 - h1), pack_bf16x2(x2 - h2, x3 - h3));
+                }
             }
         }
         float acc[2][8][4];
