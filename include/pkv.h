@@ -350,11 +350,17 @@ int pkv_paged_decode_attn_multi(const pkv_cache_desc *cache, const float *q, int
 /* pkv_paged_decode_attn_multi_e4m3 -- the multi-token step over E4M3 pools
  * (the FP8 cache above): rows, causal lengths, q/out/lse layouts, the
  * PKV_DEV_SEQ_LEN rule and the workspace (pkv_decode_multi_workspace_size)
- * as pkv_paged_decode_attn_multi; K_j, V_j, k_scale, v_scale, kernels and
- * flags as pkv_paged_decode_attn_e4m3.  Every (sequence, token) is attended
- * as its own row over a per-token view of its table row (the T rows of a
- * sequence run side by side and read the same tiles).  num_splits = 0 takes
- * pkv_decode_auto_splits_e4m3 for batch * T rows. */
+ * as pkv_paged_decode_attn_multi; K_j, V_j, k_scale, v_scale and flags as
+ * pkv_paged_decode_attn_e4m3.  With flags 0, head dims 128, power-of-two
+ * block sizes 16..256 and G * T in {4, 8, 16} (G = num_q_heads /
+ * num_kv_heads), the tcgen05 E4M3 kernel takes the T tokens as rows of one
+ * work item (causal limits per row) and each tile is read once; otherwise
+ * every (sequence, token) is attended as its own row over a per-token view
+ * of its table row.  num_splits = 0: pkv_decode_multi_auto_splits_e4m3. */
+int32_t pkv_decode_multi_auto_splits_e4m3(const pkv_cache_desc *cache, int32_t batch,
+                                          int32_t tokens_per_seq, int32_t num_q_heads,
+                                          int32_t max_seq_len);
+
 int pkv_paged_decode_attn_multi_e4m3(const pkv_cache_desc *cache, const float *q,
                                      int32_t batch, int32_t tokens_per_seq, int32_t num_q_heads,
                                      const void *k_pool, const void *v_pool,

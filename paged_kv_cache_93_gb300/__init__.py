@@ -284,8 +284,8 @@ def paged_decode_attn_multi_e4m3(q, k_pool, v_pool, k_scale, v_scale, block_tabl
         out = torch.empty(B, T, Hq, desc.head_dim_v, dtype=torch.float32, device=q.device)
     if lse is None:
         lse = torch.empty(B, T, Hq, dtype=torch.float32, device=q.device)
-    S = num_splits or int(lib.pkv_decode_auto_splits_e4m3(
-        ctypes.byref(desc), B * T, Hq, block_tables.shape[1] * desc.block_size))
+    S = num_splits or int(lib.pkv_decode_multi_auto_splits_e4m3(
+        ctypes.byref(desc), B, T, Hq, block_tables.shape[1] * desc.block_size))
     need = int(lib.pkv_decode_multi_workspace_size(B, T, Hq, desc.head_dim_v,
                                                    block_tables.shape[1], S))
     if workspace is None or workspace.numel() * workspace.element_size() < need:

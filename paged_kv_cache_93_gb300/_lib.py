@@ -66,6 +66,7 @@ SIGNATURES = {
     "pkv_paged_decode_attn_multi": (ctypes.c_int, [_DESC, _P, _i32, _i32, _i32, _P, _P, _P,
                                                    _i32, _P, _f32, _i32, _P, _sz, _P, _P, _i32,
                                                    _P]),
+    "pkv_decode_multi_auto_splits_e4m3": (_i32, [_DESC, _i32, _i32, _i32, _i32]),
     "pkv_paged_decode_attn_multi_e4m3": (ctypes.c_int, [_DESC, _P, _i32, _i32, _i32, _P, _P,
                                                         _P, _P, _P, _i32, _P, _f32, _i32, _P,
                                                         _sz, _P, _P, _i32, _P]),

@@ -398,6 +398,17 @@ extern "C" int pkv_paged_decode_attn_multi(const pkv_cache_desc *cache, const fl
                             cache->head_dim_v, out, lse, s);
 }
 
+extern "C" int32_t pkv_decode_multi_auto_splits_e4m3(const pkv_cache_desc *cache,
+                                                     int32_t batch, int32_t tokens_per_seq,
+                                                     int32_t num_q_heads, int32_t max_seq_len) {
+    if (!cache || cache->num_kv_heads <= 0 || num_q_heads <= 0 || tokens_per_seq <= 0) return 1;
+    if (gqa_tc_e4m3_kernel_supports(*cache, num_q_heads, tokens_per_seq))
+        return tc_splits(*cache, batch, max_seq_len,
+                         gqa_tc_e4m3_resident_ctas(num_q_heads / cache->num_kv_heads *
+                                                   tokens_per_seq));
+    return pkv_decode_auto_splits_e4m3(cache, batch * tokens_per_seq, num_q_heads, max_seq_len);
+}
+
 extern "C" int pkv_paged_decode_attn_multi_e4m3(
     const pkv_cache_desc *cache, const float *q, int32_t batch, int32_t tokens_per_seq,
     int32_t num_q_heads, const void *k_pool, const void *v_pool, const float *k_scale,
@@ -414,8 +425,8 @@ extern "C" int pkv_paged_decode_attn_multi_e4m3(
     if (!aligned16(out)) return PKV_ERR_ALIGNMENT;
     int32_t S = num_splits;
     if (S == 0)
-        S = pkv_decode_auto_splits_e4m3(
-            cache, rows, num_q_heads,
+        S = pkv_decode_multi_auto_splits_e4m3(
+            cache, batch, tokens_per_seq, num_q_heads,
             int32_t(std::min<int64_t>(int64_t(max_blocks) * cache->block_size, INT32_MAX)));
     const MultiLayout m = multi_layout(batch, tokens_per_seq, num_q_heads, cache->head_dim_v,
                                        max_blocks, S);
@@ -425,7 +436,26 @@ extern "C" int pkv_paged_decode_attn_multi_e4m3(
     if (!status) return PKV_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     char *ws = static_cast<char *>(workspace);
-    // one row per (sequence, token): T views of each table row, causal lengths
+    const size_t prow = size_t(S) * rows * num_q_heads;
+    if (flags == 0 && gqa_tc_e4m3_kernel_supports(*cache, num_q_heads, tokens_per_seq)) {
+        // The tensor-core kernel takes the T query tokens as rows of one work
+        // item (causal limits per row): every tile is read once.
+        DecodeArgs a{*cache, q, batch, num_q_heads, k_pool, v_pool, block_tables, max_blocks,
+                     seq_lens, scale, S, out, lse, status, s};
+        a.v_stride = cache->head_dim_v;
+        a.k_scale = k_scale;
+        a.v_scale = v_scale;
+        a.q_tokens = tokens_per_seq;
+        if (S == 1) return launch_decode_gqa_tc_e4m3(a);
+        a.out_part = reinterpret_cast<float *>(ws + m.partials);
+        a.lse_part = reinterpret_cast<float *>(ws + m.partials +
+                                               align256(prow * cache->head_dim_v * sizeof(float)));
+        st = launch_decode_gqa_tc_e4m3(a);
+        if (st != PKV_OK) return st;
+        return launch_lse_merge(S, a.out_part, a.lse_part, int64_t(rows) * num_q_heads,
+                                cache->head_dim_v, out, lse, s);
+    }
+    // otherwise one row per (sequence, token): T views of each table row
     int32_t *row_tables = reinterpret_cast<int32_t *>(ws + m.tables);
     int32_t *row_lens = reinterpret_cast<int32_t *>(ws + m.lens);
     const int64_t work = int64_t(rows) * (int64_t(max_blocks) + 1);
@@ -446,7 +476,6 @@ extern "C" int pkv_paged_decode_attn_multi_e4m3(
         return tc ? launch_decode_gqa_tc_e4m3(d) : launch_decode_generic_e4m3(d);
     };
     if (S == 1) return launch(a);
-    const size_t prow = size_t(S) * rows * num_q_heads;
     a.out_part = reinterpret_cast<float *>(ws + m.partials);
     a.lse_part = reinterpret_cast<float *>(ws + m.partials +
                                            align256(prow * cache->head_dim_v * sizeof(float)));

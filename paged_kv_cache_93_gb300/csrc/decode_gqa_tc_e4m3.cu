@@ -139,6 +139,8 @@ __device__ __forceinline__ Item fp8_item(const DecodeArgs &a, int item, bool rep
     if (L < 0 || L > int64_t(a.max_blocks) * a.cache.block_size) {
         if (report && r.s == 0) raise_status(a.status, PKV_DEV_SEQ_LEN);
         L = 0;
+    } else if (L < a.q_tokens && report && r.s == 0) {
+        raise_status(a.status, PKV_DEV_SEQ_LEN);
     }
     const int64_t chunk = 64 * ((L + 64LL * a.num_splits - 1) / (64LL * a.num_splits));
     r.len = L;
@@ -362,15 +364,25 @@ decode_gqa_tc_e4m3_kernel(const __grid_constant__ CUtensorMap tmap_k,
         auto wait_pv = [&](uint32_t j) {
             return pipe_wait(bar(kBarPvDone + (j & 1u)), (j >> 1) & 1u, a.status, abort_flag);
         };
+        // The R rows of an item are T query tokens x Gr heads: row h is query
+        // token h / Gr of sequence b, head g Gr + h % Gr (T = 1: the group).
+        // (T, Gr and the shift are re-read from the parameters where used:
+        // kept live across the tile loop they cost registers)
+        auto gr_shift = [&]() { return __ffs(R / a.q_tokens) - 1; };
         for (int item = blockIdx.x; item < num_items; item += gridDim.x) {
             const Item r = fp8_item(a, item, t == 0);
-            const int64_t row0 = int64_t(r.b) * a.num_q_heads + int64_t(r.g) * R;
-            const int64_t split0 = int64_t(r.s) * a.batch * a.num_q_heads;
+            auto row_of = [&](int h) -> int64_t {
+                const int sh = gr_shift(), Gr = R / a.q_tokens;
+                return (int64_t(r.b) * a.q_tokens + (h >> sh)) * a.num_q_heads +
+                       int64_t(r.g) * Gr + (h & (Gr - 1));
+            };
+            const int64_t split0 = int64_t(r.s) * a.batch * a.q_tokens * a.num_q_heads;
             if (r.ntiles == 0) {
-                float4 *o = reinterpret_cast<float4 *>(a.out_part + (split0 + row0) * kD);
                 for (int i = t; i < R * kD / 4; i += kSoftThreads)
-                    o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (t < R) a.lse_part[split0 + row0 + t] = -INFINITY;
+                    reinterpret_cast<float4 *>(a.out_part + (split0 + row_of(i / (kD / 4))) *
+                                                                kD)[i % (kD / 4)] =
+                        make_float4(0.f, 0.f, 0.f, 0.f);
+                if (t < R) a.lse_part[split0 + row_of(t)] = -INFINITY;
                 continue;
             }
             // ---- the item's query rows as four E4M3 terms each (rows k R + h
@@ -380,7 +392,7 @@ decode_gqa_tc_e4m3_kernel(const __grid_constant__ CUtensorMap tmap_k,
             if (w) {
                 const int h = t / kTpr, d0 = (t % kTpr) * R;
                 const float qmul = a.scale * kLog2e * a.k_scale[r.g];
-                const float4 *src = reinterpret_cast<const float4 *>(a.q + (row0 + h) * kD + d0);
+                const float4 *src = reinterpret_cast<const float4 *>(a.q + row_of(h) * kD + d0);
                 float x[R];
                 float amax = 0.f;
 #pragma unroll
@@ -425,6 +437,8 @@ decode_gqa_tc_e4m3_kernel(const __grid_constant__ CUtensorMap tmap_k,
 #pragma unroll
             for (int h = 0; h < R; ++h) l_part[h] = 0.f;
             const int32_t span = int32_t(r.end - r.begin);
+            // causal limits, from r.begin: row h sees tokens < lim0 + h / Gr
+            const int32_t lim0 = int32_t(r.len - (a.q_tokens - 1) - r.begin);
             if (softmax_bar_or(!w)) break;          // also orders qsc and mrow for all
 
             bool ok = true;
@@ -452,11 +466,14 @@ decode_gqa_tc_e4m3_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 tc::fence_before_sync();
                 mbar_arrive(bar(kBarSEmpty + buf));
                 ++tcount;
-                const bool in_span = i * kM + row < span;
+                // this token is seen by rows h >= hmin (none past the span)
+                const int32_t tok = i * kM + row, rel = tok - lim0;   // from r.begin
+                const int hmin =
+                    tok >= span ? R : rel < 0 ? 0 : min(rel + 1, a.q_tokens) << gr_shift();
                 bool need = false;
 #pragma unroll
                 for (int h = 0; h < R; ++h) {
-                    x[h] = in_span ? x[h] : -INFINITY;
+                    x[h] = h >= hmin ? x[h] : -INFINITY;
                     need |= x[h] > mrow[h] + kSlack;
                 }
                 if (softmax_bar_or(!w)) {
@@ -558,7 +575,7 @@ decode_gqa_tc_e4m3_kernel(const __grid_constant__ CUtensorMap tmap_k,
             if (t < R) {
                 const float l = (red[t] + red[16 + t]) + (red[32 + t] + red[48 + t]);
                 aux[t] = l > 0.f ? a.v_scale[r.g] / l : 0.f;
-                a.lse_part[split0 + row0 + t] = l > 0.f ? (mrow[t] + log2f(l)) * kLn2 : -INFINITY;
+                a.lse_part[split0 + row_of(t)] = l > 0.f ? (mrow[t] + log2f(l)) * kLn2 : -INFINITY;
             }
             named_barrier_sync(1, kSoftThreads);
             if (w) {
@@ -575,7 +592,7 @@ decode_gqa_tc_e4m3_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     o = fmaf(o, 0.0625f, __uint_as_float(v[2 * R + h]));
                     o = fmaf(o, 0.0625f, __uint_as_float(v[R + h]));
                     o = fmaf(o, 0.0625f, __uint_as_float(v[h]));
-                    a.out_part[(split0 + row0 + h) * kD + row] = o * aux[h];
+                    a.out_part[(split0 + row_of(h)) * kD + row] = o * aux[h];
                 }
             }
             tc::fence_before_sync();
@@ -648,9 +665,12 @@ int launch_rows(const DecodeArgs &a) {
 
 }  // namespace
 
-bool gqa_tc_e4m3_kernel_supports(const pkv_cache_desc &c, int32_t num_q_heads) {
-    if (c.num_kv_heads <= 0 || num_q_heads % c.num_kv_heads != 0) return false;
-    const int G = num_q_heads / c.num_kv_heads;
+bool gqa_tc_e4m3_kernel_supports(const pkv_cache_desc &c, int32_t num_q_heads,
+                                  int32_t q_tokens) {
+    if (c.num_kv_heads <= 0 || num_q_heads % c.num_kv_heads != 0 || q_tokens < 1 ||
+        q_tokens > 16)
+        return false;
+    const int G = num_q_heads / c.num_kv_heads * q_tokens;   // rows per item
     const bool pow2_bs = c.block_size >= 16 && c.block_size <= 256 &&
                          (c.block_size & (c.block_size - 1)) == 0;
     const int64_t rows = int64_t(c.num_blocks) * c.num_kv_heads * c.block_size;
@@ -663,7 +683,7 @@ int gqa_tc_e4m3_resident_ctas(int32_t group) {
 }
 
 int launch_decode_gqa_tc_e4m3(const DecodeArgs &a) {
-    switch (a.num_q_heads / a.cache.num_kv_heads) {
+    switch (a.num_q_heads / a.cache.num_kv_heads * a.q_tokens) {
         case 4: return launch_rows<4, PKV_E4M3_R4_RING, PKV_E4M3_R4_CTAS>(a);
         case 8: return launch_rows<8, PKV_E4M3_R8_RING, PKV_E4M3_R8_CTAS>(a);
         case 16: return launch_rows<16, 5, 2>(a);

@@ -76,8 +76,10 @@ int launch_decode_gqa_tc(const DecodeArgs &a);
 int gqa_tc_resident_ctas();
 // E4M3 pools, query groups of 4, 8 or 16, head dims 128: the tcgen05 kernel
 // with E4M3 operands.
-bool gqa_tc_e4m3_kernel_supports(const pkv_cache_desc &c, int32_t num_q_heads);
-// CTAs that kernel keeps resident for a query group of `group` heads.
+bool gqa_tc_e4m3_kernel_supports(const pkv_cache_desc &c, int32_t num_q_heads,
+                                  int32_t q_tokens = 1);
+// CTAs that kernel keeps resident for `group` rows per item (query group x
+// query tokens).
 int gqa_tc_e4m3_resident_ctas(int32_t group);
 int launch_decode_gqa_tc_e4m3(const DecodeArgs &a);
 int launch_decode_tma(const DecodeArgs &a);

@@ -283,11 +283,15 @@ def oracle_multi_e4m3(w):
     return out.reshape(B, T, *out.shape[1:]), lse.reshape(B, T, -1)
 
 
-# (cached, T, Hq, Hkv, Dk, Dv, block size): the tensor-core kernel's groups of
-# 4, 8 and 16, and shapes only the CUDA-core kernel takes
+# (cached, T, Hq, Hkv, Dk, Dv, block size): G x T = 16, 8 and 4 rows folded
+# into one tensor-core work item (G 4, 8, 4, 2, 1), and shapes run as one
+# row per (sequence, token) (G x T = 48, head dim 64, MLA dims)
 MULTI_SHAPES = [
     ([300, 7, 64], 4, 32, 8, 128, 128, 16),
     ([129, 40], 2, 16, 2, 128, 128, 32),
+    ([90, 12, 200], 2, 16, 4, 128, 128, 32),
+    ([150, 33], 2, 8, 4, 128, 128, 16),
+    ([70, 4], 4, 4, 4, 128, 128, 64),
     ([200, 3], 3, 16, 1, 128, 128, 64),
     ([77, 5], 2, 8, 4, 64, 64, 8),
     ([60, 9], 2, 16, 1, 576, 512, 64),
@@ -320,15 +324,17 @@ def test_e4m3_multi_token_forced_generic_and_causality(pkv):
 
 
 @pytest.mark.parametrize("splits", [1, 2])
-def test_e4m3_multi_token_short_sequence_is_flagged(pkv, splits):
+@pytest.mark.parametrize("T,hq", [(3, 16), (4, 8)], ids=["rows_per_token", "folded"])
+def test_e4m3_multi_token_short_sequence_is_flagged(pkv, splits, T, hq):
     """A sequence holding fewer tokens than T: its rows with no token give
-    out 0 and lse -inf, the device flags the length."""
-    w = multi_e4m3_case(9, [20, 0], 3, 16, 2, 128, 128, 16)
-    w.seq_lens = torch.tensor([23, 1], dtype=torch.int32)
+    out 0 and lse -inf, the device flags the length -- through one row per
+    (sequence, token) and through the folded tensor-core rows."""
+    w = multi_e4m3_case(9, [20, 0], T, hq, 2, 128, 128, 16)
+    w.seq_lens = torch.tensor([20 + T, 1], dtype=torch.int32)
     pkv.device_status(reset=True)
     out, lse = gpu_multi_e4m3(pkv, w, splits)
-    assert np.isneginf(lse[1, :2]).all() and (out[1, :2] == 0).all()
-    assert np.isfinite(lse[1, 2]).all() and np.isfinite(lse[0]).all()
+    assert np.isneginf(lse[1, :T - 1]).all() and (out[1, :T - 1] == 0).all()
+    assert np.isfinite(lse[1, T - 1]).all() and np.isfinite(lse[0]).all()
     ro, rl = oracle_multi_e4m3(w)
     assert_attention_close(out, lse, ro, rl, "short")
     assert pkv.device_status(reset=True) & pkv.DEV_SEQ_LEN
