@@ -494,12 +494,38 @@ class E4m3Step(Step):
         self.attend(ev_a, ev_b)
 
 
+class MultiE4m3Step(E4m3Step):
+    """Speculative verification over an FP8 (E4M3) cache: T new tokens per
+    sequence quantised into the cache, each attending causally (one
+    pkv_paged_decode_attn_multi_e4m3)."""
+    kernel_name = ("pkv_paged_decode_attn_multi_e4m3 (decode_gqa_tc_e4m3_kernel with 4 heads x "
+                   "4 tokens as the 16 rows of each work item, + lse_merge)")
+
+    def __init__(self, pkv, w, dev, splits):
+        super().__init__(pkv, w, dev, splits)
+        B, T, Hq, Dv = w.batch, w.tokens_per_seq, w.num_q_heads, w.head_dim_v
+        self.out = torch.empty(B, T, Hq, Dv, device=dev)
+        self.lse = torch.empty(B, T, Hq, device=dev)
+        need = pkv.lib.pkv_decode_multi_workspace_size(B, T, Hq, Dv, w.max_blocks, splits)
+        self.ws = torch.zeros(need, dtype=torch.uint8, device=dev)
+        self.desc = (f"slot_mapping + kv_append_e4m3 ({w.new_pos.numel()} new tokens, {T} per "
+                     f"sequence) + paged_decode_attn_multi_e4m3 ({splits} splits) = split "
+                     f"kernel with the {T} tokens as rows of each work item + lse_merge")
+
+    def kernel(self):
+        """The FP8 multi-token attention call (its split kernel and merge)."""
+        self.pkv.paged_decode_attn_multi_e4m3(self.q, self.k, self.v, self.k_scale,
+                                              self.v_scale, self.bt, self.lens, self.w.scale,
+                                              num_splits=self.splits, workspace=self.ws,
+                                              out=self.out, lse=self.lse)
+
+
 STEPS = {"long32k": Step, "mix": Step, "tiny": Step, "dcp200k": DcpStep, "agent_mla": AgentStep,
          "agent_mla_latent": AgentStep, "spec4_32k": MultiStep, "long32k_e4m3": E4m3Step,
-         "dcp200k_e4m3": DcpE4m3Step}
+         "dcp200k_e4m3": DcpE4m3Step, "spec4_32k_e4m3": MultiE4m3Step}
 DEFAULT_SPLITS = {"long32k": 16, "mix": 1, "tiny": 1, "dcp200k": 19, "agent_mla": 19,
                   "agent_mla_latent": 19, "spec4_32k": 9, "long32k_e4m3": 7,
-                  "dcp200k_e4m3": 14}
+                  "dcp200k_e4m3": 14, "spec4_32k_e4m3": 9}
 
 
 # ------------------------------------------------------------------ arms
@@ -552,7 +578,16 @@ def oracle_gbs(w, tokens: int | None, repeats: int = 1):
     times = []
     for _ in range(repeats):
         t = time.perf_counter()
-        if w.k_codes is not None:
+        if w.k_codes is not None and w.tokens_per_seq > 1:
+            # each (sequence, token) as a row seeing the sample's tokens up to its own
+            T, B = w.tokens_per_seq, q.shape[0]
+            L = (lens if end is None else end).astype(np.int64)
+            rl = np.array([max(0, L[b] - T + 1 + i) for b in range(B) for i in range(T)],
+                          dtype=np.int32)
+            oracle.paged_decode_attn_e4m3(q.reshape(B * T, *q.shape[2:]), kp, vp,
+                                          w.k_scale.numpy(), w.v_scale.numpy(),
+                                          np.repeat(bt, T, axis=0), rl, w.scale)
+        elif w.k_codes is not None:
             oracle.paged_decode_attn_e4m3(q, kp, vp, w.k_scale.numpy(), w.v_scale.numpy(), bt,
                                           lens, w.scale, tok_end=end)
         elif w.tokens_per_seq > 1:
@@ -867,7 +902,8 @@ def run_gpu(args, world, rank, local):
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3" if w.k_codes is not None else "bf16",
         "data": "synthetic",
         "config": {
             "workload": workload_desc(w, splits), "batch": w.batch,
@@ -880,8 +916,11 @@ def run_gpu(args, world, rank, local):
             "l2": f"no flush: the {total_bytes / 1e9:.3f} GB a step reads exceeds the 129 MB "
                   f"L2 (steps back to back)",
             "parallelism": "replicas" if world > 1 else "single GPU",
-            "compute": "bf16 tensor-core products (fp32 query and probabilities split into bf16 "
-                       "hi+lo), fp32 accumulate and softmax",
+            "compute": ("E4M3 tensor-core products (K/V as stored; the fp32 query as 4 and the "
+                        "probabilities as 5 E4M3 terms), fp32 accumulate and softmax"
+                        if w.k_codes is not None else
+                        "bf16 tensor-core products (fp32 query and probabilities split into bf16 "
+                        "hi+lo), fp32 accumulate and softmax"),
             "bytes": "unique K/V bytes (shared blocks once) + q + tables + appends + out/lse",
         },
         "pct_of_peak": round(100 * value / world / peak, 2),

@@ -320,6 +320,8 @@ def e4m3(w: Workload, seed: int = 11) -> Workload:
 def make(name: str, **kw) -> Workload:
     if name == "long32k_e4m3":
         return e4m3(long32k(**kw))
+    if name == "spec4_32k_e4m3":
+        return e4m3(spec_verify(**kw))
     if name == "dcp200k_e4m3":
         return e4m3(dcp200k(**kw))
     if name == "agent_mla_latent":
