@@ -310,6 +310,18 @@ int pkv_paged_decode_attn_e4m3(const pkv_cache_desc *cache, const float *q, int3
                                void *workspace, size_t workspace_bytes, float *out, float *lse,
                                int32_t flags, pkv_stream_t stream);
 
+/* pkv_paged_decode_attn_noalloc_e4m3 -- pkv_paged_decode_attn_e4m3 with the
+ * split partials in the library's scratch (the rules of
+ * pkv_paged_decode_attn_noalloc: PKV_NOALLOC_SCRATCH_BYTES, shared by all
+ * calls, PKV_ERR_WORKSPACE_TOO_SMALL when the partials do not fit). */
+int pkv_paged_decode_attn_noalloc_e4m3(const pkv_cache_desc *cache, const float *q,
+                                       int32_t batch, int32_t num_q_heads, const void *k_pool,
+                                       const void *v_pool, const float *k_scale,
+                                       const float *v_scale, const int32_t *block_tables,
+                                       int32_t max_blocks, const int32_t *seq_lens, float scale,
+                                       int32_t num_splits, float *out, float *lse, int32_t flags,
+                                       pkv_stream_t stream);
+
 /* ---------------------------------------------------------------------------
  * pkv_paged_decode_attn_multi -- several new tokens per sequence in one step
  * (e.g. verifying speculated tokens; [AX] names a speculative-verification

@@ -61,6 +61,9 @@ SIGNATURES = {
                                                      _P, _f32, _i32, _P, _P, _i32, _P]),
     "pkv_paged_decode_attn_noalloc": (ctypes.c_int, [_DESC, _P, _i32, _i32, _P, _P, _P, _i32,
                                                      _P, _f32, _i32, _P, _P, _i32, _P]),
+    "pkv_paged_decode_attn_noalloc_e4m3": (ctypes.c_int, [_DESC, _P, _i32, _i32, _P, _P, _P,
+                                                          _P, _P, _i32, _P, _f32, _i32, _P,
+                                                          _P, _i32, _P]),
     "pkv_decode_multi_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32]),
     "pkv_decode_multi_auto_splits": (_i32, [_DESC, _i32, _i32, _i32, _i32, _i32]),
     "pkv_paged_decode_attn_multi": (ctypes.c_int, [_DESC, _P, _i32, _i32, _i32, _P, _P, _P,

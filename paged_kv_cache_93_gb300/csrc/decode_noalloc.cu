@@ -85,3 +85,26 @@ extern "C" int pkv_paged_decode_attn_noalloc(const pkv_cache_desc *cache, const 
                                  max_blocks, seq_lens, scale, S, scratch, kNoAllocScratchBytes,
                                  out, lse, flags, stream);
 }
+
+extern "C" int pkv_paged_decode_attn_noalloc_e4m3(
+    const pkv_cache_desc *cache, const float *q, int32_t batch, int32_t num_q_heads,
+    const void *k_pool, const void *v_pool, const float *k_scale, const float *v_scale,
+    const int32_t *block_tables, int32_t max_blocks, const int32_t *seq_lens, float scale,
+    int32_t num_splits, float *out, float *lse, int32_t flags, pkv_stream_t stream) {
+    if (!cache || batch < 0 || num_q_heads <= 0 || num_splits < 0) return PKV_ERR_INVALID_ARG;
+    if (batch == 0) return PKV_OK;
+    int32_t S = num_splits;
+    if (S == 0) {
+        const int64_t longest = int64_t(max_blocks > 0 ? max_blocks : 0) * cache->block_size;
+        S = pkv_decode_auto_splits_e4m3(cache, batch, num_q_heads,
+                                        int32_t(longest < INT32_MAX ? longest : INT32_MAX));
+    }
+    if (pkv_decode_workspace_size(batch, num_q_heads, cache->head_dim_v, S) > kNoAllocScratchBytes)
+        return PKV_ERR_WORKSPACE_TOO_SMALL;
+    int status = PKV_OK;
+    void *scratch = scratch_address(&status);
+    if (!scratch) return status;
+    return pkv_paged_decode_attn_e4m3(cache, q, batch, num_q_heads, k_pool, v_pool, k_scale,
+                                      v_scale, block_tables, max_blocks, seq_lens, scale, S,
+                                      scratch, kNoAllocScratchBytes, out, lse, flags, stream);
+}

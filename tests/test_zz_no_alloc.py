@@ -87,3 +87,32 @@ def test_noalloc_refuses_partials_beyond_the_scratch(pkv):
         ctypes.c_float(w.scale), 256, _ptr(out), _ptr(lse), 0,
         ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     assert rc == -4        # PKV_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_noalloc_e4m3_matches_workspace_call_and_oracle(pkv):
+    """The FP8 form: the same bits as pkv_paged_decode_attn_e4m3 with a caller
+    workspace, and the oracle's attention over the stored codes."""
+    import oracle
+    dev = "cuda"
+    w = workloads.e4m3(workloads.custom(12, [3000, 700, 45], 32, 8, 128, 128, 16))
+    kc, vc = w.k_codes.to(dev), w.v_codes.to(dev)
+    ks, vs = w.k_scale.to(dev), w.v_scale.to(dev)
+    bt, lens, q = w.block_tables.to(dev), w.seq_lens.to(dev), w.q.to(dev)
+    ref_o, ref_l = pkv.paged_decode_attn_e4m3(q, kc, vc, ks, vs, bt, lens, w.scale, num_splits=5)
+    desc = pkv.cache_desc(kc, vc)
+    B, Hq = w.batch, w.num_q_heads
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    for _ in range(2):
+        out = torch.full((B, Hq, w.head_dim_v), float("nan"), device=dev)
+        lse = torch.full((B, Hq), float("nan"), device=dev)
+        rc = pkv.lib.pkv_paged_decode_attn_noalloc_e4m3(
+            ctypes.byref(desc), _ptr(q), B, Hq, _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), _ptr(bt),
+            bt.shape[1], _ptr(lens), ctypes.c_float(w.scale), 5, _ptr(out), _ptr(lse), 0, stream)
+        torch.cuda.synchronize()
+        assert rc == 0
+        assert torch.equal(out, ref_o) and torch.equal(lse, ref_l)
+    ro, rl = oracle.paged_decode_attn_e4m3(w.q.numpy(), w.k_codes.numpy(), w.v_codes.numpy(),
+                                           w.k_scale.numpy(), w.v_scale.numpy(),
+                                           w.block_tables.numpy(), w.seq_lens.numpy(), w.scale)
+    assert_attention_close(out.cpu().numpy(), lse.cpu().numpy(), ro, rl, "noalloc e4m3")
+    assert pkv.device_status() == 0
