@@ -8,13 +8,14 @@
 // and K/V tiles shared by head groups and by sequences with a common prefix
 // come from L2.  One CTA per SM walks its items tile by tile, 128 tokens a
 // tile:
-//   S^T[128 tok x 64 heads] = K_tile . Q^T          (tcgen05, M=128, N=64)
-//   online softmax over the 128 token lanes of S^T    (CUDA cores)
-//   O^T[Dv x 64 heads]     += V_tile^T . P            (tcgen05, M=128, N=64)
+//   S^T[128 tok x (64 | 64)] = K_tile . [Q_hi; Q_lo]^T  (tcgen05, M=128, N=128)
+//   online softmax over the 128 token lanes of S_hi + S_lo  (CUDA cores)
+//   O^T[Dv x 64 heads]       += V_tile^T . P              (tcgen05, M=128, N=64)
 // Tokens are the MMA's M, so the query group is N and 64 heads fit in one
 // CTA's shared memory even with the fp32 query kept exact as bf16 hi + lo
-// (Dk = 576: 147 KB).  S^T (two buffers) and O^T (Dv/128 blocks of 64
-// columns) live in TMEM: 128 + 256 of its 512 columns for Dv = 512.
+// (Dk = 576: 147 KB), the two parts side by side as one N = 128 operand
+// (one score MMA per k-step).  S^T (two buffers of 128 columns) and O^T
+// (Dv/128 blocks of 64 columns) fill TMEM's 512 columns at Dv = 512.
 //
 // Warp roles (192 threads):
 //   warp 0   TMA producer: K chunks [128 tok x 64 dims] (two 64-row boxes)
@@ -62,13 +63,13 @@ constexpr int kThreads = 192;
 constexpr int kSoftWarp0 = 2;           // warps 2..5: softmax and epilogue
 constexpr int kSoftThreads = 128;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;           // S^T buffers at columns 0 and 64
-constexpr uint32_t kColO = 128;         // O^T blocks at columns 128 + 64 j
+constexpr uint32_t kColS = 0;           // S^T buffers at columns 0 and 128 (hi | lo parts)
+constexpr uint32_t kColO = 256;         // O^T blocks at columns 256 + 64 j
 constexpr float kSlack = 8.f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kSmemLimit = 232448;
-constexpr uint32_t kIdS = tc::idesc_bf16_f32(128, 64, 0, 0);   // K-major K, K-major Q
+constexpr uint32_t kIdS = tc::idesc_bf16_f32(128, 128, 0, 0);  // K-major K, K-major [Q_hi; Q_lo]
 constexpr uint32_t kIdO = tc::idesc_bf16_f32(128, 64, 1, 1);   // MN-major V, MN-major P
 
 // mbarrier slots
@@ -95,9 +96,11 @@ struct SmemMap {
 };
 __host__ __device__ inline SmemMap smem_map(const TcShape &s) {
     SmemMap m;
+    // per 64-dim segment one [128][64] K-major block: rows 0-63 the query's
+    // high parts, rows 64-127 its low parts (one N = 128 operand)
     m.q_hi = 0;
-    m.q_lo = m.q_hi + uint32_t(s.dk_segs) * 8192;
-    m.p_hi = m.q_lo + uint32_t(s.dk_segs) * 8192;
+    m.q_lo = 8192;
+    m.p_hi = uint32_t(s.dk_segs) * 16384;
     m.p_lo = m.p_hi + kM * 128;
     m.ring = m.p_lo + kM * 128;
     m.bars = m.ring + uint32_t(s.ring) * kChunk;
@@ -112,6 +115,18 @@ __host__ __device__ inline SmemMap smem_map(const TcShape &s) {
 inline size_t tc_smem_bytes(const TcShape &s) { return 1024 + size_t(smem_map(s).end); }
 
 __device__ __forceinline__ int64_t lmin(int64_t x, int64_t y) { return x < y ? x : y; }
+
+// This thread's scores for heads 16c .. 16c + 15 of a tile: the product with
+// the query's high parts (S^T columns 0-63) plus its low parts (64-127).
+__device__ __forceinline__ void ld_scores(uint32_t ts, int c, uint32_t (&v)[16]) {
+    uint32_t lo[16];
+    tc::ld16(ts + 16 * c, v);
+    tc::ld16(ts + kN + 16 * c, lo);
+    tc::wait_ld();
+#pragma unroll
+    for (int k = 0; k < 16; ++k)
+        v[k] = __float_as_uint(__uint_as_float(v[k]) + __uint_as_float(lo[k]));
+}
 
 struct TcItem {
     int b, g, hg, s;
@@ -289,7 +304,7 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
         int stage = 0;
         uint32_t phase = 0, tcount = 0, pcount = 0, ne = 0;
         bool ok = true;
-        const uint32_t qh = sb + sm.q_hi, ql = sb + sm.q_lo;
+        const uint32_t qh = sb + sm.q_hi;
         const uint32_t ph = sb + sm.p_hi, pl = sb + sm.p_lo;
         auto wait_all = [&](uint32_t b, uint32_t parity) {
             return __all_sync(0xffffffffu, pipe_wait(b, parity, a.status, abort_flag));
@@ -306,23 +321,21 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
             if (!(ok = wait_all(bar(kBarQFull), ne & 1u))) break;
             for (int i = 0; i <= r.ntiles && ok; ++i) {
                 if (i < r.ntiles) {
-                    // ---- S^T[buf] = K_tile . (Q_hi + Q_lo)^T
+                    // ---- S^T[buf] = K_tile . [Q_hi; Q_lo]^T (sum of the halves: the scores)
                     const uint32_t buf = tcount & 1u;
                     if (!(ok = wait_all(bar(kBarSEmpty + buf), ((tcount >> 1) & 1u) ^ 1u))) break;
-                    const uint32_t d = tmem + kColS + 64 * buf;
+                    const uint32_t d = tmem + kColS + 128 * buf;
                     for (int seg = 0; seg < shp.dk_segs; ++seg) {
                         if (!(ok = wait_all(bar(kBarFull + stage), phase))) break;
                         tc::fence_after_sync();
                         if (lane == 0) {
                             const uint32_t kb = sb + sm.ring + uint32_t(stage) * kChunk;
 #pragma unroll
-                            for (int kk = 0; kk < 4; ++kk) {
-                                const uint64_t ad = tc::smem_desc(kb + 32 * kk, 16, 1024);
-                                const uint32_t qo = uint32_t(seg) * 8192 + 32 * kk;
-                                tc::mma_bf16(d, ad, tc::smem_desc(qh + qo, 16, 1024), kIdS,
-                                             (seg | kk) != 0);
-                                tc::mma_bf16(d, ad, tc::smem_desc(ql + qo, 16, 1024), kIdS, 1);
-                            }
+                            for (int kk = 0; kk < 4; ++kk)
+                                tc::mma_bf16(d, tc::smem_desc(kb + 32 * kk, 16, 1024),
+                                             tc::smem_desc(qh + uint32_t(seg) * 16384 + 32 * kk,
+                                                           16, 1024),
+                                             kIdS, (seg | kk) != 0);
                             tc::commit(bar(kBarEmpty + stage));
                         }
                         __syncwarp();
@@ -443,7 +456,7 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         const uint32_t l01 = pack_bf16x2(x0 - bf16_lo_to_f32(h01), x1 - bf16_hi_to_f32(h01));
                         const uint32_t l23 = pack_bf16x2(x2 - bf16_lo_to_f32(h23), x3 - bf16_hi_to_f32(h23));
                         // four consecutive dims share one 16-byte swizzle chunk
-                        const uint32_t off = uint32_t(d >> 6) * 8192 + swz(h, d & 63);
+                        const uint32_t off = uint32_t(d >> 6) * 16384 + swz(h, d & 63);
                         *reinterpret_cast<uint2 *>(q_hi + off) = make_uint2(h01, h23);
                         *reinterpret_cast<uint2 *>(q_lo + off) = make_uint2(l01, l23);
                     }
@@ -463,7 +476,7 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 // from TMEM in 16-column slices (first pass: does any score
                 // exceed its head's running max by more than the slack?)
                 const uint32_t buf = tcount & 1u;
-                const uint32_t ts = tl + kColS + 64 * buf;
+                const uint32_t ts = tl + kColS + 128 * buf;
                 w = pipe_wait(bar(kBarSFull + buf), (tcount >> 1) & 1u, a.status, abort_flag);
                 tc::fence_after_sync();
                 const bool valid = r.begin + int64_t(i) * kM + row < r.end;
@@ -471,8 +484,7 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     uint32_t v[16];
-                    tc::ld16(ts + 16 * c, v);
-                    tc::wait_ld();
+                    ld_scores(ts, c, v);
 #pragma unroll
                     for (int k = 0; k < 16; ++k)
                         need |= valid && __uint_as_float(v[k]) > mrow[16 * c + k] + kSlack;
@@ -487,8 +499,7 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         uint32_t v[16];
-                        tc::ld16(ts + 16 * c, v);
-                        tc::wait_ld();
+                        ld_scores(ts, c, v);
 #pragma unroll
                         for (int k = 0; k < 16; ++k) {
                             float m = valid ? __uint_as_float(v[k]) : -INFINITY;
@@ -548,8 +559,7 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     uint32_t v[16];
-                    tc::ld16(ts + 16 * c, v);
-                    tc::wait_ld();
+                    ld_scores(ts, c, v);
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
                         uint32_t hi[4], lo[4];
