@@ -51,6 +51,9 @@ PROFILES = {
     "long32k": ("decode_tma_long32k.txt", ("decode_tma.cu", "pkv_device.cuh")),
     "spec4_32k": ("decode_gqa_tc_spec4_32k.txt",
                   ("decode_gqa_tc.cu", "pkv_device.cuh", "pkv_tcgen05.cuh", "pkv_pipeline.cuh")),
+    "spec4_32k_e4m3": ("decode_gqa_tc_e4m3_spec4_32k.txt",
+                       ("decode_gqa_tc_e4m3.cu", "pkv_device.cuh", "pkv_tcgen05.cuh",
+                        "pkv_pipeline.cuh")),
     "long32k_e4m3": ("decode_gqa_tc_e4m3_long32k.txt",
                      ("decode_gqa_tc_e4m3.cu", "pkv_device.cuh", "pkv_tcgen05.cuh",
                       "pkv_pipeline.cuh")),
