@@ -37,12 +37,14 @@ int validate_decode(const pkv_cache_desc *c, const float *q, int32_t batch, int3
     return PKV_OK;
 }
 
-// The tcgen05 GQA kernels' resident CTAs take the (sequence, KV head,
-// split) items in turn, an item costing its 128-token tiles plus about one
-// tile of start-up.  Pick S for the least rounds x (tiles + 1) on sequences
-// of the longest length; a tie goes to fewer splits (less to merge).
-int32_t tc_splits(const pkv_cache_desc &c, int32_t batch, int32_t max_seq_len, int64_t ctas) {
-    const int64_t units = std::max<int64_t>(1, int64_t(batch) * c.num_kv_heads);
+// The tcgen05 GQA kernels' resident CTAs take the (sequence, KV head
+// [, head group], split) items in turn, an item costing its 128-token tiles
+// plus about one tile of start-up.  Pick S for the least rounds x (tiles + 1)
+// on sequences of the longest length; a tie goes to fewer splits (less to
+// merge).
+int32_t tc_splits(const pkv_cache_desc &c, int32_t batch, int32_t max_seq_len, int64_t ctas,
+                  int32_t head_groups = 1) {
+    const int64_t units = std::max<int64_t>(1, int64_t(batch) * c.num_kv_heads * head_groups);
     const int64_t L = std::max<int64_t>(1, max_seq_len);
     const int64_t s_max = std::min<int64_t>(kMaxSplits, (L + 127) / 128);
     int64_t best = 1, best_cost = INT64_MAX;
@@ -61,7 +63,8 @@ int32_t tc_splits(const pkv_cache_desc &c, int32_t batch, int32_t max_seq_len, i
 int32_t auto_splits(const pkv_cache_desc &c, int32_t batch, int32_t num_q_heads,
                     int32_t max_seq_len, int32_t q_tokens = 1) {
     if (gqa_tc_kernel_supports(c, num_q_heads, q_tokens))
-        return tc_splits(c, batch, max_seq_len, gqa_tc_resident_ctas());
+        return tc_splits(c, batch, max_seq_len, gqa_tc_resident_ctas(),
+                         gqa_tc_head_groups(c, num_q_heads, q_tokens));
     // Enough (sequence, KV head [, head block], split) items for ~4 per SM
     // (8 for the tcgen05 kernel), each item at least 512 tokens long.
     int64_t units = int64_t(batch) * c.num_kv_heads;
@@ -302,6 +305,14 @@ MultiLayout multi_layout(int32_t batch, int32_t tokens, int32_t num_q_heads, int
     return m;
 }
 
+// Whether a GQA kernel takes a sequence's T query tokens as extra rows of one
+// work item (the order run_split_kernel tries them in).
+bool multi_folds(const pkv_cache_desc &c, int32_t num_q_heads, int32_t tokens, int32_t flags) {
+    if (flags & PKV_DECODE_GENERIC) return false;
+    return (!(flags & PKV_DECODE_NO_TCGEN05) && gqa_tc_kernel_supports(c, num_q_heads, tokens)) ||
+           tma_kernel_supports(c, num_q_heads, tokens);
+}
+
 }  // namespace
 
 extern "C" int32_t pkv_decode_multi_auto_splits(const pkv_cache_desc *cache, int32_t batch,
@@ -310,8 +321,7 @@ extern "C" int32_t pkv_decode_multi_auto_splits(const pkv_cache_desc *cache, int
     if (!cache || cache->num_kv_heads <= 0 || num_q_heads <= 0 || tokens_per_seq <= 0) return 1;
     // Work items are (sequence, KV head, split) when the GQA kernel takes the
     // T tokens as rows of one item; (sequence x token, KV head, split) otherwise.
-    const bool folded = !(flags & PKV_DECODE_GENERIC) &&
-                        tma_kernel_supports(*cache, num_q_heads, tokens_per_seq);
+    const bool folded = multi_folds(*cache, num_q_heads, tokens_per_seq, flags);
     return auto_splits(*cache, folded ? batch : batch * tokens_per_seq, num_q_heads,
                        max_seq_len, folded ? tokens_per_seq : 1);
 }
@@ -359,8 +369,7 @@ extern "C" int pkv_paged_decode_attn_multi(const pkv_cache_desc *cache, const fl
     float *out_part = reinterpret_cast<float *>(ws + m.partials);
     float *lse_part = reinterpret_cast<float *>(
         ws + m.partials + align256(prow * cache->head_dim_v * sizeof(float)));
-    if (!(flags & PKV_DECODE_GENERIC) &&
-        tma_kernel_supports(*cache, num_q_heads, tokens_per_seq)) {
+    if (multi_folds(*cache, num_q_heads, tokens_per_seq, flags)) {
         // The GQA kernel takes the T query tokens as extra rows of each work
         // item (causal limits per row): every K/V tile is read once.
         DecodeArgs a{*cache, q, batch, num_q_heads, k_pool, v_pool, block_tables, max_blocks,
@@ -370,7 +379,7 @@ extern "C" int pkv_paged_decode_attn_multi(const pkv_cache_desc *cache, const fl
         if (S == 1) return run_split_kernel(a, flags);
         a.out_part = out_part;
         a.lse_part = lse_part;
-            st = run_split_kernel(a, flags);
+        st = run_split_kernel(a, flags);
         if (st != PKV_OK) return st;
         return launch_lse_merge(S, out_part, lse_part, int64_t(rows) * num_q_heads,
                                 cache->head_dim_v, out, lse, s);

@@ -105,22 +105,34 @@ constexpr uint32_t kSmemBytes = 1024 + kOffRing + kRing * kChunk;
 __device__ __forceinline__ int64_t lmin(int64_t x, int64_t y) { return x < y ? x : y; }
 
 struct Item {
-    int b, g, s;
+    int b, g, s, hg;
     int64_t len, begin, end;
     int ntiles;
 };
 
+// Head groups per (sequence, KV head): the item's 16 rows are 16 / T heads x
+// T query tokens, so G x T = 32 rows are two items.
+__device__ __forceinline__ int head_groups(const DecodeArgs &a) {
+    return a.num_q_heads / a.cache.num_kv_heads * a.q_tokens / kRows;
+}
+
+// item = ((b * Hkv + g) * S + s) * HG + hg: the head groups of one
+// (sequence, KV head, split) are neighbours and read the same tiles together.
 __device__ __forceinline__ Item gqa_item(const DecodeArgs &a, int item, bool report) {
     Item r;
-    r.s = item % a.num_splits;
-    const int t = item / a.num_splits;
+    const int HG = head_groups(a);
+    r.hg = item % HG;
+    const int t0 = item / HG;
+    r.s = t0 % a.num_splits;
+    const int t = t0 / a.num_splits;
     r.g = t % a.cache.num_kv_heads;
     r.b = t / a.cache.num_kv_heads;
     int64_t L = a.seq_lens[r.b];
+    report = report && r.s == 0 && r.hg == 0;
     if (L < 0 || L > int64_t(a.max_blocks) * a.cache.block_size) {
-        if (report && r.s == 0) raise_status(a.status, PKV_DEV_SEQ_LEN);
+        if (report) raise_status(a.status, PKV_DEV_SEQ_LEN);
         L = 0;
-    } else if (L < a.q_tokens && report && r.s == 0) {
+    } else if (L < a.q_tokens && report) {
         raise_status(a.status, PKV_DEV_SEQ_LEN);
     }
     const int64_t chunk = 64 * ((L + 64LL * a.num_splits - 1) / (64LL * a.num_splits));
@@ -132,10 +144,11 @@ __device__ __forceinline__ Item gqa_item(const DecodeArgs &a, int item, bool rep
 }
 
 // Row `row` of an item -> its query / output row, in head vectors: query
-// token t = row / Gr of sequence b, head g * Gr + row % Gr.
-__device__ __forceinline__ int64_t row_offset(const DecodeArgs &a, int b, int g, int row, int Gr) {
+// token t = row / Gr of sequence b, head g G + hg Gr + row % Gr.
+__device__ __forceinline__ int64_t row_offset(const DecodeArgs &a, const Item &r, int row, int Gr) {
     const int t = row / Gr, h = row - t * Gr;
-    return (int64_t(b) * a.q_tokens + t) * a.num_q_heads + int64_t(g) * Gr + h;
+    const int G = a.num_q_heads / a.cache.num_kv_heads;
+    return (int64_t(r.b) * a.q_tokens + t) * a.num_q_heads + int64_t(r.g) * G + r.hg * Gr + h;
 }
 
 // Offset of bf16 element (row, col < 64) in a [rows][64] 128-byte-swizzled
@@ -159,10 +172,10 @@ decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     auto bar = [&](int i) { return sb + kOffBars + 8u * uint32_t(i); };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int num_items = a.batch * a.cache.num_kv_heads * a.num_splits;
+    const int num_items = a.batch * a.cache.num_kv_heads * a.num_splits * head_groups(a);
     const int bs = a.cache.block_size, hkv = a.cache.num_kv_heads;
     const int box = bs < 64 ? bs : 64;                  // rows per TMA box (one block or less)
-    const int T = a.q_tokens, Gr = kRows / a.q_tokens;   // query tokens, heads per KV head
+    const int T = a.q_tokens, Gr = kRows / a.q_tokens;   // query tokens, heads per item
 
     if (threadIdx.x == 0) {
         for (int r = 0; r < kRing; ++r) {
@@ -395,7 +408,7 @@ decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 for (int i = t; i < kRows * kD / 2; i += kSoftThreads) {
                     const int rr = i / (kD / 2), d = 2 * (i % (kD / 2));
                     const float2 x = *reinterpret_cast<const float2 *>(
-                        a.q + row_offset(a, q_item.b, q_item.g, rr, Gr) * kD + d);
+                        a.q + row_offset(a, q_item, rr, Gr) * kD + d);
                     const float x0 = x.x * qscale, x1 = x.y * qscale;
                     const uint32_t hi = pack_bf16x2(x0, x1);
                     const uint32_t lo =
@@ -425,10 +438,10 @@ decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 for (int i = t; i < kRows * kD / 4; i += kSoftThreads) {
                     const int rr = i / (kD / 4), c = i % (kD / 4);
                     reinterpret_cast<float4 *>(
-                        a.out_part + (split0 + row_offset(a, r.b, r.g, rr, Gr)) * kD)[c] =
+                        a.out_part + (split0 + row_offset(a, r, rr, Gr)) * kD)[c] =
                         make_float4(0.f, 0.f, 0.f, 0.f);
                 }
-                if (t < kRows) a.lse_part[split0 + row_offset(a, r.b, r.g, t, Gr)] = -INFINITY;
+                if (t < kRows) a.lse_part[split0 + row_offset(a, r, t, Gr)] = -INFINITY;
                 continue;
             }
             bool w = staged || stage_q(r, ne);
@@ -438,7 +451,7 @@ decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
             Item nx;
             const int next = next_busy(item, nx);
             if (next >= 0 && t < kRows * 4) {
-                const float *qrow = a.q + row_offset(a, nx.b, nx.g, t >> 2, Gr) * kD + (t & 3) * 32;
+                const float *qrow = a.q + row_offset(a, nx, t >> 2, Gr) * kD + (t & 3) * 32;
                 asm volatile("prefetch.global.L2 [%0];" ::"l"(qrow));
             }
             if (t < kRows) mrow[t] = -INFINITY;
@@ -579,7 +592,7 @@ decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
             if (t < kRows) {
                 const float l = (red[t] + red[kRows + t]) + (red[2 * kRows + t] + red[3 * kRows + t]);
                 aux[t] = l > 0.f ? 1.f / l : 0.f;
-                a.lse_part[split0 + row_offset(a, r.b, r.g, t, Gr)] =
+                a.lse_part[split0 + row_offset(a, r, t, Gr)] =
                     l > 0.f ? (mrow[t] + log2f(l)) * kLn2 : -INFINITY;
             }
             named_barrier_sync(1, kSoftThreads);
@@ -590,7 +603,7 @@ decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 tc::wait_ld();
 #pragma unroll
                 for (int h = 0; h < kRows; ++h)
-                    a.out_part[(split0 + row_offset(a, r.b, r.g, h, Gr)) * kD + row] =
+                    a.out_part[(split0 + row_offset(a, r, h, Gr)) * kD + row] =
                         (__uint_as_float(hv[h]) + __uint_as_float(lv[h])) * aux[h];
             }
             tc::fence_before_sync();
@@ -641,12 +654,21 @@ bool make_map(CUtensorMap *map, const void *pool, int64_t rows, int stride, int 
 }  // namespace
 
 bool gqa_tc_kernel_supports(const pkv_cache_desc &c, int32_t num_q_heads, int32_t q_tokens) {
+    if (c.num_kv_heads <= 0 || num_q_heads % c.num_kv_heads != 0 || q_tokens < 1 ||
+        kRows % q_tokens != 0)
+        return false;
+    // 16 rows per item, or 32 as two head groups (larger groups go to the
+    // large-group kernels, which read a tile once per 64 heads)
     const int rows_per_item = num_q_heads / c.num_kv_heads * q_tokens;
     const bool pow2_bs = c.block_size >= 16 && c.block_size <= 256 &&
                          (c.block_size & (c.block_size - 1)) == 0;
     const int64_t rows = int64_t(c.num_blocks) * c.num_kv_heads * c.block_size;
-    return rows_per_item == kRows && c.head_dim_k == kD && c.head_dim_v == kD && pow2_bs &&
-           rows < (int64_t(1) << 31) - 1;
+    return (rows_per_item == kRows || rows_per_item == 2 * kRows) && c.head_dim_k == kD &&
+           c.head_dim_v == kD && pow2_bs && rows < (int64_t(1) << 31) - 1;
+}
+
+int gqa_tc_head_groups(const pkv_cache_desc &c, int32_t num_q_heads, int32_t q_tokens) {
+    return num_q_heads / c.num_kv_heads * q_tokens / kRows;
 }
 
 int gqa_tc_resident_ctas() { return sm_count() * kCtas; }
@@ -671,7 +693,8 @@ int launch_decode_gqa_tc(const DecodeArgs &a) {
     // TMEM columns each are sized for it); the persistent loop is correct
     // for any grid, so this sizes it rather than asking the occupancy
     // calculator.
-    const int64_t items = int64_t(a.batch) * a.cache.num_kv_heads * a.num_splits;
+    const int64_t items = int64_t(a.batch) * a.cache.num_kv_heads * a.num_splits *
+                          gqa_tc_head_groups(a.cache, a.num_q_heads, a.q_tokens);
     const int grid = int(std::min<int64_t>(items, int64_t(sm_count()) * kCtas));
     if (grid <= 0) return PKV_OK;
     return launch_pdl(decode_gqa_tc_kernel, dim3(grid), dim3(kThreads), kSmemBytes, a.stream, tk,

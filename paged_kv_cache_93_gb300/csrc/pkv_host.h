@@ -68,12 +68,14 @@ struct DecodeArgs {
     const float *k_scale = nullptr, *v_scale = nullptr;
 };
 bool tma_kernel_supports(const pkv_cache_desc &c, int32_t num_q_heads, int32_t q_tokens = 1);
-// 16 query rows per KV head (heads x query tokens), head dims 128: the
-// tcgen05 form of the GQA kernel.
+// 16 or 32 query rows per KV head (heads x query tokens; 32 as two head
+// groups of 16), head dims 128: the tcgen05 form of the GQA kernel.
 bool gqa_tc_kernel_supports(const pkv_cache_desc &c, int32_t num_q_heads, int32_t q_tokens);
 int launch_decode_gqa_tc(const DecodeArgs &a);
 // CTAs the tcgen05 GQA kernel keeps resident (one persistent grid).
 int gqa_tc_resident_ctas();
+// (sequence, KV head) items split into this many head groups of 16 rows
+int gqa_tc_head_groups(const pkv_cache_desc &c, int32_t num_q_heads, int32_t q_tokens);
 // E4M3 pools, query groups of 4, 8 or 16, head dims 128: the tcgen05 kernel
 // with E4M3 operands.
 bool gqa_tc_e4m3_kernel_supports(const pkv_cache_desc &c, int32_t num_q_heads,

@@ -253,7 +253,7 @@ def test_workspace_reused_across_calls(pkv):
 MLA_SHAPES = [
     ([70, 3, 200], 32, 1, 576, 512, 64),
     ([130, 1], 128, 1, 576, 512, 64),
-    ([300, 45], 64, 2, 128, 128, 32),
+    ([300, 45], 64, 2, 128, 128, 32),      # G 32, D 128: tcgen05 GQA, two head groups
     ([513, 0, 31], 64, 1, 192, 256, 128),
     ([1000], 32, 1, 64, 64, 256),
     # multiples of 64 heads: the tcgen05 kernel (ragged tiles, two KV heads,

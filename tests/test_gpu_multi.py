@@ -71,10 +71,13 @@ def oracle_multi(w):
 
 
 # (cached, Hq, Hkv, Dk, Dv, block size): GQA TMA kernel (G 4 and 8, D 128 and
-# 64), the tcgen05 kernel (128 heads over 576/512), the generic kernel (G 3).
+# 64), the tcgen05 GQA kernel (G x T of 16, or 32 as two head groups: G 8 with
+# T 4, G 16 with T 2), the tcgen05 MLA kernel (128 heads over 576/512), the
+# generic kernel (G 3).
 SHAPES = [
     ([300, 7, 64], 32, 8, 128, 128, 16),
     ([129, 40], 64, 8, 128, 128, 16),
+    ([90, 260, 2], 32, 2, 128, 128, 32),
     ([77, 5], 8, 2, 64, 64, 8),
     ([200, 3], 128, 1, 576, 512, 64),
     ([50, 9], 6, 2, 64, 64, 16),
@@ -87,9 +90,9 @@ SHAPES = [
 @pytest.mark.parametrize("splits", [1, 3, 0])
 @pytest.mark.parametrize("flags", ["auto", "no_tcgen05"])
 def test_multi_token_decode(pkv, shape, T, splits, flags):
-    """G*T = 16 rows with head dim 128 run on the tcgen05 GQA kernel, other
-    foldable shapes on the warp-level-MMA one; no_tcgen05 checks the latter
-    on the 16-row shapes too."""
+    """G*T = 16 or 32 rows with head dim 128 run on the tcgen05 GQA kernel
+    (32 as two head groups), other foldable shapes on the warp-level-MMA one;
+    no_tcgen05 checks the latter on the 16-row shapes too."""
     cached, hq, hkv, dk, dv, bs = shape
     w = multi_case(500 + T + dk, cached, T, hq, hkv, dk, dv, bs)
     f = pkv.DECODE_NO_TCGEN05 if flags == "no_tcgen05" else 0
