@@ -154,8 +154,9 @@ extern "C" int32_t pkv_decode_auto_splits_e4m3(const pkv_cache_desc *cache, int3
     if (!cache || cache->num_kv_heads <= 0 || num_q_heads <= 0) return 1;
     if (!gqa_tc_e4m3_kernel_supports(*cache, num_q_heads))
         return auto_splits(*cache, batch, num_q_heads, max_seq_len);
-    return tc_splits(*cache, batch, max_seq_len,
-                     gqa_tc_e4m3_resident_ctas(num_q_heads / cache->num_kv_heads));
+    const int32_t group = num_q_heads / cache->num_kv_heads;
+    return tc_splits(*cache, batch, max_seq_len, gqa_tc_e4m3_resident_ctas(group),
+                     gqa_tc_e4m3_head_groups(group));
 }
 
 extern "C" int pkv_paged_decode_attn_e4m3(const pkv_cache_desc *cache, const float *q,
@@ -414,7 +415,9 @@ extern "C" int32_t pkv_decode_multi_auto_splits_e4m3(const pkv_cache_desc *cache
     if (gqa_tc_e4m3_kernel_supports(*cache, num_q_heads, tokens_per_seq))
         return tc_splits(*cache, batch, max_seq_len,
                          gqa_tc_e4m3_resident_ctas(num_q_heads / cache->num_kv_heads *
-                                                   tokens_per_seq));
+                                                   tokens_per_seq),
+                         gqa_tc_e4m3_head_groups(num_q_heads / cache->num_kv_heads *
+                                                 tokens_per_seq));
     return pkv_decode_auto_splits_e4m3(cache, batch * tokens_per_seq, num_q_heads, max_seq_len);
 }
 

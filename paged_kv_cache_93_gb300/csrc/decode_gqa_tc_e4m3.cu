@@ -123,23 +123,36 @@ __device__ __forceinline__ uint32_t swz8(int row, int col) {
 }
 
 struct Item {
-    int b, g, s;
+    int b, g, s, hg;
     int64_t len, begin, end;
     int ntiles;
 };
 
-// Split s of (b, g) covers tokens [s C, min(L, (s + 1) C)), C = 64 ceil(L / 64 S).
-__device__ __forceinline__ Item fp8_item(const DecodeArgs &a, int item, bool report) {
+// Head groups of R rows per (sequence, KV head): 1, or 2 for a 32-row group
+// (G x T = 32) taken as two items of 16.
+template <int R>
+__device__ __forceinline__ int head_groups(const DecodeArgs &a) {
+    if constexpr (R < 16) return 1;   // 4 and 8 rows: the whole group
+    else return a.num_q_heads / a.cache.num_kv_heads * a.q_tokens / R;
+}
+
+// item = ((b * Hkv + g) * S + s) * HG + hg, the head group fastest (the two
+// groups of a chunk read the same tiles together).  Split s of (b, g) covers
+// tokens [s C, min(L, (s + 1) C)), C = 64 ceil(L / 64 S).
+__device__ __forceinline__ Item fp8_item(const DecodeArgs &a, int item, int HG, bool report) {
     Item r;
-    r.s = item % a.num_splits;
-    const int t = item / a.num_splits;
+    r.hg = item % HG;
+    const int t0 = item / HG;
+    r.s = t0 % a.num_splits;
+    const int t = t0 / a.num_splits;
     r.g = t % a.cache.num_kv_heads;
     r.b = t / a.cache.num_kv_heads;
     int64_t L = a.seq_lens[r.b];
+    report = report && r.s == 0 && r.hg == 0;
     if (L < 0 || L > int64_t(a.max_blocks) * a.cache.block_size) {
-        if (report && r.s == 0) raise_status(a.status, PKV_DEV_SEQ_LEN);
+        if (report) raise_status(a.status, PKV_DEV_SEQ_LEN);
         L = 0;
-    } else if (L < a.q_tokens && report && r.s == 0) {
+    } else if (L < a.q_tokens && report) {
         raise_status(a.status, PKV_DEV_SEQ_LEN);
     }
     const int64_t chunk = 64 * ((L + 64LL * a.num_splits - 1) / (64LL * a.num_splits));
@@ -170,7 +183,7 @@ decode_gqa_tc_e4m3_kernel(const __grid_constant__ CUtensorMap tmap_k,
     auto bar = [&](int i) { return sb + 8u * uint32_t(i); };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int num_items = a.batch * a.cache.num_kv_heads * a.num_splits;
+    const int num_items = a.batch * a.cache.num_kv_heads * a.num_splits * head_groups<R>(a);
     const int bs = a.cache.block_size, hkv = a.cache.num_kv_heads;
     const int box = bs < kM ? bs : kM;                 // rows per TMA box (one block or less)
 
@@ -213,7 +226,7 @@ decode_gqa_tc_e4m3_kernel(const __grid_constant__ CUtensorMap tmap_k,
         bool ok = true;
         const int nbox = kM / box;                     // boxes per tile (<= 8)
         for (int item = blockIdx.x; item < num_items && ok; item += gridDim.x) {
-            const Item r = fp8_item(a, item, false);
+            const Item r = fp8_item(a, item, head_groups<R>(a), false);
             if (r.ntiles == 0) continue;
             const int32_t *table = a.block_tables + int64_t(r.b) * a.max_blocks;
             // Rows of block 0 of this KV head stand in for boxes past the end
@@ -281,7 +294,7 @@ decode_gqa_tc_e4m3_kernel(const __grid_constant__ CUtensorMap tmap_k,
             }
         };
         for (int item = blockIdx.x; item < num_items && ok; item += gridDim.x) {
-            const Item r = fp8_item(a, item, false);
+            const Item r = fp8_item(a, item, head_groups<R>(a), false);
             if (r.ntiles == 0) continue;
             if (!(ok = wait_all(bar(kBarQFull), ne & 1u))) break;
             for (int i = 0; i <= r.ntiles && ok; ++i) {
@@ -365,16 +378,18 @@ decode_gqa_tc_e4m3_kernel(const __grid_constant__ CUtensorMap tmap_k,
             return pipe_wait(bar(kBarPvDone + (j & 1u)), (j >> 1) & 1u, a.status, abort_flag);
         };
         // The R rows of an item are T query tokens x Gr heads: row h is query
-        // token h / Gr of sequence b, head g Gr + h % Gr (T = 1: the group).
+        // token h / Gr of sequence b, head g G + hg Gr + h % Gr (T = 1, one
+        // head group: the group).
         // (T, Gr and the shift are re-read from the parameters where used:
         // kept live across the tile loop they cost registers)
         auto gr_shift = [&]() { return __ffs(R / a.q_tokens) - 1; };
         for (int item = blockIdx.x; item < num_items; item += gridDim.x) {
-            const Item r = fp8_item(a, item, t == 0);
+            const Item r = fp8_item(a, item, head_groups<R>(a), t == 0);
             auto row_of = [&](int h) -> int64_t {
                 const int sh = gr_shift(), Gr = R / a.q_tokens;
+                const int G = a.num_q_heads / a.cache.num_kv_heads;
                 return (int64_t(r.b) * a.q_tokens + (h >> sh)) * a.num_q_heads +
-                       int64_t(r.g) * Gr + (h & (Gr - 1));
+                       int64_t(r.g) * G + r.hg * Gr + (h & (Gr - 1));
             };
             const int64_t split0 = int64_t(r.s) * a.batch * a.q_tokens * a.num_q_heads;
             if (r.ntiles == 0) {
@@ -657,7 +672,8 @@ int launch_rows(const DecodeArgs &a) {
     }
     // kCtas CTAs per SM by construction (shared memory, registers and TMEM
     // columns are sized for it); the persistent loop is correct for any grid.
-    const int64_t items = int64_t(a.batch) * a.cache.num_kv_heads * a.num_splits;
+    const int64_t items = int64_t(a.batch) * a.cache.num_kv_heads * a.num_splits *
+                          (a.num_q_heads / a.cache.num_kv_heads * a.q_tokens / R);
     const int grid = int(std::min<int64_t>(items, int64_t(sm_count()) * CTAS));
     if (grid <= 0) return PKV_OK;
     return launch_pdl(kernel, dim3(grid), dim3(kThreads), S::kSmemBytes, a.stream, tk, tv, a);
@@ -674,9 +690,11 @@ bool gqa_tc_e4m3_kernel_supports(const pkv_cache_desc &c, int32_t num_q_heads,
     const bool pow2_bs = c.block_size >= 16 && c.block_size <= 256 &&
                          (c.block_size & (c.block_size - 1)) == 0;
     const int64_t rows = int64_t(c.num_blocks) * c.num_kv_heads * c.block_size;
-    return (G == 4 || G == 8 || G == 16) && c.head_dim_k == kD && c.head_dim_v == kD && pow2_bs &&
+    return (G == 4 || G == 8 || G == 16 || G == 32) && c.head_dim_k == kD && c.head_dim_v == kD && pow2_bs &&
            rows < (int64_t(1) << 31) - 1;
 }
+
+int gqa_tc_e4m3_head_groups(int32_t group) { return group == 32 ? 2 : 1; }
 
 int gqa_tc_e4m3_resident_ctas(int32_t group) {
     return sm_count() * (group == 4 ? PKV_E4M3_R4_CTAS : group == 8 ? PKV_E4M3_R8_CTAS : 2);
@@ -686,7 +704,8 @@ int launch_decode_gqa_tc_e4m3(const DecodeArgs &a) {
     switch (a.num_q_heads / a.cache.num_kv_heads * a.q_tokens) {
         case 4: return launch_rows<4, PKV_E4M3_R4_RING, PKV_E4M3_R4_CTAS>(a);
         case 8: return launch_rows<8, PKV_E4M3_R8_RING, PKV_E4M3_R8_CTAS>(a);
-        case 16: return launch_rows<16, 5, 2>(a);
+        case 16:
+        case 32: return launch_rows<16, 5, 2>(a);   // 32 rows: two head groups of 16
         default: return PKV_ERR_SHAPE;
     }
 }

@@ -76,13 +76,16 @@ int launch_decode_gqa_tc(const DecodeArgs &a);
 int gqa_tc_resident_ctas();
 // (sequence, KV head) items split into this many head groups of 16 rows
 int gqa_tc_head_groups(const pkv_cache_desc &c, int32_t num_q_heads, int32_t q_tokens);
-// E4M3 pools, query groups of 4, 8 or 16, head dims 128: the tcgen05 kernel
-// with E4M3 operands.
+// E4M3 pools, 4, 8, 16 or 32 rows per KV head (query group x query tokens;
+// 32 as two head groups of 16), head dims 128: the tcgen05 kernel with E4M3
+// operands.
 bool gqa_tc_e4m3_kernel_supports(const pkv_cache_desc &c, int32_t num_q_heads,
                                   int32_t q_tokens = 1);
 // CTAs that kernel keeps resident for `group` rows per item (query group x
 // query tokens).
 int gqa_tc_e4m3_resident_ctas(int32_t group);
+// Items per (sequence, KV head, split) for `group` rows: 2 at 32, else 1.
+int gqa_tc_e4m3_head_groups(int32_t group);
 int launch_decode_gqa_tc_e4m3(const DecodeArgs &a);
 int launch_decode_tma(const DecodeArgs &a);
 // Large query groups (G a multiple of 32, e.g. MLA-shaped 128 heads over one

@@ -62,6 +62,7 @@ SHAPES = [
     ([600, 65], 64, 4, 64),
     ([700, 5, 130], 8, 2, 128),
     ([200, 1], 16, 1, 256),
+    ([250, 3, 90], 64, 2, 16),             # group 32: two head groups of 16
 ]
 
 
@@ -292,6 +293,8 @@ MULTI_SHAPES = [
     ([90, 12, 200], 2, 16, 4, 128, 128, 32),
     ([150, 33], 2, 8, 4, 128, 128, 16),
     ([70, 4], 4, 4, 4, 128, 128, 64),
+    ([150, 40], 4, 16, 2, 128, 128, 16),      # 8 heads x 4 tokens: two head groups
+    ([80, 300], 2, 32, 2, 128, 128, 32),      # 16 heads x 2 tokens: two head groups
     ([200, 3], 3, 16, 1, 128, 128, 64),
     ([77, 5], 2, 8, 4, 64, 64, 8),
     ([60, 9], 2, 16, 1, 576, 512, 64),
