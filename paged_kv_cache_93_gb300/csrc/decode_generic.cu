@@ -5,6 +5,8 @@
 // head dimension into 16-byte bf16 vectors; each token's score is a warp
 // reduction, and the online softmax (running max m, running sum l, rescaled
 // accumulator) runs in base 2 with the query pre-multiplied by scale*log2(e).
+// A warp takes kU tokens per step -- their K rows loaded together, then their
+// V rows -- so kU row loads are in flight instead of one.
 // It handles any head dims (multiples of 8 up to 1024), any query group and
 // any block size; the TMA + tensor-core kernel covers the common GQA shapes.
 // With E4 set the pools hold E4M3 codes (8 bytes per 8 elements, decoded
@@ -14,6 +16,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "pkv.h"
 #include "pkv_device.cuh"
@@ -25,6 +28,7 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kGenericWarps = 4;
+constexpr int kU = 4;                   // tokens per step of a warp
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -47,15 +51,16 @@ __device__ __forceinline__ void unpack8_e4m3(const uint2 &u, float (&f)[8]) {
     f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
 }
 
-// Elements 8v .. 8v+7 of row `row` of a pool whose rows hold `n8` groups of 8.
+// Elements 8v .. 8v+7 of row `row` of a pool whose rows hold `n8` groups of 8,
+// as stored (16 bytes of bf16 or 8 bytes of E4M3 codes), and their values.
 template <bool E4>
-__device__ __forceinline__ void load8(const void *pool, int64_t row, int n8, int v,
-                                      float (&f)[8]) {
-    if constexpr (E4)
-        unpack8_e4m3(static_cast<const uint2 *>(pool)[row * n8 + v], f);
-    else
-        unpack8(static_cast<const uint4 *>(pool)[row * n8 + v], f);
+using Raw8 = typename std::conditional<E4, uint2, uint4>::type;
+template <bool E4>
+__device__ __forceinline__ Raw8<E4> load_raw8(const void *pool, int64_t row, int n8, int v) {
+    return static_cast<const Raw8<E4> *>(pool)[row * n8 + v];
 }
+__device__ __forceinline__ void unpack8_any(const uint4 &u, float (&f)[8]) { unpack8(u, f); }
+__device__ __forceinline__ void unpack8_any(const uint2 &u, float (&f)[8]) { unpack8_e4m3(u, f); }
 
 // KC / VC: 8-element groups per lane for K and V (ceil(dim / 8 / 32)).
 template <int KC, int VC, bool E4>
@@ -101,36 +106,76 @@ decode_generic_kernel(DecodeArgs a) {
 
     const int32_t *table = a.block_tables + int64_t(b) * a.max_blocks;
     const int vs = a.v_stride / 8;          // 8-element groups from one V row to the next
-    for (int64_t j = begin; j < end; ++j) {
-        const int32_t phys = table[j / c.block_size];
-        const bool ok = phys >= 0 && phys < c.num_blocks;
-        if (!ok && lane == 0 && (h % group) == 0) raise_status(a.status, PKV_DEV_BLOCK_ID);
-        const int64_t row = (int64_t(ok ? phys : 0) * c.num_kv_heads + g) * c.block_size +
-                            j % c.block_size;
-        float part = 0.f;
+    for (int64_t j0 = begin; j0 < end; j0 += kU) {
+        // tokens j0 .. j0 + kU - 1; those at or past `end` score -inf.  A
+        // block id out of range is flagged and its token reads as zeros.
+        int64_t row[kU];
+        bool live[kU], ok[kU];
 #pragma unroll
-        for (int i = 0; i < KC; ++i) {
-            const int v = lane + 32 * i;
-            if (v < nk && ok) {
+        for (int u = 0; u < kU; ++u) {
+            const int64_t j = j0 + u;
+            live[u] = j < end;
+            const int32_t phys = live[u] ? table[j / c.block_size] : 0;
+            ok[u] = live[u] && phys >= 0 && phys < c.num_blocks;
+            if (live[u] && !ok[u] && lane == 0 && (h % group) == 0)
+                raise_status(a.status, PKV_DEV_BLOCK_ID);
+            row[u] = (int64_t(ok[u] ? phys : 0) * c.num_kv_heads + g) * c.block_size +
+                     j % c.block_size;
+        }
+        Raw8<E4> kr[kU][KC];
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+#pragma unroll
+            for (int i = 0; i < KC; ++i) {
+                const int v = lane + 32 * i;
+                kr[u][i] = v < nk && ok[u] ? load_raw8<E4>(a.k_pool, row[u], nk, v) : Raw8<E4>{};
+            }
+        float sc[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            float part = 0.f;
+#pragma unroll
+            for (int i = 0; i < KC; ++i) {
                 float kf[8];
-                load8<E4>(a.k_pool, row, nk, v, kf);
+                unpack8_any(kr[u][i], kf);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) part = fmaf(qv[i][e], kf[e], part);
             }
+            sc[u] = part;
         }
-        const float s = warp_sum(part);
-        const float m_new = fmaxf(m, s);
+#pragma unroll
+        for (int u = 0; u < kU; ++u) sc[u] = live[u] ? warp_sum(sc[u]) : -INFINITY;
+        float m_new = m;
+#pragma unroll
+        for (int u = 0; u < kU; ++u) m_new = fmaxf(m_new, sc[u]);
         const float corr = exp2f(m - m_new);
-        const float p = exp2f(s - m_new);
-        l = l * corr + p;
+        float p[kU], psum = 0.f;
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            p[u] = exp2f(sc[u] - m_new);
+            psum += p[u];
+        }
+        l = l * corr + psum;
         m = m_new;
+        Raw8<E4> vr[kU][VC];
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+#pragma unroll
+            for (int i = 0; i < VC; ++i) {
+                const int v = lane + 32 * i;
+                vr[u][i] = v < nv && ok[u] ? load_raw8<E4>(a.v_pool, row[u], vs, v) : Raw8<E4>{};
+            }
 #pragma unroll
         for (int i = 0; i < VC; ++i) {
-            const int v = lane + 32 * i;
-            float vf[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-            if (v < nv && ok) load8<E4>(a.v_pool, row, vs, v, vf);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc[i][e] = fmaf(p, vf[e], acc[i][e] * corr);
+            for (int e = 0; e < 8; ++e) acc[i][e] *= corr;
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                float vf[8];
+                unpack8_any(vr[u][i], vf);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[i][e] = fmaf(p[u], vf[e], acc[i][e]);
+            }
         }
     }
 
