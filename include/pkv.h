@@ -228,8 +228,9 @@ int64_t pkv_interleave_partition_len(int64_t num_tokens, int32_t num_parts,
  * groups that are a multiple of 32 (head dims multiples of 64, head_dim_v
  * <= 512, power-of-two block sizes >= 32) the warp-level-MMA large-group
  * kernel; the generic CUDA-core kernel otherwise.  PKV_DECODE_GENERIC forces
- * the generic kernel.  Query groups of 16 (or 16 rows of heads x query
- * tokens in pkv_paged_decode_attn_multi) with head dims 128 and power-of-two
+ * the generic kernel.  Query groups of 16 or 32 (or 16 or 32 rows of heads x
+ * query tokens in pkv_paged_decode_attn_multi; 32 as two work items of 16
+ * heads' rows that read the same tiles) with head dims 128 and power-of-two
  * block sizes >= 16 run on a tcgen05 form of the GQA kernel.
  * PKV_DECODE_NO_TCGEN05 passes over both tcgen05 kernels (the warp-level-MMA
  * kernels take their shapes).
@@ -290,8 +291,9 @@ int pkv_paged_decode_attn_noalloc(const pkv_cache_desc *cache, const float *q, i
  * FP8 cache above): K_j = value(k code) * k_scale[g] and V_j = value(v code)
  * * v_scale[g]; q, out, lse, splits, workspace (pkv_decode_workspace_size)
  * and the status bits as pkv_paged_decode_attn; shapes as there.  Head
- * dims 128 with query groups of 4, 8 or 16 and power-of-two block sizes
- * 16..256 run on the tcgen05 tensor cores with E4M3 operands: the fp32 query
+ * dims 128 with query groups of 4, 8, 16 or 32 (32 as two work items of 16
+ * rows) and power-of-two block sizes 16..256 run on the tcgen05 tensor cores
+ * with E4M3 operands: the fp32 query
  * is carried as four E4M3 terms and the probabilities as five, each term the
  * rounding residual of the one before scaled by 16, so both keep about 16
  * significant bits and the result is fp32-accurate attention on the stored
@@ -334,10 +336,12 @@ int pkv_paged_decode_attn_noalloc_e4m3(const pkv_cache_desc *cache, const float 
  * lse [batch][T][num_q_heads], fp32.  1 <= T <= 64.  A sequence holding fewer
  * than T tokens sets PKV_DEV_SEQ_LEN and its rows with no token give out = 0,
  * lse = -inf.  Splits, kernels and flags as for pkv_paged_decode_attn
- * (num_splits = 0: pkv_decode_multi_auto_splits).  When the GQA TMA kernel
- * takes the shape with G * T <= 16 rows per KV head (G = num_q_heads /
- * num_kv_heads), the T tokens are extra rows of one work item and each K/V
- * tile is read once; otherwise every (sequence, token) is attended as its own
+ * (num_splits = 0: pkv_decode_multi_auto_splits).  When a GQA kernel takes
+ * the shape with G * T rows per KV head (G = num_q_heads / num_kv_heads) --
+ * the tcgen05 one at head dims 128 and G * T of 16 or 32 (32 as two work
+ * items of 16 rows; not with PKV_DECODE_NO_TCGEN05), the TMA one at
+ * G * T <= 16 -- the T tokens are extra rows of one work item and each K/V
+ * tile is read once (twice from L2 at 32 rows); otherwise every (sequence, token) is attended as its own
  * row.  workspace: at least
  * pkv_decode_multi_workspace_size(...) bytes (never 0: it holds the T
  * per-token views of the block tables); contents on entry do not matter.
@@ -364,8 +368,8 @@ int pkv_paged_decode_attn_multi(const pkv_cache_desc *cache, const float *q, int
  * PKV_DEV_SEQ_LEN rule and the workspace (pkv_decode_multi_workspace_size)
  * as pkv_paged_decode_attn_multi; K_j, V_j, k_scale, v_scale and flags as
  * pkv_paged_decode_attn_e4m3.  With flags 0, head dims 128, power-of-two
- * block sizes 16..256 and G * T in {4, 8, 16} (G = num_q_heads /
- * num_kv_heads), the tcgen05 E4M3 kernel takes the T tokens as rows of one
+ * block sizes 16..256 and G * T in {4, 8, 16, 32} (G = num_q_heads /
+ * num_kv_heads; 32 as two work items of 16 rows), the tcgen05 E4M3 kernel takes the T tokens as rows of one
  * work item (causal limits per row) and each tile is read once; otherwise
  * every (sequence, token) is attended as its own row over a per-token view
  * of its table row.  num_splits = 0: pkv_decode_multi_auto_splits_e4m3. */
