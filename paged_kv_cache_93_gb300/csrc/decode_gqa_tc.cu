@@ -43,6 +43,7 @@
 
 #include "pkv.h"
 #include "pkv_device.cuh"
+#include "pkv_math.cuh"
 #include "pkv_host.h"
 #include "pkv_pipeline.cuh"
 #include "pkv_tcgen05.cuh"
@@ -545,7 +546,7 @@ decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 float p[kRows];
 #pragma unroll
                 for (int h = 0; h < kRows; ++h) {
-                    p[h] = x[h] == -INFINITY ? 0.f : exp2f(x[h] - mrow[h]);
+                    p[h] = x[h] == -INFINITY ? 0.f : ex2_approx(x[h] - mrow[h]);
                     l_part[h] += p[h];
                 }
                 // this P buffer was last read by the value MMAs of tile pcount-2

@@ -47,6 +47,7 @@
 
 #include "pkv.h"
 #include "pkv_device.cuh"
+#include "pkv_math.cuh"
 #include "pkv_host.h"
 #include "pkv_pipeline.cuh"
 #include "pkv_tcgen05.cuh"
@@ -569,7 +570,7 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                             const float2 m2 = *reinterpret_cast<const float2 *>(mrow + h);
                             const float x0 = valid ? __uint_as_float(v[k]) : -INFINITY;
                             const float x1 = valid ? __uint_as_float(v[k + 1]) : -INFINITY;
-                            const float p0 = exp2f(x0 - m2.x), p1 = exp2f(x1 - m2.y);
+                            const float p0 = ex2_approx(x0 - m2.x), p1 = ex2_approx(x1 - m2.y);
                             l_part[h] += p0;
                             l_part[h + 1] += p1;
                             hi[e] = pack_bf16x2(p0, p1);
