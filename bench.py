@@ -48,7 +48,7 @@ FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
 # sources that kernel is built from (the summary's traffic counts only while
 # their hash matches).
 PROFILES = {
-    "long32k": ("decode_tma_long32k.txt", ("decode_tma.cu", "pkv_device.cuh")),
+    "long32k": ("decode_tma_long32k.txt", ("decode_tma.cu", "pkv_device.cuh", "pkv_math.cuh")),
     "spec4_32k": ("decode_gqa_tc_spec4_32k.txt",
                   ("decode_gqa_tc.cu", "pkv_device.cuh", "pkv_tcgen05.cuh", "pkv_pipeline.cuh",
                    "pkv_math.cuh")),

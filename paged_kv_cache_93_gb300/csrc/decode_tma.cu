@@ -40,6 +40,7 @@
 
 #include "pkv.h"
 #include "pkv_device.cuh"
+#include "pkv_math.cuh"
 #include "pkv_host.h"
 
 namespace pkv {
@@ -433,9 +434,9 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
                     const float m_new = fmaxf(m2[j], mx);
                     const float m_use = m_new == -INFINITY ? 0.f : m_new;
-                    alpha[j] = exp2f(m2[j] - m_use);
-                    p[0][j] = exp2f(s[0][j] - m_use);
-                    p[1][j] = exp2f(s[1][j] - m_use);
+                    alpha[j] = ex2_approx(m2[j] - m_use);
+                    p[0][j] = ex2_approx(s[0][j] - m_use);
+                    p[1][j] = ex2_approx(s[1][j] - m_use);
                     l2[j] = l2[j] * alpha[j] + p[0][j] + p[1][j];
                     m2[j] = m_new;
                 }
