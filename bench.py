@@ -527,7 +527,7 @@ class MultiE4m3Step(E4m3Step):
 STEPS = {"long32k": Step, "mix": Step, "tiny": Step, "dcp200k": DcpStep, "agent_mla": AgentStep,
          "agent_mla_latent": AgentStep, "spec4_32k": MultiStep, "long32k_e4m3": E4m3Step,
          "dcp200k_e4m3": DcpE4m3Step, "spec4_32k_e4m3": MultiE4m3Step}
-DEFAULT_SPLITS = {"long32k": 16, "mix": 1, "tiny": 1, "dcp200k": 19, "agent_mla": 19,
+DEFAULT_SPLITS = {"long32k": 9, "mix": 1, "tiny": 1, "dcp200k": 19, "agent_mla": 19,
                   "agent_mla_latent": 19, "spec4_32k": 9, "long32k_e4m3": 7,
                   "dcp200k_e4m3": 14, "spec4_32k_e4m3": 9}
 

@@ -37,8 +37,8 @@ int validate_decode(const pkv_cache_desc *c, const float *q, int32_t batch, int3
     return PKV_OK;
 }
 
-// The tcgen05 GQA kernels' resident CTAs take the (sequence, KV head
-// [, head group], split) items in turn, an item costing its 128-token tiles
+// The persistent GQA kernels' resident CTAs (tcgen05 and warp-level) take
+// the (sequence, KV head [, head group], split) items in turn, an item costing its 128-token tiles
 // plus about one tile of start-up.  Pick S for the least rounds x (tiles + 1)
 // on sequences of the longest length; a tie goes to fewer splits (less to
 // merge).
@@ -65,6 +65,11 @@ int32_t auto_splits(const pkv_cache_desc &c, int32_t batch, int32_t num_q_heads,
     if (gqa_tc_kernel_supports(c, num_q_heads, q_tokens))
         return tc_splits(c, batch, max_seq_len, gqa_tc_resident_ctas(),
                          gqa_tc_head_groups(c, num_q_heads, q_tokens));
+    // The warp-level GQA kernel is a persistent grid too: an item count just
+    // past its resident CTAs costs a second round (8 x 32K, 4 heads per KV
+    // head: 10 splits 201 us, 8 splits 161 us).
+    if (tma_kernel_supports(c, num_q_heads, q_tokens))
+        return tc_splits(c, batch, max_seq_len, tma_resident_ctas(c, num_q_heads, q_tokens));
     // Enough (sequence, KV head [, head block], split) items for ~4 per SM
     // (8 for the tcgen05 kernel), each item at least 512 tokens long.
     int64_t units = int64_t(batch) * c.num_kv_heads;

@@ -716,6 +716,14 @@ bool tma_kernel_supports(const pkv_cache_desc &c, int32_t num_q_heads, int32_t q
 // four times G = 4's warp-level MMAs per byte: one CTA of four consumer warps
 // and four stages per SM was fastest (8 x 32K, 128/8 heads: 300 us against
 // 361 us for two 2-warp CTAs and 513-570 us for three CTAs per SM).
+int tma_resident_ctas(const pkv_cache_desc &c, int32_t num_q_heads, int32_t q_tokens) {
+    const int G = num_q_heads / c.num_kv_heads * q_tokens;
+    int per_sm = c.head_dim_k == 128 ? (G == 16 ? PKV_TMA_D128G16_B : G == 8 ? PKV_TMA_D128G8_B
+                                                                             : PKV_TMA_D128_B)
+                                     : (G == 16 ? PKV_TMA_D64G16_B : PKV_TMA_D64_B);
+    return sm_count() * per_sm;
+}
+
 int launch_decode_tma(const DecodeArgs &a) {
     const int G = a.num_q_heads / a.cache.num_kv_heads * a.q_tokens;   // rows per work item
     if (a.cache.head_dim_k == 128) {

@@ -68,6 +68,8 @@ struct DecodeArgs {
     const float *k_scale = nullptr, *v_scale = nullptr;
 };
 bool tma_kernel_supports(const pkv_cache_desc &c, int32_t num_q_heads, int32_t q_tokens = 1);
+// CTAs the warp-level GQA kernel keeps resident for the shape (one persistent grid).
+int tma_resident_ctas(const pkv_cache_desc &c, int32_t num_q_heads, int32_t q_tokens = 1);
 // 16 or 32 query rows per KV head (heads x query tokens; 32 as two head
 // groups of 16), head dims 128: the tcgen05 form of the GQA kernel.
 bool gqa_tc_kernel_supports(const pkv_cache_desc &c, int32_t num_q_heads, int32_t q_tokens);
