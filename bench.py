@@ -8,6 +8,13 @@ with lse_merge.  One step = slot mapping + kv_append of the 8 decode tokens
 pkv_paged_decode_attn makes), with the KV cache resident in HBM.  Steps run
 back to back: the 1.07 GB of KV a step reads is 8x the 129 MB L2, so no
 flush is needed between them (a flush would add its own write-back traffic).
+The same step at the split count the library chooses itself (num_splits = 0)
+is timed as well and reported as `library_auto_splits`.
+
+Besides the mean over the timed steps, the line carries per-step CUDA-event
+times (median, min, mean; `ms_per_step_events`), the same step with L2
+evicted before every repetition (`cold_l2`), and the oracle on one host core
+(`cpu_baseline.single_thread`) for the four GQA workloads.
 
 Other workloads (--workload): `dcp200k` (one 200,000-token sequence split
 into 4 interleaved partitions, each attended separately and merged) and
@@ -527,9 +534,17 @@ class MultiE4m3Step(E4m3Step):
 STEPS = {"long32k": Step, "mix": Step, "tiny": Step, "dcp200k": DcpStep, "agent_mla": AgentStep,
          "agent_mla_latent": AgentStep, "spec4_32k": MultiStep, "long32k_e4m3": E4m3Step,
          "dcp200k_e4m3": DcpE4m3Step, "spec4_32k_e4m3": MultiE4m3Step}
-DEFAULT_SPLITS = {"long32k": 9, "mix": 1, "tiny": 1, "dcp200k": 19, "agent_mla": 19,
+# The 32K workload is timed at 16 splits, the split count its configuration
+# names; the split count the library picks by itself (num_splits = 0) is
+# timed too and reported beside it (`library_auto_splits`).
+DEFAULT_SPLITS = {"long32k": 16, "mix": 1, "tiny": 1, "dcp200k": 19, "agent_mla": 19,
                   "agent_mla_latent": 19, "spec4_32k": 9, "long32k_e4m3": 7,
                   "dcp200k_e4m3": 14, "spec4_32k_e4m3": 9}
+# Workloads whose line also carries the library's own split choice.
+AUTO_SPLITS_ALSO = ("long32k",)
+# Workloads of the single-threaded oracle figure (the four GQA configurations)
+# and the tokens per sequence of its sample (None = every token).
+SINGLE_THREAD_SAMPLE = {"tiny": None, "mix": None, "long32k": 8192, "dcp200k": 32768}
 
 
 # ------------------------------------------------------------------ arms
@@ -564,9 +579,10 @@ def max_over_ranks(x: float, world: int) -> float:
     return float(t.item())
 
 
-def oracle_gbs(w, tokens: int | None, repeats: int = 1):
-    """Time the CPU oracle (all host cores) over every row of `w`, restricted
-    to the first `tokens` tokens of each sequence when given."""
+def oracle_gbs(w, tokens: int | None, repeats: int = 1, num_threads: int = 0):
+    """Time the CPU oracle over every row of `w`, restricted to the first
+    `tokens` tokens of each sequence when given; `num_threads` 0 = all host
+    cores."""
     import oracle
     q, bt, lens = w.q.numpy(), w.block_tables.numpy(), w.seq_lens.numpy()
     if w.k_codes is not None:
@@ -590,16 +606,19 @@ def oracle_gbs(w, tokens: int | None, repeats: int = 1):
                           dtype=np.int32)
             oracle.paged_decode_attn_e4m3(q.reshape(B * T, *q.shape[2:]), kp, vp,
                                           w.k_scale.numpy(), w.v_scale.numpy(),
-                                          np.repeat(bt, T, axis=0), rl, w.scale)
+                                          np.repeat(bt, T, axis=0), rl, w.scale,
+                                          num_threads=num_threads)
         elif w.k_codes is not None:
             oracle.paged_decode_attn_e4m3(q, kp, vp, w.k_scale.numpy(), w.v_scale.numpy(), bt,
-                                          lens, w.scale, tok_end=end)
+                                          lens, w.scale, tok_end=end, num_threads=num_threads)
         elif w.tokens_per_seq > 1:
             # the same step on each sequence's first tokens: query t sees the
             # sample's tokens up to its own
-            oracle.paged_decode_attn_multi(q, kp, vp, bt, lens if end is None else end, w.scale)
+            oracle.paged_decode_attn_multi(q, kp, vp, bt, lens if end is None else end, w.scale,
+                                           num_threads=num_threads)
         else:
-            oracle.paged_decode_attn(q, kp, vp, bt, lens, w.scale, tok_end=end)
+            oracle.paged_decode_attn(q, kp, vp, bt, lens, w.scale, tok_end=end,
+                                     num_threads=num_threads)
         times.append(time.perf_counter() - t)
     return used, times
 
@@ -668,23 +687,29 @@ def staged(dev, tensors):
     return host, devb, views
 
 
-def run_gpu(args, world, rank, local):
-    import paged_kv_cache_93_gb300 as pkv
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    w = workloads.make(args.workload)
-    splits = args.splits or DEFAULT_SPLITS[args.workload]
-    st = STEPS[args.workload](pkv, w, dev, splits)
-    total_bytes, kernel_bytes = step_bytes(w, splits)
-    stream = torch.cuda.current_stream()
+def _events(n):
+    return [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(n)]
 
+
+def _stats(ms_list):
+    return {"mean": round(statistics.fmean(ms_list), 5),
+            "median": round(statistics.median(ms_list), 5), "min": round(min(ms_list), 5),
+            "n": len(ms_list)}
+
+
+def time_step(pkv, st, args, world, stream, sampler=None):
+    """Warm-up, then K steps replayed from a CUDA graph (the headline timing),
+    then the same K steps one by one with CUDA events around every step and
+    around its split attention kernel, then the split kernel alone back to
+    back.  Returns the figures as a dict (times in ms, max over ranks)."""
     for _ in range(args.warmup):
         st.run()
     torch.cuda.synchronize()
     if pkv.device_status(reset=True) != 0:
         raise RuntimeError("device status word set during warm-up")
 
-    # One step captured in a CUDA graph (the library's calls allocate nothing
+    # Steps captured in a CUDA graph (the library's calls allocate nothing
     # and never synchronise with the host, so they capture as they are); the
     # timed steps replay it, as a serving loop replays its decode step.
     graph = None
@@ -713,7 +738,6 @@ def run_gpu(args, world, rank, local):
     K = args.steps
     ev_start = torch.cuda.Event(enable_timing=True)
     ev_end = torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
         sampler.wait_ready()
     barrier(world)
@@ -739,17 +763,21 @@ def run_gpu(args, world, rank, local):
         raise RuntimeError("device status word set during the timed steps")
     ms = max_over_ranks(ev_start.elapsed_time(ev_end) / K, world)
 
-    # ---- the same K steps again, with events around the split attention
-    # kernel of every step: its average launch duration (for the roofline)
-    ev_k = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in range(K)]
+    # ---- the same K steps again, one by one, with events around every step
+    # and around its split attention kernel (the kernel's average launch
+    # duration is the roofline's; the step events give the per-step spread)
+    ev_k, ev_s = _events(K), _events(K)
     barrier(world)
     torch.cuda.synchronize()
     for i in range(K):
+        ev_s[i][0].record(stream)
         st.run(*ev_k[i])
+        ev_s[i][1].record(stream)
     torch.cuda.synchronize()
     barrier(world)
-    kms = max_over_ranks(statistics.fmean(a.elapsed_time(b) for a, b in ev_k), world)
+    kern = [a.elapsed_time(b) for a, b in ev_k]
+    steps = [a.elapsed_time(b) for a, b in ev_s]
+    kms = max_over_ranks(statistics.fmean(kern), world)
 
     # ---- the split kernel alone, launched back to back (context only)
     torch.cuda.synchronize()
@@ -761,10 +789,76 @@ def run_gpu(args, world, rank, local):
     b_ev.record(stream)
     torch.cuda.synchronize()
     kms_b2b = a_ev.elapsed_time(b_ev) / kb
+    if pkv.device_status(reset=True) != 0:
+        raise RuntimeError("device status word set")
+    return {"ms": ms, "kms": kms, "kms_b2b": kms_b2b, "eager_ms": eager_ms, "eager_steps": ke,
+            "graph": graph is not None, "per_graph": per_graph, "clocks": clocks,
+            "step_events": _stats(steps), "kernel_events": _stats(kern)}
+
+
+def time_cold_l2(pkv, st, reps, stream):
+    """One step captured in a CUDA graph, replayed `reps` times, each replay
+    preceded by a read of a 256 MiB buffer that evicts the 129 MB L2 (a read
+    leaves no dirty lines to write back during the step) and bracketed by
+    CUDA events: the step with nothing of its data in L2."""
+    flush = torch.empty(64 << 20, dtype=torch.float32, device=st.q.device).fill_(1.0)
+    sink = torch.empty((), dtype=torch.float32, device=st.q.device)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        st.run()
+    g.replay()
+    torch.cuda.synchronize()
+    ev = _events(reps)
+    for a, b in ev:
+        torch.sum(flush, dim=0, out=sink)
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+    torch.cuda.synchronize()
+    if pkv.device_status(reset=True) != 0:
+        raise RuntimeError("device status word set during the cold-L2 steps")
+    del flush
+    return _stats([a.elapsed_time(b) for a, b in ev])
+
+
+def run_gpu(args, world, rank, local):
+    import paged_kv_cache_93_gb300 as pkv
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = workloads.make(args.workload)
+    splits = args.splits or DEFAULT_SPLITS[args.workload]
+    st = STEPS[args.workload](pkv, w, dev, splits)
+    total_bytes, kernel_bytes = step_bytes(w, splits)
+    stream = torch.cuda.current_stream()
+    K = args.steps
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    tm = time_step(pkv, st, args, world, stream, sampler)
+    ms, kms, kms_b2b, clocks = tm["ms"], tm["kms"], tm["kms_b2b"], tm["clocks"]
+    eager_ms, ke, per_graph = tm["eager_ms"], tm["eager_steps"], tm["per_graph"]
+    graph = tm["graph"] or None
+    cold = time_cold_l2(pkv, st, min(K, 200), stream)
+
+    # ---- the same step at the library's own split choice (num_splits = 0)
+    auto = None
+    if args.workload in AUTO_SPLITS_ALSO and not args.splits:
+        s_auto = pkv.decode_auto_splits(st.k, st.v, w.batch, w.num_q_heads,
+                                        w.block_tables.shape[1] * w.block_size)
+        st_a = STEPS[args.workload](pkv, w, dev, s_auto)
+        ta = time_step(pkv, st_a, args, world, stream)
+        tb, kb_ = step_bytes(w, s_auto)
+        auto = {"num_splits": s_auto, "ms_per_step": round(ta["ms"], 5),
+                "value": round(world * tb / (ta["ms"] * 1e-3) / 1e9, 2),
+                "launch_ms": round(ta["kms"], 5),
+                "kernel_gbs": round(kb_ / (ta["kms"] * 1e-3) / 1e9, 2),
+                "ms_per_step_events": ta["step_events"]}
+        del st_a
 
     value = world * total_bytes / (ms * 1e-3) / 1e9
     peak, peak_kind = load_peak()
     kernel_gbs = kernel_bytes / (kms * 1e-3) / 1e9
+    if auto is not None:
+        auto["frac"] = round(auto["kernel_gbs"] / peak, 4)
     if getattr(st, "bound", "hbm") == "tensor":
         # a math-bound launch inside seconds of back-to-back steps: the
         # sustained bf16 tensor throughput is the denominator
@@ -897,10 +991,21 @@ def run_gpu(args, world, rank, local):
     if rank != 0:
         return
 
-    # ---- CPU baseline: the oracle on this host's cores
+    # ---- CPU baseline: the oracle on this host's cores (all of them, and one)
     tokens = None if (args.workload in ("long32k", "mix", "tiny") and not args.quick_cpu) else 2048
     used, times = oracle_gbs(w, tokens, repeats=1)
     cpu_gbs = used / min(times) / 1e9
+    single = None
+    if args.workload in SINGLE_THREAD_SAMPLE:
+        t1_tokens = SINGLE_THREAD_SAMPLE[args.workload]
+        if args.quick_cpu and t1_tokens is not None:
+            t1_tokens = min(t1_tokens, 2048)
+        used1, times1 = oracle_gbs(w, t1_tokens, repeats=1, num_threads=1)
+        single = {"value": round(used1 / min(times1) / 1e9, 4), "unit": "GB/s", "cores": 1,
+                  "kind": "oracle",
+                  "sample": ("whole workload (every row, every token)" if t1_tokens is None else
+                             f"every row, first {t1_tokens} tokens of each sequence") +
+                            ", C fp64 oracle, one thread"}
     traffic = stored_traffic(args.workload)
     seq_tokens = int(w.seq_lens.sum())
     line = {
@@ -938,11 +1043,21 @@ def run_gpu(args, world, rank, local):
             "sample": ("whole workload (every row, every token)" if tokens is None else
                        f"every row, first {tokens} tokens of each sequence") +
                       ", C fp64 oracle, all host cores",
+            "single_thread": single,
         },
         "e2e": e2e,
+        "ms_per_step_events": dict(
+            tm["step_events"],
+            how="CUDA events around every step, the step's calls made one by one"),
+        "kernel_launch_ms_events": tm["kernel_events"],
+        "cold_l2": dict(cold, value=round(world * total_bytes / (cold["median"] * 1e-3) / 1e9, 2),
+                        how="one step replayed from a CUDA graph, each repetition after a "
+                            "read of a 256 MiB buffer that evicts the 129 MB L2; CUDA events "
+                            "around the step; value at the median"),
+        "library_auto_splits": auto,
         "eager": {"ms_per_step": round(eager_ms, 5),
                   "value": round(world * total_bytes / (eager_ms * 1e-3) / 1e9, 2),
-                  "steps": ke},
+                  "steps": tm["eager_steps"]},
         "gpu_launches": st.launches * K,
         "clocks": clocks,
     }

@@ -21,6 +21,11 @@
  *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
  *    default stream) and returns a pkv_status.  A nonzero status from the host
  *    checks means nothing was launched.
+ *  - Device addresses of the library's own device variables (the status
+ *    word, the scratch of the _noalloc calls) are looked up per CUDA context
+ *    and cached; a context destroyed and recreated under the same handle
+ *    (cudaDeviceReset) is not noticed, so do not use the library across a
+ *    device reset in one process.
  *  - Conditions only the device can see (a block id outside the pool, a slot
  *    out of range, a sequence longer than its table, overlapping copy pairs,
  *    a pipeline wait that gave up) never fault: the offending item is skipped
@@ -213,7 +218,9 @@ int64_t pkv_interleave_partition_len(int64_t num_tokens, int32_t num_parts,
  * C_b = 64 * ceil(seq_lens[b] / (64 * S)); each chunk's partial (out, lse) is
  * computed separately and the partials are merged exactly as pkv_lse_merge
  * does.  num_splits = 0 picks S from the batch, the heads and the SM count.
- * S must be <= 256.  The partials live in `workspace`, which must hold at
+ * S must be <= 256.  A chunk whose kernel gave up on a pipeline wait
+ * (PKV_DEV_TIMEOUT) is abandoned: its rows come back NaN, output and LSE, and
+ * the merge passes a NaN partial on as a NaN row.  The partials live in `workspace`, which must hold at
  * least pkv_decode_workspace_size(batch, num_q_heads, head_dim_v, S) bytes
  * (0 when S == 1; `workspace` may then be NULL).  Its contents on entry do
  * not matter.
@@ -237,6 +244,24 @@ int64_t pkv_interleave_partition_len(int64_t num_tokens, int32_t num_parts,
  * ------------------------------------------------------------------------- */
 #define PKV_DECODE_GENERIC 0x1
 #define PKV_DECODE_NO_TCGEN05 0x2
+
+/* ---------------------------------------------------------------------------
+ * Test control of the failure path (the pages have no counterpart; it exists
+ * so that the bounded pipeline waits can be made to run out on purpose,
+ * without any fault).  After pkv_test_enable_withhold(1), flag
+ * PKV_DECODE_TEST_WITHHOLD makes pkv_paged_decode_attn (and its _partial
+ * and _noalloc forms) run the shape's split kernel with its copy producer
+ * issuing no copy at all and every pipeline wait limited to 1 ms: the first
+ * wait for a copy runs out, the kernel sets PKV_DEV_TIMEOUT, every role of
+ * each CTA leaves its loop with nothing in flight, and every row of the call
+ * comes back NaN (output and LSE), as any abandoned chunk does.  Only the
+ * warp-level GQA kernel and the tcgen05 large-group kernel take the flag;
+ * for other shapes, the other entry points, or while it is not enabled
+ * (pkv_test_enable_withhold(0), the default) it is PKV_ERR_INVALID_ARG.
+ * Returns PKV_OK.
+ * ------------------------------------------------------------------------- */
+#define PKV_DECODE_TEST_WITHHOLD 0x100
+int pkv_test_enable_withhold(int enable);
 
 size_t pkv_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t head_dim_v,
                                  int32_t num_splits);
@@ -273,8 +298,10 @@ int pkv_paged_decode_attn_partial(const pkv_cache_desc *cache, const float *q, i
  *    loads the library, until the process exits.  A call whose partials
  *    (pkv_decode_workspace_size for the split count used) exceed it returns
  *    PKV_ERR_WORKSPACE_TOO_SMALL and launches nothing.
- *  - The first call on each device looks up the scratch's device address;
- *    make that first call before any stream capture.
+ *  - The first call in each CUDA context looks up the scratch's device
+ *    address; make that first call before any stream capture.
+ *  - The request is checked as pkv_paged_decode_attn checks it (same
+ *    statuses) before the scratch limit is applied.
  *  - Calls share the scratch: calls that overlap on the GPU race; calls in
  *    one stream are ordered.  Nothing is allocated, on host or device.
  * ------------------------------------------------------------------------- */
@@ -393,8 +420,8 @@ int pkv_paged_decode_attn_multi_e4m3(const pkv_cache_desc *cache, const float *q
  *     out[r][:] = sum_p w_p out_part[p][r][:] / sum_p w_p,  lse[r] = M + ln sum_p w_p.
  * out_part [num_parts][rows][head_dim_v], lse_part [num_parts][rows],
  * out [rows][head_dim_v], lse [rows], all fp32.  Rows whose partials are all
- * empty (lse = -inf) give out = 0 and lse = -inf.  out/lse must not alias the
- * partials.
+ * empty (lse = -inf) give out = 0 and lse = -inf; a row with a NaN partial
+ * LSE (an abandoned chunk) gives NaN.  out/lse must not alias the partials.
  * ------------------------------------------------------------------------- */
 int pkv_lse_merge(int32_t num_parts, const float *out_part, const float *lse_part,
                   int64_t rows, int32_t head_dim_v, float *out, float *lse,

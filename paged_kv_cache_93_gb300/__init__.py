@@ -19,8 +19,9 @@ import ctypes
 import torch
 
 from . import _lib
-from ._lib import (DECODE_GENERIC, DECODE_NO_TCGEN05, DEV_BLOCK_ID, DEV_COPY_CONFLICT, DEV_SEQ_LEN, DEV_SLOT,
-                   DEV_TABLE_RANGE, DEV_TIMEOUT, CacheDesc, PkvError)
+from ._lib import (DECODE_GENERIC, DECODE_NO_TCGEN05, DECODE_TEST_WITHHOLD, DEV_BLOCK_ID,
+                   DEV_COPY_CONFLICT, DEV_SEQ_LEN, DEV_SLOT, DEV_TABLE_RANGE, DEV_TIMEOUT, CacheDesc,
+                   PkvError)
 
 __all__ = [
     "CacheDesc", "PkvError", "ValuesInKeys", "cache_desc", "kv_append", "slot_mapping", "copy_blocks",
@@ -29,7 +30,7 @@ __all__ = [
     "paged_decode_attn_multi", "lse_merge", "kv_append_e4m3", "copy_blocks_e4m3",
     "paged_decode_attn_e4m3", "paged_decode_attn_multi_e4m3",
     "device_status", "BlockManager", "library_path", "DECODE_GENERIC", "DECODE_NO_TCGEN05",
-    "DEV_BLOCK_ID",
+    "DECODE_TEST_WITHHOLD", "DEV_BLOCK_ID",
     "DEV_SLOT", "DEV_SEQ_LEN", "DEV_COPY_CONFLICT", "DEV_TIMEOUT", "DEV_TABLE_RANGE",
 ]
 

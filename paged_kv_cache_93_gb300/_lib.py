@@ -25,6 +25,7 @@ DEV_TIMEOUT = 0x10
 DEV_TABLE_RANGE = 0x20
 DECODE_GENERIC = 0x1
 DECODE_NO_TCGEN05 = 0x2
+DECODE_TEST_WITHHOLD = 0x100      # test control of the failure path (see pkv.h)
 
 
 class CacheDesc(ctypes.Structure):
@@ -74,6 +75,7 @@ SIGNATURES = {
                                                         _P, _P, _P, _i32, _P, _f32, _i32, _P,
                                                         _sz, _P, _P, _i32, _P]),
     "pkv_lse_merge": (ctypes.c_int, [_i32, _P, _P, _i64, _i32, _P, _P, _P]),
+    "pkv_test_enable_withhold": (ctypes.c_int, [ctypes.c_int]),
     "pkv_bm_create": (_P, [_i32, _i32, _P]),
     "pkv_bm_destroy": (None, [_P]),
     "pkv_bm_add_sequence": (ctypes.c_int, [_P, ctypes.POINTER(_i64)]),

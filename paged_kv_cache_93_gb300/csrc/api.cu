@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "pkv.h"
 #include "pkv_device.cuh"
@@ -11,17 +12,24 @@
 using namespace pkv;
 
 namespace {
-
 constexpr int32_t kMaxSplits = 256;
-
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+// PKV_DECODE_TEST_WITHHOLD is accepted only while a test has enabled it.
+std::atomic<int> g_test_withhold_enabled{0};
+// Pipeline wait limit under that control: long enough for any legitimate
+// stall of a small test case, short enough to keep the test quick.
+constexpr uint64_t kTestWaitNs = 1000000ull;
+}  // namespace
 
+namespace pkv {
 int validate_decode(const pkv_cache_desc *c, const float *q, int32_t batch, int32_t hq,
                     const void *k_pool, const void *v_pool, const int32_t *block_tables,
                     int32_t max_blocks, const int32_t *seq_lens, int32_t num_splits,
                     int32_t flags) {
+    const int32_t known = PKV_DECODE_GENERIC | PKV_DECODE_NO_TCGEN05 |
+                          (g_test_withhold_enabled.load() ? PKV_DECODE_TEST_WITHHOLD : 0);
     if (!c || batch < 0 || hq <= 0 || max_blocks < 0 || num_splits < 0 ||
-        num_splits > kMaxSplits || (flags & ~(PKV_DECODE_GENERIC | PKV_DECODE_NO_TCGEN05)) != 0)
+        num_splits > kMaxSplits || (flags & ~known) != 0)
         return PKV_ERR_INVALID_ARG;
     if (c->num_blocks <= 0 || c->block_size < 1 || c->block_size > 256 || c->num_kv_heads <= 0 ||
         c->head_dim_k <= 0 || c->head_dim_v <= 0)
@@ -36,6 +44,9 @@ int validate_decode(const pkv_cache_desc *c, const float *q, int32_t batch, int3
         return PKV_ERR_ALIGNMENT;
     return PKV_OK;
 }
+}  // namespace pkv
+
+namespace {
 
 // The persistent GQA kernels' resident CTAs (tcgen05 and warp-level) take
 // the (sequence, KV head [, head group], split) items in turn, an item costing its 128-token tiles
@@ -101,7 +112,25 @@ void values_from(DecodeArgs &a) {
     }
 }
 
+// The test control: the shape's split kernel with its copies withheld and a
+// short wait limit.  Only the warp-level GQA kernel and the tcgen05
+// large-group kernel read it; any other choice is refused before a launch.
+int run_withheld(const DecodeArgs &in, int32_t flags) {
+    DecodeArgs a = in;
+    a.withhold = 1;
+    a.wait_ns = kTestWaitNs;
+    if (flags & PKV_DECODE_GENERIC) return PKV_ERR_INVALID_ARG;
+    if (!(flags & PKV_DECODE_NO_TCGEN05) &&
+        gqa_tc_kernel_supports(a.cache, a.num_q_heads, a.q_tokens))
+        return PKV_ERR_INVALID_ARG;
+    if (tma_kernel_supports(a.cache, a.num_q_heads, a.q_tokens)) return launch_decode_tma(a);
+    if (!(flags & PKV_DECODE_NO_TCGEN05) && mla_tc_kernel_supports(a.cache, a.num_q_heads))
+        return launch_decode_mla_tc(a);
+    return PKV_ERR_INVALID_ARG;
+}
+
 int run_split_kernel(const DecodeArgs &a, int32_t flags) {
+    if (flags & PKV_DECODE_TEST_WITHHOLD) return run_withheld(a, flags);
     if (!(flags & PKV_DECODE_GENERIC)) {
         if (!(flags & PKV_DECODE_NO_TCGEN05) &&
             gqa_tc_kernel_supports(a.cache, a.num_q_heads, a.q_tokens))
@@ -115,6 +144,11 @@ int run_split_kernel(const DecodeArgs &a, int32_t flags) {
 }
 
 }  // namespace
+
+extern "C" int pkv_test_enable_withhold(int enable) {
+    g_test_withhold_enabled.store(enable ? 1 : 0);
+    return PKV_OK;
+}
 
 // Workspace layout: [partial outputs S x batch x heads x Dv fp32][partial
 // LSEs S x batch x heads fp32], each region 256-byte aligned.
@@ -172,6 +206,7 @@ extern "C" int pkv_paged_decode_attn_e4m3(const pkv_cache_desc *cache, const flo
                                           float scale, int32_t num_splits, void *workspace,
                                           size_t workspace_bytes, float *out, float *lse,
                                           int32_t flags, pkv_stream_t stream) {
+    if (flags & PKV_DECODE_TEST_WITHHOLD) return PKV_ERR_INVALID_ARG;
     int st = validate_decode(cache, q, batch, num_q_heads, k_pool, v_pool, block_tables,
                              max_blocks, seq_lens, num_splits, flags);
     if (st != PKV_OK || batch == 0) return st;
@@ -351,6 +386,7 @@ extern "C" int pkv_paged_decode_attn_multi(const pkv_cache_desc *cache, const fl
                                            size_t workspace_bytes, float *out, float *lse,
                                            int32_t flags, pkv_stream_t stream) {
     if (tokens_per_seq < 1 || tokens_per_seq > kMaxQueryTokens) return PKV_ERR_INVALID_ARG;
+    if (flags & PKV_DECODE_TEST_WITHHOLD) return PKV_ERR_INVALID_ARG;
     if (batch > 0 && int64_t(batch) * tokens_per_seq > 65535) return PKV_ERR_SHAPE;
     const int32_t rows = batch * tokens_per_seq;
     int st = validate_decode(cache, q, rows, num_q_heads, k_pool, v_pool, block_tables,
@@ -433,6 +469,7 @@ extern "C" int pkv_paged_decode_attn_multi_e4m3(
     const int32_t *seq_lens, float scale, int32_t num_splits, void *workspace,
     size_t workspace_bytes, float *out, float *lse, int32_t flags, pkv_stream_t stream) {
     if (tokens_per_seq < 1 || tokens_per_seq > kMaxQueryTokens) return PKV_ERR_INVALID_ARG;
+    if (flags & PKV_DECODE_TEST_WITHHOLD) return PKV_ERR_INVALID_ARG;
     if (batch > 0 && int64_t(batch) * tokens_per_seq > 65535) return PKV_ERR_SHAPE;
     const int32_t rows = batch * tokens_per_seq;
     int st = validate_decode(cache, q, rows, num_q_heads, k_pool, v_pool, block_tables,

@@ -2,6 +2,7 @@
 // word, slot mapping, kv_append, copy_blocks and the DCP interleaved slot
 // mapping.  All of these move or index whole 16-byte vectors; none does
 // floating-point arithmetic, so their results are bit-exact by construction.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -19,23 +20,57 @@ namespace {
 __device__ uint32_t g_status_word;
 
 constexpr int kMaxDevices = 64;
-std::atomic<uint32_t *> g_status_ptr[kMaxDevices];
+SymbolCache g_status_cache;
 std::atomic<int> g_sm_count[kMaxDevices];
 std::mutex g_setup_mutex;
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+CtxGetCurrentFn ctx_get_current_fn() {
+    static CtxGetCurrentFn fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            return reinterpret_cast<CtxGetCurrentFn>(p);
+        return static_cast<CtxGetCurrentFn>(nullptr);
+    }();
+    return fn;
+}
+
+// The calling thread's current CUDA context (the driver's handle), or
+// nullptr when none is current or it cannot be read.
+void *current_context() {
+    CtxGetCurrentFn fn = ctx_get_current_fn();
+    CUcontext c = nullptr;
+    if (!fn || fn(&c) != CUDA_SUCCESS) return nullptr;
+    return c;
+}
 }  // namespace
 
-uint32_t *status_word() {
+void *device_symbol_address(const void *symbol, SymbolCache &cache) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    uint32_t *p = g_status_ptr[dev].load(std::memory_order_acquire);
-    if (p) return p;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= SymbolCache::kMaxDevices)
+        return nullptr;
+    const void *ctx = current_context();
+    const SymbolCache::Entry *e = cache.entry[dev].load(std::memory_order_acquire);
+    if (e && ctx && e->ctx == ctx) return e->addr;
     std::lock_guard<std::mutex> lock(g_setup_mutex);
-    p = g_status_ptr[dev].load(std::memory_order_acquire);
-    if (p) return p;
     void *addr = nullptr;
-    if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess) return nullptr;
-    g_status_ptr[dev].store(static_cast<uint32_t *>(addr), std::memory_order_release);
-    return static_cast<uint32_t *>(addr);
+    // The lookup makes the device's primary context current if no context was.
+    if (cudaGetSymbolAddress(&addr, symbol) != cudaSuccess || !addr) return nullptr;
+    ctx = current_context();
+    e = cache.entry[dev].load(std::memory_order_acquire);
+    if (!(e && e->ctx == ctx && e->addr == addr)) {
+        // Entries are never freed: a reader may still hold the previous
+        // one, and a process sees few contexts per device.
+        cache.entry[dev].store(new SymbolCache::Entry{ctx, addr}, std::memory_order_release);
+    }
+    return addr;
+}
+
+uint32_t *status_word() {
+    return static_cast<uint32_t *>(device_symbol_address(&g_status_word, g_status_cache));
 }
 
 int sm_count() {

@@ -214,6 +214,7 @@ __global__ void lse_merge_kernel(int32_t num_parts, const float *__restrict__ ou
     const int64_t pstride = rows * tpr;   // float4s between consecutive partials
     float M = -INFINITY, W = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    bool nan_part = false;     // a partial reported as NaN (abandoned): the row is NaN
     for (int p0 = 0; p0 < num_parts; p0 += 16) {
         float l[16];
         float4 x[16];
@@ -225,7 +226,10 @@ __global__ void lse_merge_kernel(int32_t num_parts, const float *__restrict__ ou
         }
         float mc = M;
 #pragma unroll
-        for (int u = 0; u < 16; ++u) mc = fmaxf(mc, l[u]);
+        for (int u = 0; u < 16; ++u) {
+            nan_part |= l[u] != l[u];
+            mc = fmaxf(mc, l[u]);
+        }
         if (mc == -INFINITY) continue;               // every partial so far is empty
         const float rescale = expf(M - mc);          // 0 when M = -inf
         W *= rescale;
@@ -244,6 +248,12 @@ __global__ void lse_merge_kernel(int32_t num_parts, const float *__restrict__ ou
         M = mc;
     }
     float4 *orow = reinterpret_cast<float4 *>(out + r * head_dim_v);
+    if (nan_part) {
+        const float nan = __int_as_float(0x7fc00000);
+        orow[c] = make_float4(nan, nan, nan, nan);
+        if (c == 0) lse[r] = nan;
+        return;
+    }
     if (M == -INFINITY) {
         orow[c] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (c == 0) lse[r] = -INFINITY;

@@ -185,6 +185,7 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     const int num_items = a.batch * a.cache.num_kv_heads * groups * a.num_splits;
     const int bs = a.cache.block_size, hkv = a.cache.num_kv_heads;
     const int Dk = shp.dk_segs * 64, Dv = shp.dv_blocks * 128;
+    const uint64_t wlim = a.wait_ns ? a.wait_ns : kWaitLimitNs;
 
     if (threadIdx.x == 0) {
         for (int r = 0; r < shp.ring; ++r) {
@@ -222,10 +223,11 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
         }
         int stage = 0;
         uint32_t phase = 0, armed = 0, armed_parity = 0;
-        bool ok = true;
+        bool ok = a.withhold == 0;              // test control: issue no copy at all
         // Wait for a free stage and arm it for one chunk; false on abort.
         auto acquire = [&](uint32_t &dst) -> bool {
-            const bool w = pipe_wait(bar(kBarEmpty + stage), phase ^ 1u, a.status, abort_flag);
+            const bool w =
+                pipe_wait(bar(kBarEmpty + stage), phase ^ 1u, a.status, abort_flag, wlim);
             if (!__all_sync(0xffffffffu, w)) return false;
             if (lane == 0) mbar_arrive_expect_tx(bar(kBarFull + stage), kChunk);
             armed |= 1u << stage;
@@ -308,7 +310,7 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
         const uint32_t qh = sb + sm.q_hi;
         const uint32_t ph = sb + sm.p_hi, pl = sb + sm.p_lo;
         auto wait_all = [&](uint32_t b, uint32_t parity) {
-            return __all_sync(0xffffffffu, pipe_wait(b, parity, a.status, abort_flag));
+            return __all_sync(0xffffffffu, pipe_wait(b, parity, a.status, abort_flag, wlim));
         };
         auto advance = [&]() {
             if (++stage == shp.ring) {
@@ -419,10 +421,23 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
         uint8_t *q_hi = base + sm.q_hi, *q_lo = base + sm.q_lo;
         uint8_t *p_hi = base + sm.p_hi, *p_lo = base + sm.p_lo;
         uint32_t tcount = 0, pcount = 0, ne = 0;
+        // An item this CTA gives up on (a wait ran out) reports every one of
+        // its rows as NaN, output and LSE; so does every later item of the CTA.
+        bool abandoned = false;
+        auto abandon_rows = [&](int64_t orow0) {
+            float4 *o = reinterpret_cast<float4 *>(a.out_part + orow0 * Dv);
+            const float nan = __int_as_float(0x7fc00000);
+            for (int i = t; i < kN * Dv / 4; i += kSoftThreads) o[i] = make_float4(nan, nan, nan, nan);
+            if (t < kN) a.lse_part[orow0 + t] = nan;
+        };
         for (int item = blockIdx.x; item < num_items; item += gridDim.x) {
             const TcItem r = tc_item(a, item, groups, t == 0);
             const int head0 = r.g * G + r.hg * kN;
             const int64_t orow0 = (int64_t(r.s) * a.batch + r.b) * a.num_q_heads + head0;
+            if (abandoned) {
+                abandon_rows(orow0);
+                continue;
+            }
             if (r.ntiles == 0) {
                 float4 *o = reinterpret_cast<float4 *>(a.out_part + orow0 * Dv);
                 for (int i = t; i < kN * Dv / 4; i += kSoftThreads)
@@ -431,7 +446,7 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 continue;
             }
             // ---- the group's queries, pre-scaled by scale*log2(e), as bf16 hi + lo
-            bool w = pipe_wait(bar(kBarQEmpty), (ne & 1u) ^ 1u, a.status, abort_flag);
+            bool w = pipe_wait(bar(kBarQEmpty), (ne & 1u) ^ 1u, a.status, abort_flag, wlim);
             if (w) {
                 // 16-byte loads, eight in flight per thread before any is used
                 // (the query is 147 KB at Dk = 576: one load at a time would
@@ -469,7 +484,11 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
             float l_part[kN];
 #pragma unroll
             for (int h = 0; h < kN; ++h) l_part[h] = 0.f;
-            if (softmax_bar_or(!w)) break;
+            if (softmax_bar_or(!w)) {
+                abandoned = true;
+                abandon_rows(orow0);
+                continue;
+            }
 
             bool ok = true;
             for (int i = 0; i < r.ntiles; ++i) {
@@ -478,7 +497,8 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 // exceed its head's running max by more than the slack?)
                 const uint32_t buf = tcount & 1u;
                 const uint32_t ts = tl + kColS + 128 * buf;
-                w = pipe_wait(bar(kBarSFull + buf), (tcount >> 1) & 1u, a.status, abort_flag);
+                w = pipe_wait(bar(kBarSFull + buf), (tcount >> 1) & 1u, a.status, abort_flag,
+                              wlim);
                 tc::fence_after_sync();
                 const bool valid = r.begin + int64_t(i) * kM + row < r.end;
                 bool need = false;
@@ -527,7 +547,7 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         // the accumulators are quiet: tile i-1's value MMAs
                         // are done and tile i's wait for these probabilities
                         const bool wv =
-                            pipe_wait(bar(kBarPvDone), pcount & 1u, a.status, abort_flag);
+                            pipe_wait(bar(kBarPvDone), pcount & 1u, a.status, abort_flag, wlim);
                         ++pcount;
                         pv_waited = true;
                         tc::fence_after_sync();
@@ -552,7 +572,7 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 }
                 if (i > 0 && !pv_waited) {
                     // tile i-1's value MMAs have finished reading the buffer
-                    pipe_wait(bar(kBarPvDone), pcount & 1u, a.status, abort_flag);
+                    pipe_wait(bar(kBarPvDone), pcount & 1u, a.status, abort_flag, wlim);
                     ++pcount;
                 }
                 // ---- second pass: probabilities, split into bf16 hi + lo,
@@ -593,10 +613,14 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 tc::fence_before_sync();
                 mbar_arrive(bar(kBarPFull));
             }
-            if (!ok) break;
+            if (!ok) {
+                abandoned = true;
+                abandon_rows(orow0);
+                continue;
+            }
 
             // ---- epilogue: the item's last value MMAs are complete
-            w = pipe_wait(bar(kBarPvDone), pcount & 1u, a.status, abort_flag);
+            w = pipe_wait(bar(kBarPvDone), pcount & 1u, a.status, abort_flag, wlim);
             ++pcount;
             tc::fence_after_sync();
 #pragma unroll
@@ -634,7 +658,10 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
             tc::fence_before_sync();
             mbar_arrive(bar(kBarOEmpty));
             ++ne;
-            if (softmax_bar_or(!w)) break;
+            if (softmax_bar_or(!w)) {
+                abandoned = true;
+                abandon_rows(orow0);
+            }
         }
     }
 

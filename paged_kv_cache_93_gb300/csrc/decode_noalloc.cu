@@ -18,12 +18,11 @@
 // row (empty chunks included) before the merge reads it.
 #include <cuda_runtime.h>
 
-#include <atomic>
 #include <climits>
 #include <cstdint>
-#include <mutex>
 
 #include "pkv.h"
+#include "pkv_host.h"
 
 namespace {
 
@@ -31,31 +30,21 @@ constexpr size_t kNoAllocScratchBytes = PKV_NOALLOC_SCRATCH_BYTES;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::atomic<void *> g_scratch_address[kMaxDevices];
-std::mutex g_scratch_mutex;
+pkv::SymbolCache g_scratch_cache;
 
-// Device address of the scratch array on the current device.  In host code
-// the array's name is only a host-side stand-in; the address must come from
-// cudaGetSymbolAddress with the device current.  Looked up once per device.
+// Device address of the scratch array in the current context.  In host code
+// the array's name is only a host-side stand-in; the address comes from
+// cudaGetSymbolAddress with the device current, looked up on the first call
+// in each context and cached.
 void *scratch_address(int *status) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
-        *status = PKV_ERR_CUDA;
-        return nullptr;
-    }
-    void *p = g_scratch_address[dev].load(std::memory_order_acquire);
-    if (p) return p;
-    std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    p = g_scratch_address[dev].load(std::memory_order_acquire);
-    if (p) return p;
-    void *addr = nullptr;
-    if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || addr == nullptr) {
-        *status = PKV_ERR_CUDA;
-        return nullptr;
-    }
-    g_scratch_address[dev].store(addr, std::memory_order_release);
-    return addr;
+    void *p = pkv::device_symbol_address(&g_noalloc_scratch, g_scratch_cache);
+    if (!p) *status = PKV_ERR_CUDA;
+    return p;
+}
+
+int32_t table_span(const pkv_cache_desc *cache, int32_t max_blocks) {
+    const int64_t longest = int64_t(max_blocks > 0 ? max_blocks : 0) * cache->block_size;
+    return int32_t(longest < INT32_MAX ? longest : INT32_MAX);
 }
 
 }  // namespace
@@ -67,14 +56,16 @@ extern "C" int pkv_paged_decode_attn_noalloc(const pkv_cache_desc *cache, const 
                                              const int32_t *seq_lens, float scale,
                                              int32_t num_splits, float *out, float *lse,
                                              int32_t flags, pkv_stream_t stream) {
-    if (!cache || batch < 0 || num_q_heads <= 0 || num_splits < 0) return PKV_ERR_INVALID_ARG;
-    if (batch == 0) return PKV_OK;
-    int32_t S = num_splits;
-    if (S == 0) {
-        const int64_t longest = int64_t(max_blocks > 0 ? max_blocks : 0) * cache->block_size;
-        S = pkv_decode_auto_splits(cache, batch, num_q_heads,
-                                   int32_t(longest < INT32_MAX ? longest : INT32_MAX));
-    }
+    // The regular entry point's checks first, so that a bad request gets the
+    // status that call would give it.
+    int st = pkv::validate_decode(cache, q, batch, num_q_heads, k_pool, v_pool, block_tables,
+                                  max_blocks, seq_lens, num_splits, flags);
+    if (st != PKV_OK || batch == 0) return st;
+    if (!out || !lse) return PKV_ERR_INVALID_ARG;
+    if (!pkv::aligned16(out)) return PKV_ERR_ALIGNMENT;
+    const int32_t S = num_splits != 0 ? num_splits
+                                      : pkv_decode_auto_splits(cache, batch, num_q_heads,
+                                                               table_span(cache, max_blocks));
     // Partials [S][batch][heads][head_dim_v] + LSEs must fit the fixed scratch.
     if (pkv_decode_workspace_size(batch, num_q_heads, cache->head_dim_v, S) > kNoAllocScratchBytes)
         return PKV_ERR_WORKSPACE_TOO_SMALL;
@@ -91,14 +82,14 @@ extern "C" int pkv_paged_decode_attn_noalloc_e4m3(
     const void *k_pool, const void *v_pool, const float *k_scale, const float *v_scale,
     const int32_t *block_tables, int32_t max_blocks, const int32_t *seq_lens, float scale,
     int32_t num_splits, float *out, float *lse, int32_t flags, pkv_stream_t stream) {
-    if (!cache || batch < 0 || num_q_heads <= 0 || num_splits < 0) return PKV_ERR_INVALID_ARG;
-    if (batch == 0) return PKV_OK;
-    int32_t S = num_splits;
-    if (S == 0) {
-        const int64_t longest = int64_t(max_blocks > 0 ? max_blocks : 0) * cache->block_size;
-        S = pkv_decode_auto_splits_e4m3(cache, batch, num_q_heads,
-                                        int32_t(longest < INT32_MAX ? longest : INT32_MAX));
-    }
+    int st = pkv::validate_decode(cache, q, batch, num_q_heads, k_pool, v_pool, block_tables,
+                                  max_blocks, seq_lens, num_splits, flags);
+    if (st != PKV_OK || batch == 0) return st;
+    if (!v_pool || !k_scale || !v_scale || !out || !lse) return PKV_ERR_INVALID_ARG;
+    if (!pkv::aligned16(out)) return PKV_ERR_ALIGNMENT;
+    const int32_t S = num_splits != 0 ? num_splits
+                                      : pkv_decode_auto_splits_e4m3(cache, batch, num_q_heads,
+                                                                    table_span(cache, max_blocks));
     if (pkv_decode_workspace_size(batch, num_q_heads, cache->head_dim_v, S) > kNoAllocScratchBytes)
         return PKV_ERR_WORKSPACE_TOO_SMALL;
     int status = PKV_OK;

@@ -170,6 +170,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmap_k,
     const int num_items = a.batch * a.cache.num_kv_heads * a.num_splits;
     const int bs = a.cache.block_size;
     const int hkv = a.cache.num_kv_heads;
+    const uint64_t wlim = a.wait_ns ? a.wait_ns : kWaitLimitNs;
     const int seg_rows = bs < C::kStageTokens ? bs : C::kStageTokens;
     const uint32_t seg_shift = 31 - __clz(seg_rows);
     const StageLayout lay{seg_shift, uint32_t(seg_rows) * D * 2, uint32_t(seg_rows) * kRowBytes};
@@ -199,7 +200,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmap_k,
         int stage = 0;
         uint32_t phase = 0;
         uint32_t armed = 0, armed_parity = 0;   // per stage: ever armed / parity armed last
-        bool ok = true;
+        bool ok = a.withhold == 0;              // test control: issue no copy at all
         for (int item = blockIdx.x; item < num_items && ok; item += gridDim.x) {
             const ItemRange r = item_range(a, item, C::kStageTokens, false);
             const int total_segs = r.nstages * segs_per_stage;
@@ -224,7 +225,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     const uint32_t eb = smem_addr(&empty_bar[stage]);
                     const uint32_t fb = smem_addr(&full_bar[stage]);
                     int fail = 0;
-                    if (lane == 0) fail = !mbar_wait(eb, phase ^ 1u, a.status) || *abort_flag;
+                    if (lane == 0) fail = !mbar_wait(eb, phase ^ 1u, a.status, wlim) || *abort_flag;
                     if (__shfl_sync(0xffffffffu, fail, 0)) {
                         if (lane == 0) *abort_flag = 1;
                         ok = false;
@@ -283,18 +284,34 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmap_k,
         slot_head[0] = 0; slot_head[1] = 0; slot_ok[0] = tq == 0; slot_ok[1] = false;
     }
     const float qscale = a.scale * kLog2e;
-    const int T = a.q_tokens, Gr = G / a.q_tokens;    // query tokens, heads per KV head
     // ldmatrix row addresses inside a stage (constant per lane).
     const int krow = 16 * warp + (lane & 7) + ((lane >> 3) & 1) * 8;   // A = K, non-transposed
     const int vrow = 16 * warp + (lane & 7) + (lane >> 4) * 8;         // A = V^T, transposed
     const uint32_t koff = lay.row_base(krow), voff = lay.row_base(vrow);
     const int ksw = krow & 7, vsw = vrow & 7;
 
+    const int T = a.q_tokens, Gr = G / a.q_tokens;    // query tokens, heads per KV head
+    // An item this CTA gives up on (a wait ran out) reports every one of its
+    // rows as NaN, output and LSE; so does every later item of the CTA.
+    auto abandon_rows = [&](const ItemRange &r) {
+        const int64_t split0 = int64_t(r.s) * a.batch * T * a.num_q_heads;
+        for (int idx = threadIdx.x; idx < G * D; idx += W * 32) {
+            const int head = idx / D, d = idx % D;
+            const int64_t orow = split0 + row_offset(a, r.b, r.g, head, Gr);
+            a.out_part[orow * D + d] = __int_as_float(0x7fc00000);
+            if (d == 0) a.lse_part[orow] = __int_as_float(0x7fc00000);
+        }
+    };
+
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
     for (int item = blockIdx.x; item < num_items; item += gridDim.x) {
         const ItemRange r = item_range(a, item, C::kStageTokens, warp == 0 && lane == 0);
+        if (!ok) {
+            abandon_rows(r);
+            continue;
+        }
 
         // Query fragments: B operand of S^T = K . Q^T, columns [q_hi | q_lo].
         uint32_t qf[C::kKSteps][C::kNT][2];
@@ -344,7 +361,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmap_k,
 
         for (int st = 0; st < r.nstages && ok; ++st) {
             const uint32_t fb = smem_addr(&full_bar[stage]);
-            const bool waited = mbar_wait(fb, phase, a.status);
+            const bool waited = mbar_wait(fb, phase, a.status, wlim);
             if (__any_sync(0xffffffffu, !waited || *abort_flag)) {
                 if (lane == 0) *abort_flag = 1;
                 ok = false;
@@ -554,6 +571,13 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmap_k,
         }
         named_barrier_sync(1, W * 32);
         if (threadIdx.x == 0) *stop_flag = *abort_flag;
+        named_barrier_sync(1, W * 32);
+        if (*stop_flag) {
+            // some wait of this CTA gave up: the item is abandoned
+            ok = false;
+            abandon_rows(r);
+            continue;
+        }
 
         // ---- CTA merge of the warps' partial states
         const int64_t split0 = int64_t(r.s) * a.batch * T * a.num_q_heads;
@@ -578,7 +602,6 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmap_k,
             if (d == 0) a.lse_part[orow] = M != -INFINITY ? (M + log2f(lsum)) * kLn2 : -INFINITY;
         }
         named_barrier_sync(1, W * 32);
-        if (*stop_flag) break;   // same value in every consumer warp
     }
 }
 
@@ -614,6 +637,30 @@ bool make_pool_map(CUtensorMap *map, const void *pool, int64_t rows, int dim, in
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// CTAs of this instance the current device keeps resident per SM (the
+// occupancy the launch's persistent grid is sized by; the split-count model
+// uses the same figure).  Sets the kernel's shared-memory attribute first.
+// Cached per device and thread; 0 if the runtime failed.
+template <int D, int G, int W, int NSTAGES, int MINB>
+int resident_per_sm() {
+    using C = Cfg<D, G, W, NSTAGES, MINB>;
+    auto kernel = decode_tma_kernel<D, G, W, NSTAGES, MINB>;
+    static thread_local int configured_dev = -1, cached = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (configured_dev != dev) {
+        int per_sm = 0;
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(C::kSmemBytes)) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, C::kThreads,
+                                                          C::kSmemBytes) != cudaSuccess)
+            return 0;
+        cached = per_sm;
+        configured_dev = dev;
+    }
+    return cached;
+}
+
 template <int D, int G, int W, int NSTAGES, int MINB>
 int launch(const DecodeArgs &a) {
     using C = Cfg<D, G, W, NSTAGES, MINB>;
@@ -624,20 +671,8 @@ int launch(const DecodeArgs &a) {
     if (!make_pool_map(&tk, a.k_pool, rows, D, box_rows) ||
         !make_pool_map(&tv, a.v_pool, rows, D, box_rows))
         return PKV_ERR_CUDA;
-    static thread_local int configured_dev = -1;  // attribute set per device, per thread
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (configured_dev != dev) {
-        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(C::kSmemBytes)) != cudaSuccess)
-            return PKV_ERR_CUDA;
-        configured_dev = dev;
-    }
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, C::kThreads,
-                                                      C::kSmemBytes) != cudaSuccess ||
-        per_sm < 1)
-        return PKV_ERR_CUDA;
+    const int per_sm = resident_per_sm<D, G, W, NSTAGES, MINB>();
+    if (per_sm < 1) return PKV_ERR_CUDA;
     const int64_t items = int64_t(a.batch) * a.cache.num_kv_heads * a.num_splits;
     const int grid = int(std::min<int64_t>(items, int64_t(sm_count()) * per_sm));
     if (grid <= 0) return PKV_OK;
@@ -718,10 +753,27 @@ bool tma_kernel_supports(const pkv_cache_desc &c, int32_t num_q_heads, int32_t q
 // 361 us for two 2-warp CTAs and 513-570 us for three CTAs per SM).
 int tma_resident_ctas(const pkv_cache_desc &c, int32_t num_q_heads, int32_t q_tokens) {
     const int G = num_q_heads / c.num_kv_heads * q_tokens;
-    int per_sm = c.head_dim_k == 128 ? (G == 16 ? PKV_TMA_D128G16_B : G == 8 ? PKV_TMA_D128G8_B
-                                                                             : PKV_TMA_D128_B)
-                                     : (G == 16 ? PKV_TMA_D64G16_B : PKV_TMA_D64_B);
-    return sm_count() * per_sm;
+    int per_sm = 0;
+    if (c.head_dim_k == 128) {
+        switch (G) {
+            case 1: per_sm = resident_per_sm<128, 1, PKV_TMA_SHAPE_D128>(); break;
+            case 2: per_sm = resident_per_sm<128, 2, PKV_TMA_SHAPE_D128>(); break;
+            case 4: per_sm = resident_per_sm<128, 4, PKV_TMA_SHAPE_D128>(); break;
+            case 8: per_sm = resident_per_sm<128, 8, PKV_TMA_SHAPE_D128_G8>(); break;
+            case 16: per_sm = resident_per_sm<128, 16, PKV_TMA_SHAPE_D128_G16>(); break;
+            default: break;
+        }
+    } else {
+        switch (G) {
+            case 1: per_sm = resident_per_sm<64, 1, PKV_TMA_SHAPE_D64>(); break;
+            case 2: per_sm = resident_per_sm<64, 2, PKV_TMA_SHAPE_D64>(); break;
+            case 4: per_sm = resident_per_sm<64, 4, PKV_TMA_SHAPE_D64>(); break;
+            case 8: per_sm = resident_per_sm<64, 8, PKV_TMA_SHAPE_D64>(); break;
+            case 16: per_sm = resident_per_sm<64, 16, PKV_TMA_SHAPE_D64_G16>(); break;
+            default: break;
+        }
+    }
+    return sm_count() * std::max(per_sm, 1);
 }
 
 int launch_decode_tma(const DecodeArgs &a) {

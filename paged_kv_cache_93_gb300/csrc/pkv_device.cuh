@@ -90,14 +90,15 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 }
 // Bounded wait for the phase with the given parity to complete.  Returns
 // false (and raises PKV_DEV_TIMEOUT) if it has not completed within
-// kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t *status) {
+// limit_ns.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t *status,
+                                          uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t start = global_timer_ns();
     for (;;) {
         for (int i = 0; i < 64; ++i)
             if (mbar_try_wait(bar, parity)) return true;
-        if (global_timer_ns() - start > kWaitLimitNs) break;
+        if (global_timer_ns() - start > limit_ns) break;
     }
     raise_status(status, PKV_DEV_TIMEOUT);
     return false;

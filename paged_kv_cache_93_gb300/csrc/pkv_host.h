@@ -2,6 +2,7 @@
 // (not part of the public C ABI).
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -10,9 +11,35 @@
 
 namespace pkv {
 
-// Device address of the current device's status word (set up once per
-// device, with that device current).  nullptr if the CUDA runtime failed.
+// Per-device cache of a __device__ symbol's address, keyed on the CUDA
+// context it was looked up in.
+struct SymbolCache {
+    static constexpr int kMaxDevices = 64;
+    struct Entry {
+        const void *ctx;
+        void *addr;
+    };
+    std::atomic<const Entry *> entry[kMaxDevices] = {};
+};
+
+// Device address of the __device__ variable `symbol` in the calling
+// thread's current context on the current device.  In host code such a
+// variable's name is only a host-side stand-in; its device address comes
+// from cudaGetSymbolAddress, looked up again whenever the current context
+// is not the one cached (another context, or the device's primary context
+// recreated after cudaDeviceReset).  nullptr if the CUDA runtime failed.
+void *device_symbol_address(const void *symbol, SymbolCache &cache);
+
+// Device address of the current device's status word.  nullptr if the CUDA
+// runtime failed.
 uint32_t *status_word();
+
+// The argument and shape checks shared by every decode entry point (the
+// statuses documented for pkv_paged_decode_attn); PKV_OK when they pass.
+int validate_decode(const pkv_cache_desc *c, const float *q, int32_t batch, int32_t hq,
+                    const void *k_pool, const void *v_pool, const int32_t *block_tables,
+                    int32_t max_blocks, const int32_t *seq_lens, int32_t num_splits,
+                    int32_t flags);
 
 // Number of SMs of the current device (cached per device).
 int sm_count();
@@ -66,6 +93,13 @@ struct DecodeArgs {
     int32_t q_tokens = 1;
     // E4M3 pools: per-KV-head dequantisation scales (device, [num_kv_heads]).
     const float *k_scale = nullptr, *v_scale = nullptr;
+    // Pipeline waits give up after this many nanoseconds (0: the kernels'
+    // default limit).
+    uint64_t wait_ns = 0;
+    // Test control (PKV_DECODE_TEST_WITHHOLD): the producer issues no copies,
+    // so the first wait for one runs out.  Read by the warp-level GQA kernel
+    // and the tcgen05 large-group kernel only.
+    int32_t withhold = 0;
 };
 bool tma_kernel_supports(const pkv_cache_desc &c, int32_t num_q_heads, int32_t q_tokens = 1);
 // CTAs the warp-level GQA kernel keeps resident for the shape (one persistent grid).

@@ -11,17 +11,18 @@
 namespace pkv {
 
 // Bounded wait for the phase of `bar` with the given parity.  Gives up
-// (false) when another role has set *abort_flag, or after kWaitLimitNs, in
+// (false) when another role has set *abort_flag, or after limit_ns, in
 // which case it raises PKV_DEV_TIMEOUT and sets *abort_flag for the others.
 __device__ __forceinline__ bool pipe_wait(uint32_t bar, uint32_t parity, uint32_t *status,
-                                          volatile int *abort_flag) {
+                                          volatile int *abort_flag,
+                                          uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t start = global_timer_ns();
     for (;;) {
         for (int i = 0; i < 32; ++i)
             if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (global_timer_ns() - start > kWaitLimitNs) {
+        if (global_timer_ns() - start > limit_ns) {
             raise_status(status, PKV_DEV_TIMEOUT);
             *abort_flag = 1;
             return false;

@@ -59,6 +59,36 @@ def oracle_cache(w):
     return k, v, slots
 
 
+def oracle_rows(q, k, v, tables, lens, scale, rows):
+    """Oracle attention of the selected {sequence: [query heads]} of a cache
+    with one KV head: every (sequence, head) as a one-head row of its own,
+    all in one oracle call (its threads take the rows in turn).  Rows not
+    selected stay NaN."""
+    B, Hq, _ = q.shape
+    out = np.full((B, Hq, v.shape[-1]), np.nan)
+    lse = np.full((B, Hq), np.nan)
+    pairs = [(b, h) for b, heads in rows.items() for h in heads]
+    bs_, hs_ = np.array([p[0] for p in pairs]), np.array([p[1] for p in pairs])
+    o, l = oracle.paged_decode_attn(np.ascontiguousarray(q[bs_, hs_][:, None, :]), k, v,
+                                    np.ascontiguousarray(tables[bs_]),
+                                    np.ascontiguousarray(lens[bs_]), scale)
+    out[bs_, hs_], lse[bs_, hs_] = o[:, 0], l[:, 0]
+    return out, lse
+
+
+def agent_rows(w):
+    """{sequence: [heads]} checked at the shared-prefix workload's full size:
+    all heads of the first and last sequences and of those with the shortest
+    and longest suffix, and one head of every other sequence (a different
+    head each, so that every 64-head group is covered).  Also returns the
+    fully checked sequences."""
+    lens = w.seq_lens.numpy().astype(np.int64)
+    full = {0, len(lens) - 1, int(np.argmin(lens)), int(np.argmax(lens))}
+    rows = {b: (list(range(w.num_q_heads)) if b in full else [(37 * b + 11) % w.num_q_heads])
+            for b in range(len(lens))}
+    return rows, sorted(full)
+
+
 def oracle_step(w, rows=None):
     """Oracle attention after its own append.  `rows`: optional {sequence:
     [query heads]} to compute (the rest stay NaN); with one KV head the
@@ -72,14 +102,12 @@ def oracle_step(w, rows=None):
     B, Hq, _ = q.shape
     out = np.full((B, Hq, w.head_dim_v), np.nan)
     lse = np.full((B, Hq), np.nan)
+    if w.num_kv_heads == 1:
+        o, l = oracle_rows(q, k, v, tables, lens, w.scale, rows)
+        return o, l, k, v, slots
     for b, heads in rows.items():
         heads = list(heads)
-        if w.num_kv_heads == 1:
-            o, l = oracle.paged_decode_attn(q[b:b + 1, heads], k, v, tables[b:b + 1],
-                                            lens[b:b + 1], w.scale)
-            out[b, heads], lse[b, heads] = o[0], l[0]
-        else:
-            o, l = oracle.paged_decode_attn(q[b:b + 1], k, v, tables[b:b + 1], lens[b:b + 1],
-                                            w.scale)
-            out[b, heads], lse[b, heads] = o[0, heads], l[0, heads]
+        o, l = oracle.paged_decode_attn(q[b:b + 1], k, v, tables[b:b + 1], lens[b:b + 1],
+                                        w.scale)
+        out[b, heads], lse[b, heads] = o[0, heads], l[0, heads]
     return out, lse, k, v, slots

@@ -50,6 +50,29 @@ def test_library_exports_every_declared_symbol(pkv):
     assert set(_lib.SIGNATURES) == set(declared_functions())
 
 
+def test_withhold_control_is_refused_unless_enabled(pkv):
+    """The test control of the failure path is an unknown flag until a test
+    enables it, and the entry points that never take it refuse it always
+    (host checks: nothing reaches a GPU)."""
+    lib = pkv.lib
+    desc = pkv.CacheDesc(16, 16, 8, 128, 128)
+    p = ctypes.c_void_p(0x1000)
+    f = pkv.DECODE_TEST_WITHHOLD
+    assert lib.pkv_test_enable_withhold(0) == 0
+    assert lib.pkv_paged_decode_attn(ctypes.byref(desc), p, 1, 32, p, p, p, 4, p, 1.0, 1, None, 0,
+                                     p, p, f, None) == -1
+    assert lib.pkv_paged_decode_attn_partial(ctypes.byref(desc), p, 1, 32, p, p, p, 4, p, 1.0, 1,
+                                             p, p, f, None) == -1
+    try:
+        assert lib.pkv_test_enable_withhold(1) == 0
+        assert lib.pkv_paged_decode_attn_e4m3(ctypes.byref(desc), p, 1, 32, p, p, p, p, p, 4, p,
+                                              1.0, 1, None, 0, p, p, f, None) == -1
+        assert lib.pkv_paged_decode_attn_multi(ctypes.byref(desc), p, 1, 2, 32, p, p, p, 4, p,
+                                               1.0, 1, p, 1 << 20, p, p, f, None) == -1
+    finally:
+        lib.pkv_test_enable_withhold(0)
+
+
 def test_status_strings(pkv):
     for code in range(0, -9, -1):
         s = pkv.lib.pkv_status_string(code).decode()

@@ -1,9 +1,12 @@
-"""Parity at the full workload sizes, in the launch configuration the
-benchmark times: the 32K-context GQA batch (every row against the oracle),
-the 200,000-token DCP-style partition split (interleave 1 and 16, merged
-partitions against unsplit attention and the oracle), and the shared-prefix
-MLA-shaped step (bit-exact cache after copy-on-write + append; sampled rows
-of the attention against the oracle)."""
+"""Parity at the full workload sizes, in the launch configurations the
+benchmark times: the 32K-context GQA batch at the benchmark's headline split
+count and at the split count the library picks by itself (every row against
+the oracle), the 200,000-token DCP-style partition split (interleave 1 and
+16, merged partitions against unsplit attention and the oracle), and the
+shared-prefix MLA-shaped step at the benchmark's split count (bit-exact cache
+after copy-on-write + append; every head of the first, last, shortest- and
+longest-suffix sequences and one head of every sequence against the
+oracle)."""
 from __future__ import annotations
 
 import numpy as np
@@ -12,12 +15,12 @@ import torch
 
 import oracle
 import workloads
-from tests._steps import assert_attention_close, gpu_step, oracle_cache, oracle_step
+from bench import DEFAULT_SPLITS          # the split counts the benchmark times
+from tests._steps import (agent_rows, assert_attention_close, gpu_step, oracle_cache,
+                          oracle_step)
 from tests._util import bits
 
 pytestmark = pytest.mark.gpu
-
-LONG32K_SPLITS = 16      # the split count of the benchmarked 32K configuration
 
 
 @pytest.fixture(scope="module")
@@ -29,9 +32,21 @@ def pkv():
     return m
 
 
-def test_long32k_all_rows(pkv):
+@pytest.mark.parametrize("which", ["headline", "library_auto"])
+def test_long32k_all_rows(pkv, which):
+    """Every row of the 32K step, at the split count of the benchmark's
+    headline line (16, the configuration's own) and at num_splits = 0, the
+    library's choice, which the benchmark reports beside it."""
     w = workloads.long32k()
-    out, lse, k, v, slots = gpu_step(pkv, w, num_splits=LONG32K_SPLITS)
+    if which == "headline":
+        splits = DEFAULT_SPLITS["long32k"]
+        assert splits == 16
+    else:
+        splits = 0
+        auto = pkv.decode_auto_splits(w.k_pool, w.v_pool, w.batch, w.num_q_heads,
+                                      w.block_tables.shape[1] * w.block_size)
+        assert 1 <= auto <= 256
+    out, lse, k, v, slots = gpu_step(pkv, w, num_splits=splits)
     ro, rl, ok_, ov_, oslots = oracle_step(w)
     assert np.array_equal(slots.cpu().numpy(), oslots)
     # the appended tokens landed exactly where the oracle put them
@@ -107,9 +122,11 @@ def test_dcp200k_partitions_merge_to_unsplit(pkv, interleave):
 
 def test_agent_mla_shared_prefix_step(pkv):
     w = workloads.agent_mla()
-    out, lse, k, v, slots = gpu_step(pkv, w)
+    splits = DEFAULT_SPLITS["agent_mla"]
+    out, lse, k, v, slots = gpu_step(pkv, w, num_splits=splits)
     assert pkv.device_status() == 0
-    rows = {0: [0, 77, 127], 13: [5, 64], 31: [1, 100, 126]}
+    rows, full = agent_rows(w)
+    assert len(full) == 4
     ro, rl, ok_, ov_, oslots = oracle_step(w, rows)
     assert np.array_equal(slots.cpu().numpy(), oslots)
     assert np.array_equal(bits(k.cpu()), ok_) and np.array_equal(bits(v.cpu()), ov_)

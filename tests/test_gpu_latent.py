@@ -13,7 +13,7 @@ import torch
 
 import oracle
 import workloads
-from tests._steps import assert_attention_close
+from tests._steps import agent_rows, assert_attention_close, oracle_rows
 from tests._util import bits
 
 pytestmark = pytest.mark.gpu
@@ -110,10 +110,12 @@ def test_latent_copy_blocks_copies_keys_only(pkv):
     assert pkv.device_status() == 0
 
 
-def test_latent_agent_step_sampled_rows(pkv):
+def test_latent_agent_step_full_heads(pkv):
     """The shared-prefix MLA workload in the latent layout (1,152 B per token):
-    copy-on-write of the shared tail + append + attention, sampled rows
-    against the oracle."""
+    copy-on-write of the shared tail + append + attention at the benchmark's
+    19 splits; every head of four sequences (first, last, shortest and
+    longest suffix) and one head of every other sequence against the
+    oracle."""
     w = workloads.agent_mla()
     dev = "cuda"
     latent = pkv.ValuesInKeys(w.head_dim_v)
@@ -129,10 +131,12 @@ def test_latent_agent_step_sampled_rows(pkv):
     kh = _oracle_latent_cache(w)
     assert np.array_equal(bits(k.cpu()), kh), "K pool after copy-on-write + append"
     v = np.ascontiguousarray(kh[..., :w.head_dim_v])
-    rows = {0: [0, 77], 13: [5], 31: [127]}
+    rows, full = agent_rows(w)
+    assert len(full) == 4
+    ro, rl = oracle_rows(w.q.numpy(), kh, v, w.block_tables.numpy(), w.seq_lens.numpy(),
+                         w.scale, rows)
+    go, gl = out.cpu().numpy(), lse.cpu().numpy()
     for b, heads in rows.items():
-        ro, rl = oracle.paged_decode_attn(w.q.numpy()[b:b + 1, heads], kh, v,
-                                          w.block_tables.numpy()[b:b + 1],
-                                          w.seq_lens.numpy()[b:b + 1], w.scale)
-        assert_attention_close(out[b, heads].cpu().numpy()[None], lse[b, heads].cpu().numpy()[None],
-                               ro, rl, f"row {b}")
+        assert_attention_close(go[b, heads], gl[b, heads], ro[b, heads], rl[b, heads],
+                               f"latent agent seq {b}")
+    assert np.isfinite(go).all() and np.isfinite(gl).all()

@@ -20,6 +20,7 @@ import torch
 
 import workloads
 from tests._steps import assert_attention_close
+from tests._util import bits
 
 pytestmark = pytest.mark.gpu
 
@@ -59,18 +60,31 @@ def _call(pkv, name, w, dev, splits, workspace=None):
     return out.cpu().numpy(), lse.cpu().numpy()
 
 
+def _workspace_for(pkv, w, splits):
+    if splits == 0:
+        splits = pkv.decode_auto_splits(w.k_pool, w.v_pool, w.batch, w.num_q_heads,
+                                        w.block_tables.shape[1] * w.block_size)
+    need = pkv.decode_workspace_size(w.batch, w.num_q_heads, w.head_dim_v, splits)
+    return torch.empty(max(need, 16), dtype=torch.uint8, device="cuda")
+
+
 def test_noalloc_matches_workspace_entry_point_twice(pkv):
+    """The same kernels run on the same inputs, so the scratch-free call must
+    give the regular call's bits exactly; the partials only live elsewhere."""
+    import oracle
     dev = "cuda"
     cases = [(workloads.long32k(batch=2, context=8192), 16),
-             (workloads.mix(), 3)]                   # a different shape on the second call
+             (workloads.mix(), 3),                   # a different shape on the second call
+             (workloads.long32k(batch=2, context=8192), 0)]   # the split count chosen inside
     for w, splits in cases:
-        need = pkv.decode_workspace_size(w.batch, w.num_q_heads, w.head_dim_v, splits)
-        ws = torch.empty(need, dtype=torch.uint8, device=dev)
-        ref_o, ref_l = _call(pkv, "workspace", w, dev, splits, ws)
+        ref_o, ref_l = _call(pkv, "workspace", w, dev, splits, _workspace_for(pkv, w, splits))
         got_o, got_l = _call(pkv, "noalloc", w, dev, splits)
         assert np.isfinite(got_o).all()
-        assert_attention_close(got_o, got_l, ref_o.astype(np.float64),
-                               ref_l.astype(np.float64), f"noalloc {w.name}")
+        assert np.array_equal(got_o, ref_o) and np.array_equal(got_l, ref_l), w.name
+    # the num_splits = 0 call against the oracle as well
+    ro, rl = oracle.paged_decode_attn(w.q.numpy(), bits(w.k_pool), bits(w.v_pool),
+                                      w.block_tables.numpy(), w.seq_lens.numpy(), w.scale)
+    assert_attention_close(got_o, got_l, ro, rl, "noalloc, num_splits = 0")
     assert pkv.device_status() == 0
 
 
@@ -98,21 +112,45 @@ def test_noalloc_e4m3_matches_workspace_call_and_oracle(pkv):
     kc, vc = w.k_codes.to(dev), w.v_codes.to(dev)
     ks, vs = w.k_scale.to(dev), w.v_scale.to(dev)
     bt, lens, q = w.block_tables.to(dev), w.seq_lens.to(dev), w.q.to(dev)
-    ref_o, ref_l = pkv.paged_decode_attn_e4m3(q, kc, vc, ks, vs, bt, lens, w.scale, num_splits=5)
     desc = pkv.cache_desc(kc, vc)
     B, Hq = w.batch, w.num_q_heads
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
-    for _ in range(2):
+    ro, rl = oracle.paged_decode_attn_e4m3(w.q.numpy(), w.k_codes.numpy(), w.v_codes.numpy(),
+                                           w.k_scale.numpy(), w.v_scale.numpy(),
+                                           w.block_tables.numpy(), w.seq_lens.numpy(), w.scale)
+    # 5 splits twice in a row, then the split count chosen inside (num_splits = 0)
+    for splits in (5, 5, 0):
+        ref_o, ref_l = pkv.paged_decode_attn_e4m3(q, kc, vc, ks, vs, bt, lens, w.scale,
+                                                  num_splits=splits)
         out = torch.full((B, Hq, w.head_dim_v), float("nan"), device=dev)
         lse = torch.full((B, Hq), float("nan"), device=dev)
         rc = pkv.lib.pkv_paged_decode_attn_noalloc_e4m3(
             ctypes.byref(desc), _ptr(q), B, Hq, _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), _ptr(bt),
-            bt.shape[1], _ptr(lens), ctypes.c_float(w.scale), 5, _ptr(out), _ptr(lse), 0, stream)
+            bt.shape[1], _ptr(lens), ctypes.c_float(w.scale), splits, _ptr(out), _ptr(lse), 0,
+            stream)
         torch.cuda.synchronize()
         assert rc == 0
-        assert torch.equal(out, ref_o) and torch.equal(lse, ref_l)
-    ro, rl = oracle.paged_decode_attn_e4m3(w.q.numpy(), w.k_codes.numpy(), w.v_codes.numpy(),
-                                           w.k_scale.numpy(), w.v_scale.numpy(),
-                                           w.block_tables.numpy(), w.seq_lens.numpy(), w.scale)
-    assert_attention_close(out.cpu().numpy(), lse.cpu().numpy(), ro, rl, "noalloc e4m3")
+        assert torch.equal(out, ref_o) and torch.equal(lse, ref_l), f"splits {splits}"
+        assert_attention_close(out.cpu().numpy(), lse.cpu().numpy(), ro, rl,
+                               f"noalloc e4m3, num_splits = {splits}")
     assert pkv.device_status() == 0
+
+
+def test_noalloc_checks_arguments_before_the_scratch_limit(pkv):
+    """A request the regular entry point rejects gets the same status from
+    the scratch-free one, even when it would also exceed the scratch."""
+    w = workloads.custom(3, [40] * 64, 64, 8, 128, 128, 16)
+    k, v = w.k_pool.cuda(), w.v_pool.cuda()
+    desc = pkv.cache_desc(k, v)
+    out = torch.empty(64, 64, 128, device="cuda")
+    lse = torch.empty(64, 64, device="cuda")
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    args = (ctypes.byref(desc), _ptr(w.q.cuda()), 64, 64, _ptr(k), _ptr(v),
+            _ptr(w.block_tables.cuda()), w.block_tables.shape[1], _ptr(w.seq_lens.cuda()),
+            ctypes.c_float(w.scale))
+    for splits, flags in ((300, 0), (256, 0x40)):     # too many splits; an unknown flag
+        rc_reg = pkv.lib.pkv_paged_decode_attn(*args, splits, None, 0, _ptr(out), _ptr(lse),
+                                               flags, stream)
+        rc_na = pkv.lib.pkv_paged_decode_attn_noalloc(*args, splits, _ptr(out), _ptr(lse), flags,
+                                                      stream)
+        assert rc_reg == rc_na == -1                    # PKV_ERR_INVALID_ARG
