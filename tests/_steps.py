@@ -3,6 +3,8 @@ library (C ABI via the Python binding) and through the CPU oracle.  The two
 share only the seeded inputs from `workloads`."""
 from __future__ import annotations
 
+import ctypes
+
 import numpy as np
 import torch
 
@@ -31,6 +33,15 @@ def assert_attention_close(out, lse, ref_out, ref_lse, where=""):
     rel = np.linalg.norm(d, axis=1) / np.maximum(rn, 1e-30)
     rel = rel[rn > 0]
     assert rel.size == 0 or rel.max() <= ROW_REL_L2, f"{where}: row rel-L2 {rel.max():.3g}"
+
+
+def auto_splits(pkv, w):
+    """The split count num_splits = 0 resolves to for workload `w` on the
+    current device (the library's rule, sized by the table width as the
+    decode call sizes it)."""
+    desc = pkv.CacheDesc(w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim_k, w.head_dim_v)
+    return int(pkv.lib.pkv_decode_auto_splits(ctypes.byref(desc), w.batch, w.num_q_heads,
+                                              w.block_tables.shape[1] * w.block_size))
 
 
 def gpu_step(pkv, w, num_splits=0, flags=0, dev="cuda"):

@@ -16,8 +16,8 @@ import torch
 import oracle
 import workloads
 from bench import DEFAULT_SPLITS          # the split counts the benchmark times
-from tests._steps import (agent_rows, assert_attention_close, gpu_step, oracle_cache,
-                          oracle_step)
+from tests._steps import (agent_rows, assert_attention_close, auto_splits, gpu_step,
+                          oracle_cache, oracle_step)
 from tests._util import bits
 
 pytestmark = pytest.mark.gpu
@@ -43,8 +43,7 @@ def test_long32k_all_rows(pkv, which):
         assert splits == 16
     else:
         splits = 0
-        auto = pkv.decode_auto_splits(w.k_pool, w.v_pool, w.batch, w.num_q_heads,
-                                      w.block_tables.shape[1] * w.block_size)
+        auto = auto_splits(pkv, w)
         assert 1 <= auto <= 256
     out, lse, k, v, slots = gpu_step(pkv, w, num_splits=splits)
     ro, rl, ok_, ov_, oslots = oracle_step(w)

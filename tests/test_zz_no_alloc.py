@@ -19,7 +19,7 @@ import pytest
 import torch
 
 import workloads
-from tests._steps import assert_attention_close
+from tests._steps import assert_attention_close, auto_splits
 from tests._util import bits
 
 pytestmark = pytest.mark.gpu
@@ -62,8 +62,7 @@ def _call(pkv, name, w, dev, splits, workspace=None):
 
 def _workspace_for(pkv, w, splits):
     if splits == 0:
-        splits = pkv.decode_auto_splits(w.k_pool, w.v_pool, w.batch, w.num_q_heads,
-                                        w.block_tables.shape[1] * w.block_size)
+        splits = auto_splits(pkv, w)
     need = pkv.decode_workspace_size(w.batch, w.num_q_heads, w.head_dim_v, splits)
     return torch.empty(max(need, 16), dtype=torch.uint8, device="cuda")
 
