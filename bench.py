@@ -31,6 +31,7 @@ measured peak, and sequence-tokens/s.  Prints one JSON line.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import os
@@ -427,6 +428,49 @@ class AgentStep(Step):
         super().run(ev_a, ev_b)
 
 
+class AgentCascadeStep(AgentStep):
+    """The shared-prefix step with the cascade: every sequence's 128 query
+    rows over the 2,125 shared full blocks as one virtual sequence, each
+    sequence over the rest of its table (copied tail block + suffix), both
+    in one tcgen05 launch, then the merge of the two sets of partials."""
+    kernel_name = ("pkv_paged_decode_attn_cascade (prep + decode_mla_tc_kernel over the prefix "
+                   "and suffix problems in one launch + cascade merge)")
+    bound = "tensor"
+
+    def __init__(self, pkv, w, dev, splits):
+        s1, s2 = splits
+        super().__init__(pkv, w, dev, 1)
+        full = w.info["prefix"] // w.block_size
+        self.ptab = w.block_tables[0, :full].clone().to(dev)
+        mb = w.block_tables.shape[1]
+        self.s1, self.s2 = pkv.decode_cascade_splits(self.k, self.v, w.batch, w.num_q_heads, mb,
+                                                     full, s1, s2)
+        need = pkv.lib.pkv_decode_cascade_workspace_size(
+            ctypes.byref(pkv.cache_desc(self.k, self.v)), w.batch, w.num_q_heads, mb, full,
+            self.s1, self.s2)
+        self.ws = torch.zeros(need, dtype=torch.uint8, device=dev)
+        self.launches = 6   # copy, slot, append, prep, attention (both parts), merge
+        self.desc = (f"copy_blocks ({self.src.numel()} CoW pairs) + slot_mapping + kv_append "
+                     f"({self.new_pos.numel()} decode tokens) + paged_decode_attn_cascade "
+                     f"({full} shared blocks: {self.s1} prefix splits over the "
+                     f"{w.batch * w.num_q_heads} rows of all sequences, {self.s2} suffix "
+                     f"splits; one attention launch) + merge")
+
+    def kernel(self):
+        """The cascade attention call (prep, one attention launch, merge)."""
+        self.pkv.paged_decode_attn_cascade(self.q, self.k, self.v, self.ptab, self.bt, self.lens,
+                                           self.w.scale, prefix_splits=self.s1,
+                                           suffix_splits=self.s2, workspace=self.ws,
+                                           out=self.out, lse=self.lse)
+
+    def attend(self, ev_a=None, ev_b=None):
+        if ev_a is not None:
+            ev_a.record()
+        self.kernel()
+        if ev_b is not None:
+            ev_b.record()
+
+
 class MultiStep(Step):
     """Speculative verification: T new tokens per sequence appended, each
     attending causally to the cache (one pkv_paged_decode_attn_multi)."""
@@ -532,13 +576,13 @@ class MultiE4m3Step(E4m3Step):
 
 
 STEPS = {"long32k": Step, "mix": Step, "tiny": Step, "dcp200k": DcpStep, "agent_mla": AgentStep,
-         "agent_mla_latent": AgentStep, "spec4_32k": MultiStep, "long32k_e4m3": E4m3Step,
+         "agent_mla_latent": AgentStep, "agent_mla_cascade": AgentCascadeStep, "spec4_32k": MultiStep, "long32k_e4m3": E4m3Step,
          "dcp200k_e4m3": DcpE4m3Step, "spec4_32k_e4m3": MultiE4m3Step}
 # The 32K workload is timed at 16 splits, the split count its configuration
 # names; the split count the library picks by itself (num_splits = 0) is
 # timed too and reported beside it (`library_auto_splits`).
 DEFAULT_SPLITS = {"long32k": 16, "mix": 1, "tiny": 1, "dcp200k": 19, "agent_mla": 19,
-                  "agent_mla_latent": 19, "spec4_32k": 9, "long32k_e4m3": 7,
+                  "agent_mla_latent": 19, "agent_mla_cascade": (19, 2), "spec4_32k": 9, "long32k_e4m3": 7,
                   "dcp200k_e4m3": 14, "spec4_32k_e4m3": 9}
 # Workloads whose line also carries the library's own split choice.
 AUTO_SPLITS_ALSO = ("long32k",)
@@ -623,6 +667,15 @@ def oracle_gbs(w, tokens: int | None, repeats: int = 1, num_threads: int = 0):
     return used, times
 
 
+def workload_splits(args):
+    """The split count of the workload (a (prefix, suffix) pair for the
+    cascade), --splits / --suffix-splits overriding the defaults."""
+    d = DEFAULT_SPLITS[args.workload]
+    if isinstance(d, tuple):
+        return (args.splits or d[0], args.suffix_splits or d[1])
+    return args.splits or d
+
+
 def workload_desc(w, splits):
     kv = (f"head_dim {w.head_dim_k}, values = first {w.head_dim_v} dims of each key row, bf16"
           if w.v_pool is None else
@@ -630,8 +683,9 @@ def workload_desc(w, splits):
           if w.k_codes is not None else f"head_dim {w.head_dim_k}, bf16 K/V")
     return (f"{w.name}: batch {w.batch} x {int(w.seq_lens.max())} tokens, GQA "
             f"{w.num_q_heads}/{w.num_kv_heads} heads, {kv}, block "
-            f"{w.block_size}, {w.num_blocks}-block randomly permuted pool, {splits} splits + "
-            f"lse_merge")
+            f"{w.block_size}, {w.num_blocks}-block randomly permuted pool, " +
+            (f"cascade: {splits[0]} prefix + {splits[1]} suffix splits + merge"
+             if isinstance(splits, tuple) else f"{splits} splits + lse_merge"))
 
 
 def run_reference(args, world, rank):
@@ -661,7 +715,7 @@ def run_reference(args, world, rank):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * wall / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": workload_desc(w, args.splits or DEFAULT_SPLITS[args.workload]),
+        "config": {"workload": workload_desc(w, workload_splits(args)),
                    "oracle": "C, fp64, all host cores"},
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": cores,
                          "kind": "oracle", "sample": sample},
@@ -826,7 +880,7 @@ def run_gpu(args, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     w = workloads.make(args.workload)
-    splits = args.splits or DEFAULT_SPLITS[args.workload]
+    splits = workload_splits(args)
     st = STEPS[args.workload](pkv, w, dev, splits)
     total_bytes, kernel_bytes = step_bytes(w, splits)
     stream = torch.cuda.current_stream()
@@ -1072,6 +1126,8 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default="long32k", choices=sorted(STEPS))
     ap.add_argument("--splits", type=int, default=0, help="0 = the workload's default")
+    ap.add_argument("--suffix-splits", type=int, default=0,
+                    help="cascade workload: suffix split count (0 = the default)")
     ap.add_argument("--quick-cpu", action="store_true", help="smaller oracle sample")
     ap.add_argument("--eager", action="store_true",
                     help="time the calls made one by one instead of a CUDA-graph replay")

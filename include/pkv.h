@@ -78,6 +78,8 @@ typedef enum pkv_status {
                                        destination is another pair's source */
 #define PKV_DEV_TIMEOUT       0x10u /* a pipeline wait gave up (library bug) */
 #define PKV_DEV_TABLE_RANGE   0x20u /* a position past the end of its table row */
+#define PKV_DEV_PREFIX        0x40u /* cascade: a table that does not begin with the
+                                       shared prefix blocks */
 
 /* Shape of one layer's paged KV cache. */
 typedef struct pkv_cache_desc {
@@ -412,6 +414,53 @@ int pkv_paged_decode_attn_multi_e4m3(const pkv_cache_desc *cache, const float *q
                                      const int32_t *seq_lens, float scale, int32_t num_splits,
                                      void *workspace, size_t workspace_bytes, float *out,
                                      float *lse, int32_t flags, pkv_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * pkv_paged_decode_attn_cascade -- decode attention for sequences that share
+ * a prefix.  [PA] "共通ブロックの共有とコピーオンライト": sequences with a common
+ * prefix point their block tables at the same physical blocks; [AX]
+ * "エージェントワークロードの特性": agent traffic re-sends long shared prefixes.
+ * The result is pkv_paged_decode_attn's (same q, pools, tables, lengths,
+ * scale, out and lse layouts) for tables whose first prefix_blocks entries
+ * are prefix_table[0 .. prefix_blocks) (int32 device array), computed as a
+ * cascade over the P = prefix_blocks * block_size shared tokens:
+ *   1. every query row of every sequence attends to tokens [0, P) through
+ *      prefix_table: the batch x num_q_heads rows form one sequence, so each
+ *      staged prefix tile serves all the rows that need it (prefix_splits
+ *      chunks);
+ *   2. each sequence's rows attend to its own tokens [P, seq_lens[b])
+ *      through the rest of its table row (suffix_splits chunks);
+ *   3. the partials of 1 and 2 are merged as pkv_lse_merge merges.
+ * A table that does not begin with prefix_table sets PKV_DEV_PREFIX (its
+ * rows still use prefix_table for the first P tokens); seq_lens[b] < P sets
+ * PKV_DEV_SEQ_LEN.  prefix_blocks may be 0 (no shared part) up to
+ * max_blocks.  Split counts: 0 = chosen by pkv_decode_cascade_splits, else
+ * 1..256.  workspace: at least pkv_decode_cascade_workspace_size(...) bytes,
+ * 16-byte aligned; its contents on entry do not matter.  flags: 0, or
+ * PKV_DECODE_GENERIC / PKV_DECODE_NO_TCGEN05 as for pkv_paged_decode_attn.
+ * With flags 0 and query groups that are a multiple of 64 heads on the
+ * tcgen05 kernel's head dims, both parts run in ONE launch of that kernel
+ * (the suffix items fill the tail of the prefix items); otherwise as two
+ * launches of whichever split kernel takes each part's shape.
+ * ------------------------------------------------------------------------- */
+/* Resolves zero split counts in *prefix_splits / *suffix_splits (others are
+ * left as given) for the current device.  PKV_OK or PKV_ERR_INVALID_ARG. */
+int pkv_decode_cascade_splits(const pkv_cache_desc *cache, int32_t batch, int32_t num_q_heads,
+                              int32_t max_blocks, int32_t prefix_blocks,
+                              int32_t *prefix_splits, int32_t *suffix_splits);
+
+size_t pkv_decode_cascade_workspace_size(const pkv_cache_desc *cache, int32_t batch,
+                                         int32_t num_q_heads, int32_t max_blocks,
+                                         int32_t prefix_blocks, int32_t prefix_splits,
+                                         int32_t suffix_splits);
+
+int pkv_paged_decode_attn_cascade(const pkv_cache_desc *cache, const float *q, int32_t batch,
+                                  int32_t num_q_heads, const void *k_pool, const void *v_pool,
+                                  const int32_t *prefix_table, int32_t prefix_blocks,
+                                  const int32_t *block_tables, int32_t max_blocks,
+                                  const int32_t *seq_lens, float scale, int32_t prefix_splits,
+                                  int32_t suffix_splits, void *workspace, size_t workspace_bytes,
+                                  float *out, float *lse, int32_t flags, pkv_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * pkv_lse_merge -- [DCP] decode step, stage 3: correct each partial output

@@ -20,15 +20,16 @@ import torch
 
 from . import _lib
 from ._lib import (DECODE_GENERIC, DECODE_NO_TCGEN05, DECODE_TEST_WITHHOLD, DEV_BLOCK_ID,
-                   DEV_COPY_CONFLICT, DEV_SEQ_LEN, DEV_SLOT, DEV_TABLE_RANGE, DEV_TIMEOUT, CacheDesc,
-                   PkvError)
+                   DEV_COPY_CONFLICT, DEV_PREFIX, DEV_SEQ_LEN, DEV_SLOT, DEV_TABLE_RANGE,
+                   DEV_TIMEOUT, CacheDesc, PkvError)
 
 __all__ = [
     "CacheDesc", "PkvError", "ValuesInKeys", "cache_desc", "kv_append", "slot_mapping", "copy_blocks",
     "interleave_slot_mapping", "interleave_partition_len", "decode_workspace_size",
     "decode_auto_splits", "paged_decode_attn", "paged_decode_attn_partial",
     "paged_decode_attn_multi", "lse_merge", "kv_append_e4m3", "copy_blocks_e4m3",
-    "paged_decode_attn_e4m3", "paged_decode_attn_multi_e4m3",
+    "paged_decode_attn_e4m3", "paged_decode_attn_multi_e4m3", "paged_decode_attn_cascade",
+    "decode_cascade_splits", "DEV_PREFIX",
     "device_status", "BlockManager", "library_path", "DECODE_GENERIC", "DECODE_NO_TCGEN05",
     "DECODE_TEST_WITHHOLD", "DEV_BLOCK_ID",
     "DEV_SLOT", "DEV_SEQ_LEN", "DEV_COPY_CONFLICT", "DEV_TIMEOUT", "DEV_TABLE_RANGE",
@@ -241,6 +242,46 @@ def paged_decode_attn(q, k_pool, v_pool, block_tables, seq_lens, scale: float,
         ctypes.byref(desc), _ptr(q), B, Hq, _ptr(k_pool), _v_ptr(v_pool), _ptr(block_tables),
         block_tables.shape[1], _ptr(seq_lens), float(scale), S, _ptr(workspace), ws_bytes,
         _ptr(out), _ptr(lse), int(flags), _stream(stream)))
+    return out, lse
+
+
+def decode_cascade_splits(k_pool, v_pool, batch: int, num_q_heads: int, max_blocks: int,
+                          prefix_blocks: int, prefix_splits: int = 0,
+                          suffix_splits: int = 0) -> tuple[int, int]:
+    """The (prefix, suffix) split counts a cascade call uses (0 = chosen)."""
+    desc = cache_desc(k_pool, v_pool)
+    s1, s2 = ctypes.c_int32(prefix_splits), ctypes.c_int32(suffix_splits)
+    _check("pkv_decode_cascade_splits", lib.pkv_decode_cascade_splits(
+        ctypes.byref(desc), batch, num_q_heads, max_blocks, prefix_blocks, ctypes.byref(s1),
+        ctypes.byref(s2)))
+    return int(s1.value), int(s2.value)
+
+
+def paged_decode_attn_cascade(q, k_pool, v_pool, prefix_table, block_tables, seq_lens,
+                              scale: float, prefix_splits: int = 0, suffix_splits: int = 0,
+                              workspace=None, out=None, lse=None, flags: int = 0, stream=None):
+    """Decode attention of q [B, Hq, Dk] for sequences whose tables begin with
+    the shared blocks `prefix_table` [prefix_blocks] int32 -> (out, lse), as a
+    cascade: all rows over the shared prefix, each sequence over its rest,
+    merged.  Same result as paged_decode_attn on those tables."""
+    desc = _decode_common(q, k_pool, v_pool, block_tables, seq_lens)
+    _need(prefix_table, "prefix_table", torch.int32, 1)
+    B, Hq, _ = q.shape
+    if out is None:
+        out = torch.empty(B, Hq, desc.head_dim_v, dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty(B, Hq, dtype=torch.float32, device=q.device)
+    P, mb = prefix_table.shape[0], block_tables.shape[1]
+    need = int(lib.pkv_decode_cascade_workspace_size(ctypes.byref(desc), B, Hq, mb, P,
+                                                     int(prefix_splits), int(suffix_splits)))
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("pkv_paged_decode_attn_cascade", lib.pkv_paged_decode_attn_cascade(
+        ctypes.byref(desc), _ptr(q), B, Hq, _ptr(k_pool), _v_ptr(v_pool), _ptr(prefix_table), P,
+        _ptr(block_tables), mb, _ptr(seq_lens), float(scale), int(prefix_splits),
+        int(suffix_splits), _ptr(workspace), ws_bytes, _ptr(out), _ptr(lse), int(flags),
+        _stream(stream)))
     return out, lse
 
 

@@ -69,7 +69,13 @@ def build(verbose: bool = False) -> str:
     sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
     with ThreadPoolExecutor(max_workers=min(8, len(sources))) as ex:
         objs = list(ex.map(lambda s: _compile(s, headers, verbose), sources))
-    if os.path.exists(LIB) and not any(os.path.getmtime(o) > os.path.getmtime(LIB) for o in objs):
+    # the library is current if no object is newer and it was linked from
+    # exactly these objects (a removed source must not survive in it)
+    stamp = os.path.join(BUILD, "libpkv.objects")
+    listing = "\n".join(sorted(os.path.basename(o) for o in objs))
+    linked = open(stamp).read() if os.path.exists(stamp) else None
+    if (os.path.exists(LIB) and linked == listing and
+            not any(os.path.getmtime(o) > os.path.getmtime(LIB) for o in objs)):
         return LIB
     tmp = LIB + f".{os.getpid()}.tmp"
     cmd = [_nvcc(), *ARCH, "-shared", "-Xcompiler", "-fPIC", "-o", tmp, *objs]
@@ -77,6 +83,8 @@ def build(verbose: bool = False) -> str:
     if res.returncode != 0:
         raise RuntimeError(f"linking libpkv.so failed:\n{res.stdout}\n{res.stderr}")
     os.replace(tmp, LIB)
+    with open(stamp, "w") as f:
+        f.write(listing)
     return LIB
 
 

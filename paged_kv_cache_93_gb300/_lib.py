@@ -23,6 +23,7 @@ DEV_SEQ_LEN = 0x4
 DEV_COPY_CONFLICT = 0x8
 DEV_TIMEOUT = 0x10
 DEV_TABLE_RANGE = 0x20
+DEV_PREFIX = 0x40
 DECODE_GENERIC = 0x1
 DECODE_NO_TCGEN05 = 0x2
 DECODE_TEST_WITHHOLD = 0x100      # test control of the failure path (see pkv.h)
@@ -75,6 +76,12 @@ SIGNATURES = {
                                                         _P, _P, _P, _i32, _P, _f32, _i32, _P,
                                                         _sz, _P, _P, _i32, _P]),
     "pkv_lse_merge": (ctypes.c_int, [_i32, _P, _P, _i64, _i32, _P, _P, _P]),
+    "pkv_decode_cascade_splits": (ctypes.c_int, [_DESC, _i32, _i32, _i32, _i32,
+                                                 ctypes.POINTER(_i32), ctypes.POINTER(_i32)]),
+    "pkv_decode_cascade_workspace_size": (_sz, [_DESC, _i32, _i32, _i32, _i32, _i32, _i32]),
+    "pkv_paged_decode_attn_cascade": (ctypes.c_int, [_DESC, _P, _i32, _i32, _P, _P, _P, _i32, _P,
+                                                     _i32, _P, _f32, _i32, _i32, _P, _sz, _P, _P,
+                                                     _i32, _P]),
     "pkv_test_enable_withhold": (ctypes.c_int, [ctypes.c_int]),
     "pkv_bm_create": (_P, [_i32, _i32, _P]),
     "pkv_bm_destroy": (None, [_P]),

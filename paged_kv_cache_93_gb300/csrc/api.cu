@@ -145,6 +145,10 @@ int run_split_kernel(const DecodeArgs &a, int32_t flags) {
 
 }  // namespace
 
+namespace pkv {
+int run_decode_split_kernel(const DecodeArgs &a, int32_t flags) { return run_split_kernel(a, flags); }
+}  // namespace pkv
+
 extern "C" int pkv_test_enable_withhold(int enable) {
     g_test_withhold_enabled.store(enable ? 1 : 0);
     return PKV_OK;

@@ -129,28 +129,76 @@ __device__ __forceinline__ void ld_scores(uint32_t ts, int c, uint32_t (&v)[16])
         v[k] = __float_as_uint(__uint_as_float(v[k]) + __uint_as_float(lo[k]));
 }
 
+// One decode problem of a launch: its queries, tables, lengths, split count
+// and partial outputs.  A launch runs one problem, or two in one item space
+// (the cascade: every sequence's query rows over a shared prefix, and each
+// sequence's rows over its own remaining tokens).
+struct Problem {
+    const float *q;
+    const int32_t *block_tables;
+    const int32_t *seq_lens;
+    float *out_part, *lse_part;
+    int32_t batch, num_q_heads, max_blocks, num_splits;
+};
+
+Problem problem_of(const DecodeArgs &a) {
+    return Problem{a.q, a.block_tables, a.seq_lens, a.out_part, a.lse_part,
+                   a.batch, a.num_q_heads, a.max_blocks, a.num_splits};
+}
+
+// Work items of a problem: (sequence, KV head, 64-head group, split).
+__host__ __device__ inline int problem_items(const Problem &p, int hkv) {
+    return p.batch * hkv * (p.num_q_heads / hkv / kN) * p.num_splits;
+}
+
+// The problem an item of the launch belongs to (field by field, so the
+// selection stays in registers).
+__device__ __forceinline__ Problem pick(const Problem &p0, const Problem &p1, bool second) {
+    Problem r;
+    r.q = second ? p1.q : p0.q;
+    r.block_tables = second ? p1.block_tables : p0.block_tables;
+    r.seq_lens = second ? p1.seq_lens : p0.seq_lens;
+    r.out_part = second ? p1.out_part : p0.out_part;
+    r.lse_part = second ? p1.lse_part : p0.lse_part;
+    r.batch = second ? p1.batch : p0.batch;
+    r.num_q_heads = second ? p1.num_q_heads : p0.num_q_heads;
+    r.max_blocks = second ? p1.max_blocks : p0.max_blocks;
+    r.num_splits = second ? p1.num_splits : p0.num_splits;
+    return r;
+}
+
 struct TcItem {
+    Problem p;
+    int G;              // query heads per KV head of the item's problem
     int b, g, hg, s;
     int64_t begin, end;
     int ntiles;
 };
 
-__device__ __forceinline__ TcItem tc_item(const DecodeArgs &a, int item, int groups,
-                                          bool report) {
+// Item `item` of the launch: the first problem's items come first.
+__device__ __forceinline__ TcItem tc_item(const DecodeArgs &a, const Problem &p0,
+                                          const Problem &p1, int item, bool report) {
     TcItem r;
-    const int per_split = a.batch * a.cache.num_kv_heads * groups;
+    const int hkv = a.cache.num_kv_heads;
+    const int n0 = problem_items(p0, hkv);
+    const bool second = item >= n0;
+    r.p = pick(p0, p1, second);
+    if (second) item -= n0;
+    r.G = r.p.num_q_heads / hkv;
+    const int groups = r.G / kN;
+    const int per_split = r.p.batch * hkv * groups;
     r.s = item / per_split;
     int t = item % per_split;
     r.hg = t % groups;
     t /= groups;
-    r.g = t % a.cache.num_kv_heads;
-    r.b = t / a.cache.num_kv_heads;
-    int64_t L = a.seq_lens[r.b];
-    if (L < 0 || L > int64_t(a.max_blocks) * a.cache.block_size) {
+    r.g = t % hkv;
+    r.b = t / hkv;
+    int64_t L = r.p.seq_lens[r.b];
+    if (L < 0 || L > int64_t(r.p.max_blocks) * a.cache.block_size) {
         if (report && r.s == 0 && r.hg == 0 && r.g == 0) raise_status(a.status, PKV_DEV_SEQ_LEN);
         L = 0;
     }
-    const int64_t chunk = 64 * ((L + 64LL * a.num_splits - 1) / (64LL * a.num_splits));
+    const int64_t chunk = 64 * ((L + 64LL * r.p.num_splits - 1) / (64LL * r.p.num_splits));
     r.begin = int64_t(r.s) * chunk;
     r.end = lmin(L, r.begin + chunk);
     r.ntiles = r.end > r.begin ? int((r.end - r.begin + kM - 1) / kM) : 0;
@@ -166,7 +214,7 @@ __device__ __forceinline__ uint32_t swz(int row, int col) {
 __global__ void __launch_bounds__(kThreads, 1)
 decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                      const __grid_constant__ CUtensorMap tmap_v, const DecodeArgs a,
-                     const TcShape shp) {
+                     const Problem p0, const Problem p1, const TcShape shp) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -180,10 +228,8 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     auto bar = [&](int i) { return sb + sm.bars + 8u * uint32_t(i); };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int G = a.num_q_heads / a.cache.num_kv_heads;
-    const int groups = G / kN;
-    const int num_items = a.batch * a.cache.num_kv_heads * groups * a.num_splits;
     const int bs = a.cache.block_size, hkv = a.cache.num_kv_heads;
+    const int num_items = problem_items(p0, hkv) + problem_items(p1, hkv);
     const int Dk = shp.dk_segs * 64, Dv = shp.dv_blocks * 128;
     const uint64_t wlim = a.wait_ns ? a.wait_ns : kWaitLimitNs;
 
@@ -242,29 +288,36 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
             }
         };
         for (int item = blockIdx.x; item < num_items && ok; item += gridDim.x) {
-            const TcItem r = tc_item(a, item, groups, false);
+            const TcItem r = tc_item(a, p0, p1, item, false);
             if (r.ntiles == 0) continue;
-            const int32_t *table = a.block_tables + int64_t(r.b) * a.max_blocks;
+            const int32_t *table = r.p.block_tables + int64_t(r.b) * r.p.max_blocks;
             // Rows of block 0 of this KV head stand in for a half tile past
             // the end (its values are masked and its V rows zeroed).
             const int32_t standin = r.g * bs;
             int32_t yp0 = standin, yp1 = standin;
+            // Lane j holds the pool row of half tile (64 tokens) wbase + j:
+            // one coalesced load of table entries serves 16 tiles, so the
+            // ring is not left to drain behind a dependent load every tile.
+            int32_t wrow = standin;
+            int wbase = -64;
             for (int i = 0; i <= r.ntiles && ok; ++i) {
                 int32_t y0 = standin, y1 = standin;
                 if (i < r.ntiles) {
-                    int32_t y = standin;
-                    if (lane < 2) {
-                        const int64_t t = r.begin + int64_t(i) * kM + lane * kHalf;
+                    const int u0 = 2 * i;
+                    if (u0 >= wbase + 32) {
+                        wbase = u0;
+                        wrow = standin;
+                        const int64_t t = r.begin + int64_t(wbase + lane) * kHalf;
                         if (t < r.end) {
                             const int32_t phys = table[t / bs];
                             if (phys >= 0 && phys < a.cache.num_blocks)
-                                y = (phys * hkv + r.g) * bs + int32_t(t % bs);
+                                wrow = (phys * hkv + r.g) * bs + int32_t(t % bs);
                             else
                                 raise_status(a.status, PKV_DEV_BLOCK_ID);
                         }
                     }
-                    y0 = __shfl_sync(0xffffffffu, y, 0);
-                    y1 = __shfl_sync(0xffffffffu, y, 1);
+                    y0 = __shfl_sync(0xffffffffu, wrow, u0 - wbase);
+                    y1 = __shfl_sync(0xffffffffu, wrow, u0 + 1 - wbase);
                     for (int seg = 0; seg < shp.dk_segs; ++seg) {
                         uint32_t dst;
                         if (!acquire(dst)) {
@@ -319,7 +372,7 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
             }
         };
         for (int item = blockIdx.x; item < num_items && ok; item += gridDim.x) {
-            const TcItem r = tc_item(a, item, groups, false);
+            const TcItem r = tc_item(a, p0, p1, item, false);
             if (r.ntiles == 0) continue;
             if (!(ok = wait_all(bar(kBarQFull), ne & 1u))) break;
             for (int i = 0; i <= r.ntiles && ok; ++i) {
@@ -424,25 +477,25 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
         // An item this CTA gives up on (a wait ran out) reports every one of
         // its rows as NaN, output and LSE; so does every later item of the CTA.
         bool abandoned = false;
-        auto abandon_rows = [&](int64_t orow0) {
-            float4 *o = reinterpret_cast<float4 *>(a.out_part + orow0 * Dv);
+        auto abandon_rows = [&](const Problem &p, int64_t orow0) {
+            float4 *o = reinterpret_cast<float4 *>(p.out_part + orow0 * Dv);
             const float nan = __int_as_float(0x7fc00000);
             for (int i = t; i < kN * Dv / 4; i += kSoftThreads) o[i] = make_float4(nan, nan, nan, nan);
-            if (t < kN) a.lse_part[orow0 + t] = nan;
+            if (t < kN) p.lse_part[orow0 + t] = nan;
         };
         for (int item = blockIdx.x; item < num_items; item += gridDim.x) {
-            const TcItem r = tc_item(a, item, groups, t == 0);
-            const int head0 = r.g * G + r.hg * kN;
-            const int64_t orow0 = (int64_t(r.s) * a.batch + r.b) * a.num_q_heads + head0;
+            const TcItem r = tc_item(a, p0, p1, item, t == 0);
+            const int head0 = r.g * r.G + r.hg * kN;
+            const int64_t orow0 = (int64_t(r.s) * r.p.batch + r.b) * r.p.num_q_heads + head0;
             if (abandoned) {
-                abandon_rows(orow0);
+                abandon_rows(r.p, orow0);
                 continue;
             }
             if (r.ntiles == 0) {
-                float4 *o = reinterpret_cast<float4 *>(a.out_part + orow0 * Dv);
+                float4 *o = reinterpret_cast<float4 *>(r.p.out_part + orow0 * Dv);
                 for (int i = t; i < kN * Dv / 4; i += kSoftThreads)
                     o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (t < kN) a.lse_part[orow0 + t] = -INFINITY;
+                if (t < kN) r.p.lse_part[orow0 + t] = -INFINITY;
                 continue;
             }
             // ---- the group's queries, pre-scaled by scale*log2(e), as bf16 hi + lo
@@ -452,7 +505,7 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 // (the query is 147 KB at Dk = 576: one load at a time would
                 // leave the item's first tile waiting on ~150 L2 round trips)
                 const float4 *qsrc = reinterpret_cast<const float4 *>(
-                    a.q + (int64_t(r.b) * a.num_q_heads + head0) * Dk);
+                    r.p.q + (int64_t(r.b) * r.p.num_q_heads + head0) * Dk);
                 const int n4 = kN * Dk / 4;
                 for (int i0 = 0; i0 < n4; i0 += 8 * kSoftThreads) {
                     float4 x[8];
@@ -486,7 +539,7 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
             for (int h = 0; h < kN; ++h) l_part[h] = 0.f;
             if (softmax_bar_or(!w)) {
                 abandoned = true;
-                abandon_rows(orow0);
+                abandon_rows(r.p, orow0);
                 continue;
             }
 
@@ -615,7 +668,7 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
             }
             if (!ok) {
                 abandoned = true;
-                abandon_rows(orow0);
+                abandon_rows(r.p, orow0);
                 continue;
             }
 
@@ -637,12 +690,12 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
             if (t < kN) {
                 const float l = (red[t] + red[kN + t]) + (red[2 * kN + t] + red[3 * kN + t]);
                 aux[t] = l > 0.f ? 1.f / l : 0.f;
-                a.lse_part[orow0 + t] = l > 0.f ? (mrow[t] + log2f(l)) * kLn2 : -INFINITY;
+                r.p.lse_part[orow0 + t] = l > 0.f ? (mrow[t] + log2f(l)) * kLn2 : -INFINITY;
             }
             named_barrier_sync(1, kSoftThreads);
             if (w) {
                 for (int vb = 0; vb < shp.dv_blocks; ++vb) {
-                    float *orow = a.out_part + orow0 * Dv + vb * 128 + row;
+                    float *orow = r.p.out_part + orow0 * Dv + vb * 128 + row;
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         uint32_t v[16];
@@ -660,7 +713,7 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
             ++ne;
             if (softmax_bar_or(!w)) {
                 abandoned = true;
-                abandon_rows(orow0);
+                abandon_rows(r.p, orow0);
             }
         }
     }
@@ -728,7 +781,9 @@ int32_t mla_tc_work_units(const pkv_cache_desc &c, int32_t batch, int32_t num_q_
     return batch * num_q_heads / kN;
 }
 
-int launch_decode_mla_tc(const DecodeArgs &a) {
+namespace {
+// One launch over the problems' items together (p1.batch = 0: one problem).
+int launch_problems(const DecodeArgs &a, const Problem &p0, const Problem &p1) {
     const TcShape shp = tc_shape(a.cache);
     const int64_t rows = int64_t(a.cache.num_blocks) * a.cache.num_kv_heads * a.cache.block_size;
     CUtensorMap tk, tv;
@@ -746,12 +801,23 @@ int launch_decode_mla_tc(const DecodeArgs &a) {
             return PKV_ERR_CUDA;
         configured_dev = dev;
     }
-    const int G = a.num_q_heads / a.cache.num_kv_heads;
-    const int64_t items = int64_t(a.batch) * a.cache.num_kv_heads * (G / kN) * a.num_splits;
+    const int hkv = a.cache.num_kv_heads;
+    const int64_t items = int64_t(problem_items(p0, hkv)) + problem_items(p1, hkv);
     const int grid = int(std::min<int64_t>(items, sm_count()));
     if (grid <= 0) return PKV_OK;
     return launch_pdl(decode_mla_tc_kernel, dim3(grid), dim3(kThreads), smem, a.stream, tk, tv,
-                      a, shp);
+                      a, p0, p1, shp);
+}
+}  // namespace
+
+int launch_decode_mla_tc(const DecodeArgs &a) {
+    Problem none = problem_of(a);
+    none.batch = 0;
+    return launch_problems(a, problem_of(a), none);
+}
+
+int launch_decode_mla_tc_two(const DecodeArgs &first, const DecodeArgs &second) {
+    return launch_problems(first, problem_of(first), problem_of(second));
 }
 
 }  // namespace pkv

@@ -134,6 +134,13 @@ int launch_decode_mla(const DecodeArgs &a);
 bool mla_tc_kernel_supports(const pkv_cache_desc &c, int32_t num_q_heads);
 int32_t mla_tc_work_units(const pkv_cache_desc &c, int32_t batch, int32_t num_q_heads);
 int launch_decode_mla_tc(const DecodeArgs &a);
+// Two problems over the same cache in one launch of that kernel (their work
+// items walked together, the first problem's first); `second` supplies only
+// its queries, tables, lengths, batch, heads, split count and partials.
+int launch_decode_mla_tc_two(const DecodeArgs &first, const DecodeArgs &second);
+// The split kernel pkv_paged_decode_attn would launch for `a` (by shape and
+// flags); writes a.out_part / a.lse_part as [S][batch][heads] partials.
+int run_decode_split_kernel(const DecodeArgs &a, int32_t flags);
 int launch_decode_generic(const DecodeArgs &a);
 // The same over E4M3 pools (a.k_scale, a.v_scale set).
 int launch_decode_generic_e4m3(const DecodeArgs &a);

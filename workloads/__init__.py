@@ -294,6 +294,40 @@ def custom(seed: int, cached: list[int], hq: int, hkv: int, dk: int, dv: int, bs
                     new_seq, new_pos, k_new, v_new)
 
 
+def shared_prefix(seed: int, prefix_blocks: int, suffix_cached: list[int], hq: int, hkv: int,
+                  dk: int, dv: int, bs: int, latent: bool = False) -> Workload:
+    """Sequences whose first `prefix_blocks` table entries are the same
+    physical blocks, each followed by its own blocks: sequence b holds
+    prefix_blocks * bs + suffix_cached[b] tokens, then one decode token.
+    info["prefix_table"] holds the shared blocks.  latent: no value pool."""
+    g = torch.Generator().manual_seed(seed)
+    B = len(suffix_cached)
+    P = prefix_blocks * bs
+    lens = [P + c + 1 for c in suffix_cached]
+    own = [_ceil_div(n, bs) - prefix_blocks for n in lens]
+    num_blocks = prefix_blocks + sum(own) + 2
+    perm = torch.randperm(num_blocks, generator=g)
+    width = prefix_blocks + max(own)
+    tables = torch.full((B, width), -1, dtype=torch.int32)
+    tables[:, :prefix_blocks] = perm[:prefix_blocks].to(torch.int32)
+    at = prefix_blocks
+    for b in range(B):
+        tables[b, prefix_blocks:prefix_blocks + own[b]] = perm[at:at + own[b]].to(torch.int32)
+        at += own[b]
+    k_pool = _normal(g, (num_blocks, hkv, bs, dk), torch.bfloat16)
+    v_pool = None if latent else _normal(g, (num_blocks, hkv, bs, dv), torch.bfloat16)
+    q = _normal(g, (B, hq, dk))
+    new_seq, new_pos, k_new, v_new = _decode_tokens(g, [P + c for c in suffix_cached], hkv,
+                                                    dk, dv)
+    if latent:
+        v_new = None
+    w = Workload("shared_prefix", hq, hkv, dk, dv, bs, q, k_pool, v_pool, tables,
+                 torch.tensor(lens, dtype=torch.int32), 1.0 / math.sqrt(dk),
+                 new_seq, new_pos, k_new, v_new)
+    w.info = {"prefix_table": tables[0, :prefix_blocks].clone()}
+    return w
+
+
 def e4m3(w: Workload, seed: int = 11) -> Workload:
     """The same step over an FP8 (E4M3) cache.  Each KV head gets scales near
     8/448 (so an 8-sigma value is the largest code); the cache before the
@@ -326,6 +360,8 @@ def make(name: str, **kw) -> Workload:
         return e4m3(dcp200k(**kw))
     if name == "agent_mla_latent":
         return agent_mla(latent=True, **kw)
+    if name == "agent_mla_cascade":
+        return agent_mla(**kw)
     if name == "spec4_32k":
         return spec_verify(**kw)
     return {"tiny": tiny, "mix": mix, "long32k": long32k, "dcp200k": dcp200k,
