@@ -58,6 +58,16 @@
 #ifndef PKV_E4M3_R8_CTAS
 #define PKV_E4M3_R8_CTAS 3
 #endif
+// Groups of 16: two CTAs per SM, each with two softmax warp groups of four
+// warps (8 rows each) and the probabilities MN-major (a token's terms stored
+// with one 16-byte store per term half) -- the 16-row softmax was bound by
+// its own instruction chain per warp -- and four ring stages.
+#ifndef PKV_E4M3_R16_SG
+#define PKV_E4M3_R16_SG 2
+#endif
+#ifndef PKV_E4M3_R16_RING
+#define PKV_E4M3_R16_RING 4
+#endif
 
 namespace pkv {
 namespace {
@@ -65,25 +75,36 @@ namespace {
 constexpr int kM = 128;                 // tokens per tile
 constexpr int kD = 128;                 // head dim (bytes of an E4M3 row)
 constexpr int kStage = kM * kD;         // one K or V tile: 16 KB
-constexpr int kThreads = 192;
 constexpr int kSoftWarp0 = 2;
 constexpr int kSoftThreads = 128;
 constexpr int kQTerms = 4, kPTerms = 5;
+// The value product of tile i is issued after the score product of tile
+// i + kLag (and the producer loads V of tile i after K of tile i + kLag).
+// Measured at 16 rows over 8 x 32K: a lag of two (the score product of tile
+// i + 1 no longer queued behind the probabilities of tile i - 1) was no
+// faster than one, and slower at 8 rows (value stages held a tile longer).
+constexpr int kLag = 1;
 constexpr float kSlack = 8.f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-// Rows R per item, ring stages, CTAs per SM.
-template <int R, int RING, int CTAS>
+// Rows R per item, ring stages, CTAs per SM, softmax warp groups SG (each
+// of four warps, one thread per token lane, taking R / SG of the rows), and
+// the probability operand's layout: PMN = MN-major (a token's terms
+// contiguous: [128 tokens][128 B], N = 128, so a thread stores its terms
+// with one vector store per term), else K-major ([NP rows][128 tokens],
+// one byte store per term and row).
+template <int R, int RING, int CTAS, int SG, bool PMN>
 struct Cfg {
     static constexpr int kRing = RING;
     static constexpr int kCtas = CTAS;
+    static constexpr int kThreads = 64 + 128 * SG;
     static constexpr int kNQ = kQTerms * R;                         // score MMA N
-    static constexpr int kNP = (kPTerms * R + 15) / 16 * 16;        // value MMA N
+    static constexpr int kNP = PMN ? 128 : (kPTerms * R + 15) / 16 * 16;   // value MMA N
     static constexpr uint32_t kColO = 2 * kNQ;                      // S^T buffers first
     static constexpr uint32_t kTmemCols =
         2 * kNQ + kNP <= 64 ? 64 : 2 * kNQ + kNP <= 128 ? 128 : 256;
-    static constexpr uint32_t kPBytes = kNP * 128;                  // [NP rows][128 tokens]
+    static constexpr uint32_t kPBytes = kNP * 128;                  // one probability buffer
     // Shared memory after the 1024-byte misc block: the query terms
     // [4R rows][128 B], two probability buffers [NP rows][128 B], the ring.
     static constexpr uint32_t kOffP = 1024 + kNQ * 128;
@@ -164,11 +185,11 @@ __device__ __forceinline__ Item fp8_item(const DecodeArgs &a, int item, int HG, 
     return r;
 }
 
-template <int R, int RING, int CTAS>
-__global__ void __launch_bounds__(kThreads, CTAS)
+template <int R, int RING, int CTAS, int SG, bool PMN>
+__global__ void __launch_bounds__(64 + 128 * SG, CTAS)
 decode_gqa_tc_e4m3_kernel(const __grid_constant__ CUtensorMap tmap_k,
                           const __grid_constant__ CUtensorMap tmap_v, const DecodeArgs a) {
-    using S = Cfg<R, RING, CTAS>;
+    using S = Cfg<R, RING, CTAS, SG, PMN>;
     constexpr int kRing = RING;
     constexpr uint32_t kOffP = S::kOffP, kOffRing = S::kOffRing;
     extern __shared__ uint8_t smem_raw[];
@@ -195,13 +216,13 @@ decode_gqa_tc_e4m3_kernel(const __grid_constant__ CUtensorMap tmap_k,
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(kBarSFull + i), 1);
-            mbar_init(bar(kBarSEmpty + i), kSoftThreads);
-            mbar_init(bar(kBarPFull + i), kSoftThreads);
+            mbar_init(bar(kBarSEmpty + i), kSoftThreads * SG);
+            mbar_init(bar(kBarPFull + i), kSoftThreads * SG);
             mbar_init(bar(kBarPvDone + i), 1);
         }
-        mbar_init(bar(kBarQFull), kSoftThreads);
+        mbar_init(bar(kBarQFull), kSoftThreads * SG);
         mbar_init(bar(kBarQEmpty), 1);
-        mbar_init(bar(kBarOEmpty), kSoftThreads);
+        mbar_init(bar(kBarOEmpty), kSoftThreads * SG);
         mbar_init(bar(kBarDrain), 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -233,8 +254,10 @@ decode_gqa_tc_e4m3_kernel(const __grid_constant__ CUtensorMap tmap_k,
             // Rows of block 0 of this KV head stand in for boxes past the end
             // (masked scores, zeroed value rows).
             const int32_t standin = r.g * bs;
-            int32_t yprev = standin;
-            for (int i = 0; i <= r.ntiles && ok; ++i) {
+            int32_t ylag[kLag];                        // rows of tiles i - 1, i - 2
+#pragma unroll
+            for (int l = 0; l < kLag; ++l) ylag[l] = standin;
+            for (int i = 0; i < r.ntiles + kLag && ok; ++i) {
                 int32_t y = standin;                   // lane j < nbox: row of box j of tile i
                 if (i < r.ntiles && lane < nbox) {
                     const int64_t t = r.begin + int64_t(i) * kM + int64_t(lane) * box;
@@ -246,8 +269,8 @@ decode_gqa_tc_e4m3_kernel(const __grid_constant__ CUtensorMap tmap_k,
                             raise_status(a.status, PKV_DEV_BLOCK_ID);
                     }
                 }
-                // K of tile i, then V of tile i - 1: one stage each
-                for (int kv = (i < r.ntiles ? 0 : 1); kv < (i > 0 ? 2 : 1); ++kv) {
+                // K of tile i, then V of tile i - kLag: one stage each
+                for (int kv = (i < r.ntiles ? 0 : 1); kv < (i >= kLag ? 2 : 1); ++kv) {
                     const bool w = pipe_wait(bar(kBarEmpty + stage), phase ^ 1u, a.status,
                                              abort_flag);
                     if (!__all_sync(0xffffffffu, w)) {
@@ -261,14 +284,16 @@ decode_gqa_tc_e4m3_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     if (lane < nbox)
                         tma_load_2d(sb + kOffRing + uint32_t(stage) * kStage +
                                         uint32_t(lane * box) * kD,
-                                    kv == 0 ? &tmap_k : &tmap_v, 0, kv == 0 ? y : yprev,
+                                    kv == 0 ? &tmap_k : &tmap_v, 0, kv == 0 ? y : ylag[kLag - 1],
                                     bar(kBarFull + stage));
                     if (++stage == kRing) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
-                yprev = y;
+#pragma unroll
+                for (int l = kLag - 1; l > 0; --l) ylag[l] = ylag[l - 1];
+                ylag[0] = y;
             }
         }
         // leave no copy in flight into this CTA's shared memory
@@ -280,7 +305,8 @@ decode_gqa_tc_e4m3_kernel(const __grid_constant__ CUtensorMap tmap_k,
     } else if (warp == 1) {
         // -------------------------------------------------------- MMA issuer
         constexpr uint32_t kIdS = tc::idesc_e4m3_f32(128, S::kNQ, 0, 0);   // K-major K, K-major Q
-        constexpr uint32_t kIdO = tc::idesc_e4m3_f32(128, S::kNP, 1, 0);   // MN-major V, K-major P
+        // MN-major V; P K-major, or MN-major when PMN
+        constexpr uint32_t kIdO = tc::idesc_e4m3_f32(128, S::kNP, 1, PMN ? 1 : 0);
         int stage = 0;
         uint32_t phase = 0, tcount = 0, pcount = 0, ne = 0;
         bool ok = true;
@@ -298,7 +324,7 @@ decode_gqa_tc_e4m3_kernel(const __grid_constant__ CUtensorMap tmap_k,
             const Item r = fp8_item(a, item, head_groups<R>(a), false);
             if (r.ntiles == 0) continue;
             if (!(ok = wait_all(bar(kBarQFull), ne & 1u))) break;
-            for (int i = 0; i <= r.ntiles && ok; ++i) {
+            for (int i = 0; i < r.ntiles + kLag && ok; ++i) {
                 if (i < r.ntiles) {
                     // ---- S^T[buf] = K_tile . Qterms^T
                     const uint32_t buf = tcount & 1u;
@@ -319,9 +345,9 @@ decode_gqa_tc_e4m3_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     advance();
                     ++tcount;
                 }
-                if (i > 0) {
+                if (i >= kLag) {
                     // ---- O^T += V_tile^T . Pterms^T for tile j
-                    const int j = i - 1;
+                    const int j = i - kLag;
                     const uint32_t pbuf = pcount & 1u;
                     if (!(ok = wait_all(bar(kBarPFull + pbuf), (pcount >> 1) & 1u))) break;
                     if (j == 0 && !(ok = wait_all(bar(kBarOEmpty), (ne & 1u) ^ 1u))) break;
@@ -342,11 +368,16 @@ decode_gqa_tc_e4m3_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     if (lane == 0) {
                         const uint32_t vb = sb + kOffRing + uint32_t(stage) * kStage;
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
+                        for (int kk = 0; kk < 4; ++kk) {
+                            // 32 tokens a step: 32 rows of the MN-major layouts,
+                            // 32 bytes along a K-major row
+                            const uint32_t pa = pb + pbuf * S::kPBytes;
                             tc::mma_e4m3(tmem + S::kColO,
                                          tc::smem_desc(vb + 4096 * kk, 16384, 1024),
-                                         tc::smem_desc(pb + pbuf * S::kPBytes + 32 * kk, 16, 1024),
+                                         PMN ? tc::smem_desc(pa + 4096 * kk, 16384, 1024)
+                                             : tc::smem_desc(pa + 32 * kk, 16, 1024),
                                          kIdO, (j | kk) != 0);
+                        }
                         tc::commit(bar(kBarEmpty + stage));
                         tc::commit(bar(kBarPvDone + pbuf));
                     }
@@ -364,20 +395,37 @@ decode_gqa_tc_e4m3_kernel(const __grid_constant__ CUtensorMap tmap_k,
         __syncwarp();
     } else {
         // -------------------------------------------- softmax and epilogue
-        const int t = threadIdx.x - kSoftWarp0 * 32;     // 0..127
+        // SG groups of four warps; group grp takes rows h0 .. h0 + RG - 1, each
+        // thread one token lane (S^T) / value row (O^T) of its quadrant.
+        constexpr int RG = R / SG;
+        const int grp = (warp - kSoftWarp0) >> 2;
+        const int tt = threadIdx.x - kSoftWarp0 * 32;            // 0 .. 128 SG - 1
+        const int t = tt - 128 * grp;                              // 0..127 within the group
+        const int h0 = grp * RG;
         const int quad = warp & 3;
         const int row = quad * 32 + lane;                // token lane of S^T, value row of O^T
         const uint32_t tl = tmem + (uint32_t(quad * 32) << 16);
         uint8_t *qs = base + kOffQ, *ps = base + kOffP;
-        constexpr int kTpr = 128 / R;                    // threads per query row in the split
+        constexpr int kTpr = 128 * SG / R;               // threads per query row in the split
+        constexpr int kDpt = kD / kTpr;                  // query dims per thread
         uint32_t tcount = 0, pcount = 0, ne = 0;
-        // the pad rows of both probability buffers stay zero
-        for (int i = t; i < 2 * int(S::kPBytes) / 16; i += kSoftThreads)
+        // the pad rows (columns) of both probability buffers stay zero
+        for (int i = tt; i < 2 * int(S::kPBytes) / 16; i += kSoftThreads * SG)
             reinterpret_cast<uint4 *>(ps)[i] = make_uint4(0, 0, 0, 0);
         fence_proxy_async_smem();
         auto wait_pv = [&](uint32_t j) {
             return pipe_wait(bar(kBarPvDone + (j & 1u)), (j >> 1) & 1u, a.status, abort_flag);
         };
+        // barrier 1 + grp over this group's 128 threads (an OR of `pred`)
+        auto gbar_or = [&](bool pred) -> bool {
+            uint32_t v;
+            asm volatile(
+                "{ .reg .pred p, q; setp.ne.u32 p, %1, 0; bar.red.or.pred q, %2, 128, p; "
+                "selp.u32 %0, 1, 0, q; }"
+                : "=r"(v) : "r"(uint32_t(pred)), "r"(1 + grp) : "memory");
+            return v != 0;
+        };
+        auto gbar = [&]() { named_barrier_sync(1 + uint32_t(grp), 128); };
         // The R rows of an item are T query tokens x Gr heads: row h is query
         // token h / Gr of sequence b, head g G + hg Gr + h % Gr (T = 1, one
         // head group: the group).
@@ -385,7 +433,7 @@ decode_gqa_tc_e4m3_kernel(const __grid_constant__ CUtensorMap tmap_k,
         // kept live across the tile loop they cost registers)
         auto gr_shift = [&]() { return __ffs(R / a.q_tokens) - 1; };
         for (int item = blockIdx.x; item < num_items; item += gridDim.x) {
-            const Item r = fp8_item(a, item, head_groups<R>(a), t == 0);
+            const Item r = fp8_item(a, item, head_groups<R>(a), tt == 0);
             auto row_of = [&](int h) -> int64_t {
                 const int sh = gr_shift(), Gr = R / a.q_tokens;
                 const int G = a.num_q_heads / a.cache.num_kv_heads;
@@ -394,25 +442,25 @@ decode_gqa_tc_e4m3_kernel(const __grid_constant__ CUtensorMap tmap_k,
             };
             const int64_t split0 = int64_t(r.s) * a.batch * a.q_tokens * a.num_q_heads;
             if (r.ntiles == 0) {
-                for (int i = t; i < R * kD / 4; i += kSoftThreads)
+                for (int i = tt; i < R * kD / 4; i += kSoftThreads * SG)
                     reinterpret_cast<float4 *>(a.out_part + (split0 + row_of(i / (kD / 4))) *
                                                                 kD)[i % (kD / 4)] =
                         make_float4(0.f, 0.f, 0.f, 0.f);
-                if (t < R) a.lse_part[split0 + row_of(t)] = -INFINITY;
+                if (tt < R) a.lse_part[split0 + row_of(tt)] = -INFINITY;
                 continue;
             }
             // ---- the item's query rows as four E4M3 terms each (rows k R + h
-            // of the score MMA's K-major B operand); thread t holds R dims of
-            // row t / kTpr
+            // of the score MMA's K-major B operand); thread tt holds kDpt dims
+            // of row tt / kTpr (a row of this thread's own group)
             bool w = pipe_wait(bar(kBarQEmpty), (ne & 1u) ^ 1u, a.status, abort_flag);
             if (w) {
-                const int h = t / kTpr, d0 = (t % kTpr) * R;
+                const int h = tt / kTpr, d0 = (tt % kTpr) * kDpt;
                 const float qmul = a.scale * kLog2e * a.k_scale[r.g];
                 const float4 *src = reinterpret_cast<const float4 *>(a.q + row_of(h) * kD + d0);
-                float x[R];
+                float x[kDpt];
                 float amax = 0.f;
 #pragma unroll
-                for (int v = 0; v < R / 4; ++v) {
+                for (int v = 0; v < kDpt / 4; ++v) {
                     const float4 f = src[v];
                     x[4 * v] = f.x * qmul;
                     x[4 * v + 1] = f.y * qmul;
@@ -420,7 +468,7 @@ decode_gqa_tc_e4m3_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     x[4 * v + 3] = f.w * qmul;
                 }
 #pragma unroll
-                for (int e = 0; e < R; ++e) amax = fmaxf(amax, fabsf(x[e]));
+                for (int e = 0; e < kDpt; ++e) amax = fmaxf(amax, fabsf(x[e]));
 #pragma unroll
                 for (int o = kTpr / 2; o > 0; o >>= 1)
                     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
@@ -428,13 +476,13 @@ decode_gqa_tc_e4m3_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 // magnitude lies in [128, 256), below E4M3's 448
                 const int e2 = amax > 0.f ? max(ilogbf(amax), -110) : 0;
                 const float inv = ldexpf(1.f, 7 - e2);
-                if (t % kTpr == 0) qsc[h] = ldexpf(1.f, e2 - 7);
+                if (tt % kTpr == 0) qsc[h] = ldexpf(1.f, e2 - 7);
 #pragma unroll
-                for (int e = 0; e < R; ++e) x[e] *= inv;
+                for (int e = 0; e < kDpt; ++e) x[e] *= inv;
 #pragma unroll
                 for (int k = 0; k < kQTerms; ++k)
 #pragma unroll
-                    for (int e = 0; e < R; e += 4) {
+                    for (int e = 0; e < kDpt; e += 4) {
                         const uint32_t c01 = e4m3x2_from_f32(x[e], x[e + 1]);
                         const uint32_t c23 = e4m3x2_from_f32(x[e + 2], x[e + 3]);
                         *reinterpret_cast<uint32_t *>(qs + swz8(k * R + h, d0 + e)) =
@@ -448,35 +496,34 @@ decode_gqa_tc_e4m3_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 fence_proxy_async_smem();
             }
             mbar_arrive(bar(kBarQFull));
-            if (t < R) mrow[t] = -INFINITY;
-            float l_part[R];
+            if (t < RG) mrow[h0 + t] = -INFINITY;
+            float l_part[RG];
 #pragma unroll
-            for (int h = 0; h < R; ++h) l_part[h] = 0.f;
+            for (int j = 0; j < RG; ++j) l_part[j] = 0.f;
             const int32_t span = int32_t(r.end - r.begin);
             // causal limits, from r.begin: row h sees tokens < lim0 + h / Gr
             const int32_t lim0 = int32_t(r.len - (a.q_tokens - 1) - r.begin);
-            if (softmax_bar_or(!w)) break;          // also orders qsc and mrow for all
+            if (gbar_or(!w)) break;          // also orders qsc and mrow in the group
 
             bool ok = true;
             for (int i = 0; i < r.ntiles; ++i) {
                 const uint32_t buf = tcount & 1u;
                 w = pipe_wait(bar(kBarSFull + buf), (tcount >> 1) & 1u, a.status, abort_flag);
-                float x[R];
+                float x[RG];
                 {
-                    uint32_t v[S::kNQ];
+                    uint32_t v[kQTerms][RG];
                     tc::fence_after_sync();
 #pragma unroll
-                    for (int c = 0; c < S::kNQ / 16; ++c)
-                        tc::ld16(tl + S::kNQ * buf + 16 * c,
-                                 *reinterpret_cast<uint32_t(*)[16]>(v + 16 * c));
+                    for (int k = 0; k < kQTerms; ++k)
+                        tc::ldn<RG>(tl + S::kNQ * buf + k * R + h0, v[k]);
                     tc::wait_ld();
 #pragma unroll
-                    for (int h = 0; h < R; ++h) {      // fold the query terms back
-                        float s = __uint_as_float(v[3 * R + h]);
-                        s = fmaf(s, 0.0625f, __uint_as_float(v[2 * R + h]));
-                        s = fmaf(s, 0.0625f, __uint_as_float(v[R + h]));
-                        s = fmaf(s, 0.0625f, __uint_as_float(v[h]));
-                        x[h] = s * qsc[h];
+                    for (int j = 0; j < RG; ++j) {      // fold the query terms back
+                        float s = __uint_as_float(v[3][j]);
+                        s = fmaf(s, 0.0625f, __uint_as_float(v[2][j]));
+                        s = fmaf(s, 0.0625f, __uint_as_float(v[1][j]));
+                        s = fmaf(s, 0.0625f, __uint_as_float(v[0][j]));
+                        x[j] = s * qsc[h0 + j];
                     }
                 }
                 tc::fence_before_sync();
@@ -488,84 +535,105 @@ decode_gqa_tc_e4m3_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     tok >= span ? R : rel < 0 ? 0 : min(rel + 1, a.q_tokens) << gr_shift();
                 bool need = false;
 #pragma unroll
-                for (int h = 0; h < R; ++h) {
-                    x[h] = h >= hmin ? x[h] : -INFINITY;
-                    need |= x[h] > mrow[h] + kSlack;
+                for (int j = 0; j < RG; ++j) {
+                    x[j] = h0 + j >= hmin ? x[j] : -INFINITY;
+                    need |= x[j] > mrow[h0 + j] + kSlack;
                 }
-                if (softmax_bar_or(!w)) {
+                if (gbar_or(!w)) {
                     ok = false;
                     break;
                 }
-                if (softmax_bar_or(need)) {
+                if (gbar_or(need)) {
 #pragma unroll
-                    for (int h = 0; h < R; ++h) {
-                        float m = x[h];
+                    for (int j = 0; j < RG; ++j) {
+                        float m = x[j];
                         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
                         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
                         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
                         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
                         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-                        if (lane == h) red[quad * 16 + h] = m;
+                        if (lane == j) red[quad * 16 + h0 + j] = m;
                     }
-                    named_barrier_sync(1, kSoftThreads);
-                    if (t < R) {
-                        const float tm = fmaxf(fmaxf(red[t], red[16 + t]),
-                                               fmaxf(red[32 + t], red[48 + t]));
-                        const float mo = mrow[t], mn = fmaxf(mo, tm);
-                        aux[t] = (mo == -INFINITY || mn == -INFINITY) ? 0.f : exp2f(mo - mn);
-                        mrow[t] = mn;
+                    gbar();
+                    if (t < RG) {
+                        const int h = h0 + t;
+                        const float tm = fmaxf(fmaxf(red[h], red[16 + h]),
+                                               fmaxf(red[32 + h], red[48 + h]));
+                        const float mo = mrow[h], mn = fmaxf(mo, tm);
+                        aux[h] = (mo == -INFINITY || mn == -INFINITY) ? 0.f : exp2f(mo - mn);
+                        mrow[h] = mn;
                     }
-                    named_barrier_sync(1, kSoftThreads);
+                    gbar();
 #pragma unroll
-                    for (int h = 0; h < R; ++h) l_part[h] *= aux[h];
+                    for (int j = 0; j < RG; ++j) l_part[j] *= aux[h0 + j];
                     if (i > 0) {
                         // the accumulators are quiet once the previous tile's
-                        // value MMAs are done
+                        // value MMAs are done: rescale this group's columns
                         const bool wv = wait_pv(pcount - 1);
                         tc::fence_after_sync();
                         if (wv) {
 #pragma unroll
-                            for (int c = 0; c < S::kNP / 16; ++c) {
-                                uint32_t v[16];
-                                const uint32_t ta = tl + S::kColO + 16 * c;
-                                tc::ld16(ta, v);
+                            for (int k = 0; k < kPTerms; ++k) {
+                                uint32_t v[RG];
+                                const uint32_t ta = tl + S::kColO + k * R + h0;
+                                tc::ldn<RG>(ta, v);
                                 tc::wait_ld();
 #pragma unroll
-                                for (int k = 0; k < 16; ++k)
-                                    v[k] = __float_as_uint(__uint_as_float(v[k]) *
-                                                           aux[(16 * c + k) % R]);
-                                tc::st16(ta, v);
+                                for (int j = 0; j < RG; ++j)
+                                    v[j] = __float_as_uint(__uint_as_float(v[j]) * aux[h0 + j]);
+                                tc::stn<RG>(ta, v);
                             }
                             tc::wait_st();
                         }
                     }
                 }
-                float p[R];
+                float p[RG];
 #pragma unroll
-                for (int h = 0; h < R; ++h) {
-                    p[h] = x[h] == -INFINITY ? 0.f : ex2_approx(x[h] - mrow[h]);
-                    l_part[h] += p[h];
+                for (int j = 0; j < RG; ++j) {
+                    p[j] = x[j] == -INFINITY ? 0.f : ex2_approx(x[j] - mrow[h0 + j]);
+                    l_part[j] += p[j];
                 }
                 // this P buffer was last read by the value MMAs of tile pcount-2
                 if (pcount >= 2) wait_pv(pcount - 2);
                 {
-                    // five E4M3 terms of each probability (p <= 2^8), term k of
-                    // row h at row k R + h of the value MMA's K-major B
-                    // operand, this thread's token its column
+                    // five E4M3 terms of each probability (p <= 2^8): term k of
+                    // row h is column k R + h of the value MMA's B operand,
+                    // this thread's token its row (MN-major) or its column
                     uint8_t *pa = ps + (pcount & 1u) * S::kPBytes;
 #pragma unroll
-                    for (int k = 0; k < kPTerms; ++k)
+                    for (int k = 0; k < kPTerms; ++k) {
+                        uint32_t word[(RG + 3) / 4];
 #pragma unroll
-                        for (int h = 0; h < R; h += 2) {
-                            const uint32_t c = e4m3x2_from_f32(p[h], p[h + 1]);
-                            pa[swz8(k * R + h, row)] = uint8_t(c);
-                            pa[swz8(k * R + h + 1, row)] = uint8_t(c >> 8);
+                        for (int j = 0; j < RG; j += 2) {
+                            const uint32_t c = e4m3x2_from_f32(p[j], p[j + 1]);
+                            if constexpr (PMN) {
+                                if ((j & 3) == 0) word[j >> 2] = c;
+                                else word[j >> 2] |= c << 16;
+                            } else {
+                                pa[swz8(k * R + h0 + j, row)] = uint8_t(c);
+                                pa[swz8(k * R + h0 + j + 1, row)] = uint8_t(c >> 8);
+                            }
                             if (k + 1 < kPTerms) {
                                 const float2 v = e4m3x2_to_f32(c);
-                                p[h] = (p[h] - v.x) * 16.f;
-                                p[h + 1] = (p[h + 1] - v.y) * 16.f;
+                                p[j] = (p[j] - v.x) * 16.f;
+                                p[j + 1] = (p[j + 1] - v.y) * 16.f;
                             }
                         }
+                        if constexpr (PMN) {
+                            // bytes k R + h0 .. + RG of this token's 128-byte row:
+                            // inside one 16-byte chunk (RG divides 16)
+                            const int n0 = k * R + h0;
+                            uint8_t *dst = pa + row * 128 + (((n0 >> 4) ^ (row & 7)) << 4) +
+                                           (n0 & 15);
+                            if constexpr (RG == 16)
+                                *reinterpret_cast<uint4 *>(dst) =
+                                    make_uint4(word[0], word[1], word[2], word[3]);
+                            else if constexpr (RG == 8)
+                                *reinterpret_cast<uint2 *>(dst) = make_uint2(word[0], word[1]);
+                            else
+                                *reinterpret_cast<uint32_t *>(dst) = word[0];
+                        }
+                    }
                 }
                 fence_proxy_async_smem();
                 tc::fence_before_sync();
@@ -578,43 +646,42 @@ decode_gqa_tc_e4m3_kernel(const __grid_constant__ CUtensorMap tmap_k,
             w = wait_pv(pcount - 1);
             tc::fence_after_sync();
 #pragma unroll
-            for (int h = 0; h < R; ++h) {
-                float s = l_part[h];
+            for (int j = 0; j < RG; ++j) {
+                float s = l_part[j];
                 s += __shfl_xor_sync(0xffffffffu, s, 16);
                 s += __shfl_xor_sync(0xffffffffu, s, 8);
                 s += __shfl_xor_sync(0xffffffffu, s, 4);
                 s += __shfl_xor_sync(0xffffffffu, s, 2);
                 s += __shfl_xor_sync(0xffffffffu, s, 1);
-                if (lane == h) red[quad * 16 + h] = s;
+                if (lane == j) red[quad * 16 + h0 + j] = s;
             }
-            named_barrier_sync(1, kSoftThreads);
-            if (t < R) {
-                const float l = (red[t] + red[16 + t]) + (red[32 + t] + red[48 + t]);
-                aux[t] = l > 0.f ? a.v_scale[r.g] / l : 0.f;
-                a.lse_part[split0 + row_of(t)] = l > 0.f ? (mrow[t] + log2f(l)) * kLn2 : -INFINITY;
+            gbar();
+            if (t < RG) {
+                const int h = h0 + t;
+                const float l = (red[h] + red[16 + h]) + (red[32 + h] + red[48 + h]);
+                aux[h] = l > 0.f ? a.v_scale[r.g] / l : 0.f;
+                a.lse_part[split0 + row_of(h)] = l > 0.f ? (mrow[h] + log2f(l)) * kLn2 : -INFINITY;
             }
-            named_barrier_sync(1, kSoftThreads);
+            gbar();
             if (w) {
-                uint32_t v[S::kNP];
+                uint32_t v[kPTerms][RG];
 #pragma unroll
-                for (int c = 0; c < S::kNP / 16; ++c)
-                    tc::ld16(tl + S::kColO + 16 * c,
-                             *reinterpret_cast<uint32_t(*)[16]>(v + 16 * c));
+                for (int k = 0; k < kPTerms; ++k) tc::ldn<RG>(tl + S::kColO + k * R + h0, v[k]);
                 tc::wait_ld();
 #pragma unroll
-                for (int h = 0; h < R; ++h) {          // fold the probability terms back
-                    float o = __uint_as_float(v[4 * R + h]);
-                    o = fmaf(o, 0.0625f, __uint_as_float(v[3 * R + h]));
-                    o = fmaf(o, 0.0625f, __uint_as_float(v[2 * R + h]));
-                    o = fmaf(o, 0.0625f, __uint_as_float(v[R + h]));
-                    o = fmaf(o, 0.0625f, __uint_as_float(v[h]));
-                    a.out_part[(split0 + row_of(h)) * kD + row] = o * aux[h];
+                for (int j = 0; j < RG; ++j) {          // fold the probability terms back
+                    float o = __uint_as_float(v[4][j]);
+                    o = fmaf(o, 0.0625f, __uint_as_float(v[3][j]));
+                    o = fmaf(o, 0.0625f, __uint_as_float(v[2][j]));
+                    o = fmaf(o, 0.0625f, __uint_as_float(v[1][j]));
+                    o = fmaf(o, 0.0625f, __uint_as_float(v[0][j]));
+                    a.out_part[(split0 + row_of(h0 + j)) * kD + row] = o * aux[h0 + j];
                 }
             }
             tc::fence_before_sync();
             mbar_arrive(bar(kBarOEmpty));
             ++ne;
-            if (softmax_bar_or(!w)) break;
+            if (gbar_or(!w)) break;
         }
     }
 
@@ -653,10 +720,10 @@ bool make_byte_map(CUtensorMap *map, const void *pool, int64_t rows, int box) {
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int R, int RING, int CTAS>
+template <int R, int RING, int CTAS, int SG, bool PMN>
 int launch_rows(const DecodeArgs &a) {
-    using S = Cfg<R, RING, CTAS>;
-    auto kernel = decode_gqa_tc_e4m3_kernel<R, RING, CTAS>;
+    using S = Cfg<R, RING, CTAS, SG, PMN>;
+    auto kernel = decode_gqa_tc_e4m3_kernel<R, RING, CTAS, SG, PMN>;
     const int64_t rows = int64_t(a.cache.num_blocks) * a.cache.num_kv_heads * a.cache.block_size;
     const int box = std::min(a.cache.block_size, kM);
     CUtensorMap tk, tv;
@@ -677,7 +744,7 @@ int launch_rows(const DecodeArgs &a) {
                           (a.num_q_heads / a.cache.num_kv_heads * a.q_tokens / R);
     const int grid = int(std::min<int64_t>(items, int64_t(sm_count()) * CTAS));
     if (grid <= 0) return PKV_OK;
-    return launch_pdl(kernel, dim3(grid), dim3(kThreads), S::kSmemBytes, a.stream, tk, tv, a);
+    return launch_pdl(kernel, dim3(grid), dim3(S::kThreads), S::kSmemBytes, a.stream, tk, tv, a);
 }
 
 }  // namespace
@@ -703,10 +770,11 @@ int gqa_tc_e4m3_resident_ctas(int32_t group) {
 
 int launch_decode_gqa_tc_e4m3(const DecodeArgs &a) {
     switch (a.num_q_heads / a.cache.num_kv_heads * a.q_tokens) {
-        case 4: return launch_rows<4, PKV_E4M3_R4_RING, PKV_E4M3_R4_CTAS>(a);
-        case 8: return launch_rows<8, PKV_E4M3_R8_RING, PKV_E4M3_R8_CTAS>(a);
+        case 4: return launch_rows<4, PKV_E4M3_R4_RING, PKV_E4M3_R4_CTAS, 1, false>(a);
+        case 8: return launch_rows<8, PKV_E4M3_R8_RING, PKV_E4M3_R8_CTAS, 1, false>(a);
         case 16:
-        case 32: return launch_rows<16, 5, 2>(a);   // 32 rows: two head groups of 16
+        case 32:   // 32 rows: two head groups of 16
+            return launch_rows<16, PKV_E4M3_R16_RING, 2, PKV_E4M3_R16_SG, (PKV_E4M3_R16_SG > 1)>(a);
         default: return PKV_ERR_SHAPE;
     }
 }

@@ -103,6 +103,43 @@ __device__ __forceinline__ void st16(uint32_t taddr, const uint32_t (&r)[16]) {
           "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]),
           "r"(r[13]), "r"(r[14]), "r"(r[15]) : "memory");
 }
+// The same for 4 consecutive columns.
+__device__ __forceinline__ void ld4(uint32_t taddr, uint32_t (&r)[4]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr) : "memory");
+}
+__device__ __forceinline__ void st4(uint32_t taddr, const uint32_t (&r)[4]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};"
+                 ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]) : "memory");
+}
+// The same for 8 consecutive columns.
+__device__ __forceinline__ void ld8(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+          "=r"(r[6]), "=r"(r[7])
+        : "r"(taddr) : "memory");
+}
+__device__ __forceinline__ void st8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
+          "r"(r[6]), "r"(r[7]) : "memory");
+}
+// N (4, 8 or 16) consecutive columns.
+template <int N>
+__device__ __forceinline__ void ldn(uint32_t taddr, uint32_t (&r)[N]) {
+    if constexpr (N == 4) ld4(taddr, r);
+    else if constexpr (N == 8) ld8(taddr, r);
+    else ld16(taddr, r);
+}
+template <int N>
+__device__ __forceinline__ void stn(uint32_t taddr, const uint32_t (&r)[N]) {
+    if constexpr (N == 4) st4(taddr, r);
+    else if constexpr (N == 8) st8(taddr, r);
+    else st16(taddr, r);
+}
 __device__ __forceinline__ void wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
