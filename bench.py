@@ -549,6 +549,40 @@ class E4m3Step(Step):
         self.attend(ev_a, ev_b)
 
 
+class AgentE4m3Step(E4m3Step):
+    """The shared-prefix MLA step over an FP8 (E4M3) cache: copy-on-write of
+    each sequence's shared tail block (its codes), the quantising append of
+    the decode tokens, one pkv_paged_decode_attn_e4m3 (the suffixes are
+    appended once, before timing)."""
+    kernel_name = ("pkv_paged_decode_attn_e4m3 (decode_mla_tc_kernel, E4M3 mode: codes "
+                   "expanded exactly to fp16 in shared memory, tcgen05 kind::f16, + lse_merge)")
+    bound = "tensor"
+
+    def __init__(self, pkv, w, dev, splits):
+        super().__init__(pkv, w, dev, splits)
+        self.src, self.dst = w.cow_src.to(dev), w.cow_dst.to(dev)
+        pkv.copy_blocks_e4m3(self.k, self.v, self.src, self.dst)
+        last = torch.zeros(w.new_seq.numel(), dtype=torch.bool)
+        last[torch.cumsum(torch.bincount(w.new_seq.long()), 0) - 1] = True
+        setup = (~last).to(dev)
+        sl = pkv.slot_mapping(self.k, self.v, self.bt, self.new_seq[setup], self.new_pos[setup])
+        pkv.kv_append_e4m3(self.k, self.v, self.k_new[setup], self.v_new[setup], sl,
+                           self.k_scale, self.v_scale)
+        keep = last.to(dev)
+        self.new_seq, self.new_pos = self.new_seq[keep], self.new_pos[keep]
+        self.k_new = self.k_new[keep].contiguous()
+        self.v_new = self.v_new[keep].contiguous()
+        self.slots = torch.empty(self.new_pos.numel(), dtype=torch.int64, device=dev)
+        self.launches = 5   # copy, slot, append, split, merge
+        self.desc = (f"copy_blocks ({self.src.numel()} CoW pairs) + slot_mapping + "
+                     f"kv_append_e4m3 ({self.new_pos.numel()} decode tokens) + "
+                     f"paged_decode_attn_e4m3 ({splits} splits) = split kernel + lse_merge")
+
+    def run(self, ev_a=None, ev_b=None):
+        self.pkv.copy_blocks_e4m3(self.k, self.v, self.src, self.dst)
+        super().run(ev_a, ev_b)
+
+
 class MultiE4m3Step(E4m3Step):
     """Speculative verification over an FP8 (E4M3) cache: T new tokens per
     sequence quantised into the cache, each attending causally (one
@@ -577,13 +611,14 @@ class MultiE4m3Step(E4m3Step):
 
 STEPS = {"long32k": Step, "mix": Step, "tiny": Step, "dcp200k": DcpStep, "agent_mla": AgentStep,
          "agent_mla_latent": AgentStep, "agent_mla_cascade": AgentCascadeStep, "spec4_32k": MultiStep, "long32k_e4m3": E4m3Step,
-         "dcp200k_e4m3": DcpE4m3Step, "spec4_32k_e4m3": MultiE4m3Step}
+         "dcp200k_e4m3": DcpE4m3Step, "spec4_32k_e4m3": MultiE4m3Step,
+         "agent_mla_e4m3": AgentE4m3Step}
 # The 32K workload is timed at 16 splits, the split count its configuration
 # names; the split count the library picks by itself (num_splits = 0) is
 # timed too and reported beside it (`library_auto_splits`).
 DEFAULT_SPLITS = {"long32k": 16, "mix": 1, "tiny": 1, "dcp200k": 19, "agent_mla": 19,
                   "agent_mla_latent": 19, "agent_mla_cascade": (19, 2), "spec4_32k": 9, "long32k_e4m3": 7,
-                  "dcp200k_e4m3": 14, "spec4_32k_e4m3": 9}
+                  "dcp200k_e4m3": 14, "spec4_32k_e4m3": 9, "agent_mla_e4m3": 19}
 # Workloads whose line also carries the library's own split choice.
 AUTO_SPLITS_ALSO = ("long32k",)
 # Workloads of the single-threaded oracle figure (the four GQA configurations)
@@ -1079,7 +1114,11 @@ def run_gpu(args, world, rank, local):
             "l2": f"no flush: the {total_bytes / 1e9:.3f} GB a step reads exceeds the 129 MB "
                   f"L2 (steps back to back)",
             "parallelism": "replicas" if world > 1 else "single GPU",
-            "compute": ("E4M3 tensor-core products (K/V as stored; the fp32 query as 4 and the "
+            "compute": ("E4M3 codes expanded exactly to fp16 in shared memory, fp16 "
+                        "tensor-core products (the fp32 query and probabilities split into "
+                        "fp16 hi+lo), fp32 accumulate and softmax"
+                        if w.k_codes is not None and w.num_q_heads // w.num_kv_heads >= 64 else
+                        "E4M3 tensor-core products (K/V as stored; the fp32 query as 4 and the "
                         "probabilities as 5 E4M3 terms), fp32 accumulate and softmax"
                         if w.k_codes is not None else
                         "bf16 tensor-core products (fp32 query and probabilities split into bf16 "

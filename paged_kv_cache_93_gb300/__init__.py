@@ -94,6 +94,14 @@ def cache_desc(k_pool: torch.Tensor, v_pool) -> CacheDesc:
     return CacheDesc(nb, bs, hkv, dk, v_pool.shape[3])
 
 
+def _bf16_desc(k_pool: torch.Tensor, v_pool) -> CacheDesc:
+    """cache_desc for the calls that take bf16 pools only (the C calls size
+    every row from the element count at two bytes an element, so a code pool
+    given to them would be read and written past its end)."""
+    _need(k_pool, "k_pool", torch.bfloat16, 4)
+    return cache_desc(k_pool, v_pool)
+
+
 def device_status(reset: bool = True, stream=None) -> int:
     """Synchronize `stream` and return the device status word (PKV_DEV_* bits)."""
     flags = ctypes.c_uint32(0)
@@ -120,7 +128,7 @@ def slot_mapping(k_pool, v_pool, block_tables, seq_ids, positions, out=None, str
 def kv_append(k_pool, v_pool, k_new, v_new, slots, stream=None) -> None:
     """Write k_new [T, Hkv, Dk] / v_new [T, Hkv, Dv] (bf16) at slots [T] (int64).
     With v_pool = ValuesInKeys(Dv), v_new must be None (only K is written)."""
-    desc = cache_desc(k_pool, v_pool)
+    desc = _bf16_desc(k_pool, v_pool)
     _need(k_new, "k_new", torch.bfloat16, 3)
     if isinstance(v_pool, ValuesInKeys):
         if v_new is not None:
@@ -134,8 +142,9 @@ def kv_append(k_pool, v_pool, k_new, v_new, slots, stream=None) -> None:
 
 
 def copy_blocks(k_pool, v_pool, src, dst, stream=None) -> None:
-    """Copy-on-write duplication: block src[i] -> block dst[i] (int32 device arrays)."""
-    desc = cache_desc(k_pool, v_pool)
+    """Copy-on-write duplication: block src[i] -> block dst[i] (int32 device
+    arrays), bf16 pools (copy_blocks_e4m3 for code pools)."""
+    desc = _bf16_desc(k_pool, v_pool)
     _need(src, "src", torch.int32, 1)
     _need(dst, "dst", torch.int32, 1)
     if src.numel() != dst.numel():
@@ -208,12 +217,12 @@ def decode_workspace_size(batch: int, num_q_heads: int, head_dim_v: int, num_spl
 
 
 def decode_auto_splits(k_pool, v_pool, batch: int, num_q_heads: int, max_seq_len: int) -> int:
-    desc = cache_desc(k_pool, v_pool)
+    desc = _bf16_desc(k_pool, v_pool)
     return int(lib.pkv_decode_auto_splits(ctypes.byref(desc), batch, num_q_heads, max_seq_len))
 
 
 def _decode_common(q, k_pool, v_pool, block_tables, seq_lens):
-    desc = cache_desc(k_pool, v_pool)
+    desc = _bf16_desc(k_pool, v_pool)
     _need(q, "q", torch.float32, 3)
     _need(block_tables, "block_tables", torch.int32, 2)
     _need(seq_lens, "seq_lens", torch.int32, 1)
@@ -249,7 +258,7 @@ def decode_cascade_splits(k_pool, v_pool, batch: int, num_q_heads: int, max_bloc
                           prefix_blocks: int, prefix_splits: int = 0,
                           suffix_splits: int = 0) -> tuple[int, int]:
     """The (prefix, suffix) split counts a cascade call uses (0 = chosen)."""
-    desc = cache_desc(k_pool, v_pool)
+    desc = _bf16_desc(k_pool, v_pool)
     s1, s2 = ctypes.c_int32(prefix_splits), ctypes.c_int32(suffix_splits)
     _check("pkv_decode_cascade_splits", lib.pkv_decode_cascade_splits(
         ctypes.byref(desc), batch, num_q_heads, max_blocks, prefix_blocks, ctypes.byref(s1),
@@ -363,7 +372,7 @@ def paged_decode_attn_multi(q, k_pool, v_pool, block_tables, seq_lens, scale: fl
                             flags: int = 0, stream=None):
     """Several new tokens per sequence (q [B, T, Hq, Dk]); query t attends to
     the first seq_lens[b] - T + 1 + t tokens -> (out [B, T, Hq, Dv], lse [B, T, Hq])."""
-    desc = cache_desc(k_pool, v_pool)
+    desc = _bf16_desc(k_pool, v_pool)
     _need(q, "q", torch.float32, 4)
     _need(block_tables, "block_tables", torch.int32, 2)
     _need(seq_lens, "seq_lens", torch.int32, 1)

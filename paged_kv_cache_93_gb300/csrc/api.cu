@@ -143,6 +143,17 @@ int run_split_kernel(const DecodeArgs &a, int32_t flags) {
     return launch_decode_generic(a);
 }
 
+// The split kernel over E4M3 pools: the tcgen05 GQA kernel (4 to 32 rows
+// per KV head, head dims 128), the tcgen05 large-group kernel (64 or more
+// heads per KV head), else the CUDA-core kernel.
+int run_split_kernel_e4m3(const DecodeArgs &a, int32_t flags) {
+    if (flags == 0 && gqa_tc_e4m3_kernel_supports(a.cache, a.num_q_heads))
+        return launch_decode_gqa_tc_e4m3(a);
+    if (flags == 0 && mla_tc_kernel_supports(a.cache, a.num_q_heads))
+        return launch_decode_mla_tc_e4m3(a);
+    return launch_decode_generic_e4m3(a);
+}
+
 }  // namespace
 
 namespace pkv {
@@ -216,12 +227,9 @@ extern "C" int pkv_paged_decode_attn_e4m3(const pkv_cache_desc *cache, const flo
     if (st != PKV_OK || batch == 0) return st;
     if (!v_pool || !k_scale || !v_scale || !out || !lse) return PKV_ERR_INVALID_ARG;
     if (!aligned16(out)) return PKV_ERR_ALIGNMENT;
-    // the tensor-core kernel where it takes the shape, the CUDA-core one
+    // a tensor-core kernel where one takes the shape, the CUDA-core one
     // otherwise (or when a flag asks for it)
-    const bool tc = flags == 0 && gqa_tc_e4m3_kernel_supports(*cache, num_q_heads);
-    auto launch = [&](const DecodeArgs &d) {
-        return tc ? launch_decode_gqa_tc_e4m3(d) : launch_decode_generic_e4m3(d);
-    };
+    auto launch = [&](const DecodeArgs &d) { return run_split_kernel_e4m3(d, flags); };
     int32_t S = num_splits;
     if (S == 0)
         S = pkv_decode_auto_splits_e4m3(
@@ -524,15 +532,12 @@ extern "C" int pkv_paged_decode_attn_multi_e4m3(
                     dim3(threads), 0, s, block_tables, seq_lens, batch, tokens_per_seq,
                     max_blocks, row_tables, row_lens);
     if (st != PKV_OK) return st;
-    const bool tc = flags == 0 && gqa_tc_e4m3_kernel_supports(*cache, num_q_heads);
     DecodeArgs a{*cache, q, rows, num_q_heads, k_pool, v_pool, row_tables, max_blocks,
                  row_lens, scale, S, out, lse, status, s};
     a.v_stride = cache->head_dim_v;
     a.k_scale = k_scale;
     a.v_scale = v_scale;
-    auto launch = [&](const DecodeArgs &d) {
-        return tc ? launch_decode_gqa_tc_e4m3(d) : launch_decode_generic_e4m3(d);
-    };
+    auto launch = [&](const DecodeArgs &d) { return run_split_kernel_e4m3(d, flags); };
     if (S == 1) return launch(a);
     a.out_part = reinterpret_cast<float *>(ws + m.partials);
     a.lse_part = reinterpret_cast<float *>(ws + m.partials +

@@ -72,6 +72,14 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kSmemLimit = 232448;
 constexpr uint32_t kIdS = tc::idesc_bf16_f32(128, 128, 0, 0);  // K-major K, K-major [Q_hi; Q_lo]
 constexpr uint32_t kIdO = tc::idesc_bf16_f32(128, 64, 1, 1);   // MN-major V, MN-major P
+// FP8 (E4M3) cache: the codes are turned into fp16 (exactly) by two
+// converter warps, so the products run on fp16 operands.
+constexpr uint32_t kIdS16 = tc::idesc_f16_f32(128, 128, 0, 0);
+constexpr uint32_t kIdO16 = tc::idesc_f16_f32(128, 64, 1, 1);
+constexpr int kThreadsF8 = 256;         // warps 6-7: converters
+constexpr int kConvWarp0 = 6;
+constexpr int kConvThreads = 64;
+constexpr int kCodeBytes = 8192;        // one chunk's E4M3 codes, in the upper half of its stage
 
 // mbarrier slots
 constexpr int kBarFull = 0;             // + stage: chunk landed (TMA bytes)
@@ -83,7 +91,9 @@ constexpr int kBarPvDone = 21;          // value MMAs of a tile done (MMA commit
 constexpr int kBarQFull = 22;           // query written (128 arrivals)
 constexpr int kBarQEmpty = 23;          // score MMAs of an item done (MMA commit)
 constexpr int kBarOEmpty = 24;          // accumulators read out (128 arrivals)
-constexpr int kBarDrain = 25;   // 26 of the 32 slots
+constexpr int kBarDrain = 25;
+constexpr int kBarLanded = 26;          // + stage, FP8: the chunk's codes landed (TMA bytes)
+constexpr int kNumBars = kBarLanded + kMaxRing;
 
 struct TcShape {
     int dk_segs;      // Dk / 64
@@ -105,12 +115,12 @@ __host__ __device__ inline SmemMap smem_map(const TcShape &s) {
     m.p_lo = m.p_hi + kM * 128;
     m.ring = m.p_lo + kM * 128;
     m.bars = m.ring + uint32_t(s.ring) * kChunk;
-    m.mrow = m.bars + 32 * 8;
+    m.mrow = m.bars + kNumBars * 8;
     m.aux = m.mrow + kN * 4;
     m.red = m.aux + kN * 4;
     m.slot = m.red + 4 * kN * 4;
     m.flag = m.slot + 4;
-    m.end = m.flag + 12;
+    m.end = m.flag + 4;
     return m;
 }
 inline size_t tc_smem_bytes(const TcShape &s) { return 1024 + size_t(smem_map(s).end); }
@@ -118,15 +128,17 @@ inline size_t tc_smem_bytes(const TcShape &s) { return 1024 + size_t(smem_map(s)
 __device__ __forceinline__ int64_t lmin(int64_t x, int64_t y) { return x < y ? x : y; }
 
 // This thread's scores for heads 16c .. 16c + 15 of a tile: the product with
-// the query's high parts (S^T columns 0-63) plus its low parts (64-127).
-__device__ __forceinline__ void ld_scores(uint32_t ts, int c, uint32_t (&v)[16]) {
+// the query's high parts (S^T columns 0-63) plus its low parts (64-127),
+// times `mul` (1 for a bf16 cache; the item's power-of-two query scale over
+// an FP8 one).
+__device__ __forceinline__ void ld_scores(uint32_t ts, int c, uint32_t (&v)[16], float mul) {
     uint32_t lo[16];
     tc::ld16(ts + 16 * c, v);
     tc::ld16(ts + kN + 16 * c, lo);
     tc::wait_ld();
 #pragma unroll
     for (int k = 0; k < 16; ++k)
-        v[k] = __float_as_uint(__uint_as_float(v[k]) + __uint_as_float(lo[k]));
+        v[k] = __float_as_uint((__uint_as_float(v[k]) + __uint_as_float(lo[k])) * mul);
 }
 
 // One decode problem of a launch: its queries, tables, lengths, split count
@@ -211,7 +223,14 @@ __device__ __forceinline__ uint32_t swz(int row, int col) {
     return uint32_t(row) * 128 + (uint32_t(((col >> 3) ^ row) & 7) << 4) + uint32_t(col & 7) * 2;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+// F8: the pools hold E4M3 codes (a.k_scale, a.v_scale per KV head).  The
+// producer lands each chunk's 8 KB of codes in the upper half of its ring
+// stage and the converter warps expand them, exactly, into fp16 over the
+// whole stage in the layout the bf16 copies have; the query and the
+// probabilities are fp16 hi + lo, the query scaled by a power of two per
+// item so that both parts stay inside fp16's range.
+template <bool F8>
+__global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
 decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                      const __grid_constant__ CUtensorMap tmap_v, const DecodeArgs a,
                      const Problem p0, const Problem p1, const TcShape shp) {
@@ -235,8 +254,10 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
 
     if (threadIdx.x == 0) {
         for (int r = 0; r < shp.ring; ++r) {
-            mbar_init(bar(kBarFull + r), 1);
+            // bf16: the producer's arrival + TMA bytes; FP8: the converters
+            mbar_init(bar(kBarFull + r), F8 ? kConvThreads : 1);
             mbar_init(bar(kBarEmpty + r), 1);
+            if (F8) mbar_init(bar(kBarLanded + r), 1);
         }
         mbar_init(bar(kBarSFull), 1);
         mbar_init(bar(kBarSFull + 1), 1);
@@ -270,15 +291,19 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
         int stage = 0;
         uint32_t phase = 0, armed = 0, armed_parity = 0;
         bool ok = a.withhold == 0;              // test control: issue no copy at all
+        // bf16: the chunk fills its stage; FP8: its codes fill the upper half
+        // and the converters complete the stage.
+        const int bar_full = F8 ? kBarLanded : kBarFull;
         // Wait for a free stage and arm it for one chunk; false on abort.
         auto acquire = [&](uint32_t &dst) -> bool {
             const bool w =
                 pipe_wait(bar(kBarEmpty + stage), phase ^ 1u, a.status, abort_flag, wlim);
             if (!__all_sync(0xffffffffu, w)) return false;
-            if (lane == 0) mbar_arrive_expect_tx(bar(kBarFull + stage), kChunk);
+            if (lane == 0)
+                mbar_arrive_expect_tx(bar(bar_full + stage), F8 ? kCodeBytes : kChunk);
             armed |= 1u << stage;
             armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-            dst = sb + sm.ring + uint32_t(stage) * kChunk;
+            dst = sb + sm.ring + uint32_t(stage) * kChunk + (F8 ? kCodeBytes : 0);
             return true;
         };
         auto advance = [&]() {
@@ -325,8 +350,16 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                             break;
                         }
                         if (lane == 0) {
-                            tma_load_3d(dst, &tmap_k, 0, y0, seg, bar(kBarFull + stage));
-                            tma_load_3d(dst + 8192, &tmap_k, 0, y1, seg, bar(kBarFull + stage));
+                            if constexpr (F8) {
+                                // [128 rows][64 codes]: the segment's bytes of each row
+                                tma_load_2d(dst, &tmap_k, seg * 64, y0, bar(bar_full + stage));
+                                tma_load_2d(dst + 4096, &tmap_k, seg * 64, y1,
+                                            bar(bar_full + stage));
+                            } else {
+                                tma_load_3d(dst, &tmap_k, 0, y0, seg, bar(kBarFull + stage));
+                                tma_load_3d(dst + 8192, &tmap_k, 0, y1, seg,
+                                            bar(kBarFull + stage));
+                            }
                         }
                         advance();
                     }
@@ -339,9 +372,14 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                                 ok = false;
                                 break;
                             }
-                            if (lane == 0)
-                                tma_load_3d(dst, &tmap_v, 0, h ? yp1 : yp0, 2 * vb,
-                                            bar(kBarFull + stage));
+                            if (lane == 0) {
+                                if constexpr (F8)   // [64 rows][128 codes]
+                                    tma_load_2d(dst, &tmap_v, vb * 128, h ? yp1 : yp0,
+                                                bar(bar_full + stage));
+                                else
+                                    tma_load_3d(dst, &tmap_v, 0, h ? yp1 : yp0, 2 * vb,
+                                                bar(kBarFull + stage));
+                            }
                             advance();
                         }
                 }
@@ -353,7 +391,7 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
         if (lane == 0)
             for (int s = 0; s < shp.ring; ++s)
                 if (armed & (1u << s))
-                    mbar_wait(bar(kBarFull + s), (armed_parity >> s) & 1u, a.status);
+                    mbar_wait(bar(bar_full + s), (armed_parity >> s) & 1u, a.status);
         __syncwarp();
     } else if (warp == 1) {
         // -------------------------------------------------------- MMA issuer
@@ -391,7 +429,7 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                                 tc::mma_bf16(d, tc::smem_desc(kb + 32 * kk, 16, 1024),
                                              tc::smem_desc(qh + uint32_t(seg) * 16384 + 32 * kk,
                                                            16, 1024),
-                                             kIdS, (seg | kk) != 0);
+                                             F8 ? kIdS16 : kIdS, (seg | kk) != 0);
                             tc::commit(bar(kBarEmpty + stage));
                         }
                         __syncwarp();
@@ -417,7 +455,7 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         for (int h = 0; h < 2; ++h) {
                             if (!(ok = wait_all(bar(kBarFull + stage), phase))) break;
                             const int first_bad = nvalid - h * kHalf;
-                            if (first_bad < kHalf) {
+                            if (!F8 && first_bad < kHalf) {
                                 // Value rows past the end may hold any bits
                                 // (NaN times a zero probability is NaN).
                                 uint8_t *vt = base + sm.ring + size_t(stage) * kChunk;
@@ -439,10 +477,10 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                                     const uint64_t ad =
                                         tc::smem_desc(vbase + 2048 * kk, 8192, 1024);
                                     const uint32_t po = uint32_t(h * kHalf + 16 * kk) * 128;
-                                    tc::mma_bf16(d, ad, tc::smem_desc(ph + po, 8192, 1024), kIdO,
-                                                 (j | h | kk) != 0);
-                                    tc::mma_bf16(d, ad, tc::smem_desc(pl + po, 8192, 1024), kIdO,
-                                                 1);
+                                    tc::mma_bf16(d, ad, tc::smem_desc(ph + po, 8192, 1024),
+                                                 F8 ? kIdO16 : kIdO, (j | h | kk) != 0);
+                                    tc::mma_bf16(d, ad, tc::smem_desc(pl + po, 8192, 1024),
+                                                 F8 ? kIdO16 : kIdO, 1);
                                 }
                                 tc::commit(bar(kBarEmpty + stage));
                             }
@@ -464,7 +502,7 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
             mbar_wait(bar(kBarDrain), 0, a.status);
         }
         __syncwarp();
-    } else {
+    } else if (warp < kSoftWarp0 + 4) {
         // -------------------------------------------- softmax and epilogue
         const int t = threadIdx.x - kSoftWarp0 * 32;     // 0..127
         const int quad = warp & 3;                       // TMEM lane quadrant
@@ -499,14 +537,54 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 continue;
             }
             // ---- the group's queries, pre-scaled by scale*log2(e), as bf16 hi + lo
+            // (FP8: also by the key scale and a power of two, as fp16 hi + lo)
             bool w = pipe_wait(bar(kBarQEmpty), (ne & 1u) ^ 1u, a.status, abort_flag, wlim);
+            // 16-byte loads, eight in flight per thread before any is used
+            // (the query is 147 KB at Dk = 576: one load at a time would
+            // leave the item's first tile waiting on ~150 L2 round trips)
+            const float4 *qsrc = reinterpret_cast<const float4 *>(
+                r.p.q + (int64_t(r.b) * r.p.num_q_heads + head0) * Dk);
+            const int n4 = kN * Dk / 4;
+            float cq = qscale;     // factor of the stored query
+            float mul = 1.f;       // factor of the scores read back
+            if constexpr (F8) {
+                // The stored query is q c 2^-e, c = scale log2(e) k_scale: 2^e
+                // brings the item's largest |q c| into [2^13, 2^14), below
+                // fp16's largest finite value, with the low parts of all but
+                // the smallest elements still normal; the scores are read
+                // back times 2^e (exact).
+                float m = 0.f;
+                if (w) {
+                    for (int i0 = 0; i0 < n4; i0 += 8 * kSoftThreads) {
+                        float4 x[8];
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            const int i = i0 + u * kSoftThreads + t;
+                            x[u] = i < n4 ? __ldg(qsrc + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
+#pragma unroll
+                        for (int u = 0; u < 8; ++u)
+                            m = fmaxf(m, fmaxf(fmaxf(fabsf(x[u].x), fabsf(x[u].y)),
+                                               fmaxf(fabsf(x[u].z), fabsf(x[u].w))));
+                    }
+                }
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+                if (lane == 0) red[quad * kN] = m;
+                w = !softmax_bar_or(!w);
+                const float c = qscale * a.k_scale[r.g];
+                const float big = fmaxf(fmaxf(red[0], red[kN]), fmaxf(red[2 * kN], red[3 * kN])) *
+                                  fabsf(c);
+                int e = 0;
+                if (big > 0.f && big <= 3.402823466e38f)
+                    e = min(max(int((__float_as_uint(big) >> 23) & 0xffu) - 127 - 13, -100), 100);
+                cq = c * __uint_as_float(uint32_t(127 - e) << 23);
+                mul = __uint_as_float(uint32_t(127 + e) << 23);
+            }
             if (w) {
-                // 16-byte loads, eight in flight per thread before any is used
-                // (the query is 147 KB at Dk = 576: one load at a time would
-                // leave the item's first tile waiting on ~150 L2 round trips)
-                const float4 *qsrc = reinterpret_cast<const float4 *>(
-                    r.p.q + (int64_t(r.b) * r.p.num_q_heads + head0) * Dk);
-                const int n4 = kN * Dk / 4;
                 for (int i0 = 0; i0 < n4; i0 += 8 * kSoftThreads) {
                     float4 x[8];
 #pragma unroll
@@ -519,11 +597,20 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         const int i = i0 + u * kSoftThreads + t;
                         if (i >= n4) continue;
                         const int h = (4 * i) / Dk, d = (4 * i) % Dk;
-                        const float x0 = x[u].x * qscale, x1 = x[u].y * qscale;
-                        const float x2 = x[u].z * qscale, x3 = x[u].w * qscale;
-                        const uint32_t h01 = pack_bf16x2(x0, x1), h23 = pack_bf16x2(x2, x3);
-                        const uint32_t l01 = pack_bf16x2(x0 - bf16_lo_to_f32(h01), x1 - bf16_hi_to_f32(h01));
-                        const uint32_t l23 = pack_bf16x2(x2 - bf16_lo_to_f32(h23), x3 - bf16_hi_to_f32(h23));
+                        const float x0 = x[u].x * cq, x1 = x[u].y * cq;
+                        const float x2 = x[u].z * cq, x3 = x[u].w * cq;
+                        uint32_t h01, h23, l01, l23;
+                        if constexpr (F8) {
+                            h01 = pack_f16x2(x0, x1);
+                            h23 = pack_f16x2(x2, x3);
+                            l01 = pack_f16x2(x0 - f16_lo_to_f32(h01), x1 - f16_hi_to_f32(h01));
+                            l23 = pack_f16x2(x2 - f16_lo_to_f32(h23), x3 - f16_hi_to_f32(h23));
+                        } else {
+                            h01 = pack_bf16x2(x0, x1);
+                            h23 = pack_bf16x2(x2, x3);
+                            l01 = pack_bf16x2(x0 - bf16_lo_to_f32(h01), x1 - bf16_hi_to_f32(h01));
+                            l23 = pack_bf16x2(x2 - bf16_lo_to_f32(h23), x3 - bf16_hi_to_f32(h23));
+                        }
                         // four consecutive dims share one 16-byte swizzle chunk
                         const uint32_t off = uint32_t(d >> 6) * 16384 + swz(h, d & 63);
                         *reinterpret_cast<uint2 *>(q_hi + off) = make_uint2(h01, h23);
@@ -558,7 +645,7 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     uint32_t v[16];
-                    ld_scores(ts, c, v);
+                    ld_scores(ts, c, v, mul);
 #pragma unroll
                     for (int k = 0; k < 16; ++k)
                         need |= valid && __uint_as_float(v[k]) > mrow[16 * c + k] + kSlack;
@@ -573,7 +660,7 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         uint32_t v[16];
-                        ld_scores(ts, c, v);
+                        ld_scores(ts, c, v, mul);
 #pragma unroll
                         for (int k = 0; k < 16; ++k) {
                             float m = valid ? __uint_as_float(v[k]) : -INFINITY;
@@ -633,7 +720,7 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     uint32_t v[16];
-                    ld_scores(ts, c, v);
+                    ld_scores(ts, c, v, mul);
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
                         uint32_t hi[4], lo[4];
@@ -646,9 +733,15 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                             const float p0 = ex2_approx(x0 - m2.x), p1 = ex2_approx(x1 - m2.y);
                             l_part[h] += p0;
                             l_part[h + 1] += p1;
-                            hi[e] = pack_bf16x2(p0, p1);
-                            lo[e] = pack_bf16x2(p0 - bf16_lo_to_f32(hi[e]),
-                                                p1 - bf16_hi_to_f32(hi[e]));
+                            if constexpr (F8) {
+                                hi[e] = pack_f16x2(p0, p1);
+                                lo[e] = pack_f16x2(p0 - f16_lo_to_f32(hi[e]),
+                                                   p1 - f16_hi_to_f32(hi[e]));
+                            } else {
+                                hi[e] = pack_bf16x2(p0, p1);
+                                lo[e] = pack_bf16x2(p0 - bf16_lo_to_f32(hi[e]),
+                                                    p1 - bf16_hi_to_f32(hi[e]));
+                            }
                         }
                         const int chunk = 2 * c + half;
                         const uint32_t off =
@@ -689,7 +782,8 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
             named_barrier_sync(1, kSoftThreads);
             if (t < kN) {
                 const float l = (red[t] + red[kN + t]) + (red[2 * kN + t] + red[3 * kN + t]);
-                aux[t] = l > 0.f ? 1.f / l : 0.f;
+                // FP8: the values' scale goes with 1 / l
+                aux[t] = l > 0.f ? (F8 ? a.v_scale[r.g] : 1.f) / l : 0.f;
                 r.p.lse_part[orow0 + t] = l > 0.f ? (mrow[t] + log2f(l)) * kLn2 : -INFINITY;
             }
             named_barrier_sync(1, kSoftThreads);
@@ -714,6 +808,88 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
             if (softmax_bar_or(!w)) {
                 abandoned = true;
                 abandon_rows(r.p, orow0);
+            }
+        }
+    } else {
+        if constexpr (F8) {
+            // ------------------------------------------ E4M3 -> fp16 converters
+            // A chunk's codes are 512 pieces of 16, eight per thread: piece p
+            // of a key chunk ([128 rows][64 codes]) is row p / 4, dims
+            // 16 (p % 4) .. + 15 of the segment; of a value chunk ([64 rows]
+            // [128 codes]) row p / 8, dims 16 (p % 8) .. + 15 of the block.
+            // Eight consecutive threads read 128 consecutive bytes and store
+            // to disjoint banks (value pieces of the second 64 dims store
+            // their two halves in the other order).  Value rows past the end
+            // of the sequence are written as zeros (any bits may sit there,
+            // and NaN times a zero probability is NaN).
+            const int t = threadIdx.x - kConvWarp0 * 32;    // 0..63
+            int stage = 0;
+            uint32_t phase = 0;
+            auto convert = [&](bool is_v, int keep) -> bool {
+                const bool w =
+                    pipe_wait(bar(kBarLanded + stage), phase, a.status, abort_flag, wlim);
+                uint8_t *st = base + sm.ring + size_t(stage) * kChunk;
+                uint4 cd[8];
+                if (w) {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        cd[k] = *reinterpret_cast<const uint4 *>(st + kCodeBytes +
+                                                                 16 * (t + 64 * k));
+                }
+                // every code is read before fp16 values overwrite the stage
+                if (bar_red_or(2, kConvThreads, !w)) return false;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int p = t + 64 * k;
+                    int row, q2;
+                    uint32_t off;
+                    bool zero = false, swap = false;
+                    if (is_v) {
+                        row = p >> 3;
+                        const int q = p & 7;
+                        off = uint32_t(q >> 2) * 8192 + uint32_t(row) * 128;
+                        q2 = 2 * (q & 3);
+                        zero = row >= keep;
+                        swap = (q & 4) != 0;
+                    } else {
+                        row = p >> 2;
+                        off = uint32_t(row) * 128;
+                        q2 = 2 * (p & 3);
+                    }
+                    const uint2 f0 = e4m3x4_to_f16x4(cd[k].x), f1 = e4m3x4_to_f16x4(cd[k].y);
+                    const uint2 f2 = e4m3x4_to_f16x4(cd[k].z), f3 = e4m3x4_to_f16x4(cd[k].w);
+                    uint4 lo = make_uint4(f0.x, f0.y, f1.x, f1.y);
+                    uint4 hi = make_uint4(f2.x, f2.y, f3.x, f3.y);
+                    if (zero) lo = hi = make_uint4(0, 0, 0, 0);
+                    const uint32_t o0 = off + (uint32_t((q2 ^ row) & 7) << 4);
+                    const uint32_t o1 = off + (uint32_t(((q2 + 1) ^ row) & 7) << 4);
+                    *reinterpret_cast<uint4 *>(st + (swap ? o1 : o0)) = swap ? hi : lo;
+                    *reinterpret_cast<uint4 *>(st + (swap ? o0 : o1)) = swap ? lo : hi;
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(bar(kBarFull + stage));
+                if (++stage == shp.ring) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+                return true;
+            };
+            // the producer's order of chunks
+            bool ok = true;
+            for (int item = blockIdx.x; item < num_items && ok; item += gridDim.x) {
+                const TcItem r = tc_item(a, p0, p1, item, false);
+                if (r.ntiles == 0) continue;
+                for (int i = 0; i <= r.ntiles && ok; ++i) {
+                    if (i < r.ntiles)
+                        for (int seg = 0; seg < shp.dk_segs && ok; ++seg) ok = convert(false, kM);
+                    if (i > 0) {
+                        const int64_t tok0 = r.begin + int64_t(i - 1) * kM;
+                        const int nvalid = int(lmin(kM, r.end - tok0));
+                        for (int vb = 0; vb < shp.dv_blocks && ok; ++vb)
+                            for (int h = 0; h < 2 && ok; ++h)
+                                ok = convert(true, nvalid - h * kHalf);
+                    }
+                }
             }
         }
     }
@@ -755,6 +931,21 @@ bool make_box_map(CUtensorMap *map, const void *pool, int64_t rows, int dim, int
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The E4M3 pool as rows of `dim` one-byte codes (`stride` bytes apart); one
+// box = 64 rows x `box_x` codes, unswizzled ([64][box_x] in shared memory).
+bool make_code_map(CUtensorMap *map, const void *pool, int64_t rows, int dim, int stride,
+                   int box_x) {
+    auto fn = tc_encode_fn();
+    if (!fn) return false;
+    cuuint64_t gdim[2] = {cuuint64_t(dim), cuuint64_t(rows)};
+    cuuint64_t gstride[1] = {cuuint64_t(stride)};
+    cuuint32_t box[2] = {cuuint32_t(box_x), cuuint32_t(kHalf)};
+    cuuint32_t estride[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(pool), gdim, gstride, box,
+              estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 TcShape tc_shape(const pkv_cache_desc &c) {
     TcShape s{c.head_dim_k / 64, c.head_dim_v / 128, 0};
     const size_t fixed = tc_smem_bytes(s);
@@ -783,19 +974,23 @@ int32_t mla_tc_work_units(const pkv_cache_desc &c, int32_t batch, int32_t num_q_
 
 namespace {
 // One launch over the problems' items together (p1.batch = 0: one problem).
+template <bool F8>
 int launch_problems(const DecodeArgs &a, const Problem &p0, const Problem &p1) {
     const TcShape shp = tc_shape(a.cache);
     const int64_t rows = int64_t(a.cache.num_blocks) * a.cache.num_kv_heads * a.cache.block_size;
     CUtensorMap tk, tv;
-    if (!make_box_map(&tk, a.k_pool, rows, a.cache.head_dim_k, a.cache.head_dim_k, 1) ||
-        !make_box_map(&tv, a.v_pool, rows, a.cache.head_dim_v, a.v_stride, 2))
-        return PKV_ERR_CUDA;
+    const bool maps =
+        F8 ? make_code_map(&tk, a.k_pool, rows, a.cache.head_dim_k, a.cache.head_dim_k, 64) &&
+                 make_code_map(&tv, a.v_pool, rows, a.cache.head_dim_v, a.v_stride, 128)
+           : make_box_map(&tk, a.k_pool, rows, a.cache.head_dim_k, a.cache.head_dim_k, 1) &&
+                 make_box_map(&tv, a.v_pool, rows, a.cache.head_dim_v, a.v_stride, 2);
+    if (!maps) return PKV_ERR_CUDA;
     const size_t smem = tc_smem_bytes(shp);
     static thread_local int configured_dev = -1;
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_dev != dev) {
-        if (cudaFuncSetAttribute(decode_mla_tc_kernel,
+        if (cudaFuncSetAttribute(decode_mla_tc_kernel<F8>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kSmemLimit) != cudaSuccess)
             return PKV_ERR_CUDA;
@@ -805,19 +1000,25 @@ int launch_problems(const DecodeArgs &a, const Problem &p0, const Problem &p1) {
     const int64_t items = int64_t(problem_items(p0, hkv)) + problem_items(p1, hkv);
     const int grid = int(std::min<int64_t>(items, sm_count()));
     if (grid <= 0) return PKV_OK;
-    return launch_pdl(decode_mla_tc_kernel, dim3(grid), dim3(kThreads), smem, a.stream, tk, tv,
-                      a, p0, p1, shp);
+    return launch_pdl(decode_mla_tc_kernel<F8>, dim3(grid), dim3(F8 ? kThreadsF8 : kThreads),
+                      smem, a.stream, tk, tv, a, p0, p1, shp);
 }
 }  // namespace
 
 int launch_decode_mla_tc(const DecodeArgs &a) {
     Problem none = problem_of(a);
     none.batch = 0;
-    return launch_problems(a, problem_of(a), none);
+    return launch_problems<false>(a, problem_of(a), none);
 }
 
 int launch_decode_mla_tc_two(const DecodeArgs &first, const DecodeArgs &second) {
-    return launch_problems(first, problem_of(first), problem_of(second));
+    return launch_problems<false>(first, problem_of(first), problem_of(second));
+}
+
+int launch_decode_mla_tc_e4m3(const DecodeArgs &a) {
+    Problem none = problem_of(a);
+    none.batch = 0;
+    return launch_problems<true>(a, problem_of(a), none);
 }
 
 }  // namespace pkv

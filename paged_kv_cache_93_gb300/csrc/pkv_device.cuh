@@ -39,6 +39,33 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return out;
 }
 
+// Two fp32 -> fp16x2 (nearest even): `lo` in bits 0-15, `hi` in 16-31.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t out;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(out) : "f"(hi), "f"(lo));
+    return out;
+}
+// The fp16 in bits 0-15 / 16-31 of `packed` as fp32 (exact).
+__device__ __forceinline__ float f16_lo_to_f32(uint32_t packed) {
+    float f;
+    asm("{ .reg .b16 l, h; mov.b32 {l, h}, %1; cvt.f32.f16 %0, l; }" : "=f"(f) : "r"(packed));
+    return f;
+}
+__device__ __forceinline__ float f16_hi_to_f32(uint32_t packed) {
+    float f;
+    asm("{ .reg .b16 l, h; mov.b32 {l, h}, %1; cvt.f32.f16 %0, h; }" : "=f"(f) : "r"(packed));
+    return f;
+}
+// Four E4M3 codes (bytes 0-3 of `codes`) -> four fp16 values, exact (every
+// E4M3 value is an fp16 value): .x holds codes 0 and 1, .y codes 2 and 3.
+__device__ __forceinline__ uint2 e4m3x4_to_f16x4(uint32_t codes) {
+    uint32_t a, b;
+    asm("{ .reg .b16 l, h; mov.b32 {l, h}, %2; cvt.rn.f16x2.e4m3x2 %0, l; "
+        "cvt.rn.f16x2.e4m3x2 %1, h; }"
+        : "=r"(a), "=r"(b) : "r"(codes));
+    return make_uint2(a, b);
+}
+
 // Two fp32 -> two E4M3 codes (nearest, ties to even; magnitudes beyond the
 // largest finite 448 give +-448): `lo` in bits 0-7, `hi` in bits 8-15.
 __device__ __forceinline__ uint32_t e4m3x2_from_f32(float lo, float hi) {

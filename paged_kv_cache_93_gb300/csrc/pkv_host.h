@@ -138,6 +138,9 @@ int launch_decode_mla_tc(const DecodeArgs &a);
 // items walked together, the first problem's first); `second` supplies only
 // its queries, tables, lengths, batch, heads, split count and partials.
 int launch_decode_mla_tc_two(const DecodeArgs &first, const DecodeArgs &second);
+// The same kernel over E4M3 pools (a.k_scale, a.v_scale set, values in
+// their own pool): the codes are expanded to fp16 in shared memory, exactly.
+int launch_decode_mla_tc_e4m3(const DecodeArgs &a);
 // The split kernel pkv_paged_decode_attn would launch for `a` (by shape and
 // flags); writes a.out_part / a.lse_part as [S][batch][heads] partials.
 int run_decode_split_kernel(const DecodeArgs &a, int32_t flags);

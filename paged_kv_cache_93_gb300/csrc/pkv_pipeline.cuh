@@ -30,6 +30,17 @@ __device__ __forceinline__ bool pipe_wait(uint32_t bar, uint32_t parity, uint32_
     }
 }
 
+// Named barrier `id` over `threads` threads (whole warps); every participant
+// gets the OR of their predicates.
+__device__ __forceinline__ bool bar_red_or(uint32_t id, uint32_t threads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{ .reg .pred p, q; setp.ne.u32 p, %1, 0; bar.red.or.pred q, %2, %3, p; "
+        "selp.u32 %0, 1, 0, q; }"
+        : "=r"(r) : "r"(uint32_t(pred)), "r"(id), "r"(threads) : "memory");
+    return r != 0;
+}
+
 // Named barrier 1 over the 128 softmax threads; every participant gets the
 // OR of their predicates.
 __device__ __forceinline__ bool softmax_bar_or(bool pred) {

@@ -33,7 +33,15 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, in
            (uint32_t(b_mn) << 16) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
 }
 
-// D[tmem] (+)= A[smem] x B[smem]; `accumulate` = 0 overwrites D.
+// Instruction descriptor: fp16 x fp16 -> fp32 (kind::f16 with both operand
+// format fields 0), M x N, majors as above.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, int a_mn, int b_mn) {
+    return (1u << 4) | (uint32_t(a_mn) << 15) | (uint32_t(b_mn) << 16) |
+           (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem] x B[smem]; `accumulate` = 0 overwrites D.  Both
+// operands bf16, or both fp16 (the instruction descriptor says which).
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                          uint32_t idesc, uint32_t accumulate) {
     asm volatile(

@@ -270,3 +270,23 @@ def test_e4m3_host_rules(pkv):
     assert lib.pkv_copy_blocks_e4m3(ctypes.byref(one), p, p, p, p, 1, None) == -2
     # the split choice: enough items for the resident CTAs
     assert 1 <= lib.pkv_decode_auto_splits_e4m3(ctypes.byref(ok), 8, 8, 32768) <= 256
+
+
+def test_binding_keeps_code_pools_out_of_bf16_calls(pkv):
+    """The bf16 calls size rows at two bytes an element; the binding refuses
+    one-byte code pools for them (they have E4M3 forms) before any C call."""
+    import torch
+    k = torch.zeros(4, 1, 16, 64, dtype=torch.uint8)
+    v = torch.zeros(4, 1, 16, 64, dtype=torch.uint8)
+    i32 = torch.zeros(1, dtype=torch.int32)
+    q = torch.zeros(1, 2, 64)
+    bt = torch.zeros(1, 4, dtype=torch.int32)
+    with pytest.raises(TypeError, match="k_pool must be torch.bfloat16"):
+        pkv.copy_blocks(k, v, i32, i32)
+    with pytest.raises(TypeError, match="k_pool must be torch.bfloat16"):
+        pkv.kv_append(k, v, torch.zeros(1, 1, 64, dtype=torch.bfloat16),
+                      torch.zeros(1, 1, 64, dtype=torch.bfloat16), torch.zeros(1, dtype=torch.int64))
+    with pytest.raises(TypeError, match="k_pool must be torch.bfloat16"):
+        pkv.paged_decode_attn(q, k, v, bt, i32, 0.125)
+    with pytest.raises(TypeError, match="k_pool must be torch.bfloat16"):
+        pkv.paged_decode_attn_partial(q, k, v, bt, i32, 0.125, 2)

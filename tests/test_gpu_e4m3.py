@@ -10,7 +10,7 @@ import torch
 
 import oracle
 import workloads
-from tests._steps import assert_attention_close
+from tests._steps import agent_rows, assert_attention_close
 from tests._util import bits
 
 pytestmark = pytest.mark.gpu
@@ -98,6 +98,132 @@ def test_e4m3_generic_shapes(pkv, shape, splits):
     assert np.array_equal(k, rk) and np.array_equal(v, rv)
     assert_attention_close(out, lse, ro, rl, f"e4m3 generic {shape}/{splits}")
     assert pkv.device_status() == 0
+
+
+# The MLA shape over an FP8 cache: 128 (or 64) query heads over one 576-dim
+# key / 512-dim value head, ragged lengths across 128-token tiles.
+MLA_SHAPES = [
+    ([700, 3, 255, 128], 128, 1, 576, 512, 64),
+    ([1000, 65], 64, 1, 576, 512, 128),
+    ([300, 129], 256, 2, 576, 512, 64),
+]
+
+
+@pytest.mark.parametrize("shape", MLA_SHAPES,
+                         ids=lambda s: f"G{s[1]//s[2]}_Hkv{s[2]}_bs{s[5]}")
+@pytest.mark.parametrize("splits", [1, 3, 0])
+def test_e4m3_mla_shape_matches_oracle(pkv, shape, splits):
+    cached, hq, hkv, dk, dv, bs = shape
+    w = workloads.e4m3(workloads.custom(90 + hq + bs, cached, hq, hkv, dk, dv, bs))
+    out, lse, k, v = gpu_e4m3_step(pkv, w, splits)
+    ro, rl, rk, rv = oracle_e4m3_step(w)
+    assert np.array_equal(k, rk) and np.array_equal(v, rv), "pools after the append"
+    assert_attention_close(out, lse, ro, rl, f"e4m3 MLA {shape}/{splits}")
+    assert pkv.device_status() == 0
+
+
+def test_e4m3_mla_nan_codes_in_unused_slots_do_not_leak(pkv):
+    """NaN codes in the slots past each sequence's end (and possibly in the
+    block whose rows stand in for half tiles past the end): the value rows
+    past the end are written as zeros, the scores there are masked."""
+    bs = 64
+    w = workloads.e4m3(workloads.custom(15, [100, 190, 63], 128, 1, 576, 512, bs,
+                                        extra_blocks=0))
+    for b in range(w.batch):
+        L = int(w.seq_lens[b])
+        last = int(w.block_tables[b, (L - 1) // bs])
+        w.k_codes[last, :, L % bs or bs:] = 0x7F
+        w.v_codes[last, :, L % bs or bs:] = 0xFF
+    ro, rl, *_ = oracle_e4m3_step(w)
+    for splits in (1, 2):
+        out, lse, *_ = gpu_e4m3_step(pkv, w, splits)
+        assert np.isfinite(out).all() and np.isfinite(lse).all()
+        assert_attention_close(out, lse, ro, rl, f"MLA nan tail/{splits}")
+        assert pkv.device_status() == 0
+
+
+@pytest.mark.parametrize("splits", [1, 3])
+def test_e4m3_mla_rising_scores(pkv, splits):
+    """MLA shape, keys growing along the sequence: the running max keeps
+    rising past the slack and the accumulators are rescaled in TMEM."""
+    bs = 64
+    w = workloads.custom(95, [1500, 700], 128, 1, 576, 512, bs)
+    k = w.k_pool.float()
+    for b in range(2):
+        L = int(w.seq_lens[b])
+        j = np.arange(L)
+        blk = w.block_tables[b, j // bs].long()
+        k[blk, :, torch.from_numpy(j % bs)] *= torch.from_numpy(1.0 + 6.0 * j / L).float()[:, None,
+                                                                                         None]
+    w.k_pool = k.to(torch.bfloat16)
+    w = workloads.e4m3(w)
+    w.k_scale *= 7.0                                      # keep the grown keys in range
+    w.k_codes = (w.k_pool.float() / w.k_scale.view(1, -1, 1, 1)).clamp(-448, 448).to(
+        torch.float8_e4m3fn).view(torch.uint8)
+    out, lse, *_ = gpu_e4m3_step(pkv, w, splits)
+    ro, rl, *_ = oracle_e4m3_step(w)
+    assert_attention_close(out, lse, ro, rl, f"MLA rising/{splits}")
+    assert pkv.device_status() == 0
+
+
+@pytest.mark.parametrize("factor", [0.0, 1e-3, 8.0])
+def test_e4m3_mla_query_magnitudes(pkv, factor):
+    """The query is stored as fp16 hi + lo after scaling by a power of two
+    chosen per work item from its largest element: a zero, a tiny and a
+    large query (the first sequence's; the second stays as drawn) keep the
+    tolerances."""
+    w = workloads.custom(96, [400, 260], 128, 1, 576, 512, 64)
+    w.q[0] *= factor
+    w = workloads.e4m3(w)
+    ro, rl, *_ = oracle_e4m3_step(w)
+    for splits in (1, 3):
+        out, lse, *_ = gpu_e4m3_step(pkv, w, splits)
+        assert_attention_close(out, lse, ro, rl, f"MLA query x{factor}/{splits}")
+        assert pkv.device_status() == 0
+
+
+def test_e4m3_agent_mla_full_size_sampled_rows(pkv):
+    """The shared-prefix MLA step at full size over an FP8 cache (32
+    sequences over a 136,040-token shared prefix; copy-on-write of the
+    shared tail block's codes, the quantising append of every suffix and
+    decode token, attention at the benchmark's split count): the pools byte
+    for byte, and every head of four sequences and one head of every other
+    sequence against the oracle."""
+    from bench import DEFAULT_SPLITS
+    w = workloads.make("agent_mla_e4m3")
+    dev = "cuda"
+    k, v = w.k_codes.to(dev), w.v_codes.to(dev)
+    ks, vs = w.k_scale.to(dev), w.v_scale.to(dev)
+    bt = w.block_tables.to(dev)
+    pkv.copy_blocks_e4m3(k, v, w.cow_src.to(dev), w.cow_dst.to(dev))
+    slots = pkv.slot_mapping(k, v, bt, w.new_seq.to(dev), w.new_pos.to(dev))
+    pkv.kv_append_e4m3(k, v, w.k_new.to(dev), w.v_new.to(dev), slots, ks, vs)
+    out, lse = pkv.paged_decode_attn_e4m3(w.q.to(dev), k, v, ks, vs, bt, w.seq_lens.to(dev),
+                                          w.scale, num_splits=DEFAULT_SPLITS["agent_mla_e4m3"])
+    torch.cuda.synchronize()
+    assert pkv.device_status() == 0
+    kc, vc = w.k_codes.numpy().copy(), w.v_codes.numpy().copy()
+    # a block copy moves bytes: the oracle's copy over the code pools viewed
+    # as 16-bit words
+    assert oracle.copy_blocks(kc.view(np.uint16), vc.view(np.uint16), w.cow_src.numpy(),
+                              w.cow_dst.numpy()) == 0
+    sl = oracle.slot_mapping(w.block_tables.numpy(), w.new_seq.numpy(), w.new_pos.numpy(),
+                             w.block_size)
+    assert oracle.kv_append_e4m3(kc, vc, bits(w.k_new), bits(w.v_new), w.k_scale.numpy(),
+                                 w.v_scale.numpy(), sl, w.block_size) == 0
+    assert np.array_equal(k.cpu().numpy(), kc) and np.array_equal(v.cpu().numpy(), vc)
+    rows, full = agent_rows(w)
+    assert len(full) == 4
+    pairs = [(b, h) for b, heads in rows.items() for h in heads]
+    bs_, hs_ = np.array([p[0] for p in pairs]), np.array([p[1] for p in pairs])
+    # with one KV head every (sequence, head) is a one-head row of its own
+    ro, rl = oracle.paged_decode_attn_e4m3(np.ascontiguousarray(w.q.numpy()[bs_, hs_][:, None]),
+                                           kc, vc, w.k_scale.numpy(), w.v_scale.numpy(),
+                                           np.ascontiguousarray(w.block_tables.numpy()[bs_]),
+                                           np.ascontiguousarray(w.seq_lens.numpy()[bs_]),
+                                           w.scale)
+    go, gl = out.cpu().numpy(), lse.cpu().numpy()
+    assert_attention_close(go[bs_, hs_], gl[bs_, hs_], ro[:, 0], rl[:, 0], "agent MLA e4m3")
 
 
 @pytest.mark.parametrize("shape", SHAPES[:3], ids=lambda s: f"G{s[1]//s[2]}_bs{s[3]}")

@@ -334,8 +334,9 @@ def e4m3(w: Workload, seed: int = 11) -> Workload:
     step holds torch's float8_e4m3fn cast of the bf16 pools divided by their
     head's scale, clipped to +-448 -- a stand-in for a cache filled by
     earlier appends.  The step's new tokens stay bf16 (the append quantises
-    them).  Needs a separate value pool."""
-    assert w.v_pool is not None and w.cow_src.numel() == 0
+    them).  Needs a separate value pool.  A step with copy-on-write pairs
+    copies the blocks' codes."""
+    assert w.v_pool is not None
     g = torch.Generator().manual_seed(seed)
     hkv = w.num_kv_heads
     ks = (8.0 / 448.0) * (1.0 + 0.5 * torch.rand(hkv, generator=g))
@@ -358,6 +359,8 @@ def make(name: str, **kw) -> Workload:
         return e4m3(spec_verify(**kw))
     if name == "dcp200k_e4m3":
         return e4m3(dcp200k(**kw))
+    if name == "agent_mla_e4m3":
+        return e4m3(agent_mla(**kw))
     if name == "agent_mla_latent":
         return agent_mla(latent=True, **kw)
     if name == "agent_mla_cascade":
