@@ -149,7 +149,7 @@ int run_split_kernel(const DecodeArgs &a, int32_t flags) {
 int run_split_kernel_e4m3(const DecodeArgs &a, int32_t flags) {
     if (flags == 0 && gqa_tc_e4m3_kernel_supports(a.cache, a.num_q_heads))
         return launch_decode_gqa_tc_e4m3(a);
-    if (flags == 0 && mla_tc_kernel_supports(a.cache, a.num_q_heads))
+    if (flags == 0 && mla_tc_e4m3_kernel_supports(a.cache, a.num_q_heads))
         return launch_decode_mla_tc_e4m3(a);
     return launch_decode_generic_e4m3(a);
 }

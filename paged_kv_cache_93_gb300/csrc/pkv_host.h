@@ -140,6 +140,7 @@ int launch_decode_mla_tc(const DecodeArgs &a);
 int launch_decode_mla_tc_two(const DecodeArgs &first, const DecodeArgs &second);
 // The same kernel over E4M3 pools (a.k_scale, a.v_scale set, values in
 // their own pool): the codes are expanded to fp16 in shared memory, exactly.
+bool mla_tc_e4m3_kernel_supports(const pkv_cache_desc &c, int32_t num_q_heads);
 int launch_decode_mla_tc_e4m3(const DecodeArgs &a);
 // The split kernel pkv_paged_decode_attn would launch for `a` (by shape and
 // flags); writes a.out_part / a.lse_part as [S][batch][heads] partials.
