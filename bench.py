@@ -66,6 +66,12 @@ PROFILES = {
     "long32k_e4m3": ("decode_gqa_tc_e4m3_long32k.txt",
                      ("decode_gqa_tc_e4m3.cu", "pkv_device.cuh", "pkv_tcgen05.cuh",
                       "pkv_pipeline.cuh", "pkv_math.cuh")),
+    "agent_mla": ("decode_mla_tc_agent_mla.txt",
+                  ("decode_mla_tc.cu", "pkv_device.cuh", "pkv_tcgen05.cuh", "pkv_pipeline.cuh",
+                   "pkv_math.cuh")),
+    "agent_mla_e4m3": ("decode_mla_tc_e4m3_agent_mla.txt",
+                       ("decode_mla_tc.cu", "pkv_device.cuh", "pkv_tcgen05.cuh",
+                        "pkv_pipeline.cuh", "pkv_math.cuh")),
 }
 
 

@@ -22,7 +22,13 @@ def assert_attention_close(out, lse, ref_out, ref_lse, where=""):
     assert out.shape == ref_out.shape and lse.shape == ref_lse.shape, where
     err = np.abs(out - ref_out)
     bad = ~((err <= OUT_ABS) | (err <= OUT_REL * np.abs(ref_out)))
-    assert not bad.any(), f"{where}: out mismatch at {np.argwhere(bad)[:5]} max err {err.max():.3g}"
+    if bad.any():
+        idx = np.argwhere(bad)
+        rows = sorted({tuple(r[:-1]) for r in idx.tolist()})
+        raise AssertionError(
+            f"{where}: out mismatch in {len(idx)} elements of {len(rows)} rows {rows[:12]}, "
+            f"last-axis indices {idx[:, -1].min()}..{idx[:, -1].max()}, first at "
+            f"{idx[:5].tolist()}, max err {err.max():.3g}")
     empty = np.isneginf(ref_lse)
     assert np.array_equal(np.isneginf(lse), empty), f"{where}: empty rows differ"
     lerr = np.abs(lse[~empty] - ref_lse[~empty])

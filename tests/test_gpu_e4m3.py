@@ -343,10 +343,11 @@ def test_e4m3_bad_seq_len_and_block_id_are_flagged(pkv):
 
 
 def test_e4m3_full_size_sampled_rows(pkv):
-    """8 x 32K GQA step (32/8 heads, block 16) over an E4M3 cache: three
-    whole sequences against the oracle."""
+    """8 x 32K GQA step (32/8 heads, block 16) over an E4M3 cache at the
+    benchmark's split count: three whole sequences against the oracle."""
+    from bench import DEFAULT_SPLITS
     w = workloads.make("long32k_e4m3")
-    out, lse, *_ = gpu_e4m3_step(pkv, w, 0)
+    out, lse, *_ = gpu_e4m3_step(pkv, w, DEFAULT_SPLITS["long32k_e4m3"])
     assert pkv.device_status() == 0
     k, v = oracle_e4m3_cache(w)
     for b in (0, 3, 7):
@@ -467,3 +468,69 @@ def test_e4m3_multi_token_short_sequence_is_flagged(pkv, splits, T, hq):
     ro, rl = oracle_multi_e4m3(w)
     assert_attention_close(out, lse, ro, rl, "short")
     assert pkv.device_status(reset=True) & pkv.DEV_SEQ_LEN
+
+
+def test_e4m3_spec4_full_size_sampled_rows(pkv):
+    """Speculative verification at 8 x 32K over an FP8 cache (4 new tokens
+    per sequence, the benchmark's split count): whole (sequence, token) rows
+    against the oracle."""
+    from bench import DEFAULT_SPLITS
+    w = workloads.make("spec4_32k_e4m3")
+    out, lse = gpu_multi_e4m3(pkv, w, DEFAULT_SPLITS["spec4_32k_e4m3"])
+    k, v = oracle_e4m3_cache(w)
+    T = w.tokens_per_seq
+    for b, t in [(0, 0), (3, 2), (7, 3)]:
+        end = np.array([int(w.seq_lens[b]) - (T - 1) + t], dtype=np.int32)
+        ro, rl = oracle.paged_decode_attn_e4m3(w.q.numpy()[b:b + 1, t], k, v, w.k_scale.numpy(),
+                                               w.v_scale.numpy(), w.block_tables.numpy()[b:b + 1],
+                                               w.seq_lens.numpy()[b:b + 1], w.scale, tok_end=end)
+        assert_attention_close(out[b, t][None], lse[b, t][None], ro, rl, f"row {b}/{t}")
+    assert pkv.device_status() == 0
+
+
+@pytest.mark.parametrize("interleave", [1, 16])
+def test_e4m3_dcp200k_full_size(pkv, interleave):
+    """The 200,000-token DCP step over an FP8 cache as the benchmark runs it:
+    every token quantised into its interleaved partition, the 4 partitions as
+    the rows of one E4M3 call at the benchmark's split count, then merged;
+    the pools byte for byte, every partition and the merge against the
+    oracle."""
+    from bench import DEFAULT_SPLITS
+    w = workloads.e4m3(workloads.dcp200k(interleave=interleave))
+    N, P, bs = int(w.seq_lens[0]), w.num_parts, w.block_size
+    dev = "cuda"
+    k, v = w.k_codes.to(dev), w.v_codes.to(dev)
+    ks, vs = w.k_scale.to(dev), w.v_scale.to(dev)
+    ptab = w.part_tables.to(dev)
+    kt, vt = w.k_tokens.to(dev), w.v_tokens.to(dev)
+    pkv.kv_append_e4m3(k, v, kt[:N - 1], vt[:N - 1],
+                       pkv.interleave_slot_mapping(k, v, 0, N - 1, P, interleave, ptab), ks, vs)
+    pkv.kv_append_e4m3(k, v, w.k_new.to(dev), w.v_new.to(dev),
+                       pkv.interleave_slot_mapping(k, v, N - 1, 1, P, interleave, ptab), ks, vs)
+    plen = torch.tensor([pkv.interleave_partition_len(N, P, interleave, r) for r in range(P)],
+                        dtype=torch.int32)
+    pq = w.q.to(dev).expand(P, w.num_q_heads, w.head_dim_k).contiguous()
+    po, pl = pkv.paged_decode_attn_e4m3(pq, k, v, ks, vs, ptab, plen.to(dev), w.scale,
+                                        num_splits=DEFAULT_SPLITS["dcp200k_e4m3"])
+    mo, ml = pkv.lse_merge(po.unsqueeze(1), pl.unsqueeze(1))
+    torch.cuda.synchronize()
+    assert pkv.device_status() == 0
+    kc, vc = w.k_codes.numpy().copy(), w.v_codes.numpy().copy()
+    part, local = oracle.interleave(N, P, interleave)
+    pslots = oracle.slot_mapping(w.part_tables.numpy(), part, local, bs)
+    assert oracle.kv_append_e4m3(kc, vc, bits(w.k_tokens), bits(w.v_tokens), w.k_scale.numpy(),
+                                 w.v_scale.numpy(), pslots, bs) == 0
+    assert np.array_equal(k.cpu().numpy(), kc) and np.array_equal(v.cpu().numpy(), vc)
+    counts = np.bincount(part, minlength=P).astype(np.int32)
+    assert counts.tolist() == plen.tolist()
+    ro, rl = [], []
+    for r in range(P):
+        o, l = oracle.paged_decode_attn_e4m3(w.q.numpy(), kc, vc, w.k_scale.numpy(),
+                                             w.v_scale.numpy(), w.part_tables.numpy()[r:r + 1],
+                                             counts[r:r + 1], w.scale)
+        ro.append(o)
+        rl.append(l)
+        assert_attention_close(po[r:r + 1].cpu().numpy(), pl[r:r + 1].cpu().numpy(), o, l,
+                               f"partition {r}")
+    oo, ol = oracle.lse_merge(np.stack(ro), np.stack(rl))
+    assert_attention_close(mo.cpu().numpy(), ml.cpu().numpy(), oo, ol, "merged")

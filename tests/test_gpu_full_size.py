@@ -2,7 +2,9 @@
 benchmark times: the 32K-context GQA batch at the benchmark's headline split
 count and at the split count the library picks by itself (every row against
 the oracle), the 200,000-token DCP-style partition split (interleave 1 and
-16, merged partitions against unsplit attention and the oracle), and the
+16, merged partitions against unsplit attention and the oracle; the
+partitions also as the rows of one batched launch at the benchmark's split
+count), and the
 shared-prefix MLA-shaped step at the benchmark's split count (bit-exact cache
 after copy-on-write + append; every head of the first, last, shortest- and
 longest-suffix sequences and one head of every sequence against the
@@ -112,11 +114,23 @@ def test_dcp200k_partitions_merge_to_unsplit(pkv, interleave):
         pl.append(l)
         assert_attention_close(out_p[r].cpu().numpy(), lse_p[r].cpu().numpy(), o, l,
                                f"partition {r}")
+    # the benchmark's launch: the P partitions as the P rows of one batch
+    # (the query repeated), at its split count, then the merge of the P results
+    pq = q.expand(P, w.num_q_heads, w.head_dim_k).contiguous()
+    bo, bl = pkv.paged_decode_attn(pq, k, v, ptab, plen.to(dev), w.scale,
+                                   num_splits=DEFAULT_SPLITS["dcp200k"])
+    bmo, bml = pkv.lse_merge(bo.unsqueeze(1), bl.unsqueeze(1))
+    torch.cuda.synchronize()
+    assert pkv.device_status() == 0
+    for r in range(P):
+        assert_attention_close(bo[r:r + 1].cpu().numpy(), bl[r:r + 1].cpu().numpy(), po[r],
+                               pl[r], f"batched partition {r}")
     mo, ml = oracle.lse_merge(np.stack(po), np.stack(pl))
     np.testing.assert_allclose(mo, ro, rtol=0, atol=1e-12)     # the oracle agrees with itself
     np.testing.assert_allclose(ml, rl, rtol=0, atol=1e-12)
     assert_attention_close(out_u.cpu().numpy(), lse_u.cpu().numpy(), ro, rl, "unsplit")
     assert_attention_close(out_m.cpu().numpy(), lse_m.cpu().numpy(), ro, rl, "merged partitions")
+    assert_attention_close(bmo.cpu().numpy(), bml.cpu().numpy(), ro, rl, "batched, merged")
 
 
 def test_agent_mla_shared_prefix_step(pkv):

@@ -122,10 +122,12 @@ def test_multi_token_short_sequence_is_flagged(pkv, T, hq, splits, dk):
 
 
 def test_multi_token_full_size_sampled_rows(pkv):
-    """Speculative verification at 8 x 32K (4 new tokens per sequence, 16
-    splits), sampled (sequence, token, head) rows against the oracle."""
+    """Speculative verification at 8 x 32K (4 new tokens per sequence, at
+    the benchmark's split count), sampled (sequence, token, head) rows
+    against the oracle."""
+    from bench import DEFAULT_SPLITS
     w = workloads.spec_verify()
-    out, lse = gpu_multi(pkv, w, 16)
+    out, lse = gpu_multi(pkv, w, DEFAULT_SPLITS["spec4_32k"])
     assert pkv.device_status() == 0
     k, v, _ = oracle_cache(w)
     T = w.tokens_per_seq
