@@ -35,6 +35,7 @@ import ctypes
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -135,6 +136,14 @@ def kernel_flops(w):
         (w.head_dim_k + w.head_dim_v) * 2
 
 
+def code_only(text: str) -> str:
+    """C++ source without its comments and blank space: the profile summaries
+    are tied to the code they measured, not to its comments."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def stored_traffic(workload):
     """Per-launch DRAM bytes from the workload's committed ncu summary, if it
     was taken on the current kernel sources (else None)."""
@@ -144,8 +153,9 @@ def stored_traffic(workload):
     try:
         h = hashlib.sha256()
         for src in sources:
-            with open(os.path.join(ROOT, "paged_kv_cache_93_gb300", "csrc", src), "rb") as f:
-                h.update(f.read())
+            with open(os.path.join(ROOT, "paged_kv_cache_93_gb300", "csrc", src),
+                      encoding="utf-8") as f:
+                h.update(code_only(f.read()).encode())
         vals = {}
         with open(os.path.join(ROOT, "profiles", name), encoding="utf-8") as f:
             for line in f:

@@ -17,18 +17,22 @@
 // (one score MMA per k-step).  S^T (two buffers of 128 columns) and O^T
 // (Dv/128 blocks of 64 columns) fill TMEM's 512 columns at Dv = 512.
 //
-// Warp roles (192 threads):
+// Warp roles (192 threads; 256 over an FP8 cache):
 //   warp 0   TMA producer: K chunks [128 tok x 64 dims] (two 64-row boxes)
 //            and V chunks [64 tok x 128 dims] (one box, two 64-column
-//            segments), 16 KB each, through a ring of 16 KB stages.
+//            segments), 16 KB each, through a ring of 16 KB stages (FP8:
+//            the same chunks as 8 KB of codes, through a ring of code
+//            stages).
 //   warp 1   owns the TMEM allocation; lane 0 issues every MMA and commits
 //            completions to mbarriers.  It zeroes V rows past the end of a
-//            sequence before they meet the tensor core.
+//            sequence before they meet the tensor core (bf16).
 //   warps 2-5  softmax and epilogue, one thread per TMEM lane (token row of
 //            S^T, value row of O^T).  They pre-scale and split the query,
 //            turn scores into probabilities (bf16 hi + lo, written in the
 //            MMA's operand layout), keep per-thread partial sums, and write
 //            the normalised output and LSE.
+//   warps 6-7  FP8 only: converters, E4M3 codes -> fp16 ring stages in the
+//            bf16 chunks' layout (value rows past the end written as zeros).
 // The running max of each head is raised only when a score exceeds it by
 // more than 8 (log2 units); then the tile max is formed across the token
 // lanes and the accumulators are rescaled in TMEM.  Otherwise
