@@ -21,8 +21,8 @@
 //   warp 0   TMA producer: K chunks [128 tok x 64 dims] (two 64-row boxes)
 //            and V chunks [64 tok x 128 dims] (one box, two 64-column
 //            segments), 16 KB each, through a ring of 16 KB stages (FP8:
-//            the same chunks as 8 KB of codes, through a ring of code
-//            stages).
+//            the same chunks as 8 KB of codes, landed in the upper half of
+//            the stage).
 //   warp 1   owns the TMEM allocation; lane 0 issues every MMA and commits
 //            completions to mbarriers.  It zeroes V rows past the end of a
 //            sequence before they meet the tensor core (bf16).
@@ -31,8 +31,10 @@
 //            turn scores into probabilities (bf16 hi + lo, written in the
 //            MMA's operand layout), keep per-thread partial sums, and write
 //            the normalised output and LSE.
-//   warps 6-7  FP8 only: converters, E4M3 codes -> fp16 ring stages in the
-//            bf16 chunks' layout (value rows past the end written as zeros).
+//   warps 6-7  FP8 only: converters, expanding each stage's codes in place
+//            into fp16 in the bf16 chunks' layout (value rows past the end
+//            written as zeros).  A stage is rewritten only after its codes
+//            landed, i.e. a whole copy after its previous MMAs released it.
 // The running max of each head is raised only when a score exceeds it by
 // more than 8 (log2 units); then the tile max is formed across the token
 // lanes and the accumulators are rescaled in TMEM.  Otherwise
@@ -83,7 +85,7 @@ constexpr uint32_t kIdO16 = tc::idesc_f16_f32(128, 64, 1, 1);
 constexpr int kThreadsF8 = 256;         // warps 6-7: converters
 constexpr int kConvWarp0 = 6;
 constexpr int kConvThreads = 64;
-constexpr int kCodeBytes = 8192;        // one chunk's E4M3 codes (a code stage)
+constexpr int kCodeBytes = 8192;        // one chunk's E4M3 codes, in the upper half of its stage
 
 // mbarrier slots
 constexpr int kBarFull = 0;             // + stage: chunk landed (TMA bytes)
@@ -96,20 +98,18 @@ constexpr int kBarQFull = 22;           // query written (128 arrivals)
 constexpr int kBarQEmpty = 23;          // score MMAs of an item done (MMA commit)
 constexpr int kBarOEmpty = 24;          // accumulators read out (128 arrivals)
 constexpr int kBarDrain = 25;
-constexpr int kBarLanded = 26;          // + code stage, FP8: codes landed (TMA bytes)
-constexpr int kBarCodeFree = 34;        // + code stage, FP8: codes read (64 arrivals)
-constexpr int kNumBars = kBarCodeFree + kMaxRing;
+constexpr int kBarLanded = 26;          // + stage, FP8: the chunk's codes landed (TMA bytes)
+constexpr int kNumBars = kBarLanded + kMaxRing;
 
 struct TcShape {
     int dk_segs;      // Dk / 64
     int dv_blocks;    // Dv / 128
-    int ring;         // ring stages (16 KB: one chunk as the MMAs read it)
-    int codes;        // FP8: code stages (8 KB: one chunk as stored); 0 for bf16
+    int ring;         // ring stages
 };
 
 // Shared-memory map, offsets from a 1024-byte-aligned base.
 struct SmemMap {
-    uint32_t q_hi, q_lo, p_hi, p_lo, ring, codes, bars, mrow, aux, red, slot, flag, end;
+    uint32_t q_hi, q_lo, p_hi, p_lo, ring, bars, mrow, aux, red, slot, flag, end;
 };
 __host__ __device__ inline SmemMap smem_map(const TcShape &s) {
     SmemMap m;
@@ -120,9 +120,8 @@ __host__ __device__ inline SmemMap smem_map(const TcShape &s) {
     m.p_hi = uint32_t(s.dk_segs) * 16384;
     m.p_lo = m.p_hi + kM * 128;
     m.ring = m.p_lo + kM * 128;
-    m.codes = m.ring + uint32_t(s.ring) * kChunk;
-    m.bars = m.codes + uint32_t(s.codes) * kCodeBytes;
-    m.mrow = m.bars + (s.codes ? kNumBars : kBarLanded) * 8;
+    m.bars = m.ring + uint32_t(s.ring) * kChunk;
+    m.mrow = m.bars + kNumBars * 8;
     m.aux = m.mrow + kN * 4;
     m.red = m.aux + kN * 4;
     m.slot = m.red + 4 * kN * 4;
@@ -231,12 +230,11 @@ __device__ __forceinline__ uint32_t swz(int row, int col) {
 }
 
 // F8: the pools hold E4M3 codes (a.k_scale, a.v_scale per KV head).  The
-// producer lands each chunk's 8 KB of codes in a ring of code stages; the
-// converter warps read a chunk's codes (freeing its code stage at once) and
-// expand them, exactly, into fp16 in a ring stage, in the layout the bf16
-// copies have.  The query and the probabilities are fp16 hi + lo, the query
-// scaled by a power of two per item so that both parts stay inside fp16's
-// range.
+// producer lands each chunk's 8 KB of codes in the upper half of its ring
+// stage and the converter warps expand them, exactly, into fp16 over the
+// whole stage in the layout the bf16 copies have; the query and the
+// probabilities are fp16 hi + lo, the query scaled by a power of two per
+// item so that both parts stay inside fp16's range.
 template <bool F8>
 __global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
 decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
@@ -265,10 +263,7 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
             // bf16: the producer's arrival + TMA bytes; FP8: the converters
             mbar_init(bar(kBarFull + r), F8 ? kConvThreads : 1);
             mbar_init(bar(kBarEmpty + r), 1);
-        }
-        for (int r = 0; r < shp.codes; ++r) {
-            mbar_init(bar(kBarLanded + r), 1);
-            mbar_init(bar(kBarCodeFree + r), kConvThreads);
+            if (F8) mbar_init(bar(kBarLanded + r), 1);
         }
         mbar_init(bar(kBarSFull), 1);
         mbar_init(bar(kBarSFull + 1), 1);
@@ -302,23 +297,23 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
         int stage = 0;
         uint32_t phase = 0, armed = 0, armed_parity = 0;
         bool ok = a.withhold == 0;              // test control: issue no copy at all
-        // bf16: the copies fill the ring stages; FP8: the code stages.
-        const int nst = F8 ? shp.codes : shp.ring;
-        const int bar_full = F8 ? kBarLanded : kBarFull, bar_empty = F8 ? kBarCodeFree : kBarEmpty;
-        const uint32_t st_base = F8 ? sm.codes : sm.ring, st_bytes = F8 ? kCodeBytes : kChunk;
+        // bf16: the chunk fills its stage; FP8: its codes fill the upper half
+        // and the converters complete the stage.
+        const int bar_full = F8 ? kBarLanded : kBarFull;
         // Wait for a free stage and arm it for one chunk; false on abort.
         auto acquire = [&](uint32_t &dst) -> bool {
             const bool w =
-                pipe_wait(bar(bar_empty + stage), phase ^ 1u, a.status, abort_flag, wlim);
+                pipe_wait(bar(kBarEmpty + stage), phase ^ 1u, a.status, abort_flag, wlim);
             if (!__all_sync(0xffffffffu, w)) return false;
-            if (lane == 0) mbar_arrive_expect_tx(bar(bar_full + stage), st_bytes);
+            if (lane == 0)
+                mbar_arrive_expect_tx(bar(bar_full + stage), F8 ? kCodeBytes : kChunk);
             armed |= 1u << stage;
             armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-            dst = sb + st_base + uint32_t(stage) * st_bytes;
+            dst = sb + sm.ring + uint32_t(stage) * kChunk + (F8 ? kCodeBytes : 0);
             return true;
         };
         auto advance = [&]() {
-            if (++stage == nst) {
+            if (++stage == shp.ring) {
                 stage = 0;
                 phase ^= 1u;
             }
@@ -400,7 +395,7 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
         }
         // Leave no copy in flight into this CTA's shared memory.
         if (lane == 0)
-            for (int s = 0; s < nst; ++s)
+            for (int s = 0; s < shp.ring; ++s)
                 if (armed & (1u << s))
                     mbar_wait(bar(bar_full + s), (armed_parity >> s) & 1u, a.status);
         __syncwarp();
@@ -834,25 +829,21 @@ decode_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
             // of the sequence are written as zeros (any bits may sit there,
             // and NaN times a zero probability is NaN).
             const int t = threadIdx.x - kConvWarp0 * 32;    // 0..63
-            int stage = 0, cstage = 0;
-            uint32_t phase = 0, cphase = 0;
+            int stage = 0;
+            uint32_t phase = 0;
             auto convert = [&](bool is_v, int keep) -> bool {
-                if (!pipe_wait(bar(kBarLanded + cstage), cphase, a.status, abort_flag, wlim))
-                    return false;
-                const uint8_t *src = base + sm.codes + size_t(cstage) * kCodeBytes;
-                uint4 cd[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    cd[k] = *reinterpret_cast<const uint4 *>(src + 16 * (t + 64 * k));
-                mbar_arrive(bar(kBarCodeFree + cstage));   // the codes are in registers
-                if (++cstage == shp.codes) {
-                    cstage = 0;
-                    cphase ^= 1u;
-                }
-                // the ring stage is free once the MMAs of its previous chunk are done
-                if (!pipe_wait(bar(kBarEmpty + stage), phase ^ 1u, a.status, abort_flag, wlim))
-                    return false;
+                const bool w =
+                    pipe_wait(bar(kBarLanded + stage), phase, a.status, abort_flag, wlim);
                 uint8_t *st = base + sm.ring + size_t(stage) * kChunk;
+                uint4 cd[8];
+                if (w) {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        cd[k] = *reinterpret_cast<const uint4 *>(st + kCodeBytes +
+                                                                 16 * (t + 64 * k));
+                }
+                // every code is read before fp16 values overwrite the stage
+                if (bar_red_or(2, kConvThreads, !w)) return false;
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     const int p = t + 64 * k;
@@ -961,41 +952,30 @@ bool make_code_map(CUtensorMap *map, const void *pool, int64_t rows, int dim, in
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// bf16: as many ring stages as fit.  FP8: as many (ring stage, code stage)
-// pairs as fit (2 at Dk 576), then code stages in what is left.
-TcShape tc_shape(const pkv_cache_desc &c, bool f8) {
-    TcShape s{c.head_dim_k / 64, c.head_dim_v / 128, 0, f8 ? 1 : 0};
-    const size_t fixed = tc_smem_bytes(s) - (f8 ? kCodeBytes : 0);
-    const int64_t room = int64_t(kSmemLimit) - int64_t(std::min<size_t>(fixed, kSmemLimit));
-    if (!f8) {
-        s.ring = int(std::min<int64_t>(room / kChunk, kMaxRing));
-    } else {
-        s.ring = int(std::min<int64_t>(room / (kChunk + kCodeBytes), kMaxRing));
-        s.codes = int(std::min<int64_t>((room - int64_t(s.ring) * kChunk) / kCodeBytes, kMaxRing));
-    }
+TcShape tc_shape(const pkv_cache_desc &c) {
+    TcShape s{c.head_dim_k / 64, c.head_dim_v / 128, 0};
+    const size_t fixed = tc_smem_bytes(s);
+    const int ring = int((kSmemLimit - std::min<size_t>(fixed, kSmemLimit)) / kChunk);
+    s.ring = std::min(ring, kMaxRing);
     return s;
-}
-
-bool shape_supported(const pkv_cache_desc &c, int32_t num_q_heads) {
-    const int G = num_q_heads / c.num_kv_heads;
-    const bool pow2_bs = c.block_size >= kHalf && c.block_size <= 256 &&
-                         (c.block_size & (c.block_size - 1)) == 0;
-    const int64_t rows = int64_t(c.num_blocks) * c.num_kv_heads * c.block_size;
-    if (G % kN != 0 || !pow2_bs || rows >= (int64_t(1) << 31) - 1) return false;
-    return c.head_dim_k % 64 == 0 && c.head_dim_k >= 64 && c.head_dim_v % 128 == 0 &&
-           c.head_dim_v <= 512;
 }
 
 }  // namespace
 
 bool mla_tc_kernel_supports(const pkv_cache_desc &c, int32_t num_q_heads) {
-    return shape_supported(c, num_q_heads) && tc_shape(c, false).ring >= 2;
+    const int G = num_q_heads / c.num_kv_heads;
+    const bool pow2_bs = c.block_size >= kHalf && c.block_size <= 256 &&
+                         (c.block_size & (c.block_size - 1)) == 0;
+    const int64_t rows = int64_t(c.num_blocks) * c.num_kv_heads * c.block_size;
+    if (G % kN != 0 || !pow2_bs || rows >= (int64_t(1) << 31) - 1) return false;
+    if (c.head_dim_k % 64 != 0 || c.head_dim_k < 64 || c.head_dim_v % 128 != 0 ||
+        c.head_dim_v > 512)
+        return false;
+    return tc_shape(c).ring >= 2;
 }
 
 bool mla_tc_e4m3_kernel_supports(const pkv_cache_desc &c, int32_t num_q_heads) {
-    if (!shape_supported(c, num_q_heads)) return false;
-    const TcShape s = tc_shape(c, true);
-    return s.ring >= 2 && s.codes >= 1;
+    return mla_tc_kernel_supports(c, num_q_heads);
 }
 
 int32_t mla_tc_work_units(const pkv_cache_desc &c, int32_t batch, int32_t num_q_heads) {
@@ -1006,7 +986,7 @@ namespace {
 // One launch over the problems' items together (p1.batch = 0: one problem).
 template <bool F8>
 int launch_problems(const DecodeArgs &a, const Problem &p0, const Problem &p1) {
-    const TcShape shp = tc_shape(a.cache, F8);
+    const TcShape shp = tc_shape(a.cache);
     const int64_t rows = int64_t(a.cache.num_blocks) * a.cache.num_kv_heads * a.cache.block_size;
     CUtensorMap tk, tv;
     const bool maps =
