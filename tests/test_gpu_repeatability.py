@@ -127,3 +127,26 @@ def test_e4m3_calls_repeat_bit_for_bit(pkv, case, splits):
                                                num_splits=splits),
             ro, rl, f"{name}/{splits}")
     assert pkv.device_status() == 0
+
+
+@pytest.mark.parametrize("splits", [(3, 2), (1, 1)])
+def test_cascade_calls_repeat_bit_for_bit(pkv, splits):
+    """The cascade's single launch over two problems (all rows over the
+    shared prefix, each sequence over the rest) on the tcgen05 kernel."""
+    w = workloads.shared_prefix(31, 6, [400, 37, 900], 128, 1, 576, 512, 64)
+    dev = "cuda"
+    k, v, bt = w.k_pool.to(dev), w.v_pool.to(dev), w.block_tables.to(dev)
+    slots = pkv.slot_mapping(k, v, bt, w.new_seq.to(dev), w.new_pos.to(dev))
+    pkv.kv_append(k, v, w.k_new.to(dev), w.v_new.to(dev), slots)
+    q, lens, ptab = w.q.to(dev), w.seq_lens.to(dev), w.info["prefix_table"].to(dev)
+    ko, vo = bits(w.k_pool), bits(w.v_pool)
+    sl = oracle.slot_mapping(w.block_tables.numpy(), w.new_seq.numpy(), w.new_pos.numpy(),
+                             w.block_size)
+    assert oracle.kv_append(ko, vo, bits(w.k_new), bits(w.v_new), sl, w.block_size) == 0
+    ro, rl = oracle.paged_decode_attn(w.q.numpy(), ko, vo, w.block_tables.numpy(),
+                                      w.seq_lens.numpy(), w.scale)
+    _repeat(lambda: pkv.paged_decode_attn_cascade(q, k, v, ptab, bt, lens, w.scale,
+                                                  prefix_splits=splits[0],
+                                                  suffix_splits=splits[1]),
+            ro, rl, f"cascade/{splits}")
+    assert pkv.device_status() == 0
