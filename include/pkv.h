@@ -326,8 +326,14 @@ int pkv_paged_decode_attn_noalloc(const pkv_cache_desc *cache, const float *q, i
  * is carried as four E4M3 terms and the probabilities as five, each term the
  * rounding residual of the one before scaled by 16, so both keep about 16
  * significant bits and the result is fp32-accurate attention on the stored
- * values.  Other shapes, or flags PKV_DECODE_GENERIC / PKV_DECODE_NO_TCGEN05,
- * run a CUDA-core kernel that decodes the codes exactly.
+ * values.  Query groups that are a multiple of 64 heads (the MLA shape:
+ * 128 heads over one 576-dim key / 512-dim value head; head dims multiples
+ * of 64 / 128, power-of-two block sizes 64..256) run on the tcgen05
+ * large-group kernel: each chunk's codes are expanded exactly into fp16 in
+ * shared memory and the products run in fp16 with the query (scaled by a
+ * power of two per work item) and the probabilities as fp16 hi + lo.
+ * Other shapes, or flags PKV_DECODE_GENERIC / PKV_DECODE_NO_TCGEN05, run a
+ * CUDA-core kernel that decodes the codes exactly.
  * ------------------------------------------------------------------------- */
 /* The split count num_splits = 0 resolves to in pkv_paged_decode_attn_e4m3. */
 int32_t pkv_decode_auto_splits_e4m3(const pkv_cache_desc *cache, int32_t batch,
