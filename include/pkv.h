@@ -252,12 +252,14 @@ int64_t pkv_interleave_partition_len(int64_t num_tokens, int32_t num_parts,
  * so that the bounded pipeline waits can be made to run out on purpose,
  * without any fault).  After pkv_test_enable_withhold(1), flag
  * PKV_DECODE_TEST_WITHHOLD makes pkv_paged_decode_attn (and its _partial
- * and _noalloc forms) run the shape's split kernel with its copy producer
+ * and _noalloc forms, and pkv_paged_decode_attn_e4m3 and its _noalloc form
+ * for query groups of 64+ heads) run the shape's split kernel with its copy producer
  * issuing no copy at all and every pipeline wait limited to 1 ms: the first
  * wait for a copy runs out, the kernel sets PKV_DEV_TIMEOUT, every role of
  * each CTA leaves its loop with nothing in flight, and every row of the call
  * comes back NaN (output and LSE), as any abandoned chunk does.  Only the
- * warp-level GQA kernel and the tcgen05 large-group kernel take the flag;
+ * warp-level GQA kernel and the tcgen05 large-group kernel (both of its
+ * modes) take the flag;
  * for other shapes, the other entry points, or while it is not enabled
  * (pkv_test_enable_withhold(0), the default) it is PKV_ERR_INVALID_ARG.
  * Returns PKV_OK.

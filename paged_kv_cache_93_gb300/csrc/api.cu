@@ -145,8 +145,19 @@ int run_split_kernel(const DecodeArgs &a, int32_t flags) {
 
 // The split kernel over E4M3 pools: the tcgen05 GQA kernel (4 to 32 rows
 // per KV head, head dims 128), the tcgen05 large-group kernel (64 or more
-// heads per KV head), else the CUDA-core kernel.
+// heads per KV head), else the CUDA-core kernel.  Under the test control
+// only the large-group kernel runs (it reads it); anything else is refused.
 int run_split_kernel_e4m3(const DecodeArgs &a, int32_t flags) {
+    if (flags & PKV_DECODE_TEST_WITHHOLD) {
+        if (flags != PKV_DECODE_TEST_WITHHOLD ||
+            gqa_tc_e4m3_kernel_supports(a.cache, a.num_q_heads) ||
+            !mla_tc_e4m3_kernel_supports(a.cache, a.num_q_heads))
+            return PKV_ERR_INVALID_ARG;
+        DecodeArgs w = a;
+        w.withhold = 1;
+        w.wait_ns = kTestWaitNs;
+        return launch_decode_mla_tc_e4m3(w);
+    }
     if (flags == 0 && gqa_tc_e4m3_kernel_supports(a.cache, a.num_q_heads))
         return launch_decode_gqa_tc_e4m3(a);
     if (flags == 0 && mla_tc_e4m3_kernel_supports(a.cache, a.num_q_heads))
@@ -221,12 +232,16 @@ extern "C" int pkv_paged_decode_attn_e4m3(const pkv_cache_desc *cache, const flo
                                           float scale, int32_t num_splits, void *workspace,
                                           size_t workspace_bytes, float *out, float *lse,
                                           int32_t flags, pkv_stream_t stream) {
-    if (flags & PKV_DECODE_TEST_WITHHOLD) return PKV_ERR_INVALID_ARG;
     int st = validate_decode(cache, q, batch, num_q_heads, k_pool, v_pool, block_tables,
                              max_blocks, seq_lens, num_splits, flags);
     if (st != PKV_OK || batch == 0) return st;
     if (!v_pool || !k_scale || !v_scale || !out || !lse) return PKV_ERR_INVALID_ARG;
     if (!aligned16(out)) return PKV_ERR_ALIGNMENT;
+    // the test control: only for shapes of the large-group kernel
+    if ((flags & PKV_DECODE_TEST_WITHHOLD) &&
+        (flags != PKV_DECODE_TEST_WITHHOLD || gqa_tc_e4m3_kernel_supports(*cache, num_q_heads) ||
+         !mla_tc_e4m3_kernel_supports(*cache, num_q_heads)))
+        return PKV_ERR_INVALID_ARG;
     // a tensor-core kernel where one takes the shape, the CUDA-core one
     // otherwise (or when a flag asks for it)
     auto launch = [&](const DecodeArgs &d) { return run_split_kernel_e4m3(d, flags); };

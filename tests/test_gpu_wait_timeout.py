@@ -11,7 +11,9 @@ limits each wait to 1 ms, so the first wait for a copy runs out while
 nothing is in flight.  Checked for the warp-level GQA kernel and the tcgen05
 large-group kernel: the call returns promptly, the status word holds
 PKV_DEV_TIMEOUT, every row is reported NaN, and the next ordinary call on
-the same device is right (against the oracle) with a clean status word.
+the same device is right (against the oracle) with a clean status word;
+also for the large-group kernel's E4M3 mode, whose converter warps wait for
+codes that never land.
 """
 from __future__ import annotations
 
@@ -78,6 +80,45 @@ def test_wait_that_runs_out_is_reported_and_the_device_recovers(pkv, name, shape
     ro, rl = oracle.paged_decode_attn(w.q.numpy(), bits(w.k_pool), bits(w.v_pool),
                                       w.block_tables.numpy(), w.seq_lens.numpy(), w.scale)
     assert_attention_close(out2.cpu().numpy(), lse2.cpu().numpy(), ro, rl, f"{name} after")
+
+
+def test_e4m3_large_group_wait_that_runs_out(pkv):
+    """The same over an FP8 cache on the large-group kernel's E4M3 mode,
+    whose converter warps wait for codes that never land: the converters,
+    the MMA issuer and the softmax all leave with nothing in flight."""
+    w = workloads.e4m3(workloads.custom(26, [900, 200], 128, 1, 576, 512, 64))
+    dev = "cuda"
+    q, k, v = w.q.to(dev), w.k_codes.to(dev), w.v_codes.to(dev)
+    ks, vs = w.k_scale.to(dev), w.v_scale.to(dev)
+    bt, lens = w.block_tables.to(dev), w.seq_lens.to(dev)
+    assert pkv.device_status(reset=True) == 0
+    assert pkv.lib.pkv_test_enable_withhold(1) == 0
+    try:
+        t0 = time.perf_counter()
+        out, lse = pkv.paged_decode_attn_e4m3(q, k, v, ks, vs, bt, lens, w.scale, num_splits=2,
+                                              flags=pkv.DECODE_TEST_WITHHOLD)
+        torch.cuda.synchronize()
+        elapsed = time.perf_counter() - t0
+        # a GQA shape over an FP8 cache runs another kernel: refused
+        g = workloads.e4m3(workloads.custom(27, [300, 40], 32, 8, 128, 128, 16))
+        with pytest.raises(pkv.PkvError):
+            pkv.paged_decode_attn_e4m3(g.q.to(dev), g.k_codes.to(dev), g.v_codes.to(dev),
+                                       g.k_scale.to(dev), g.v_scale.to(dev),
+                                       g.block_tables.to(dev), g.seq_lens.to(dev), g.scale,
+                                       num_splits=2, flags=pkv.DECODE_TEST_WITHHOLD)
+    finally:
+        pkv.lib.pkv_test_enable_withhold(0)
+    assert elapsed < 10.0, f"the call took {elapsed:.1f} s"
+    status = pkv.device_status(reset=True)
+    assert status == pkv.DEV_TIMEOUT, f"status word {status:#x}"
+    assert torch.isnan(out).all() and torch.isnan(lse).all()
+    out2, lse2 = pkv.paged_decode_attn_e4m3(q, k, v, ks, vs, bt, lens, w.scale, num_splits=2)
+    torch.cuda.synchronize()
+    assert pkv.device_status(reset=True) == 0
+    ro, rl = oracle.paged_decode_attn_e4m3(w.q.numpy(), w.k_codes.numpy(), w.v_codes.numpy(),
+                                           w.k_scale.numpy(), w.v_scale.numpy(),
+                                           w.block_tables.numpy(), w.seq_lens.numpy(), w.scale)
+    assert_attention_close(out2.cpu().numpy(), lse2.cpu().numpy(), ro, rl, "e4m3 after")
 
 
 def test_partials_of_abandoned_chunks_are_nan(pkv):
