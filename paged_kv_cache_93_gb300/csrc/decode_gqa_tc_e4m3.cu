@@ -519,10 +519,10 @@ decode_gqa_tc_e4m3_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     tc::wait_ld();
 #pragma unroll
                     for (int j = 0; j < RG; ++j) {      // fold the query terms back
-                        float s = __uint_as_float(v[3][j]);
-                        s = fmaf(s, 0.0625f, __uint_as_float(v[2][j]));
-                        s = fmaf(s, 0.0625f, __uint_as_float(v[1][j]));
-                        s = fmaf(s, 0.0625f, __uint_as_float(v[0][j]));
+                        float s = __uint_as_float(v[kQTerms - 1][j]);
+#pragma unroll
+                        for (int k = kQTerms - 2; k >= 0; --k)
+                            s = fmaf(s, 0.0625f, __uint_as_float(v[k][j]));
                         x[j] = s * qsc[h0 + j];
                     }
                 }
@@ -670,11 +670,10 @@ decode_gqa_tc_e4m3_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 tc::wait_ld();
 #pragma unroll
                 for (int j = 0; j < RG; ++j) {          // fold the probability terms back
-                    float o = __uint_as_float(v[4][j]);
-                    o = fmaf(o, 0.0625f, __uint_as_float(v[3][j]));
-                    o = fmaf(o, 0.0625f, __uint_as_float(v[2][j]));
-                    o = fmaf(o, 0.0625f, __uint_as_float(v[1][j]));
-                    o = fmaf(o, 0.0625f, __uint_as_float(v[0][j]));
+                    float o = __uint_as_float(v[kPTerms - 1][j]);
+#pragma unroll
+                    for (int k = kPTerms - 2; k >= 0; --k)
+                        o = fmaf(o, 0.0625f, __uint_as_float(v[k][j]));
                     a.out_part[(split0 + row_of(h0 + j)) * kD + row] = o * aux[h0 + j];
                 }
             }
