@@ -355,8 +355,8 @@ class DcpE4m3Step(DcpStep):
     """The DCP step over an FP8 (E4M3) cache: the 200K tokens are quantised
     into their partitions by the E4M3 append, the partitions attended in one
     pkv_paged_decode_attn_e4m3 call and merged."""
-    kernel_name = ("pkv_paged_decode_attn_e4m3 over the partitions (decode_gqa_tc_e4m3_kernel, "
-                   "groups of 8) + its split merge")
+    kernel_name = ("decode_gqa_tc_e4m3_kernel over the partitions (split attention, "
+                   "pkv_paged_decode_attn_partial_e4m3, groups of 8)")
 
     def __init__(self, pkv, w, dev, splits):
         self.pkv, self.w, self.splits = pkv, w, splits
@@ -384,6 +384,8 @@ class DcpE4m3Step(DcpStep):
         self.slots = torch.empty(1, dtype=torch.int64, device=dev)
         self.ws = torch.zeros(max(1, pkv.decode_workspace_size(P, Hq, Dv, splits)),
                               dtype=torch.uint8, device=dev)
+        self.sp_out = torch.empty(splits, P, Hq, Dv, device=dev)
+        self.sp_lse = torch.empty(splits, P, Hq, device=dev)
         self.launches = 2 + 2 + 1
         self.desc = (f"interleave slot + kv_append_e4m3 (decode token) + "
                      f"paged_decode_attn_e4m3 over the {P} partitions in one launch "
@@ -391,10 +393,10 @@ class DcpE4m3Step(DcpStep):
                      f"partition results")
 
     def kernel(self):
-        self.pkv.paged_decode_attn_e4m3(self.pq, self.k, self.v, self.k_scale, self.v_scale,
-                                        self.ptab, self.plen, self.w.scale,
-                                        num_splits=self.splits, workspace=self.ws, out=self.pout,
-                                        lse=self.plse)
+        self.pkv.paged_decode_attn_partial_e4m3(self.pq, self.k, self.v, self.k_scale,
+                                                self.v_scale, self.ptab, self.plen, self.w.scale,
+                                                self.splits, out_part=self.sp_out,
+                                                lse_part=self.sp_lse)
 
     def run(self, ev_a=None, ev_b=None):
         p, w = self.pkv, self.w
@@ -402,11 +404,15 @@ class DcpE4m3Step(DcpStep):
                                   out=self.slots)
         p.kv_append_e4m3(self.k, self.v, self.k_new, self.v_new, self.slots, self.k_scale,
                          self.v_scale)
-        if ev_a is not None:
+        if ev_a is None:
+            p.paged_decode_attn_e4m3(self.pq, self.k, self.v, self.k_scale, self.v_scale,
+                                     self.ptab, self.plen, w.scale, num_splits=self.splits,
+                                     workspace=self.ws, out=self.pout, lse=self.plse)
+        else:
             ev_a.record()
-        self.kernel()
-        if ev_b is not None:
+            self.kernel()
             ev_b.record()
+            p.lse_merge(self.sp_out, self.sp_lse, out=self.pout, lse=self.plse)
         p.lse_merge(self.pout, self.plse, out=self.out[0], lse=self.lse[0])
 
 
@@ -522,9 +528,9 @@ class MultiStep(Step):
 class E4m3Step(Step):
     """The 32K decode step over an FP8 (E4M3) cache: slot mapping, the
     quantising append of the decode tokens, one pkv_paged_decode_attn_e4m3."""
-    kernel_name = ("pkv_paged_decode_attn_e4m3 (decode_gqa_tc_e4m3_kernel: tcgen05 "
-                   "kind::f8f6f4, E4M3 K/V as stored, the query as 4 and the probabilities as "
-                   "5 E4M3 terms, + lse_merge)")
+    kernel_name = ("decode_gqa_tc_e4m3_kernel (split attention, "
+                   "pkv_paged_decode_attn_partial_e4m3: tcgen05 kind::f8f6f4, E4M3 K/V as "
+                   "stored, the query as 4 and the probabilities as 5 E4M3 terms)")
 
     def __init__(self, pkv, w, dev, splits):
         self.pkv, self.w, self.splits = pkv, w, splits
@@ -539,23 +545,36 @@ class E4m3Step(Step):
         self.lse = torch.empty(B, Hq, device=dev)
         self.ws = torch.zeros(max(1, pkv.decode_workspace_size(B, Hq, w.head_dim_v, splits)),
                               dtype=torch.uint8, device=dev)
+        self.out_part = torch.empty(splits, B, Hq, w.head_dim_v, device=dev)
+        self.lse_part = torch.empty(splits, B, Hq, device=dev)
         self.launches = 4   # slot, append, split, merge
         self.desc = (f"slot_mapping + kv_append_e4m3 ({w.new_pos.numel()} decode tokens) + "
                      f"paged_decode_attn_e4m3 ({splits} splits) = split kernel + lse_merge")
 
     def kernel(self):
-        """The FP8 attention call (its split kernel and merge)."""
-        self.pkv.paged_decode_attn_e4m3(self.q, self.k, self.v, self.k_scale, self.v_scale,
-                                        self.bt, self.lens, self.w.scale,
-                                        num_splits=self.splits, workspace=self.ws, out=self.out,
-                                        lse=self.lse)
+        """The FP8 split attention kernel alone (the roofline's kernel)."""
+        self.pkv.paged_decode_attn_partial_e4m3(self.q, self.k, self.v, self.k_scale,
+                                                self.v_scale, self.bt, self.lens, self.w.scale,
+                                                self.splits, out_part=self.out_part,
+                                                lse_part=self.lse_part)
 
     def attend(self, ev_a=None, ev_b=None):
-        if ev_a is not None:
-            ev_a.record()
+        """What pkv_paged_decode_attn_e4m3 launches: the split kernel, then the
+        merge (events, if given, bracket the split kernel)."""
+        if self.splits == 1 or ev_a is None:
+            if ev_a is not None:
+                ev_a.record()
+            self.pkv.paged_decode_attn_e4m3(self.q, self.k, self.v, self.k_scale, self.v_scale,
+                                            self.bt, self.lens, self.w.scale,
+                                            num_splits=self.splits, workspace=self.ws,
+                                            out=self.out, lse=self.lse)
+            if ev_b is not None:
+                ev_b.record()
+            return
+        ev_a.record()
         self.kernel()
-        if ev_b is not None:
-            ev_b.record()
+        ev_b.record()
+        self.pkv.lse_merge(self.out_part, self.lse_part, out=self.out, lse=self.lse)
 
     def run(self, ev_a=None, ev_b=None):
         p = self.pkv
@@ -570,8 +589,9 @@ class AgentE4m3Step(E4m3Step):
     each sequence's shared tail block (its codes), the quantising append of
     the decode tokens, one pkv_paged_decode_attn_e4m3 (the suffixes are
     appended once, before timing)."""
-    kernel_name = ("pkv_paged_decode_attn_e4m3 (decode_mla_tc_kernel, E4M3 mode: codes "
-                   "expanded exactly to fp16 in shared memory, tcgen05 kind::f16, + lse_merge)")
+    kernel_name = ("decode_mla_tc_kernel, E4M3 mode (split attention, "
+                   "pkv_paged_decode_attn_partial_e4m3: codes expanded exactly to fp16 in shared "
+                   "memory, tcgen05 kind::f16)")
     bound = "tensor"
 
     def __init__(self, pkv, w, dev, splits):
@@ -624,17 +644,25 @@ class MultiE4m3Step(E4m3Step):
                                               num_splits=self.splits, workspace=self.ws,
                                               out=self.out, lse=self.lse)
 
+    def attend(self, ev_a=None, ev_b=None):
+        if ev_a is not None:
+            ev_a.record()
+        self.kernel()
+        if ev_b is not None:
+            ev_b.record()
+
 
 STEPS = {"long32k": Step, "mix": Step, "tiny": Step, "dcp200k": DcpStep, "agent_mla": AgentStep,
-         "agent_mla_latent": AgentStep, "agent_mla_cascade": AgentCascadeStep, "spec4_32k": MultiStep, "long32k_e4m3": E4m3Step,
-         "dcp200k_e4m3": DcpE4m3Step, "spec4_32k_e4m3": MultiE4m3Step,
-         "agent_mla_e4m3": AgentE4m3Step}
+         "agent_mla_latent": AgentStep, "agent_mla_cascade": AgentCascadeStep,
+         "spec4_32k": MultiStep, "long32k_e4m3": E4m3Step, "dcp200k_e4m3": DcpE4m3Step,
+         "spec4_32k_e4m3": MultiE4m3Step, "agent_mla_e4m3": AgentE4m3Step}
 # The 32K workload is timed at 16 splits, the split count its configuration
 # names; the split count the library picks by itself (num_splits = 0) is
 # timed too and reported beside it (`library_auto_splits`).
 DEFAULT_SPLITS = {"long32k": 16, "mix": 1, "tiny": 1, "dcp200k": 19, "agent_mla": 19,
-                  "agent_mla_latent": 19, "agent_mla_cascade": (19, 2), "spec4_32k": 9, "long32k_e4m3": 7,
-                  "dcp200k_e4m3": 14, "spec4_32k_e4m3": 9, "agent_mla_e4m3": 19}
+                  "agent_mla_latent": 19, "agent_mla_cascade": (19, 2), "spec4_32k": 9,
+                  "long32k_e4m3": 7, "dcp200k_e4m3": 14, "spec4_32k_e4m3": 9,
+                  "agent_mla_e4m3": 19}
 # Workloads whose line also carries the library's own split choice.
 AUTO_SPLITS_ALSO = ("long32k",)
 # Workloads of the single-threaded oracle figure (the four GQA configurations)
@@ -874,6 +902,11 @@ def time_step(pkv, st, args, world, stream, sampler=None):
     ev_k, ev_s = _events(K), _events(K)
     barrier(world)
     torch.cuda.synchronize()
+    # The GPU first spins (~0.3 ms of clock cycles per step) while the host
+    # enqueues the steps, so the steps then run back to back and no event
+    # bracket holds a wait for the host's next launch (a short step's calls
+    # can take the host longer than the GPU).
+    torch.cuda._sleep(int(K * 0.3e-3 * 2.0e9))
     for i in range(K):
         ev_s[i][0].record(stream)
         st.run(*ev_k[i])

@@ -349,6 +349,23 @@ int pkv_paged_decode_attn_e4m3(const pkv_cache_desc *cache, const float *q, int3
                                void *workspace, size_t workspace_bytes, float *out, float *lse,
                                int32_t flags, pkv_stream_t stream);
 
+/* The per-chunk partials of pkv_paged_decode_attn_e4m3, as
+ * pkv_paged_decode_attn_partial gives them for a bf16 cache: out_part
+ * [S][batch][num_q_heads][head_dim_v] and lse_part [S][batch][num_q_heads]
+ * (caller-owned device buffers, out_part 16-byte aligned), S = num_splits >= 1,
+ * chunk s of row b covering [s*C_b, min(seq_lens[b], (s+1)*C_b)) with
+ * C_b = 64 * ceil(seq_lens[b] / (64 * S)); an empty chunk gives out = 0 and
+ * lse = -inf.  pkv_lse_merge of these equals pkv_paged_decode_attn_e4m3 at the
+ * same S.  The [DCP] page's stage 3 merges such partials, one per
+ * partition.  The test control flag is refused (PKV_ERR_INVALID_ARG). */
+int pkv_paged_decode_attn_partial_e4m3(const pkv_cache_desc *cache, const float *q,
+                                       int32_t batch, int32_t num_q_heads, const void *k_pool,
+                                       const void *v_pool, const float *k_scale,
+                                       const float *v_scale, const int32_t *block_tables,
+                                       int32_t max_blocks, const int32_t *seq_lens, float scale,
+                                       int32_t num_splits, float *out_part, float *lse_part,
+                                       int32_t flags, pkv_stream_t stream);
+
 /* pkv_paged_decode_attn_noalloc_e4m3 -- pkv_paged_decode_attn_e4m3 with the
  * split partials in the library's scratch (the rules of
  * pkv_paged_decode_attn_noalloc: PKV_NOALLOC_SCRATCH_BYTES, shared by all

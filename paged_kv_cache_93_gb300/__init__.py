@@ -28,7 +28,8 @@ __all__ = [
     "interleave_slot_mapping", "interleave_partition_len", "decode_workspace_size",
     "decode_auto_splits", "paged_decode_attn", "paged_decode_attn_partial",
     "paged_decode_attn_multi", "lse_merge", "kv_append_e4m3", "copy_blocks_e4m3",
-    "paged_decode_attn_e4m3", "paged_decode_attn_multi_e4m3", "paged_decode_attn_cascade",
+    "paged_decode_attn_e4m3", "paged_decode_attn_partial_e4m3", "paged_decode_attn_multi_e4m3",
+    "paged_decode_attn_cascade",
     "decode_cascade_splits", "DEV_PREFIX",
     "device_status", "BlockManager", "library_path", "DECODE_GENERIC", "DECODE_NO_TCGEN05",
     "DECODE_TEST_WITHHOLD", "DEV_BLOCK_ID",
@@ -319,6 +320,28 @@ def paged_decode_attn_e4m3(q, k_pool, v_pool, k_scale, v_scale, block_tables, se
         _ptr(v_scale), _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), float(scale),
         S, _ptr(workspace), ws_bytes, _ptr(out), _ptr(lse), int(flags), _stream(stream)))
     return out, lse
+
+
+def paged_decode_attn_partial_e4m3(q, k_pool, v_pool, k_scale, v_scale, block_tables,
+                                   seq_lens, scale: float, num_splits: int, out_part=None,
+                                   lse_part=None, flags: int = 0, stream=None):
+    """Per-split partials over an E4M3 cache -> (out_part [S, B, Hq, Dv],
+    lse_part [S, B, Hq])."""
+    desc = _e4m3_desc(k_pool, v_pool, k_scale, v_scale)
+    _need(q, "q", torch.float32, 3)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    B, Hq, _ = q.shape
+    S = int(num_splits)
+    if out_part is None:
+        out_part = torch.empty(S, B, Hq, desc.head_dim_v, dtype=torch.float32, device=q.device)
+    if lse_part is None:
+        lse_part = torch.empty(S, B, Hq, dtype=torch.float32, device=q.device)
+    _check("pkv_paged_decode_attn_partial_e4m3", lib.pkv_paged_decode_attn_partial_e4m3(
+        ctypes.byref(desc), _ptr(q), B, Hq, _ptr(k_pool), _ptr(v_pool), _ptr(k_scale),
+        _ptr(v_scale), _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), float(scale),
+        S, _ptr(out_part), _ptr(lse_part), int(flags), _stream(stream)))
+    return out_part, lse_part
 
 
 def paged_decode_attn_multi_e4m3(q, k_pool, v_pool, k_scale, v_scale, block_tables, seq_lens,

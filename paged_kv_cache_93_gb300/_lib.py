@@ -63,6 +63,9 @@ SIGNATURES = {
                                                      _P, _f32, _i32, _P, _P, _i32, _P]),
     "pkv_paged_decode_attn_noalloc": (ctypes.c_int, [_DESC, _P, _i32, _i32, _P, _P, _P, _i32,
                                                      _P, _f32, _i32, _P, _P, _i32, _P]),
+    "pkv_paged_decode_attn_partial_e4m3": (ctypes.c_int, [_DESC, _P, _i32, _i32, _P, _P, _P,
+                                                          _P, _P, _i32, _P, _f32, _i32, _P,
+                                                          _P, _i32, _P]),
     "pkv_paged_decode_attn_noalloc_e4m3": (ctypes.c_int, [_DESC, _P, _i32, _i32, _P, _P, _P,
                                                           _P, _P, _i32, _P, _f32, _i32, _P,
                                                           _P, _i32, _P]),

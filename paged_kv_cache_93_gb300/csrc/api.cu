@@ -272,6 +272,29 @@ extern "C" int pkv_paged_decode_attn_e4m3(const pkv_cache_desc *cache, const flo
                             cache->head_dim_v, out, lse, s);
 }
 
+extern "C" int pkv_paged_decode_attn_partial_e4m3(
+    const pkv_cache_desc *cache, const float *q, int32_t batch, int32_t num_q_heads,
+    const void *k_pool, const void *v_pool, const float *k_scale, const float *v_scale,
+    const int32_t *block_tables, int32_t max_blocks, const int32_t *seq_lens, float scale,
+    int32_t num_splits, float *out_part, float *lse_part, int32_t flags, pkv_stream_t stream) {
+    int st = validate_decode(cache, q, batch, num_q_heads, k_pool, v_pool, block_tables,
+                             max_blocks, seq_lens, num_splits, flags);
+    if (st != PKV_OK || batch == 0) return st;
+    if (num_splits < 1) return PKV_ERR_INVALID_ARG;
+    if (flags & PKV_DECODE_TEST_WITHHOLD) return PKV_ERR_INVALID_ARG;
+    if (!v_pool || !k_scale || !v_scale || !out_part || !lse_part) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(out_part)) return PKV_ERR_ALIGNMENT;
+    uint32_t *status = status_word();
+    if (!status) return PKV_ERR_CUDA;
+    DecodeArgs a{*cache, q, batch, num_q_heads, k_pool, v_pool, block_tables, max_blocks,
+                 seq_lens, scale, num_splits, out_part, lse_part, status,
+                 reinterpret_cast<cudaStream_t>(stream)};
+    a.v_stride = cache->head_dim_v;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    return run_split_kernel_e4m3(a, flags);
+}
+
 extern "C" int pkv_paged_decode_attn(const pkv_cache_desc *cache, const float *q, int32_t batch,
                                      int32_t num_q_heads, const void *k_pool, const void *v_pool,
                                      const int32_t *block_tables, int32_t max_blocks,
@@ -335,13 +358,14 @@ namespace {
 constexpr int32_t kMaxQueryTokens = 64;
 
 // Row r = b * T + t of a multi-token step reads sequence b's table and
-// attends to its first seq_lens[b] - T + 1 + t tokens.  A negative length
-// (a sequence holding fewer than T tokens) is flagged by the split kernel
-// and treated as empty there.
+// attends to its first seq_lens[b] - T + 1 + t tokens.  A sequence holding
+// fewer than T tokens is flagged here (PKV_DEV_SEQ_LEN); its rows of
+// negative length are treated as empty by the split kernel.
 __global__ void multi_rows_kernel(const int32_t *__restrict__ block_tables,
                                   const int32_t *__restrict__ seq_lens, int32_t batch,
                                   int32_t tokens, int32_t max_blocks,
-                                  int32_t *__restrict__ row_tables, int32_t *__restrict__ row_lens) {
+                                  int32_t *__restrict__ row_tables, int32_t *__restrict__ row_lens,
+                                  uint32_t *__restrict__ status) {
     pdl_wait();
     pdl_launch_dependents();
     const int64_t rows = int64_t(batch) * tokens;
@@ -354,6 +378,7 @@ __global__ void multi_rows_kernel(const int32_t *__restrict__ block_tables,
         } else {
             const int64_t r = u - entries, b = r / tokens;
             row_lens[r] = seq_lens[b] - (tokens - 1) + int32_t(r - b * tokens);
+            if (r == b * tokens && seq_lens[b] < tokens) raise_status(status, PKV_DEV_SEQ_LEN);
         }
     }
 }
@@ -445,6 +470,7 @@ extern "C" int pkv_paged_decode_attn_multi(const pkv_cache_desc *cache, const fl
                      seq_lens, scale, S, out, lse, status, s};
         values_from(a);
         a.q_tokens = tokens_per_seq;
+        a.flag_below = tokens_per_seq;
         if (S == 1) return run_split_kernel(a, flags);
         a.out_part = out_part;
         a.lse_part = lse_part;
@@ -462,7 +488,7 @@ extern "C" int pkv_paged_decode_attn_multi(const pkv_cache_desc *cache, const fl
                     dim3(unsigned(std::min<int64_t>((work + threads - 1) / threads,
                                                     int64_t(sm_count()) * 8))),
                     dim3(threads), 0, s, block_tables, seq_lens, batch, tokens_per_seq,
-                    max_blocks, row_tables, row_lens);
+                    max_blocks, row_tables, row_lens, status);
     if (st != PKV_OK) return st;
     DecodeArgs a{*cache, q, rows, num_q_heads, k_pool, v_pool, row_tables, max_blocks,
                  row_lens, scale, S, out, lse, status, s};
@@ -527,6 +553,7 @@ extern "C" int pkv_paged_decode_attn_multi_e4m3(
         a.k_scale = k_scale;
         a.v_scale = v_scale;
         a.q_tokens = tokens_per_seq;
+        a.flag_below = tokens_per_seq;
         if (S == 1) return launch_decode_gqa_tc_e4m3(a);
         a.out_part = reinterpret_cast<float *>(ws + m.partials);
         a.lse_part = reinterpret_cast<float *>(ws + m.partials +
@@ -545,7 +572,7 @@ extern "C" int pkv_paged_decode_attn_multi_e4m3(
                     dim3(unsigned(std::min<int64_t>((work + threads - 1) / threads,
                                                     int64_t(sm_count()) * 8))),
                     dim3(threads), 0, s, block_tables, seq_lens, batch, tokens_per_seq,
-                    max_blocks, row_tables, row_lens);
+                    max_blocks, row_tables, row_lens, status);
     if (st != PKV_OK) return st;
     DecodeArgs a{*cache, q, rows, num_q_heads, k_pool, v_pool, row_tables, max_blocks,
                  row_lens, scale, S, out, lse, status, s};

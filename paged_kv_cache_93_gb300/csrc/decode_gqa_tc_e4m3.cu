@@ -174,7 +174,7 @@ __device__ __forceinline__ Item fp8_item(const DecodeArgs &a, int item, int HG, 
     if (L < 0 || L > int64_t(a.max_blocks) * a.cache.block_size) {
         if (report) raise_status(a.status, PKV_DEV_SEQ_LEN);
         L = 0;
-    } else if (L < a.q_tokens && report) {
+    } else if (L < a.flag_below && report) {
         raise_status(a.status, PKV_DEV_SEQ_LEN);
     }
     const int64_t chunk = 64 * ((L + 64LL * a.num_splits - 1) / (64LL * a.num_splits));
@@ -257,18 +257,37 @@ decode_gqa_tc_e4m3_kernel(const __grid_constant__ CUtensorMap tmap_k,
             int32_t ylag[kLag];                        // rows of tiles i - 1, i - 2
 #pragma unroll
             for (int l = 0; l < kLag; ++l) ylag[l] = standin;
+            // One table read resolves the boxes of tpg tiles (lane j: box
+            // j % nbox of tile j / nbox of the group); the next group's
+            // entries are loaded a group ahead, so no table read waits in
+            // front of a copy.
+            const int tpg = 32 / nbox;
+            auto first_token = [&](int i0) -> int64_t {   // of this lane's box, or -1
+                const int ti = i0 + lane / nbox;
+                const int64_t t = r.begin + int64_t(ti) * kM + int64_t(lane % nbox) * box;
+                return ti < r.ntiles && t < r.end ? t : -1;
+            };
+            auto fetch = [&](int i0) -> int32_t {
+                const int64_t t = first_token(i0);
+                return t >= 0 ? table[t / bs] : 0;
+            };
+            int32_t phys_next = fetch(0);
+            int32_t yg = standin;
             for (int i = 0; i < r.ntiles + kLag && ok; ++i) {
-                int32_t y = standin;                   // lane j < nbox: row of box j of tile i
-                if (i < r.ntiles && lane < nbox) {
-                    const int64_t t = r.begin + int64_t(i) * kM + int64_t(lane) * box;
-                    if (t < r.end) {
-                        const int32_t phys = table[t / bs];
+                if (i % tpg == 0) {
+                    const int32_t phys = phys_next;
+                    phys_next = fetch(i + tpg);
+                    const int64_t t = first_token(i);
+                    yg = standin;
+                    if (t >= 0) {
                         if (phys >= 0 && phys < a.cache.num_blocks)
-                            y = (phys * hkv + r.g) * bs + int32_t(t % bs);
+                            yg = (phys * hkv + r.g) * bs + int32_t(t % bs);
                         else
                             raise_status(a.status, PKV_DEV_BLOCK_ID);
                     }
                 }
+                // lane j < nbox: row of box j of tile i
+                const int32_t y = __shfl_sync(0xffffffffu, yg, (i % tpg) * nbox + lane % nbox);
                 // K of tile i, then V of tile i - kLag: one stage each
                 for (int kv = (i < r.ntiles ? 0 : 1); kv < (i >= kLag ? 2 : 1); ++kv) {
                     const bool w = pipe_wait(bar(kBarEmpty + stage), phase ^ 1u, a.status,

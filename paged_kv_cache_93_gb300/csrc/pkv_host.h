@@ -91,6 +91,10 @@ struct DecodeArgs {
     // first seq_lens[b] - T + 1 + t tokens.  Only the GQA TMA kernel reads
     // T; the other kernels are given one row per (sequence, token) instead.
     int32_t q_tokens = 1;
+    // A sequence whose seq_len is below this sets PKV_DEV_SEQ_LEN (the
+    // multi-token call: T, a sequence that cannot hold its T new tokens); 0
+    // for the decode calls, where seq_len 0 is an empty row.
+    int32_t flag_below = 0;
     // E4M3 pools: per-KV-head dequantisation scales (device, [num_kv_heads]).
     const float *k_scale = nullptr, *v_scale = nullptr;
     // Pipeline waits give up after this many nanoseconds (0: the kernels'

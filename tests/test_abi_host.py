@@ -271,6 +271,17 @@ def test_e4m3_host_rules(pkv):
     # the split choice: enough items for the resident CTAs
     assert 1 <= lib.pkv_decode_auto_splits_e4m3(ctypes.byref(ok), 8, 8, 32768) <= 256
 
+    def partial(S=1, out_part=p, lse_part=p, k_scale=p, flags=0):
+        return lib.pkv_paged_decode_attn_partial_e4m3(ctypes.byref(ok), p, 1, 8, p, p, k_scale,
+                                                      p, p, 4, p, 1.0, S, out_part, lse_part,
+                                                      flags, None)
+    assert partial(S=0) == -1                          # the partials need S >= 1
+    assert partial(out_part=None) == -1
+    assert partial(lse_part=None) == -1
+    assert partial(k_scale=None) == -1
+    assert partial(out_part=odd) == -3                 # out_part 16-byte aligned
+    assert partial(flags=pkv.DECODE_TEST_WITHHOLD) == -1
+
 
 def test_binding_keeps_code_pools_out_of_bf16_calls(pkv):
     """The bf16 calls size rows at two bytes an element; the binding refuses

@@ -111,10 +111,11 @@ def test_distinct_k_and_v_dims(pkv):
     assert_attention_close(out.cpu().numpy(), lse.cpu().numpy(), ro, rl, "576/512")
 
 
-@pytest.mark.parametrize("flags", [0, 1])
+@pytest.mark.parametrize("flags", [0, 1, 2])
 @pytest.mark.parametrize("hq", [16, 64], ids=["G4", "G16"])
 def test_partials_match_oracle_token_ranges(pkv, flags, hq):
-    """Split s of row b covers [s*C, min(L, (s+1)*C)), C = 64*ceil(L/(64*S))."""
+    """Split s of row b covers [s*C, min(L, (s+1)*C)), C = 64*ceil(L/(64*S));
+    a row of length 0 is an empty row, not a flagged one."""
     w = workloads.custom(31, [400, 70, 1, 0], hq, 4, 128, 128, 16)
     S = 5
     dev = "cuda"
@@ -123,7 +124,7 @@ def test_partials_match_oracle_token_ranges(pkv, flags, hq):
     lens[3] = 0
     op, lp = pkv.paged_decode_attn_partial(w.q.to(dev), k, v, bt, lens.to(dev), w.scale, S,
                                            flags=flags)
-    torch.cuda.synchronize()
+    assert pkv.device_status() == 0
     kb, vb = bits(w.k_pool), bits(w.v_pool)
     L = lens.numpy().astype(np.int64)
     C = 64 * (-(-L // (64 * S)))

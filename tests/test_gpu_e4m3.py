@@ -122,6 +122,52 @@ def test_e4m3_mla_shape_matches_oracle(pkv, shape, splits):
     assert pkv.device_status() == 0
 
 
+# (cached tokens, Hq, Hkv, Dk, Dv, block size): the four tcgen05 FP8 GQA
+# forms, the large-group (MLA-shaped) form and a CUDA-core shape (head dim
+# 64); the last row is made empty
+PARTIAL_SHAPES = [
+    ([900, 70, 1, 0], 32, 8, 128, 128, 16),
+    ([700, 129, 0], 16, 2, 128, 128, 32),
+    ([1000, 65, 0], 64, 4, 128, 128, 64),
+    ([600, 3, 0], 64, 2, 128, 128, 16),
+    ([800, 1, 0], 128, 1, 576, 512, 64),
+    ([500, 33, 0], 16, 4, 64, 64, 16),
+]
+
+
+@pytest.mark.parametrize("shape", PARTIAL_SHAPES,
+                         ids=lambda s: f"G{s[1]//s[2]}_D{s[3]}_bs{s[5]}")
+def test_e4m3_partials_match_oracle_token_ranges(pkv, shape):
+    """Split s of row b covers [s*C, min(L, (s+1)*C)), C = 64*ceil(L/(64*S));
+    an empty row or chunk gives (0, -inf); the merged partials are the
+    attention call's result at the same split count, bit for bit."""
+    lens, hq, hkv, dk, dv, bs = shape
+    w = workloads.e4m3(workloads.custom(60 + hq + bs, lens, hq, hkv, dk, dv, bs))
+    w.seq_lens[-1] = 0                                 # an empty row
+    S = 5
+    dev = "cuda"
+    k, v = w.k_codes.to(dev), w.v_codes.to(dev)
+    ks, vs = w.k_scale.to(dev), w.v_scale.to(dev)
+    bt, sl, q = w.block_tables.to(dev), w.seq_lens.to(dev), w.q.to(dev)
+    op, lp = pkv.paged_decode_attn_partial_e4m3(q, k, v, ks, vs, bt, sl, w.scale, S)
+    out, lse = pkv.paged_decode_attn_e4m3(q, k, v, ks, vs, bt, sl, w.scale, num_splits=S)
+    mo, ml = pkv.lse_merge(op, lp)
+    torch.cuda.synchronize()
+    assert pkv.device_status() == 0
+    L = w.seq_lens.numpy().astype(np.int64)
+    C = 64 * (-(-L // (64 * S)))
+    args = (w.q.numpy(), w.k_codes.numpy(), w.v_codes.numpy(), w.k_scale.numpy(),
+            w.v_scale.numpy(), w.block_tables.numpy(), L.astype(np.int32), w.scale)
+    for s in range(S):
+        begin = np.minimum(s * C, L).astype(np.int32)
+        end = np.minimum((s + 1) * C, L).astype(np.int32)
+        ro, rl = oracle.paged_decode_attn_e4m3(*args, tok_begin=begin, tok_end=end)
+        assert_attention_close(op[s].cpu().numpy(), lp[s].cpu().numpy(), ro, rl, f"split {s}")
+    assert torch.equal(mo, out) and torch.equal(ml, lse), "merged partials vs the call"
+    ro, rl = oracle.paged_decode_attn_e4m3(*args)
+    assert_attention_close(mo.cpu().numpy(), ml.cpu().numpy(), ro, rl, "merged partials")
+
+
 def test_e4m3_mla_nan_codes_in_unused_slots_do_not_leak(pkv):
     """NaN codes in the slots past each sequence's end (and possibly in the
     block whose rows stand in for half tiles past the end): the value rows
@@ -455,16 +501,18 @@ def test_e4m3_multi_token_forced_generic_and_causality(pkv):
 
 @pytest.mark.parametrize("splits", [1, 2])
 @pytest.mark.parametrize("T,hq", [(3, 16), (4, 8)], ids=["rows_per_token", "folded"])
-def test_e4m3_multi_token_short_sequence_is_flagged(pkv, splits, T, hq):
-    """A sequence holding fewer tokens than T: its rows with no token give
-    out 0 and lse -inf, the device flags the length -- through one row per
-    (sequence, token) and through the folded tensor-core rows."""
+@pytest.mark.parametrize("held", ["one", "T-1"])
+def test_e4m3_multi_token_short_sequence_is_flagged(pkv, splits, T, hq, held):
+    """A sequence holding fewer tokens than T (one, or T - 1): its rows with
+    no token give out 0 and lse -inf, the device flags the length -- through
+    one row per (sequence, token) and through the folded tensor-core rows."""
+    n = 1 if held == "one" else T - 1
     w = multi_e4m3_case(9, [20, 0], T, hq, 2, 128, 128, 16)
-    w.seq_lens = torch.tensor([20 + T, 1], dtype=torch.int32)
+    w.seq_lens = torch.tensor([20 + T, n], dtype=torch.int32)
     pkv.device_status(reset=True)
     out, lse = gpu_multi_e4m3(pkv, w, splits)
-    assert np.isneginf(lse[1, :T - 1]).all() and (out[1, :T - 1] == 0).all()
-    assert np.isfinite(lse[1, T - 1]).all() and np.isfinite(lse[0]).all()
+    assert np.isneginf(lse[1, :T - n]).all() and (out[1, :T - n] == 0).all()
+    assert np.isfinite(lse[1, T - n:]).all() and np.isfinite(lse[0]).all()
     ro, rl = oracle_multi_e4m3(w)
     assert_attention_close(out, lse, ro, rl, "short")
     assert pkv.device_status(reset=True) & pkv.DEV_SEQ_LEN

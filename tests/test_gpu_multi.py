@@ -106,16 +106,20 @@ def test_multi_token_decode(pkv, shape, T, splits, flags):
                          ids=["rows12_per_token", "rows16_folded", "rows16_folded_G8"])
 @pytest.mark.parametrize("splits", [1, 2])
 @pytest.mark.parametrize("dk", [64, 128])
-def test_multi_token_short_sequence_is_flagged(pkv, T, hq, splits, dk):
-    """A sequence holding fewer tokens than T: the queries with no token are
-    empty (out 0, lse -inf), the others attend to what there is, and the
-    device flags the length -- through the per-token rows (G*T = 12) and
-    through the GQA kernel's folded rows (G*T = 16)."""
+@pytest.mark.parametrize("held", ["one", "T-1"])
+def test_multi_token_short_sequence_is_flagged(pkv, T, hq, splits, dk, held):
+    """A sequence holding fewer tokens than T (one, or T - 1: then no row is
+    of negative length): the queries with no token are empty (out 0, lse
+    -inf), the others attend to what there is, and the device flags the
+    length -- through the per-token rows (G*T = 12) and through the GQA
+    kernel's folded rows (G*T = 16)."""
+    n = 1 if held == "one" else T - 1
     w = multi_case(3, [20, 0], T, hq, 2, dk, dk, 16)
-    w.seq_lens = torch.tensor([20 + T, 1], dtype=torch.int32)  # sequence 1 holds 1 < T tokens
+    w.seq_lens = torch.tensor([20 + T, n], dtype=torch.int32)  # sequence 1 holds n < T tokens
+    pkv.device_status(reset=True)
     out, lse = gpu_multi(pkv, w, splits)
-    assert np.isneginf(lse[1, :T - 1]).all() and (out[1, :T - 1] == 0).all()
-    assert np.isfinite(lse[1, T - 1]).all() and np.isfinite(lse[0]).all()
+    assert np.isneginf(lse[1, :T - n]).all() and (out[1, :T - n] == 0).all()
+    assert np.isfinite(lse[1, T - n:]).all() and np.isfinite(lse[0]).all()
     ro, rl = oracle_multi(w)
     assert_attention_close(out, lse, ro, rl, f"short T{T}")
     assert pkv.device_status() & pkv.DEV_SEQ_LEN
