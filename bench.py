@@ -902,15 +902,18 @@ def time_step(pkv, st, args, world, stream, sampler=None):
     ev_k, ev_s = _events(K), _events(K)
     barrier(world)
     torch.cuda.synchronize()
-    # The GPU first spins (~0.3 ms of clock cycles per step) while the host
-    # enqueues the steps, so the steps then run back to back and no event
-    # bracket holds a wait for the host's next launch (a short step's calls
-    # can take the host longer than the GPU).
-    torch.cuda._sleep(int(K * 0.3e-3 * 2.0e9))
-    for i in range(K):
-        ev_s[i][0].record(stream)
-        st.run(*ev_k[i])
-        ev_s[i][1].record(stream)
+    # In batches of 64 steps, each behind a spin of the GPU (~0.3 ms of
+    # clock cycles per step) during which the host enqueues the batch: the
+    # steps of a batch then run back to back and no event bracket holds a
+    # wait for the host's next launch (a short step's calls can take the
+    # host longer than the GPU; a batch stays within the launch queue).
+    for i0 in range(0, K, 64):
+        n = min(64, K - i0)
+        torch.cuda._sleep(int(n * 0.3e-3 * 2.0e9))
+        for i in range(i0, i0 + n):
+            ev_s[i][0].record(stream)
+            st.run(*ev_k[i])
+            ev_s[i][1].record(stream)
     torch.cuda.synchronize()
     barrier(world)
     kern = [a.elapsed_time(b) for a, b in ev_k]

@@ -58,6 +58,9 @@
 #ifndef PKV_E4M3_R8_CTAS
 #define PKV_E4M3_R8_CTAS 3
 #endif
+#ifndef PKV_E4M3_R8_SG
+#define PKV_E4M3_R8_SG 1
+#endif
 // Groups of 16: two CTAs per SM, each with two softmax warp groups of four
 // warps (8 rows each) and the probabilities MN-major (a token's terms stored
 // with one 16-byte store per term half) -- the 16-row softmax was bound by
@@ -66,7 +69,19 @@
 #define PKV_E4M3_R16_SG 2
 #endif
 #ifndef PKV_E4M3_R16_RING
-#define PKV_E4M3_R16_RING 4
+#define PKV_E4M3_R16_RING 5
+#endif
+// Probability buffers (1 or 2) per form: one buffer frees its bytes for a
+// ring stage, the softmax then writes tile i + 1's terms after the value
+// product of tile i.
+#ifndef PKV_E4M3_R4_PBUF
+#define PKV_E4M3_R4_PBUF 2
+#endif
+#ifndef PKV_E4M3_R8_PBUF
+#define PKV_E4M3_R8_PBUF 2
+#endif
+#ifndef PKV_E4M3_R16_PBUF
+#define PKV_E4M3_R16_PBUF 1
 #endif
 
 namespace pkv {
@@ -89,12 +104,12 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 // Rows R per item, ring stages, CTAs per SM, softmax warp groups SG (each
-// of four warps, one thread per token lane, taking R / SG of the rows), and
-// the probability operand's layout: PMN = MN-major (a token's terms
+// of four warps, one thread per token lane, taking R / SG of the rows), the
+// probability operand's layout: PMN = MN-major (a token's terms
 // contiguous: [128 tokens][128 B], N = 128, so a thread stores its terms
 // with one vector store per term), else K-major ([NP rows][128 tokens],
-// one byte store per term and row).
-template <int R, int RING, int CTAS, int SG, bool PMN>
+// one byte store per term and row), and the probability buffers NPB.
+template <int R, int RING, int CTAS, int SG, bool PMN, int NPB>
 struct Cfg {
     static constexpr int kRing = RING;
     static constexpr int kCtas = CTAS;
@@ -106,12 +121,13 @@ struct Cfg {
         2 * kNQ + kNP <= 64 ? 64 : 2 * kNQ + kNP <= 128 ? 128 : 256;
     static constexpr uint32_t kPBytes = kNP * 128;                  // one probability buffer
     // Shared memory after the 1024-byte misc block: the query terms
-    // [4R rows][128 B], two probability buffers [NP rows][128 B], the ring.
+    // [4R rows][128 B], NPB probability buffers [NP rows][128 B], the ring.
     static constexpr uint32_t kOffP = 1024 + kNQ * 128;
-    static constexpr uint32_t kOffRing = kOffP + 2 * kPBytes;
+    static constexpr uint32_t kOffRing = kOffP + NPB * kPBytes;
     static constexpr uint32_t kSmemBytes = 1024 + kOffRing + RING * kStage;
     static_assert(kOffP % 1024 == 0 && kOffRing % 1024 == 0, "1024-byte-aligned operands");
     static_assert(RING <= 8, "mbarrier slots for at most 8 stages");
+    static_assert(NPB == 1 || NPB == 2, "one or two probability buffers");
 };
 
 // mbarrier slots
@@ -185,11 +201,11 @@ __device__ __forceinline__ Item fp8_item(const DecodeArgs &a, int item, int HG, 
     return r;
 }
 
-template <int R, int RING, int CTAS, int SG, bool PMN>
+template <int R, int RING, int CTAS, int SG, bool PMN, int NPB>
 __global__ void __launch_bounds__(64 + 128 * SG, CTAS)
 decode_gqa_tc_e4m3_kernel(const __grid_constant__ CUtensorMap tmap_k,
                           const __grid_constant__ CUtensorMap tmap_v, const DecodeArgs a) {
-    using S = Cfg<R, RING, CTAS, SG, PMN>;
+    using S = Cfg<R, RING, CTAS, SG, PMN, NPB>;
     constexpr int kRing = RING;
     constexpr uint32_t kOffP = S::kOffP, kOffRing = S::kOffRing;
     extern __shared__ uint8_t smem_raw[];
@@ -367,8 +383,8 @@ decode_gqa_tc_e4m3_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 if (i >= kLag) {
                     // ---- O^T += V_tile^T . Pterms^T for tile j
                     const int j = i - kLag;
-                    const uint32_t pbuf = pcount & 1u;
-                    if (!(ok = wait_all(bar(kBarPFull + pbuf), (pcount >> 1) & 1u))) break;
+                    const uint32_t pbuf = pcount % NPB;
+                    if (!(ok = wait_all(bar(kBarPFull + pbuf), (pcount / NPB) & 1u))) break;
                     if (j == 0 && !(ok = wait_all(bar(kBarOEmpty), (ne & 1u) ^ 1u))) break;
                     if (!(ok = wait_all(bar(kBarFull + stage), phase))) break;
                     const int64_t tok0 = r.begin + int64_t(j) * kM;
@@ -428,12 +444,12 @@ decode_gqa_tc_e4m3_kernel(const __grid_constant__ CUtensorMap tmap_k,
         constexpr int kTpr = 128 * SG / R;               // threads per query row in the split
         constexpr int kDpt = kD / kTpr;                  // query dims per thread
         uint32_t tcount = 0, pcount = 0, ne = 0;
-        // the pad rows (columns) of both probability buffers stay zero
-        for (int i = tt; i < 2 * int(S::kPBytes) / 16; i += kSoftThreads * SG)
+        // the pad rows (columns) of the probability buffers stay zero
+        for (int i = tt; i < NPB * int(S::kPBytes) / 16; i += kSoftThreads * SG)
             reinterpret_cast<uint4 *>(ps)[i] = make_uint4(0, 0, 0, 0);
         fence_proxy_async_smem();
         auto wait_pv = [&](uint32_t j) {
-            return pipe_wait(bar(kBarPvDone + (j & 1u)), (j >> 1) & 1u, a.status, abort_flag);
+            return pipe_wait(bar(kBarPvDone + j % NPB), (j / NPB) & 1u, a.status, abort_flag);
         };
         // barrier 1 + grp over this group's 128 threads (an OR of `pred`)
         auto gbar_or = [&](bool pred) -> bool {
@@ -612,13 +628,14 @@ decode_gqa_tc_e4m3_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     p[j] = x[j] == -INFINITY ? 0.f : ex2_approx(x[j] - mrow[h0 + j]);
                     l_part[j] += p[j];
                 }
-                // this P buffer was last read by the value MMAs of tile pcount-2
-                if (pcount >= 2) wait_pv(pcount - 2);
+                // this P buffer was last read by the value MMAs of tile
+                // pcount - NPB
+                if (pcount >= NPB) wait_pv(pcount - NPB);
                 {
                     // five E4M3 terms of each probability (p <= 2^8): term k of
                     // row h is column k R + h of the value MMA's B operand,
                     // this thread's token its row (MN-major) or its column
-                    uint8_t *pa = ps + (pcount & 1u) * S::kPBytes;
+                    uint8_t *pa = ps + (pcount % NPB) * S::kPBytes;
 #pragma unroll
                     for (int k = 0; k < kPTerms; ++k) {
                         uint32_t word[(RG + 3) / 4];
@@ -656,7 +673,7 @@ decode_gqa_tc_e4m3_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 }
                 fence_proxy_async_smem();
                 tc::fence_before_sync();
-                mbar_arrive(bar(kBarPFull + (pcount & 1u)));
+                mbar_arrive(bar(kBarPFull + pcount % NPB));
                 ++pcount;
             }
             if (!ok) break;
@@ -738,10 +755,10 @@ bool make_byte_map(CUtensorMap *map, const void *pool, int64_t rows, int box) {
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int R, int RING, int CTAS, int SG, bool PMN>
+template <int R, int RING, int CTAS, int SG, bool PMN, int NPB>
 int launch_rows(const DecodeArgs &a) {
-    using S = Cfg<R, RING, CTAS, SG, PMN>;
-    auto kernel = decode_gqa_tc_e4m3_kernel<R, RING, CTAS, SG, PMN>;
+    using S = Cfg<R, RING, CTAS, SG, PMN, NPB>;
+    auto kernel = decode_gqa_tc_e4m3_kernel<R, RING, CTAS, SG, PMN, NPB>;
     const int64_t rows = int64_t(a.cache.num_blocks) * a.cache.num_kv_heads * a.cache.block_size;
     const int box = std::min(a.cache.block_size, kM);
     CUtensorMap tk, tv;
@@ -788,11 +805,15 @@ int gqa_tc_e4m3_resident_ctas(int32_t group) {
 
 int launch_decode_gqa_tc_e4m3(const DecodeArgs &a) {
     switch (a.num_q_heads / a.cache.num_kv_heads * a.q_tokens) {
-        case 4: return launch_rows<4, PKV_E4M3_R4_RING, PKV_E4M3_R4_CTAS, 1, false>(a);
-        case 8: return launch_rows<8, PKV_E4M3_R8_RING, PKV_E4M3_R8_CTAS, 1, false>(a);
+        case 4:
+            return launch_rows<4, PKV_E4M3_R4_RING, PKV_E4M3_R4_CTAS, 1, false, PKV_E4M3_R4_PBUF>(a);
+        case 8:
+            return launch_rows<8, PKV_E4M3_R8_RING, PKV_E4M3_R8_CTAS, PKV_E4M3_R8_SG,
+                               (PKV_E4M3_R8_SG > 1), PKV_E4M3_R8_PBUF>(a);
         case 16:
         case 32:   // 32 rows: two head groups of 16
-            return launch_rows<16, PKV_E4M3_R16_RING, 2, PKV_E4M3_R16_SG, (PKV_E4M3_R16_SG > 1)>(a);
+            return launch_rows<16, PKV_E4M3_R16_RING, 2, PKV_E4M3_R16_SG, (PKV_E4M3_R16_SG > 1),
+                               PKV_E4M3_R16_PBUF>(a);
         default: return PKV_ERR_SHAPE;
     }
 }
