@@ -58,6 +58,10 @@ FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
 # their hash matches).
 PROFILES = {
     "long32k": ("decode_tma_long32k.txt", ("decode_tma.cu", "pkv_device.cuh", "pkv_math.cuh")),
+    "dcp200k": ("decode_tma_dcp200k.txt", ("decode_tma.cu", "pkv_device.cuh", "pkv_math.cuh")),
+    "dcp200k_e4m3": ("decode_gqa_tc_e4m3_dcp200k.txt",
+                     ("decode_gqa_tc_e4m3.cu", "pkv_device.cuh", "pkv_tcgen05.cuh",
+                      "pkv_pipeline.cuh", "pkv_math.cuh")),
     "spec4_32k": ("decode_gqa_tc_spec4_32k.txt",
                   ("decode_gqa_tc.cu", "pkv_device.cuh", "pkv_tcgen05.cuh", "pkv_pipeline.cuh",
                    "pkv_math.cuh")),
