@@ -241,38 +241,20 @@ decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
             // Rows of block 0 of this KV head stand in for boxes past the end
             // (masked scores, zeroed value rows).
             const int32_t standin = r.g * bs;
-            // One table read resolves the boxes of tpg tiles (lane j: box
-            // j % nbox of tile j / nbox of the group); the next group's
-            // entries are loaded a group ahead, so no table read waits in
-            // front of a copy.
-            const int tpg = 32 / nbox;
-            auto first_token = [&](int i0) -> int64_t {   // of this lane's box, or -1
-                const int ti = i0 + lane / nbox;
-                const int64_t t = r.begin + int64_t(ti) * kM + int64_t(lane % nbox) * box;
-                return ti < r.ntiles && t < r.end ? t : -1;
-            };
-            auto fetch = [&](int i0) -> int32_t {
-                const int64_t t = first_token(i0);
-                return t >= 0 ? table[t / bs] : 0;
-            };
-            int32_t phys_next = fetch(0);
-            int32_t yg = standin;
             int32_t yprev = standin;
             for (int i = 0; i <= r.ntiles && ok; ++i) {
-                if (i % tpg == 0) {
-                    const int32_t phys = phys_next;
-                    phys_next = fetch(i + tpg);
-                    const int64_t t = first_token(i);
-                    yg = standin;
-                    if (t >= 0) {
+                // lane j < nbox: global row of box j of tile i
+                int32_t y = standin;
+                if (i < r.ntiles && lane < nbox) {
+                    const int64_t t = r.begin + int64_t(i) * kM + int64_t(lane) * box;
+                    if (t < r.end) {
+                        const int32_t phys = table[t / bs];
                         if (phys >= 0 && phys < a.cache.num_blocks)
-                            yg = (phys * hkv + r.g) * bs + int32_t(t % bs);
+                            y = (phys * hkv + r.g) * bs + int32_t(t % bs);
                         else
                             raise_status(a.status, PKV_DEV_BLOCK_ID);
                     }
                 }
-                // lane j < nbox: global row of box j of tile i
-                const int32_t y = __shfl_sync(0xffffffffu, yg, (i % tpg) * nbox + lane % nbox);
                 // stage h of a tile: tokens 64h..64h+63; lane j issues box j
                 // (after lane 0 armed the stage), box j - h * per_stage of it
                 for (int kv = (i < r.ntiles ? 0 : 1); kv < (i > 0 ? 2 : 1) && ok; ++kv) {

@@ -205,30 +205,20 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmap_k,
             const ItemRange r = item_range(a, item, C::kStageTokens, false);
             const int total_segs = r.nstages * segs_per_stage;
             const int32_t *table = a.block_tables + int64_t(r.b) * a.max_blocks;
-            // first token of segment base + lane, or -1 (no token there)
-            auto first_token = [&](int base) -> int64_t {
-                const int sg = base + lane;
-                const int64_t ts = r.begin + int64_t(sg) * seg_rows;
-                return sg < total_segs && ts < r.end ? ts : -1;
-            };
-            auto fetch = [&](int base) -> int32_t {
-                const int64_t ts = first_token(base);
-                return ts >= 0 ? table[ts / bs] : 0;
-            };
-            // the next 32 segments' table entries load while these are issued
-            int32_t phys_next = fetch(0);
             for (int base = 0; base < total_segs && ok; base += 32) {
                 // Lane i resolves segment base + i to a global row; block 0
                 // of this KV head stands in for segments without a token.
-                const int32_t phys = phys_next;
-                phys_next = fetch(base + 32);
                 int32_t y = r.g * bs;
-                const int64_t ts = first_token(base);
-                if (ts >= 0) {
-                    if (phys >= 0 && phys < a.cache.num_blocks)
-                        y = (phys * hkv + r.g) * bs + int32_t(ts % bs);
-                    else
-                        raise_status(a.status, PKV_DEV_BLOCK_ID);
+                const int sg = base + lane;
+                if (sg < total_segs) {
+                    const int64_t ts = r.begin + int64_t(sg) * seg_rows;
+                    if (ts < r.end) {
+                        const int32_t phys = table[ts / bs];
+                        if (phys >= 0 && phys < a.cache.num_blocks)
+                            y = (phys * hkv + r.g) * bs + int32_t(ts % bs);
+                        else
+                            raise_status(a.status, PKV_DEV_BLOCK_ID);
+                    }
                 }
                 const int nseg = min(32, total_segs - base);
                 for (int k = 0; k < nseg; k += segs_per_stage) {
