@@ -45,7 +45,8 @@
 // ring stages each (measured on 8 x 32K: 89.8 us against 96.5 us for two
 // CTAs with five stages at groups of 4; 97.4 us against 102.5 us at groups
 // of 8, whose registers then go from 121 to 96 with a 24-byte spill).
-// Groups of 16 keep two CTAs with five stages.
+// Groups of 8 on two CTAs with two softmax groups (SG 2, probabilities
+// MN-major) matched three CTAs per DCP step but did not beat it.
 #ifndef PKV_E4M3_R4_RING
 #define PKV_E4M3_R4_RING 3
 #endif
@@ -64,7 +65,9 @@
 // Groups of 16: two CTAs per SM, each with two softmax warp groups of four
 // warps (8 rows each) and the probabilities MN-major (a token's terms stored
 // with one 16-byte store per term half) -- the 16-row softmax was bound by
-// its own instruction chain per warp -- and four ring stages.
+// its own instruction chain per warp -- and five ring stages beside one
+// probability buffer (108.9 us per speculative step against 111.2 us with
+// four stages and two buffers).
 #ifndef PKV_E4M3_R16_SG
 #define PKV_E4M3_R16_SG 2
 #endif
