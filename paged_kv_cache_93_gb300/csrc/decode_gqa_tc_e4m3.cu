@@ -157,6 +157,21 @@ constexpr uint32_t kOffQ = 1024;
 
 __device__ __forceinline__ int64_t lmin(int64_t x, int64_t y) { return x < y ? x : y; }
 
+// The next terms' inputs after the E4M3 codes c (bits 0-7: x0's, 8-15:
+// x1's): x_i <- 16 (x_i - v_i), v_i the value of code i, as one
+// mixed-precision fma per element on v_i in fp16 (every E4M3 value is an
+// fp16 value): 16 x_i - 16 v_i.  v_i is x_i rounded to four significant
+// bits, so the difference, its product by 16 and hence the single rounding
+// of the fma are exact -- the same bits as a subtraction then a product.
+__device__ __forceinline__ void residual16(uint32_t c, float &x0, float &x1) {
+    uint32_t h2;
+    asm("{ .reg .b16 c; cvt.u16.u32 c, %1; cvt.rn.f16x2.e4m3x2 %0, c; }" : "=r"(h2) : "r"(c));
+    const float a0 = 16.f * x0, a1 = 16.f * x1;
+    asm("{ .reg .b16 l, h, m; mov.b16 m, 0xCC00; mov.b32 {l, h}, %2; "
+        "fma.rn.f32.f16 %0, l, m, %3; fma.rn.f32.f16 %1, h, m, %4; }"   // m = -16
+        : "=f"(x0), "=f"(x1) : "r"(h2), "f"(a0), "f"(a1));
+}
+
 // Byte offset of (row, column < 128) in a [rows][128 B] array with the
 // 128-byte swizzle (8-row atoms 1024-byte aligned).
 __device__ __forceinline__ uint32_t swz8(int row, int col) {
@@ -525,11 +540,8 @@ decode_gqa_tc_e4m3_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         const uint32_t c23 = e4m3x2_from_f32(x[e + 2], x[e + 3]);
                         *reinterpret_cast<uint32_t *>(qs + swz8(k * R + h, d0 + e)) =
                             c01 | (c23 << 16);
-                        const float2 v01 = e4m3x2_to_f32(c01), v23 = e4m3x2_to_f32(c23);
-                        x[e] = (x[e] - v01.x) * 16.f;
-                        x[e + 1] = (x[e + 1] - v01.y) * 16.f;
-                        x[e + 2] = (x[e + 2] - v23.x) * 16.f;
-                        x[e + 3] = (x[e + 3] - v23.y) * 16.f;
+                        residual16(c01, x[e], x[e + 1]);
+                        residual16(c23, x[e + 2], x[e + 3]);
                     }
                 fence_proxy_async_smem();
             }
@@ -652,11 +664,7 @@ decode_gqa_tc_e4m3_kernel(const __grid_constant__ CUtensorMap tmap_k,
                                 pa[swz8(k * R + h0 + j, row)] = uint8_t(c);
                                 pa[swz8(k * R + h0 + j + 1, row)] = uint8_t(c >> 8);
                             }
-                            if (k + 1 < kPTerms) {
-                                const float2 v = e4m3x2_to_f32(c);
-                                p[j] = (p[j] - v.x) * 16.f;
-                                p[j + 1] = (p[j + 1] - v.y) * 16.f;
-                            }
+                            if (k + 1 < kPTerms) residual16(c, p[j], p[j + 1]);
                         }
                         if constexpr (PMN) {
                             // bytes k R + h0 .. + RG of this token's 128-byte row:
