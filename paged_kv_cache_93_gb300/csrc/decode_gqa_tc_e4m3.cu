@@ -589,11 +589,17 @@ decode_gqa_tc_e4m3_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     x[j] = h0 + j >= hmin ? x[j] : -INFINITY;
                     need |= x[j] > mrow[h0 + j] + kSlack;
                 }
-                if (gbar_or(!w)) {
-                    ok = false;
-                    break;
+                // one group barrier in the common case (no failed wait, no
+                // rise of a running max); the rare cases are told apart after it
+                bool rise = false;
+                if (gbar_or(need || !w)) {
+                    if (gbar_or(!w)) {
+                        ok = false;
+                        break;
+                    }
+                    rise = gbar_or(need);
                 }
-                if (gbar_or(need)) {
+                if (rise) {
 #pragma unroll
                     for (int j = 0; j < RG; ++j) {
                         float m = x[j];
