@@ -911,9 +911,11 @@ def time_step(pkv, st, args, world, stream, sampler=None):
     # steps of a batch then run back to back and no event bracket holds a
     # wait for the host's next launch (a short step's calls can take the
     # host longer than the GPU; a batch stays within the launch queue).
+    spin = getattr(torch.cuda, "_sleep", None)   # torch's spin kernel (clock cycles)
     for i0 in range(0, K, 64):
         n = min(64, K - i0)
-        torch.cuda._sleep(int(n * 0.3e-3 * 2.0e9))
+        if spin is not None:
+            spin(int(n * 0.3e-3 * 2.0e9))
         for i in range(i0, i0 + n):
             ev_s[i][0].record(stream)
             st.run(*ev_k[i])
